@@ -1,0 +1,299 @@
+"""Seeded synthetic hybrid batches (inputs only — no attention arithmetic lives here).
+
+Both the CUDA path and the fp64 oracle are fed from these generators; this module computes
+nothing of the method. A batch is one layer of one serving iteration: some prompt chunks
+(prefill / extend) and some decoding sequences over one paged K/V pool
+("Week 6: Beyond PyTorch: Custom Kernel과 vLLM", §"한 스텝에 여러 종류의 request 섞기" and
+§"PagedAttention").
+
+Recipe (also stated in the design notes):
+  * integer choices (lengths, prefix offsets) come from ``random.Random(seed)``;
+  * physical blocks are a ``torch.randperm`` of the pool (seed-derived CPU generator), so a
+    sequence's logical blocks are scattered;
+  * Q, K, V are N(0, 1) fp32 draws from a seed-derived ``torch.Generator`` on the target
+    device, rounded to bf16; draw order: q_prefill, q_decode, k_pool, v_pool;
+  * the pool holds sum(ceil(kv_len/16)) blocks plus 5 % spare; spare blocks, the unused slots
+    of every sequence's last block, and the block-table entries past each sequence's end (which
+    point at a spare block) are poisoned with bf16 NaN, so any read outside the visible rows
+    shows up as NaN in the output.
+"""
+from __future__ import annotations
+
+import math
+import random
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import torch
+
+HEAD_DIM = 128
+BLOCK_SIZE = 16
+BF16_NAN_BITS = 0x7FC0
+
+
+@dataclass
+class HybridBatch:
+    """One hybrid batch. Tensors live on ``device``; host lists mirror the int32 tables."""
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    q_lens: List[int]               # prefill chunk lengths
+    prefill_kv_lens: List[int]      # cached rows of each prefill sequence (chunk included)
+    decode_kv_lens: List[int]       # cached rows of each decode sequence (new token included)
+    scale: float
+    q_prefill: torch.Tensor         # bf16 [Tp][Hq][D]
+    q_decode: torch.Tensor          # bf16 [Nd][Hq][D]
+    k_pool: torch.Tensor            # bf16 [NB][Hkv][16][D]
+    v_pool: torch.Tensor            # bf16 [NB][Hkv][16][D]
+    block_tables: torch.Tensor      # int32 [Np+Nd][max_blocks_per_seq]
+    cu_seqlens_q: torch.Tensor      # int32 [Np+1]
+    kv_lens: torch.Tensor           # int32 [Np+Nd]
+    seed: int = 0
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_prefill_seqs(self) -> int:
+        return len(self.q_lens)
+
+    @property
+    def num_decode_seqs(self) -> int:
+        return len(self.decode_kv_lens)
+
+    @property
+    def num_prefill_tokens(self) -> int:
+        return int(sum(self.q_lens))
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_pool.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def host_cu_seqlens(self) -> List[int]:
+        cu = [0]
+        for n in self.q_lens:
+            cu.append(cu[-1] + n)
+        return cu
+
+    @property
+    def host_kv_lens(self) -> List[int]:
+        return list(self.prefill_kv_lens) + list(self.decode_kv_lens)
+
+    def to(self, device) -> "HybridBatch":
+        """A copy with every tensor moved to ``device``."""
+        kw = dict(self.__dict__)
+        for k, v in list(kw.items()):
+            if isinstance(v, torch.Tensor):
+                kw[k] = v.to(device)
+        return HybridBatch(**kw)
+
+
+def _blocks(n: int) -> int:
+    return (n + BLOCK_SIZE - 1) // BLOCK_SIZE
+
+
+def make_batch(num_q_heads: int, num_kv_heads: int, q_lens: Sequence[int],
+               prefill_kv_lens: Sequence[int], decode_kv_lens: Sequence[int], seed: int,
+               device="cpu", scale: Optional[float] = None, permute: bool = True,
+               spare_frac: float = 0.05, poison: bool = True, std: float = 1.0,
+               name: str = "") -> HybridBatch:
+    """Build one seeded hybrid batch (see the module docstring for the recipe)."""
+    q_lens = [int(x) for x in q_lens]
+    prefill_kv_lens = [int(x) for x in prefill_kv_lens]
+    decode_kv_lens = [int(x) for x in decode_kv_lens]
+    assert len(q_lens) == len(prefill_kv_lens)
+    D = HEAD_DIM
+    Hq, Hkv = int(num_q_heads), int(num_kv_heads)
+    lens = prefill_kv_lens + decode_kv_lens
+    nseq = len(lens)
+    need = [_blocks(L) for L in lens]
+    used = sum(need)
+    spare = max(1, int(math.ceil(spare_frac * used))) if poison else 0
+    nb = max(1, used + spare)
+    maxb = max([1] + need)
+
+    # physical block assignment: a random permutation of the pool, handed out in order
+    g_cpu = torch.Generator().manual_seed(seed * 1_000_003 + 11)
+    perm = torch.randperm(nb, generator=g_cpu) if permute else torch.arange(nb)
+    spare_ids = perm[used:].tolist()
+    tail_fill = spare_ids[0] if spare_ids else 0
+    bt = torch.full((max(nseq, 1), maxb), tail_fill, dtype=torch.int32)
+    pos = 0
+    for s, n in enumerate(need):
+        bt[s, :n] = perm[pos:pos + n].to(torch.int32)
+        pos += n
+    if nseq == 0:
+        bt = bt[:0]
+
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed * 1_000_003 + 29)
+
+    def draw(*shape):
+        x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
+        if std != 1.0:
+            x = x * std
+        return x.to(torch.bfloat16)
+
+    tp = sum(q_lens)
+    q_prefill = draw(tp, Hq, D)
+    q_decode = draw(len(decode_kv_lens), Hq, D)
+    k_pool = draw(nb, Hkv, BLOCK_SIZE, D)
+    v_pool = draw(nb, Hkv, BLOCK_SIZE, D)
+
+    if poison:
+        nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+        if spare_ids:
+            idx = torch.tensor(spare_ids, dtype=torch.long, device=dev)
+            k_pool[idx] = nan
+            v_pool[idx] = nan
+        for s, L in enumerate(lens):
+            r = L % BLOCK_SIZE
+            if r:
+                last = int(bt[s, need[s] - 1])
+                k_pool[last, :, r:, :] = nan
+                v_pool[last, :, r:, :] = nan
+
+    cu = [0]
+    for n in q_lens:
+        cu.append(cu[-1] + n)
+    return HybridBatch(
+        num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=BLOCK_SIZE, q_lens=q_lens,
+        prefill_kv_lens=prefill_kv_lens, decode_kv_lens=decode_kv_lens,
+        scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
+        q_prefill=q_prefill, q_decode=q_decode, k_pool=k_pool, v_pool=v_pool,
+        block_tables=bt.to(dev), cu_seqlens_q=torch.tensor(cu, dtype=torch.int32, device=dev),
+        kv_lens=torch.tensor(lens, dtype=torch.int32, device=dev), seed=seed, name=name)
+
+
+# ----------------------------------------------------------------------------------------------
+# The evaluation configurations: attention shapes of the models the POD-Attention digest
+# evaluates (Yi-6B, Llama-2-7B, Llama-3-8B, 4K-32K context; "장문맥에서 커지는 이점").
+# ----------------------------------------------------------------------------------------------
+
+CONFIG_NAMES = {
+    1: "tiny hybrid batch (Hq2/Hkv1, chunk 64 @ 64, 4 decodes)",
+    2: "Llama-2-7B attention (32/32, chunk 512 @ 3584, 32 decodes ctx U[2048,4096])",
+    3: "Llama-3-8B attention (32/8, chunk 1024 @ U[0,15360], 64 decodes ctx U[8192,16384])",
+    4: "Yi-6B attention (32/4, chunk 2048 @ 28672, 16 decodes ctx U[16384,32768])",
+}
+
+
+def config_lengths(i: int):
+    """(Hq, Hkv, q_lens, prefill_kv_lens, decode_kv_lens) of configuration i (seed = i)."""
+    rng = random.Random(i)
+    if i == 1:
+        return 2, 1, [64], [128], [100, 150, 233, 300]
+    if i == 2:
+        return 32, 32, [512], [4096], [rng.randint(2048, 4096) for _ in range(32)]
+    if i == 3:
+        dec = [rng.randint(8192, 16384) for _ in range(64)]
+        off = rng.randint(0, 15360)
+        return 32, 8, [1024], [off + 1024], dec
+    if i == 4:
+        return 32, 4, [2048], [28672 + 2048], [rng.randint(16384, 32768) for _ in range(16)]
+    raise ValueError(f"unknown configuration {i}")
+
+
+def config(i: int, device="cpu", **kw) -> HybridBatch:
+    """Configuration i (1..4) as a seeded batch on ``device``."""
+    Hq, Hkv, ql, pkv, dkv = config_lengths(i)
+    return make_batch(Hq, Hkv, ql, pkv, dkv, seed=i, device=device, name=CONFIG_NAMES[i], **kw)
+
+
+# ----------------------------------------------------------------------------------------------
+# Mixed-kind structural example: two decodes, one extend of 8 tokens after a cached prefix,
+# one fresh prefill of 4 tokens — 14 new tokens in the step ("Week 6: Beyond PyTorch",
+# §"한 스텝에 여러 종류의 request 섞기"). The prefix length of the extend is not printed; it
+# is a parameter here.
+# ----------------------------------------------------------------------------------------------
+
+def mixed_kind_example(prefix_c: int = 24, ctx_a: int = 37, ctx_b: int = 5, seed: int = 0,
+                       num_q_heads: int = 4, num_kv_heads: int = 2,
+                       device="cpu") -> HybridBatch:
+    """Requests A, B (decode, one token each), C (extend, 8 tokens after `prefix_c` cached
+    rows) and D (prefill, 4 tokens, no cache)."""
+    q_lens = [8, 4]                      # C, D
+    prefill_kv = [prefix_c + 8, 4]       # C sees its prefix; D has none
+    decode_kv = [ctx_a, ctx_b]           # A, B
+    return make_batch(num_q_heads, num_kv_heads, q_lens, prefill_kv, decode_kv, seed=seed,
+                      device=device, name="mixed-kind example (A,B decode; C extend; D prefill)")
+
+
+# ----------------------------------------------------------------------------------------------
+# Configuration 5: a seeded 200-iteration hybrid-batching trace on the Llama-3-8B shape.
+# A chunked-prefill scheduler with a 2048-token budget takes every running decode first, then
+# fills the rest of the budget with prompt chunks in FIFO order ("LLMSO - W4", §"Prefill-Decode
+# 분리 스케줄링": decode first, then prefill up to the token budget).
+# ----------------------------------------------------------------------------------------------
+
+@dataclass
+class TraceStep:
+    q_lens: List[int]
+    prefill_kv_lens: List[int]
+    decode_kv_lens: List[int]
+
+
+def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
+          decode_targets=(19, 38, 56, 75)) -> List[TraceStep]:
+    """Iteration shapes of mix 'a' (decode-heavy) or 'b' (prefill-heavy).
+
+    (a) prompts log-uniform in [4096, 32768], outputs geometric with mean 256;
+    (b) prompts lognormal with mean 16384 (sigma 0.5 in log space), clipped to
+        [4096, 32768], outputs geometric with mean 64.
+    The number of running decodes is held at a target that changes every quarter of the trace
+    (19, 38, 56, 75 sequences -> 152, 304, 448, 600 decode (seq, kv-head) units for 8 KV heads:
+    just above multiples of the SM count). A finished decode is replaced by a request whose
+    prompt is already cached (a warm request); prompt chunks come from a FIFO of new requests.
+    """
+    assert mix in ("a", "b")
+    rng = random.Random(seed * 31 + (1 if mix == "a" else 2))
+
+    def prompt_len():
+        if mix == "a":
+            return int(math.exp(rng.uniform(math.log(4096), math.log(32768))))
+        sigma = 0.5
+        mu = math.log(16384) - sigma * sigma / 2
+        return int(min(32768, max(4096, rng.lognormvariate(mu, sigma))))
+
+    def out_len():
+        mean = 256 if mix == "a" else 64
+        n = 1
+        while rng.random() > 1.0 / mean:
+            n += 1
+        return n
+
+    decodes = []    # [context length, tokens left]
+    fifo = []       # [prompt length, rows already prefilled]
+    steps = []
+    for it in range(iters):
+        target = decode_targets[(it * len(decode_targets)) // iters]
+        decodes = [d for d in decodes if d[1] > 0]
+        while len(decodes) < target:
+            decodes.append([prompt_len(), out_len()])
+        while len(fifo) < 4:
+            fifo.append([prompt_len(), 0])
+        dec_lens = []
+        for d in decodes:
+            d[0] += 1                     # the new token's K/V is appended before attention
+            d[1] -= 1
+            dec_lens.append(d[0])
+        left = budget - len(dec_lens)
+        ql, pkv = [], []
+        for r in fifo:
+            if left <= 0:
+                break
+            c = min(left, r[0] - r[1])
+            if c <= 0:
+                continue
+            ql.append(c)
+            pkv.append(r[1] + c)
+            r[1] += c
+            left -= c
+        fifo = [r for r in fifo if r[1] < r[0]]
+        steps.append(TraceStep(ql, pkv, dec_lens))
+    return steps

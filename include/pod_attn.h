@@ -1,0 +1,237 @@
+/*
+ * pod_attn.h — C ABI of the GB300 (sm_103a) hybrid prefill+decode attention library.
+ *
+ * One launch computes, for one attention layer of one serving iteration:
+ *   - the causal chunked-prefill ("extend") attention of each prompt chunk against its cached
+ *     prefix plus the earlier tokens of the same chunk, and
+ *   - the single-query decode attention of each decoding sequence,
+ * both over one paged K/V cache (block size 16, grouped-query attention).
+ *
+ * Sources (web pages; titles and sections are what the citations below name):
+ *   [POD]    "POD-Attention: hybrid batching" digest of the ASPLOS 2025 paper, Silicon & Systems
+ *            (siliconandsystems.com/ko/articles/pod-attention-hybrid-batching).
+ *   [BEYOND] "Week 6: Beyond PyTorch: Custom Kernel과 vLLM" lecture (core-sig.pytorch.kr).
+ *   [LLMSO]  "LLMSO - W4 - Optimization & Frameworks" (seojhoon.tistory.com).
+ *
+ * What is computed (the definition every variant reaches, up to rounding order):
+ *   [BEYOND] §"Attention에 적용하기": out = softmax(q·Kᵀ·scale)·V, with the causal rule of
+ *   §"Non-Causal vs. Causal Attention" and the extend semantics of
+ *   §"한 스텝에 여러 종류의 request 섞기": a prefill token at local index i of a chunk of q_len
+ *   tokens whose sequence holds kv_len cached rows (the chunk's own K/V included) sits at
+ *   absolute position p = kv_len - q_len + i and attends to rows 0..p. A decode token is an
+ *   extend of one token: it attends to all kv_len rows.
+ *   [POD] §"가상 CTA와 SM별 균형": fusing the two operations reorders independent tiles only,
+ *   it does not change the mathematical result.
+ *
+ * Conventions shared by every entry point:
+ *   - head_dim is 128, the paged block size is 16 tokens, all tensors are bf16 (IEEE bfloat16,
+ *     little-endian), accumulation is fp32, outputs are rounded once to bf16 (nearest-even).
+ *   - Layouts (row-major, innermost last, no padding):
+ *       q_prefill, o_prefill : [num_prefill_tokens][num_q_heads][128]   (tokens of all chunks,
+ *                                                                        concatenated)
+ *       q_decode,  o_decode  : [num_decode_seqs][num_q_heads][128]
+ *       k_pool, v_pool       : [num_blocks][num_kv_heads][16][128]      (one (block, kv-head)
+ *                                                                        is 4 KiB contiguous)
+ *       block_tables         : int32 [num_prefill_seqs + num_decode_seqs][max_blocks_per_seq];
+ *                              row s maps logical block j of sequence s to a physical block
+ *                              ([BEYOND] §"PagedAttention", [LLMSO] §"PagedAttention —
+ *                              메모리 단편화를 없애는 커널"). Prefill sequences come first, then
+ *                              decode sequences. Entries at or beyond ceil(kv_len/16) are never
+ *                              read.
+ *       cu_seqlens_q         : int32 [num_prefill_seqs + 1], cu[0] = 0, cu[Np] =
+ *                              num_prefill_tokens; chunk s owns tokens [cu[s], cu[s+1]).
+ *       kv_lens              : int32 [num_prefill_seqs + num_decode_seqs], prefill sequences
+ *                              first. kv_len counts cached rows including this step's new
+ *                              tokens, whose K/V must already be in the pool.
+ *   - Query head h reads kv-head h / (num_q_heads / num_kv_heads) ([LLMSO] §"KV 헤드 줄이기").
+ *   - The caller owns every device buffer and every stream. The library owns only the opaque
+ *     host plan (and the two CUDA events a plan holds), freed by pod_attn_plan_destroy.
+ *   - No C++ exception crosses this boundary. Every function returns a status or a value.
+ *   - pod_attn_run never allocates device memory and never synchronises the host.
+ */
+#ifndef POD_ATTN_H_
+#define POD_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. Negative values are errors. */
+typedef enum {
+  POD_ATTN_OK = 0,
+  POD_ATTN_ERR_INVALID_ARG = -1,  /* a null pointer, a bad length or an inconsistent shape */
+  POD_ATTN_ERR_UNSUPPORTED = -2,  /* head_dim != 128, block_size != 16, group size > 16, ... */
+  POD_ATTN_ERR_WORKSPACE = -3,    /* workspace too small or not 256-byte aligned */
+  POD_ATTN_ERR_CUDA = -4,         /* a CUDA runtime call failed (no device, launch error, ...) */
+  POD_ATTN_ERR_BAD_INDEX = -5,    /* device-detected: a block-table entry outside [0, num_blocks) */
+  POD_ATTN_ERR_TIMEOUT = -6       /* device-detected: a bounded pipeline wait ran out */
+} pod_attn_status;
+
+/* How the plan's work is launched. All three compute identical results on identical inputs;
+ * they differ only in scheduling ([POD] §"동시 실행만으로 부족한 이유" and
+ * §"재현과 장비 평가 기준" compare exactly these three). */
+typedef enum {
+  POD_ATTN_FUSED = 0,   /* one persistent launch; each CTA picks prefill or decode work by SM */
+  POD_ATTN_SERIAL = 1,  /* a prefill-only launch, then a decode-only launch, on `stream` */
+  POD_ATTN_STREAMS = 2  /* prefill on `stream`, decode on `stream2`, joined back on `stream` */
+} pod_attn_variant;
+
+/* Shapes of one hybrid batch. */
+typedef struct {
+  int32_t num_q_heads;         /* Hq >= 1 */
+  int32_t num_kv_heads;        /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 16 */
+  int32_t head_dim;            /* must be 128 */
+  int32_t block_size;          /* must be 16 */
+  int32_t num_prefill_seqs;    /* Np >= 0 */
+  int32_t num_prefill_tokens;  /* sum of chunk lengths; 0 iff Np == 0 */
+  int32_t num_decode_seqs;     /* Nd >= 0 */
+  int32_t num_blocks;          /* physical blocks in each of k_pool and v_pool */
+  int32_t max_blocks_per_seq;  /* row length of block_tables */
+  float scale;                 /* softmax scale, typically 1/sqrt(128) */
+} pod_attn_problem;
+
+/* Planner and launch options. Zero-initialise for defaults. */
+typedef struct {
+  int32_t num_sms;          /* SMs the planner sizes the grid for; 0 = query the current device */
+  int32_t ctas_per_sm;      /* resident CTAs per SM; 0 = auto (2: one TMEM half each) */
+  int32_t max_prefill_ctas; /* prefill items allowed to run at once on one SM while decode work
+                               remains ([POD] §"가상 CTA와 SM별 균형": cap prefill so it does not
+                               crowd out decode); 0 = auto */
+  int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head); 0 = auto */
+  int32_t prefill_splits;   /* force this many KV splits per prefill (tile, head); 0 = auto */
+  int32_t instrument;       /* nonzero: record (SM, kind, start, end) per work item */
+  pod_attn_variant variant; /* launch variant, see above */
+} pod_attn_options;
+
+typedef struct pod_attn_plan_s* pod_attn_plan_t;
+
+/* Summary of a plan (what the planner decided). */
+typedef struct {
+  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, 128-row tile, q-head, kv-split) */
+  int32_t num_decode_items;   /* virtual decode CTAs: (seq, kv-head, kv-split) */
+  int32_t num_units;          /* outputs assembled from more than one split */
+  int32_t num_sms;            /* SM count the grid was sized for */
+  int32_t ctas_per_sm;
+  int32_t max_prefill_ctas;
+  int32_t grid_fused;         /* CTAs of the fused launch */
+  int32_t grid_prefill;       /* CTAs of the prefill-only launch (serial / streams) */
+  int32_t grid_decode;        /* CTAs of the decode-only launch (serial / streams) */
+  int32_t smem_bytes;         /* dynamic shared memory per CTA (one budget for both kinds) */
+  int32_t threads_per_cta;
+  int32_t item_words;         /* int32 words per work item in pod_attn_plan_items' output */
+  uint64_t workspace_bytes;   /* same as pod_attn_workspace_bytes */
+  double est_prefill_flops;   /* algorithmic FLOPs: 4*d*Hq per visible (query, key) pair */
+  double est_prefill_bytes;   /* algorithmic bytes: K/V once per kv-head, Q in, O out */
+  double est_decode_bytes;    /* algorithmic bytes: every cached K/V row once, q in, o out */
+  double est_decode_flops;
+} pod_attn_plan_info;
+
+/* Per-item record written when options.instrument is set ([POD] §"예측 가능한 지연시간과 진단":
+ * the runtime should expose the virtual-CTA mix, occupancy and tile choice). */
+typedef struct {
+  int32_t smid;      /* SM that ran the item */
+  int32_t kind;      /* 0 = prefill, 1 = decode */
+  int32_t item;      /* index within its kind's item list */
+  int32_t cta;       /* blockIdx.x of the CTA that ran it */
+  uint64_t t_start;  /* %globaltimer, ns */
+  uint64_t t_end;
+} pod_attn_item_record;
+
+/* Plan one hybrid batch on the host ([POD] §"가상 CTA와 SM별 균형": enumerate virtual prefill
+ * and decode CTAs, limit prefill splits, size the grid by SM; §"동시 실행만으로 부족한 이유":
+ * avoid wave-quantisation tails).
+ *   problem         : shapes (read only).
+ *   h_cu_seqlens_q  : host int32 [Np + 1] (read only, may be NULL when Np == 0).
+ *   h_kv_lens       : host int32 [Np + Nd] (read only, may be NULL when Np + Nd == 0).
+ *   options         : may be NULL (defaults).
+ *   out             : receives a new plan, owned by the caller until pod_attn_plan_destroy.
+ * Host only: it touches no device memory. With options->num_sms > 0 it calls no CUDA function
+ * except cudaEventCreate (whose failure is tolerated; the STREAMS variant then reports
+ * POD_ATTN_ERR_CUDA at run time).
+ * Errors: INVALID_ARG (nulls, kv_len < q_len, q_len < 1, decode kv_len < 1, kv_len beyond
+ * max_blocks_per_seq*16, cu_seqlens not starting at 0 or not non-decreasing, token total
+ * mismatch), UNSUPPORTED (head_dim, block size, group size), CUDA (num_sms == 0 and no device). */
+pod_attn_status pod_attn_plan(const pod_attn_problem* problem, const int32_t* h_cu_seqlens_q,
+                              const int32_t* h_kv_lens, const pod_attn_options* options,
+                              pod_attn_plan_t* out);
+
+/* Device workspace the plan needs, in bytes (0 for a NULL plan). Holds the work lists, the
+ * scheduling counters, split-KV partials and the optional instrumentation records. */
+size_t pod_attn_workspace_bytes(pod_attn_plan_t plan);
+
+/* Copy the plan's work lists into the workspace and zero its counters and status word, on
+ * `stream` (asynchronous; the plan must stay alive until the copy has run). Must be called
+ * once after pod_attn_plan and before the first pod_attn_run with this workspace; a workspace
+ * serves one plan at a time. Calling it again resets the device status.
+ *   workspace       : device pointer, 256-byte aligned, >= pod_attn_workspace_bytes(plan).
+ * Errors: INVALID_ARG (null plan/workspace), WORKSPACE (too small / misaligned), CUDA. */
+pod_attn_status pod_attn_upload(pod_attn_plan_t plan, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Launch the hybrid attention for the uploaded plan (asynchronous on `stream`).
+ *   q_prefill, o_prefill : device bf16, see layouts (may be NULL when Np == 0).
+ *   q_decode,  o_decode  : device bf16, see layouts (may be NULL when Nd == 0).
+ *   k_pool, v_pool       : device bf16 paged pools, 16-byte aligned.
+ *   d_block_tables       : device int32 [Np + Nd][max_blocks_per_seq].
+ *   d_cu_seqlens_q, d_kv_lens : device copies of the arrays given to pod_attn_plan (same
+ *                          values; the kernels read q offsets and kv lengths from them).
+ *   workspace            : the workspace passed to pod_attn_upload for this plan.
+ *   stream, stream2      : cudaStream_t values (NULL = legacy default stream); stream2 is
+ *                          used by the STREAMS variant only and may equal NULL otherwise.
+ * Inputs are read only; o_prefill / o_decode are overwritten entirely. Runs of the same
+ * workspace must not overlap in time. The counters reset themselves at the end of a run, so
+ * back-to-back runs need no further upload. Launch-time errors are returned here; errors the
+ * kernels detect (BAD_INDEX, TIMEOUT) land in the workspace status word, see
+ * pod_attn_last_device_status. */
+pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const void* q_decode,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* d_block_tables, const int32_t* d_cu_seqlens_q,
+                             const int32_t* d_kv_lens, void* o_prefill, void* o_decode,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* stream2);
+
+/* Synchronise `stream`, read and clear the device status word of `workspace`.
+ * Returns OK, BAD_INDEX, TIMEOUT, or CUDA if the synchronisation itself failed. After
+ * BAD_INDEX or TIMEOUT the outputs of that run are unspecified and the workspace must be
+ * re-uploaded before the next run. */
+pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspace, void* stream);
+
+/* Fill *info with the plan summary. Errors: INVALID_ARG. */
+pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info* info);
+
+/* Copy the host work lists: prefill items first, then decode items, then the unit table, each
+ * item info.item_words int32 words (see DESIGN of the item encoding in the planner source).
+ *   out   : host buffer of `capacity` int32 words.
+ *   count : receives the number of words written.
+ * Used to check the planner bit for bit. Errors: INVALID_ARG (null, capacity too small). */
+pod_attn_status pod_attn_plan_items(pod_attn_plan_t plan, int32_t* out, size_t capacity,
+                                    size_t* count);
+
+/* Copy the instrumentation records of the last run (synchronises `stream`).
+ *   out    : host array of `capacity` records; count receives the number written (one per
+ *            item, prefill items first). Errors: INVALID_ARG (instrumentation off), CUDA. */
+pod_attn_status pod_attn_read_records(pod_attn_plan_t plan, const void* workspace,
+                                      pod_attn_item_record* out, size_t capacity,
+                                      size_t* count, void* stream);
+
+/* Free the plan (NULL is ignored). */
+void pod_attn_plan_destroy(pod_attn_plan_t plan);
+
+/* Static English description of a status code. */
+const char* pod_attn_status_string(pod_attn_status status);
+
+/* Test hook for the bounded-wait failure path (no GPU fault involved): launches one CTA that
+ * waits on an mbarrier nobody arrives on, with a spin limit of `spin_limit` polls, and
+ * records POD_ATTN_ERR_TIMEOUT in the workspace status word when the limit runs out.
+ *   workspace : device pointer with at least 256 bytes.
+ * Read the outcome with pod_attn_last_device_status. Errors: INVALID_ARG, CUDA. */
+pod_attn_status pod_attn_selftest_timeout(void* workspace, int32_t spin_limit, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POD_ATTN_H_ */

@@ -1,0 +1,184 @@
+"""fp64 CPU oracle of hybrid prefill+decode attention — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of
+``bench.py`` may import this package. The product (``hybrid_prefill_decode_gb300``) never
+imports it, and this package imports nothing from the product.
+
+Two independent implementations live here:
+
+* ``oracle.c`` (compiled with gcc, OpenMP): gather through the block table, fp64 scores,
+  3-pass safe softmax, weighted sum — "Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
+  §"Attention에 적용하기", §"Safe softmax (3-pass, 수치 안정성 확보)", §"PagedAttention",
+  §"한 스텝에 여러 종류의 request 섞기"; split-KV partials and their exact merge —
+  "LLMSO - W4 - Optimization & Frameworks", §"FlashDecoding — decode 단계의 병렬성 확보".
+* ``bruteforce.py`` (NumPy): the full masked score matrix of each sequence, for tiny cases.
+
+Inputs are the bf16 tensors of a batch (passed as uint16 bit patterns); results are float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library next to it (plain gcc, -O2, OpenMP)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_int64
+            D = ctypes.c_double
+            lib.oracle_num_threads.restype = I
+            lib.oracle_attend_range.restype = I
+            lib.oracle_attend_range.argtypes = [P, P, L, L, I, I, I, I, P, P, L, D, P, P, P, P]
+            lib.oracle_merge.restype = None
+            lib.oracle_merge.argtypes = [I, P, P, P, I, P]
+            lib.oracle_attend_row.restype = I
+            lib.oracle_attend_row.argtypes = [P, P, L, I, I, I, I, P, P, L, D, P, P]
+            lib.oracle_rows.restype = I
+            lib.oracle_rows.argtypes = [I, I, I, I, I, I, L, I, D, P, P, P, P, P, P, P,
+                                        L, P, P, P, P]
+            lib.oracle_hybrid_attention.restype = I
+            lib.oracle_hybrid_attention.argtypes = [I, I, I, I, I, I, L, I, D, P, P, P, P,
+                                                    P, P, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the C oracle uses on this host."""
+    return int(_load().oracle_num_threads())
+
+
+def _u16(a) -> np.ndarray:
+    """bf16 tensor (torch) or uint16 array -> contiguous uint16 numpy array of the bit patterns."""
+    if isinstance(a, np.ndarray):
+        assert a.dtype == np.uint16
+        return np.ascontiguousarray(a)
+    import torch  # the generators hand out torch tensors; only their bits are used here
+    assert a.dtype == torch.bfloat16, a.dtype
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy()
+                                .view(np.uint16))
+
+
+def _i32(a) -> np.ndarray:
+    if isinstance(a, np.ndarray):
+        return np.ascontiguousarray(a, dtype=np.int32)
+    return np.ascontiguousarray(a.detach().cpu().numpy(), dtype=np.int32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class _Batch:
+    """The arrays of a hybrid batch in the form the C oracle reads."""
+
+    def __init__(self, b):
+        self.Hq, self.Hkv = int(b.num_q_heads), int(b.num_kv_heads)
+        self.D, self.BS = int(b.head_dim), int(b.block_size)
+        self.Np, self.Nd = int(b.num_prefill_seqs), int(b.num_decode_seqs)
+        self.scale = float(b.scale)
+        self.q_prefill = _u16(b.q_prefill)
+        self.q_decode = _u16(b.q_decode)
+        self.k_pool = _u16(b.k_pool)
+        self.v_pool = _u16(b.v_pool)
+        self.block_tables = _i32(b.block_tables)
+        self.cu = _i32(b.cu_seqlens_q)
+        self.kv_lens = _i32(b.kv_lens)
+        self.num_blocks = int(self.k_pool.shape[0])
+        self.maxb = int(self.block_tables.shape[1]) if self.block_tables.ndim == 2 else 0
+        self.tp = int(self.cu[-1]) if self.Np > 0 else 0
+
+    def common(self):
+        return (self.Hq, self.Hkv, self.D, self.BS, self.Np, self.Nd, self.num_blocks,
+                self.maxb, self.scale, _ptr(self.q_prefill), _ptr(self.q_decode),
+                _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.block_tables),
+                _ptr(self.cu), _ptr(self.kv_lens))
+
+
+def hybrid_attention(batch):
+    """All outputs of a hybrid batch: (o_prefill [Tp][Hq][D], o_decode [Nd][Hq][D]), float64.
+
+    ``batch`` is any object with the fields of ``hybrid_prefill_decode_gb300.workloads
+    .HybridBatch`` (shapes, bf16 tensors, int32 tables)."""
+    b = _Batch(batch)
+    o_p = np.zeros((b.tp, b.Hq, b.D), dtype=np.float64)
+    o_d = np.zeros((b.Nd, b.Hq, b.D), dtype=np.float64)
+    rc = _load().oracle_hybrid_attention(*b.common(), _ptr(o_p), _ptr(o_d))
+    if rc != 0:
+        raise ValueError(f"oracle_hybrid_attention failed with code {rc}")
+    return o_p, o_d
+
+
+def rows(batch, kinds, indices, heads) -> np.ndarray:
+    """Selected output rows [n][D] (float64): kind 0 = prefill token index, 1 = decode seq."""
+    b = _Batch(batch)
+    kinds = np.ascontiguousarray(kinds, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int64)
+    heads = np.ascontiguousarray(heads, dtype=np.int32)
+    n = int(kinds.shape[0])
+    out = np.zeros((n, b.D), dtype=np.float64)
+    rc = _load().oracle_rows(*b.common(), n, _ptr(kinds), _ptr(indices), _ptr(heads),
+                             _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_rows failed with code {rc}")
+    return out
+
+
+def attend_range(q_row, bt_row, j0, j1, kv_head, batch_like):
+    """Split-KV partial state (m, l, o_unnormalised[D]) of one query over keys [j0, j1)."""
+    lib = _load()
+    q = _u16(q_row)
+    bt = _i32(bt_row)
+    kp, vp = _u16(batch_like.k_pool), _u16(batch_like.v_pool)
+    D = int(q.shape[-1])
+    o = np.zeros(D, dtype=np.float64)
+    x = np.zeros(max(1, j1 - j0), dtype=np.float64)
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    rc = lib.oracle_attend_range(_ptr(q), _ptr(bt), j0, j1, kv_head,
+                                 int(batch_like.num_kv_heads), D, int(batch_like.block_size),
+                                 _ptr(kp), _ptr(vp), int(kp.shape[0]),
+                                 float(batch_like.scale), ctypes.byref(m), ctypes.byref(l),
+                                 _ptr(o), _ptr(x))
+    if rc != 0:
+        raise ValueError(f"oracle_attend_range failed with code {rc}")
+    return m.value, l.value, o
+
+
+def merge(ms, ls, os_) -> np.ndarray:
+    """Exact merge of split partials (m_i, l_i, o_i) into the normalised output row."""
+    ms = np.ascontiguousarray(ms, dtype=np.float64)
+    ls = np.ascontiguousarray(ls, dtype=np.float64)
+    os_ = np.ascontiguousarray(os_, dtype=np.float64)
+    n, D = os_.shape
+    out = np.zeros(D, dtype=np.float64)
+    _load().oracle_merge(n, _ptr(ms), _ptr(ls), _ptr(os_), D, _ptr(out))
+    return out

@@ -1,0 +1,402 @@
+"""Benchmark of hybrid prefill+decode attention on one GB300 (or N independent replicas).
+
+One step = one pass of the whole hot path over one hybrid batch: the fused persistent kernel
+computes the chunked-prefill attention and every decode attention of the batch (one attention
+layer of one serving iteration). Default workload: the Llama-2-7B attention shape (32 query /
+32 KV heads, head_dim 128, one 512-token chunk after a 3584-token prefix, 32 decodes with
+contexts uniform in [2048, 4096], paged block 16), synthetic N(0,1) bf16 inputs.
+
+Timing: CUDA events on the launching stream around each step; a 256 MiB buffer is written
+between steps (outside the events) so every step starts with a cold L2. The headline value is
+the fused variant's mean us/iter; the serial (two launches back to back) and two-stream variants
+run on the same buffers for the speedup figures. `e2e` repeats the fused step through the
+public C ABI from pinned host buffers (plan + upload + run + copies in the timed region).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "hybrid prefill+decode attention µs/iter, % of roofline, speedup vs serial"
+UNIT = "us/iter"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]),
+                "measured")
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _workload_name(cfg: int, batch) -> str:
+    from hybrid_prefill_decode_gb300 import workloads as W
+    return W.CONFIG_NAMES[cfg] + f", head_dim 128, paged block 16, bf16"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(parts)
+            except Exception:
+                pass
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def cpu_baseline(batch, target_s: float = 12.0):
+    """The fp64 oracle as it stands, on this host's cores, on a bounded sample of the workload's
+    query rows (every decode row and every k-th prefill row, all heads), scaled to one iteration
+    by the number of visible (query, key) pairs."""
+    import numpy as np
+    import oracle
+    Hq = batch.num_q_heads
+    cu = batch.host_cu_seqlens
+    pre_rows = []                         # (token index, visible keys)
+    for s, (q, L) in enumerate(zip(batch.q_lens, batch.prefill_kv_lens)):
+        for i in range(q):
+            pre_rows.append((cu[s] + i, L - q + i + 1))
+    dec_rows = [(d, L) for d, L in enumerate(batch.decode_kv_lens)]
+    total_pairs = Hq * (sum(v for _, v in pre_rows) + sum(v for _, v in dec_rows))
+    # calibrate on the decode rows, then pick the prefill stride to fill the time budget
+    t0 = time.perf_counter()
+    kinds = [1] * (len(dec_rows) * Hq)
+    idx = [d for d, _ in dec_rows for _ in range(Hq)]
+    heads = list(range(Hq)) * len(dec_rows)
+    if kinds:
+        oracle.rows(batch, kinds, idx, heads)
+    t_dec = time.perf_counter() - t0
+    dec_pairs = Hq * sum(v for _, v in dec_rows)
+    rate = dec_pairs / max(t_dec, 1e-6)   # pairs per second
+    stride = 1
+    if pre_rows:
+        want = max(1.0, target_s - t_dec) * rate
+        pre_pairs_all = Hq * sum(v for _, v in pre_rows)
+        stride = max(1, int(math.ceil(pre_pairs_all / want)))
+    sample = pre_rows[::stride]
+    t1 = time.perf_counter()
+    if sample:
+        oracle.rows(batch, [0] * (len(sample) * Hq), [r for r, _ in sample for _ in range(Hq)],
+                    list(range(Hq)) * len(sample))
+    t_pre = time.perf_counter() - t1
+    samp_pairs = dec_pairs + Hq * sum(v for _, v in sample)
+    elapsed = t_dec + t_pre
+    us_per_iter = elapsed * 1e6 * total_pairs / max(samp_pairs, 1)
+    return {"value": us_per_iter, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"all {len(dec_rows)} decode rows and every {stride}-th of "
+                       f"{len(pre_rows)} prefill rows, all {Hq} heads "
+                       f"({samp_pairs / total_pairs:.1%} of the iteration's visible pairs, "
+                       f"{elapsed:.1f} s), scaled by visible (query, key) pairs"),
+            "seconds": elapsed}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 CPU oracle timed on this host (rank 0 only)."""
+    if rank != 0:
+        return
+    from hybrid_prefill_decode_gb300 import workloads as W
+    batch = W.config(args.config, device="cpu")
+    vals = []
+    for k in range(args.warmup + args.steps):
+        r = cpu_baseline(batch, target_s=args.ref_step_s)
+        if k >= args.warmup:
+            vals.append(r)
+    value = statistics.mean(v["value"] for v in vals)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": _workload_name(args.config, batch), "config_index": args.config},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
+                            "kind": "oracle", "sample": vals[0]["sample"]},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", default=None, help="profile mode: run only this variant, no extras")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    assert args.warmup >= 3 or args.only, "at least 3 warm-up steps"
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+
+    from hybrid_prefill_decode_gb300 import binding as B
+    from hybrid_prefill_decode_gb300 import build as build_mod
+    from hybrid_prefill_decode_gb300 import roofline as R
+    from hybrid_prefill_decode_gb300 import workloads as W
+    build_mod.build()
+    B.load()
+
+    dev = torch.device(f"cuda:{local}")
+    batch = W.config(args.config, device=dev)
+    work = R.batch_work(batch.num_q_heads, batch.num_kv_heads, batch.q_lens,
+                        batch.prefill_kv_lens, batch.decode_kv_lens)
+    hbm, tf_burst, tf_sust, peak_src = _peaks()
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(device=dev)
+    o_p = torch.empty_like(batch.q_prefill)
+    o_d = torch.empty_like(batch.q_decode)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    variants = [args.only] if args.only else ["fused", "serial", "streams"]
+    plans = {}
+    for v in variants:
+        plan = B.Plan.for_batch(batch, variant=v)
+        ws = plan.alloc_workspace(dev)
+        plan.upload(ws, stream)
+        plans[v] = (plan, ws)
+
+    def step(v):
+        plan, ws = plans[v]
+        B.run_batch(plan, batch, ws, o_p, o_d, stream=stream, stream2=side)
+
+    if args.only:                    # profiling mode: warm-up + K plain steps, nothing else
+        for _ in range(args.warmup + args.steps):
+            step(args.only)
+        torch.cuda.synchronize()
+        st = plans[args.only][0].device_status(plans[args.only][1])
+        print(json.dumps({"profile_run": args.only, "status": st}))
+        return
+
+    def timed(v, k, sampler=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for a, b in evs:
+            flush.fill_(1)                       # cold L2 for every step (outside the events)
+            a.record(stream)
+            step(v)
+            b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if dist:
+            dist.barrier()
+        return [a.elapsed_time(b) * 1e3 for a, b in evs], wall
+
+    for v in variants:
+        for _ in range(args.warmup):
+            step(v)
+    torch.cuda.synchronize()
+    for v in variants:
+        assert plans[v][0].device_status(plans[v][1]) == B.OK, v
+
+    results = {}
+    clocks = None
+    for v in variants:
+        if v == "fused":
+            with ClockSampler(local) as cs:
+                results[v] = timed(v, args.steps)
+            clocks = cs.summary()
+        else:
+            results[v] = timed(v, args.steps)
+    # outputs of the timed runs agree bit for bit across variants (same items, same arithmetic)
+    for v in variants:
+        assert plans[v][0].device_status(plans[v][1]) == B.OK, v
+
+    def agg(us_list):
+        mean = statistics.mean(us_list)
+        if dist:
+            t = torch.tensor([mean], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            mean = float(t.item())
+        return mean
+
+    us = {v: agg(results[v][0]) for v in variants}
+    med = {v: statistics.median(results[v][0]) for v in variants}
+
+    # ---- e2e through the public C ABI from pinned host buffers --------------------------------
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(batch, k).cpu().pin_memory() for k in
+                ("q_prefill", "q_decode", "block_tables", "cu_seqlens_q", "kv_lens")}
+        dq_p, dq_d = torch.empty_like(batch.q_prefill), torch.empty_like(batch.q_decode)
+        dbt, dcu, dkv = (torch.empty_like(batch.block_tables), torch.empty_like(batch.cu_seqlens_q),
+                         torch.empty_like(batch.kv_lens))
+        ho_p = torch.empty(o_p.shape, dtype=o_p.dtype, pin_memory=True)
+        ho_d = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
+        ws = plans["fused"][1]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = ho_p.numel() * ho_p.element_size() + ho_d.numel() * ho_d.element_size()
+
+        def e2e_step():
+            for dst, key in ((dq_p, "q_prefill"), (dq_d, "q_decode"), (dbt, "block_tables"),
+                             (dcu, "cu_seqlens_q"), (dkv, "kv_lens")):
+                dst.copy_(host[key], non_blocking=True)
+            plan = B.Plan.for_batch(batch, variant="fused")   # host planning of this batch
+            plan.upload(ws, stream)
+            plan.run(dq_p, dq_d, batch.k_pool, batch.v_pool, dbt, dcu, dkv, o_p, o_d, ws,
+                     stream=stream)
+            ho_p.copy_(o_p, non_blocking=True)
+            ho_d.copy_(o_d, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            return plan
+
+        for _ in range(args.warmup):
+            e2e_step()
+        ts = []
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            ts.append((time.perf_counter() - t0) * 1e6)
+        e2e = {"value": agg(ts), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    t_fused = us["fused"] * 1e-6
+    tstar = work.t_star(hbm, tf_burst)
+    bound = work.bound(hbm, tf_burst)
+    if bound == "hbm":
+        achieved = work.bytes / t_fused / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src}
+    else:
+        achieved = work.prefill_flops / t_fused / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": achieved / tf_burst, "traffic": None,
+                "peak_source": f"{peak_src} bf16 burst"}
+    traffic = _traffic_from_profiles(args.config)
+    if traffic is not None:
+        roof["traffic"] = traffic
+    out = {
+        "metric": METRIC, "value": us["fused"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us["fused"] / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _workload_name(args.config, batch), "config_index": args.config,
+                   "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "median_us": med["fused"],
+        "hybrid_roofline": {"t_star_us": tstar * 1e6, "frac_of_t_star": tstar / t_fused,
+                            "bytes": work.bytes, "prefill_flops": work.prefill_flops,
+                            "hbm_gbs": hbm, "bf16_tflops": tf_burst,
+                            "frac_vs_8tbs_spec": (work.bytes / 8000e9) / t_fused},
+        "tbs": work.bytes / t_fused / 1e12,
+        "prefill_tflops": work.prefill_flops / t_fused / 1e12,
+        "roofline": roof,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if "serial" in us:
+        out["serial_us"] = us["serial"]
+        out["speedup_vs_serial"] = us["serial"] / us["fused"]
+    if "streams" in us:
+        out["streams_us"] = us["streams"]
+        out["speedup_vs_streams"] = us["streams"] / us["fused"]
+    if e2e:
+        out["e2e"] = e2e
+    if not args.no_cpu and world == 1:
+        cpu_batch = batch.to("cpu")
+        out["cpu_baseline"] = {k: v for k, v in cpu_baseline(cpu_batch).items() if k != "seconds"}
+    print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _traffic_from_profiles(cfg):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if present."""
+    path = os.path.join(ROOT, "profiles", f"traffic_config{cfg}.json")
+    try:
+        d = json.load(open(path))
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,221 @@
+// planner.cpp — host planner of the hybrid prefill+decode launch.
+//
+// "POD-Attention" digest (Silicon & Systems), §"가상 CTA와 SM별 균형": a normal grid of CTAs
+// is mapped onto virtual prefill and decode CTAs; the number of CTAs one prefill chunk may
+// generate is limited so decode work is not pushed out. §"동시 실행만으로 부족한 이유": a CTA
+// count just above a multiple of what the SMs hold at once costs a whole extra wave.
+//
+// This file turns one hybrid batch into two work lists (virtual CTAs):
+//   prefill item = (chunk s, 128-row query tile t, query head h, KV split k)
+//   decode item  = (sequence d, kv-head g, KV split k)   — one item serves all G query heads
+//                  of the kv-head (GQA grouping, "LLMSO - W4", §"KV 헤드 줄이기")
+// and sizes the persistent grid: num_sms x ctas_per_sm CTAs that pull items from the two lists.
+//
+// Split planning. Every item gets a cost (decode: 8 per 16-row K/V block, i.e. its bytes in
+// KiB; prefill: 28 per 128x64 tile, its tensor-core time expressed in the same byte-time units
+// at a 6.8 TB/s : 1 PFLOP/s balance). With W the total cost and S the CTA slots, an output whose
+// cost exceeds W / (4 S) is split along the keys ("LLMSO - W4", §"FlashDecoding — decode 단계의
+// 병렬성 확보") into at most 64 (decode) or 8 (prefill) parts of at least 12 blocks / 8 tiles, so
+// no single item can leave a long tail after the others finish. Items are then ordered longest
+// first. All arithmetic is integer, so the plan is reproducible bit for bit.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "pod_internal.h"
+
+namespace pod {
+namespace {
+
+constexpr int64_t kDecodeBlockCost = 8;   // 16 rows x (K + V) x 128 x bf16 = 8 KiB
+constexpr int64_t kPrefillTileCost = 28;  // 4*128*64*128 FLOPs at the byte-time balance
+constexpr int kMinDecodeBlocksPerSplit = 12;
+constexpr int kMaxDecodeSplits = 64;
+constexpr int kMinPrefillTilesPerSplit = 8;
+constexpr int kMaxPrefillSplits = 8;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Pending {
+  int64_t cost;
+  int32_t w[kItemWords];
+};
+
+}  // namespace
+
+pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, const int32_t* kv,
+                           const pod_attn_options& opt, int num_sms, pod_attn_plan_s* plan) {
+  const int Hq = prob.num_q_heads, Hkv = prob.num_kv_heads;
+  const int Np = prob.num_prefill_seqs, Nd = prob.num_decode_seqs;
+  if (Hq < 1 || Hkv < 1 || Np < 0 || Nd < 0 || prob.num_prefill_tokens < 0 ||
+      prob.num_blocks < 0 || prob.max_blocks_per_seq < 0 || !std::isfinite(prob.scale))
+    return POD_ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return POD_ATTN_ERR_INVALID_ARG;
+  if (prob.head_dim != kHeadDim || prob.block_size != kBlockSize) return POD_ATTN_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G > kMaxGroup) return POD_ATTN_ERR_UNSUPPORTED;
+  if ((Np == 0) != (prob.num_prefill_tokens == 0)) return POD_ATTN_ERR_INVALID_ARG;
+  if (Np > 0 && cu == nullptr) return POD_ATTN_ERR_INVALID_ARG;
+  if (Np + Nd > 0 && (kv == nullptr || prob.num_blocks < 1 || prob.max_blocks_per_seq < 1))
+    return POD_ATTN_ERR_INVALID_ARG;
+  if (num_sms < 1) return POD_ATTN_ERR_INVALID_ARG;
+  // TMA row coordinates of the pools are int32.
+  if ((int64_t)prob.num_blocks * Hkv * kBlockSize >= (int64_t(1) << 31))
+    return POD_ATTN_ERR_UNSUPPORTED;
+  const int64_t max_rows = (int64_t)prob.max_blocks_per_seq * kBlockSize;
+  if (Np > 0) {
+    if (cu[0] != 0 || cu[Np] != prob.num_prefill_tokens) return POD_ATTN_ERR_INVALID_ARG;
+    for (int s = 0; s < Np; ++s) {
+      int64_t q = (int64_t)cu[s + 1] - cu[s];
+      if (q < 1 || kv[s] < q || kv[s] > max_rows) return POD_ATTN_ERR_INVALID_ARG;
+    }
+  }
+  for (int d = 0; d < Nd; ++d)
+    if (kv[Np + d] < 1 || kv[Np + d] > max_rows) return POD_ATTN_ERR_INVALID_ARG;
+
+  plan->prob = prob;
+  plan->opt = opt;
+  plan->group = G;
+  plan->num_sms = num_sms;
+  plan->ctas_per_sm = opt.ctas_per_sm > 0 ? std::min(opt.ctas_per_sm, 2) : 2;
+  plan->cu.assign(cu ? cu : nullptr, cu ? cu + Np + 1 : nullptr);
+  plan->kv.assign(kv ? kv : nullptr, kv ? kv + Np + Nd : nullptr);
+  const int64_t slots = (int64_t)num_sms * plan->ctas_per_sm;
+
+  // ---- enumerate outputs (before splitting) and their costs --------------------------------
+  struct PUnit { int s, t, h; int64_t kend; int64_t ntiles; };
+  struct DUnit { int d, g; int64_t L; int64_t nblk; };
+  std::vector<PUnit> pu;
+  std::vector<DUnit> du;
+  int64_t total = 0;
+  double pf = 0, pb = 0, db = 0, df = 0;
+  const double row_bytes = 4.0 * Hkv * kHeadDim;  // K + V, bf16
+  for (int s = 0; s < Np; ++s) {
+    const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
+    pf += 4.0 * kHeadDim * Hq * (double)(q * P + q * (q + 1) / 2);
+    pb += (double)L * row_bytes + 4.0 * q * Hq * kHeadDim;
+    for (int64_t t = 0; t < ceil_div(q, kTileM); ++t) {
+      const int64_t kend = P + std::min(q, (t + 1) * kTileM);
+      const int64_t nt = ceil_div(kend, kTileN);
+      for (int h = 0; h < Hq; ++h) {
+        pu.push_back({s, (int)t, h, kend, nt});
+        total += nt * kPrefillTileCost;
+      }
+    }
+  }
+  for (int d = 0; d < Nd; ++d) {
+    const int64_t L = kv[Np + d];
+    db += (double)L * row_bytes + 4.0 * Hq * kHeadDim;
+    df += 4.0 * kHeadDim * Hq * (double)L;
+    for (int g = 0; g < Hkv; ++g) {
+      du.push_back({d, g, L, ceil_div(L, kBlockSize)});
+      total += ceil_div(L, kBlockSize) * kDecodeBlockCost;
+    }
+  }
+  plan->est_prefill_flops = pf;
+  plan->est_prefill_bytes = pb;
+  plan->est_decode_bytes = db;
+  plan->est_decode_flops = df;
+  const int64_t target = std::max<int64_t>(1, total / (slots * 4));
+
+  // ---- split and emit ----------------------------------------------------------------------
+  std::vector<Pending> lp, ld;
+  plan->units.clear();
+  int p_slots = 0, d_slots = 0;
+  auto add_unit = [&](int nsplit, int kind) {
+    int u = (int)(plan->units.size() / kUnitWords);
+    int first = kind == 0 ? p_slots : d_slots;
+    (kind == 0 ? p_slots : d_slots) += nsplit;
+    plan->units.insert(plan->units.end(), {nsplit, first, kind, 0});
+    return u;
+  };
+  for (const PUnit& x : pu) {
+    int64_t ns;
+    if (opt.prefill_splits > 0) {
+      ns = opt.prefill_splits;
+    } else {
+      ns = ceil_div(x.ntiles * kPrefillTileCost, target);
+      ns = std::min<int64_t>(ns, std::max<int64_t>(1, x.ntiles / kMinPrefillTilesPerSplit));
+      ns = std::min<int64_t>(ns, kMaxPrefillSplits);
+    }
+    ns = std::max<int64_t>(1, std::min(ns, x.ntiles));
+    const int64_t chunk = ceil_div(x.ntiles, ns);
+    ns = ceil_div(x.ntiles, chunk);
+    const int u = ns > 1 ? add_unit((int)ns, 0) : -1;
+    for (int64_t k = 0; k < ns; ++k) {
+      const int64_t t0 = k * chunk, t1 = std::min(x.ntiles, (k + 1) * chunk);
+      Pending it{(t1 - t0) * kPrefillTileCost,
+                 {0, x.s, x.t, x.h, (int32_t)(t0 * kTileN),
+                  (int32_t)std::min(x.kend, t1 * kTileN), u, (int32_t)k}};
+      lp.push_back(it);
+    }
+  }
+  for (const DUnit& x : du) {
+    int64_t ns;
+    if (opt.decode_splits > 0) {
+      ns = opt.decode_splits;
+    } else {
+      ns = ceil_div(x.nblk * kDecodeBlockCost, target);
+      ns = std::min<int64_t>(ns, std::max<int64_t>(1, x.nblk / kMinDecodeBlocksPerSplit));
+      ns = std::min<int64_t>(ns, kMaxDecodeSplits);
+    }
+    ns = std::max<int64_t>(1, std::min(ns, x.nblk));
+    const int64_t chunk = ceil_div(x.nblk, ns);
+    ns = ceil_div(x.nblk, chunk);
+    const int u = ns > 1 ? add_unit((int)ns, 1) : -1;
+    for (int64_t k = 0; k < ns; ++k) {
+      const int64_t b0 = k * chunk, b1 = std::min(x.nblk, (k + 1) * chunk);
+      Pending it{(b1 - b0) * kDecodeBlockCost,
+                 {1, x.d, x.g, 0, (int32_t)(b0 * kBlockSize),
+                  (int32_t)std::min(x.L, b1 * kBlockSize), u, (int32_t)k}};
+      ld.push_back(it);
+    }
+  }
+  // longest first (stable: ties keep enumeration order)
+  auto by_cost = [](const Pending& a, const Pending& b) { return a.cost > b.cost; };
+  std::stable_sort(lp.begin(), lp.end(), by_cost);
+  std::stable_sort(ld.begin(), ld.end(), by_cost);
+  plan->items_p.clear();
+  plan->items_d.clear();
+  for (auto& it : lp) plan->items_p.insert(plan->items_p.end(), it.w, it.w + kItemWords);
+  for (auto& it : ld) plan->items_d.insert(plan->items_d.end(), it.w, it.w + kItemWords);
+  plan->num_p_slots = p_slots;
+  plan->num_d_slots = d_slots;
+
+  const int n_p = (int)lp.size(), n_d = (int)ld.size();
+  int cap = opt.max_prefill_ctas > 0 ? opt.max_prefill_ctas : (n_p > 0 && n_d > 0 ? 1 : 2);
+  plan->max_prefill_per_sm = std::max(1, std::min(cap, plan->ctas_per_sm));
+  plan->grid_fused = (int)std::min<int64_t>(slots, n_p + n_d);
+  plan->grid_prefill = (int)std::min<int64_t>(slots, n_p);
+  plan->grid_decode = (int)std::min<int64_t>(slots, n_d);
+
+  // ---- workspace layout --------------------------------------------------------------------
+  WorkspaceLayout& w = plan->ws;
+  size_t off = 0;
+  w.status = off;
+  off += 256;
+  w.counters = off;
+  w.counter_block_words = kCounterHeader + (size_t)num_sms;
+  off = align256(off + 3 * w.counter_block_words * 4);
+  w.arrive = off;
+  off = align256(off + plan->units.size() / kUnitWords * 4);
+  w.zero_bytes = off;
+  w.items_p = off;
+  off = align256(off + plan->items_p.size() * 4);
+  w.items_d = off;
+  off = align256(off + plan->items_d.size() * 4);
+  w.units = off;
+  off = align256(off + plan->units.size() * 4);
+  w.partial_p = off;
+  off = align256(off + (size_t)p_slots * kPrefillSlotFloats * 4);
+  w.partial_d = off;
+  off = align256(off + (size_t)d_slots * decode_slot_floats(G) * 4);
+  w.records = off;
+  if (opt.instrument) off = align256(off + (size_t)(n_p + n_d) * sizeof(pod_attn_item_record));
+  w.total = off;
+  return POD_ATTN_OK;
+}
+
+}  // namespace pod

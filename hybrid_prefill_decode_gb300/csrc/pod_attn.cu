@@ -1,0 +1,1171 @@
+// pod_attn.cu — GB300 (sm_103a) kernels and C ABI of hybrid prefill+decode attention.
+//
+// One persistent kernel runs two kinds of virtual CTAs ("POD-Attention" digest, Silicon &
+// Systems, §"동시 실행만으로 부족한 이유" and §"가상 CTA와 SM별 균형"):
+//
+//  * prefill item — 128 query rows of one chunk and one query head against a range of keys:
+//    S = Q·Kᵀ and O += P·V on the tcgen05 tensor cores with S and O in TMEM, Q/K/V staged by TMA
+//    through the paged block table, causal mask and online softmax (running max m and sum l,
+//    rescale by 2^(m_old - m_new); "Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
+//    §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를 줄이는 방향").
+//    Warp 0 issues TMA, warp 1 issues MMAs, warps 2-5 (one per TMEM lane quarter) do the softmax
+//    with one query row per thread.
+//  * decode item — one sequence, one kv-head with its G query heads, a range of 16-row paged
+//    blocks: each warp streams its blocks into a private two-slot shared-memory ring with 4 KiB
+//    bulk copies, holds q in registers (4 dims per lane), reduces q·k across the warp with
+//    shuffles, and keeps an online softmax per head ("LLMSO - W4", §"FlashDecoding — decode 단계의
+//    병렬성 확보", §"KV 헤드 줄이기").
+//
+// Each hardware CTA reads %smid and a per-SM counter of running prefill items, and takes the
+// next prefill ticket while its SM is under the prefill cap, else the next decode ticket, so both
+// kinds share every SM (§"가상 CTA와 SM별 균형"). Outputs split along the keys are merged exactly
+// by log-sum-exp by whichever split finishes last (no CTA ever waits for another CTA, so the two
+// kinds cannot deadlock; §"가상 CTA와 SM별 균형": exact synchronisation where partials meet).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "pod_internal.h"
+#include "ptx.cuh"
+
+namespace pod {
+
+using namespace ptx;
+
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: no healthy wait comes close
+
+struct Params {
+  const uint16_t* q_prefill;
+  const uint16_t* q_decode;
+  const uint16_t* k_pool;
+  const uint16_t* v_pool;
+  const int32_t* block_tables;
+  const int32_t* cu_seqlens;
+  const int32_t* kv_lens;
+  uint16_t* o_prefill;
+  uint16_t* o_decode;
+  const int32_t* items_p;
+  const int32_t* items_d;
+  const int32_t* units;
+  float* partial_p;
+  float* partial_d;
+  int32_t* counters;  // this launch mode's counter block
+  int32_t* arrive;
+  int32_t* status;    // [0] status word, [1] unused
+  pod_attn_item_record* records;
+  int32_t n_items_p, n_items_d;
+  int32_t Hq, Hkv, G, Np, Nd, num_blocks, maxb;
+  int32_t pool_rows;  // num_blocks * Hkv * 16: first row past the pools (TMA fills zeros)
+  int32_t num_sms;
+  int32_t max_prefill_per_sm;
+  int32_t mode;
+  float scale_log2;   // scale * log2(e): scores are kept in base-2 units
+  uint64_t timeout_ns;
+};
+
+struct SmemCtl {
+  uint64_t q_full;
+  uint64_t kv_full[kKvStages];
+  uint64_t kv_empty[kKvStages];
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_done;
+  uint64_t dslot[kWarps][kDecodeSlots];
+  uint32_t tmem_base;
+  int abort;
+  int item_kind;
+  int item_idx;
+  int merge_last;
+};
+static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
+
+// Pipeline positions; each role advances the fields it owns, across items.
+struct PipeState {
+  uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, o_cnt = 0;
+  uint32_t dphase = 0;  // decode ring: one parity bit per slot
+};
+
+constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, 0, 0);     // S = Q Kᵀ, both K-major
+constexpr uint32_t kIdescPV = idesc_bf16(kTileM, kHeadDim, 0, 1);  // O += P V, V is N-major
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  return static_cast<uint16_t>(pack_bf16x2(f, 0.f) & 0xFFFFu);
+}
+
+// ============================================================================ prefill item
+__device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
+                             const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
+                             SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = it[1], t = it[2], h = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
+  const int g = h / p.G;
+  const int q0 = p.cu_seqlens[s];
+  const int qlen = p.cu_seqlens[s + 1] - q0;
+  const int L = p.kv_lens[s];
+  const int P = L - qlen;  // cached prefix rows before this chunk
+  const int ntiles = (ke - kb + kTileN - 1) / kTileN;
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sKV = sQ + kSmemQ;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
+      const uint32_t qbar = smem_u32(&ctl->q_full);
+      mbar_arrive_expect_tx(qbar, kSmemQ);
+      tma_load_3d(sQ, tmq, qbar, 0, h, q0 + t * kTileM);
+      tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h, q0 + t * kTileM);
+      for (int j = 0; j < ntiles; ++j) {
+        const int stage = ps.kv_cnt & 1;
+        const uint32_t ph = (ps.kv_cnt >> 1) & 1;
+        if (!mbar_wait(smem_u32(&ctl->kv_empty[stage]), ph ^ 1, wc)) break;
+        const uint32_t full = smem_u32(&ctl->kv_full[stage]);
+        mbar_arrive_expect_tx(full, kSmemStage);
+        const uint32_t sK = sKV + stage * kSmemStage, sV = sK + kSmemKTile;
+        for (int b = 0; b < kTileN / kBlockSize; ++b) {
+          const int key0 = kb + j * kTileN + b * kBlockSize;
+          int y = p.pool_rows;  // past the pool: the copy lands as zeros
+          if (key0 < ke) {
+            int phys = bt_row[key0 >> 4];
+            if (phys < 0 || phys >= p.num_blocks) {
+              record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+              phys = 0;
+            }
+            y = (phys * p.Hkv + g) * kBlockSize;
+          }
+          tma_load_2d(sK + b * 2048, tmk, full, 0, y);
+          tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y);
+          tma_load_2d(sV + b * 2048, tmv, full, 0, y);
+          tma_load_2d(sV + 8192 + b * 2048, tmv, full, 64, y);
+        }
+        ps.kv_cnt++;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t tmem = ctl->tmem_base;
+    bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc);
+    ps.q_cnt++;
+    tc_fence_after();
+    int prev_stage = 0;
+    uint32_t prev_s = 0;
+    auto issue_pv = [&](int stage, uint32_t scnt, bool first) -> bool {
+      const uint32_t sb = scnt & 1;
+      if (!mbar_wait(smem_u32(&ctl->p_ready[sb]), (scnt >> 1) & 1, wc)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sV = sKV + stage * kSmemStage + kSmemKTile;
+        const uint32_t aP = tmem + kTmemS0 + sb * kTileN;
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          // V tile is N-major: 64-column halves 8 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
+          const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
+          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(smem_u32(&ctl->o_done));
+        umma_commit(smem_u32(&ctl->kv_empty[stage]));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int stage = ps.kv_cnt & 1;
+      const uint32_t ph = (ps.kv_cnt >> 1) & 1;
+      if (!mbar_wait(smem_u32(&ctl->kv_full[stage]), ph, wc)) {
+        ok = false;
+        break;
+      }
+      const int tile0 = kb + j * kTileN;
+      if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
+        // Rows past the sequence end inside its last block may hold anything (even NaN); P is
+        // zero there but 0 * NaN is not, so clear those V rows before the PV product.
+        const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
+        uint8_t* vbase = smem + kSmemQ + stage * kSmemStage + kSmemKTile;
+        for (int c = lane; c < (r1 - r0) * 16; c += 32) {
+          const int r = r0 + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
+          *reinterpret_cast<uint4*>(vbase + half * 8192 + r * 128 + q16 * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      const uint32_t sb = ps.s_cnt & 1;
+      if (lane == 0) {
+        const uint32_t sK = sKV + stage * kSmemStage;
+        const uint32_t dS = tmem + kTmemS0 + sb * kTileN;
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sQ + half * (kSmemQ / 2) + koff, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + half * (kSmemKTile / 2) + koff, 16, 1024);
+          umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&ctl->s_full[sb]));
+      }
+      __syncwarp();
+      if (j > 0 && !issue_pv(prev_stage, prev_s, j == 1)) {
+        ok = false;
+        break;
+      }
+      prev_stage = stage;
+      prev_s = ps.s_cnt;
+      ps.kv_cnt++;
+      ps.s_cnt++;
+    }
+    if (ok && ntiles > 0) issue_pv(prev_stage, prev_s, ntiles == 1);
+  } else {
+    // ------------------------------------------------------------------ softmax (1 row/thread)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int qi = t * kTileM + row;  // local index of this thread's query in the chunk
+    const bool valid = qi < qlen;
+    const int limit = min(P + qi + 1, ke);  // keys [kb, limit) are visible to this row
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const uint32_t sb = ps.s_cnt & 1;
+      if (!mbar_wait(smem_u32(&ctl->s_full[sb]), (ps.s_cnt >> 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32(trow + kTmemS0 + sb * kTileN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(trow + kTmemS0 + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld_wait();
+      const int nvis = limit - (kb + j * kTileN);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float x = c < nvis ? u2f(sr[c]) * p.scale_log2 : -INFINITY;
+        sr[c] = f2u(x);
+        mt = fmaxf(mt, x);
+      }
+      // Lazy rescale: keep the old reference max while the new scores exceed it by at most
+      // 2^8; exponents stay bounded and O, l remain consistent with the reference max.
+      const float m_new = fmaxf(m, mt);
+      const bool resc = m_new > m + 8.f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2(m - m_new);
+        m = m_new;
+      }
+      const float mref = m == -INFINITY ? 0.f : m;
+      float rs = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(u2f(sr[2 * c]) - mref), p1 = ex2(u2f(sr[2 * c + 1]) - mref);
+        rs += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + rs;
+      if (j > 0) {
+        // O holds PV of the previous tile once that MMA is done; rescale it if any row needs.
+        if (!mbar_wait(smem_u32(&ctl->o_done), ps.o_cnt & 1, wc)) {
+          ok = false;
+          break;
+        }
+        ps.o_cnt++;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(trow + kTmemO + ch * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+            tmem_st32(trow + kTmemO + ch * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      tmem_st32(trow + kTmemS0 + sb * kTileN, pk);  // P (bf16 pairs) over S's first 32 columns
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl->p_ready[sb]));
+      ps.s_cnt++;
+    }
+    if (ok && ntiles > 0) {
+      ok = mbar_wait(smem_u32(&ctl->o_done), ps.o_cnt & 1, wc);
+      ps.o_cnt++;
+      tc_fence_after();
+    }
+    // ------------------------------------------------------------------ epilogue
+    if (ok) {
+      if (unit < 0) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim;
+#pragma unroll 1
+        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(trow + kTmemO + ch * 32, o);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      } else {
+        const int nsplit = p.units[unit * kUnitWords + 0];
+        const int slot0 = p.units[unit * kUnitWords + 1];
+        float* slot = p.partial_p + (size_t)(slot0 + split) * kPrefillSlotFloats;
+#pragma unroll 1
+        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(trow + kTmemO + ch * 32, o);
+          tmem_ld_wait();
+          float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + ch * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(u2f(o[4 * i]), u2f(o[4 * i + 1]), u2f(o[4 * i + 2]), u2f(o[4 * i + 3]));
+        }
+        slot[kTileM * kHeadDim + row] = m;
+        slot[kTileM * kHeadDim + kTileM + row] = l;
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (row == 0) ctl->merge_last = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+        named_bar_sync(1, 128);
+        if (ctl->merge_last) {
+          __threadfence();
+          if (valid) {
+            float mx = -INFINITY;
+            for (int k = 0; k < nsplit; ++k) {
+              const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
+              mx = fmaxf(mx, __ldcg(sl + kTileM * kHeadDim + row));
+            }
+            float den = 0.f;
+            for (int k = 0; k < nsplit; ++k) {
+              const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
+              const float mk = __ldcg(sl + kTileM * kHeadDim + row);
+              if (mk != -INFINITY) den += ex2(mk - mx) * __ldcg(sl + kTileM * kHeadDim + kTileM + row);
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim;
+#pragma unroll 1
+            for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+              float acc[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+              for (int k = 0; k < nsplit; ++k) {
+                const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
+                const float mk = __ldcg(sl + kTileM * kHeadDim + row);
+                if (mk == -INFINITY) continue;
+                const float f = ex2(mk - mx) * inv;
+                const float4* src = reinterpret_cast<const float4*>(sl + row * kHeadDim + ch * 32);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const float4 v = __ldcg(src + c);
+                  acc[4 * c] += f * v.x;
+                  acc[4 * c + 1] += f * v.y;
+                  acc[4 * c + 2] += f * v.z;
+                  acc[4 * c + 3] += f * v.w;
+                }
+              }
+              uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
+                                   pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
+                                   pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
+                                   pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+            }
+          }
+          if (row == 0) p.arrive[unit] = 0;  // ready for the next run
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+}
+
+// ============================================================================ decode item
+// Reduce-scatter of 16 per-row partial dot products over the 32 lanes of a warp (each lane
+// holds 4 of the 128 dims): five butterfly steps halve the values per lane, the last one adds
+// the lane pair. Afterwards lanes 2r and 2r+1 both hold the full dot product of row r.
+__device__ __forceinline__ float rowdot_scatter(float (&v)[16], int lane) {
+  float a[8];
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float send = hi ? v[i] : v[i + 8];
+      const float keep = hi ? v[i + 8] : v[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  float b[4];
+  {
+    const bool hi = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = hi ? a[i] : a[i + 4];
+      const float keep = hi ? a[i + 4] : a[i];
+      b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  float c[2];
+  {
+    const bool hi = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = hi ? b[i] : b[i + 2];
+      const float keep = hi ? b[i + 2] : b[i];
+      c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  const bool hi = lane & 2;
+  const float send = hi ? c[0] : c[1];
+  const float keep = hi ? c[1] : c[0];
+  float d = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
+
+template <int GT>
+__device__ void decode_item(const Params& p, const int32_t* it, uint8_t* smem, SmemCtl* ctl,
+                            PipeState& ps, const WaitCtx& wc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = it[1], g = it[2], kb = it[4], ke = it[5], unit = it[6], split = it[7];
+  const int G = p.G;
+  const int32_t* bt_row = p.block_tables + (size_t)(p.Np + d) * p.maxb;
+  const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
+  const int blk0 = kb / kBlockSize;
+  const int nmine = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* ring = smem + warp * kDecodeSlots * kSmemDecodeSlot;
+  float* ps_x = reinterpret_cast<float*>(smem + kSmemUnion) + warp * kMaxGroup * kBlockSize;
+
+  // q in registers: 4 consecutive dims per lane, premultiplied by scale*log2(e)
+  float q[GT][4], o[GT][4], m[GT], ls[GT];
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    m[h] = -INFINITY;
+    ls[h] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[h][k] = q[h][k] = 0.f;
+    if (h < G) {
+      const uint2 r = *reinterpret_cast<const uint2*>(
+          p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + lane * 4);
+      q[h][0] = bf16lo(r.x) * p.scale_log2;
+      q[h][1] = bf16hi(r.x) * p.scale_log2;
+      q[h][2] = bf16lo(r.y) * p.scale_log2;
+      q[h][3] = bf16hi(r.y) * p.scale_log2;
+    }
+  }
+
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
+    const int slot = i & 1;
+    int phys = bt_row[blk0 + warp + i * kWarps];
+    if (phys < 0 || phys >= p.num_blocks) {
+      record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+      phys = 0;
+    }
+    const size_t off = ((size_t)phys * p.Hkv + g) * (kBlockSize * kHeadDim);
+    const uint32_t bar = smem_u32(&ctl->dslot[warp][slot]);
+    const uint32_t dst = smem_u32(ring + slot * kSmemDecodeSlot);
+    mbar_arrive_expect_tx(bar, kSmemDecodeSlot);
+    bulk_load(dst, p.k_pool + off, kSmemDecodeSlot / 2, bar, pol);
+    bulk_load(dst + kSmemDecodeSlot / 2, p.v_pool + off, kSmemDecodeSlot / 2, bar, pol);
+  };
+  if (lane == 0) {
+    if (nmine > 0) issue(0);
+    if (nmine > 1) issue(1);
+  }
+  bool ok = true;
+  const int r = lane >> 1;  // the row whose full score this lane holds after the reduction
+  for (int i = 0; i < nmine; ++i) {
+    const int slot = i & 1;
+    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc)) {
+      ok = false;
+      break;
+    }
+    ps.dphase ^= 1u << slot;
+    const int key0 = kb + (warp + i * kWarps) * kBlockSize;
+    const int nv = min(kBlockSize, ke - key0);
+    const uint16_t* Ks = reinterpret_cast<const uint16_t*>(ring + slot * kSmemDecodeSlot);
+    const uint16_t* Vs = Ks + kBlockSize * kHeadDim;
+    uint2 kr[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) kr[c] = *reinterpret_cast<const uint2*>(Ks + c * kHeadDim + lane * 4);
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      if (h < G) {
+        float part[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          part[c] = q[h][0] * bf16lo(kr[c].x) + q[h][1] * bf16hi(kr[c].x) +
+                    q[h][2] * bf16lo(kr[c].y) + q[h][3] * bf16hi(kr[c].y);
+        float sc = rowdot_scatter(part, lane);
+        sc = r < nv ? sc : -INFINITY;
+        float bm = sc;
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        if (bm > m[h]) {  // warp-uniform
+          const float alpha = ex2(m[h] - bm);
+          m[h] = bm;
+          ls[h] *= alpha;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[h][k] *= alpha;
+        }
+        const float pv = r < nv ? ex2(sc - m[h]) : 0.f;
+        if ((lane & 1) == 0) {
+          ls[h] += pv;
+          ps_x[h * kBlockSize + r] = pv;
+        }
+      }
+    }
+    __syncwarp();
+    uint2 vr[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) vr[c] = *reinterpret_cast<const uint2*>(Vs + c * kHeadDim + lane * 4);
+    if (nv < kBlockSize) {
+      // rows past the sequence end may hold anything; their weight is 0 and so is their value
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c >= nv) vr[c] = make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      if (h < G) {
+        const float4* pp = reinterpret_cast<const float4*>(ps_x + h * kBlockSize);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 w = pp[c4];
+          const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint2 v = vr[c4 * 4 + e];
+            o[h][0] += wv[e] * bf16lo(v.x);
+            o[h][1] += wv[e] * bf16hi(v.x);
+            o[h][2] += wv[e] * bf16lo(v.y);
+            o[h][3] += wv[e] * bf16hi(v.y);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + 2 < nmine) issue(i + 2);
+  }
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) ls[h] += __shfl_xor_sync(0xffffffffu, ls[h], off);
+  }
+
+  // ---- combine the warps' partial states (ring memory is free once every warp is done) ----
+  __syncthreads();
+  float* scr = reinterpret_cast<float*>(smem);  // [kWarps][GT][kScr]: o[128], m, l (16-B rows)
+  constexpr int kScr = kHeadDim + 4;
+  constexpr int kRow = kHeadDim + 2;            // global partial slot row: o[128], m, l
+  if (ok) {
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      if (h < G) {
+        float* dst = scr + (warp * GT + h) * kScr;
+        *reinterpret_cast<float4*>(dst + lane * 4) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        if (lane == 0) {
+          dst[kHeadDim] = m[h];
+          dst[kHeadDim + 1] = ls[h];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (!ctl->abort) {
+    const int nsplit = unit >= 0 ? p.units[unit * kUnitWords + 0] : 1;
+    const int slot0 = unit >= 0 ? p.units[unit * kUnitWords + 1] : 0;
+    float* slot = unit >= 0 ? p.partial_d + (size_t)(slot0 + split) * decode_slot_floats(G) : nullptr;
+    for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kThreads) {
+      const int h = idx / kHeadDim, c = idx % kHeadDim;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, scr[(w * GT + h) * kScr + kHeadDim]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* src = scr + (w * GT + h) * kScr;
+        const float mw = src[kHeadDim];
+        if (mw == -INFINITY) continue;
+        const float f = ex2(mw - mx);
+        num += f * src[c];
+        den += f * src[kHeadDim + 1];
+      }
+      if (unit < 0) {
+        p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + c] = f2bf(num / den);
+      } else {
+        slot[h * kRow + c] = num;
+        if (c == 0) {
+          slot[h * kRow + kHeadDim] = mx;
+          slot[h * kRow + kHeadDim + 1] = den;
+        }
+      }
+    }
+    if (unit >= 0) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) ctl->merge_last = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+      __syncthreads();
+      if (ctl->merge_last) {
+        __threadfence();
+        for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kThreads) {
+          const int h = idx / kHeadDim, c = idx % kHeadDim;
+          float mx = -INFINITY;
+          for (int k = 0; k < nsplit; ++k)
+            mx = fmaxf(mx, __ldcg(p.partial_d + (size_t)(slot0 + k) * decode_slot_floats(G) + h * kRow + kHeadDim));
+          float num = 0.f, den = 0.f;
+          for (int k = 0; k < nsplit; ++k) {
+            const float* sl = p.partial_d + (size_t)(slot0 + k) * decode_slot_floats(G) + h * kRow;
+            const float mk = __ldcg(sl + kHeadDim);
+            if (mk == -INFINITY) continue;
+            const float f = ex2(mk - mx);
+            num += f * __ldcg(sl + c);
+            den += f * __ldcg(sl + kHeadDim + 1);
+          }
+          p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + c] = f2bf(num / den);
+        }
+        if (threadIdx.x == 0) p.arrive[unit] = 0;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ============================================================================ scheduler
+__device__ __forceinline__ void pick_item(const Params& p, int sm, SmemCtl* ctl) {
+  int32_t* cnt = p.counters;
+  int kind = -1, idx = 0;
+  if (p.mode == kModePrefillOnly) {
+    const int t = atomicAdd(&cnt[0], 1);
+    if (t < p.n_items_p) kind = 0, idx = t;
+  } else if (p.mode == kModeDecodeOnly) {
+    const int t = atomicAdd(&cnt[1], 1);
+    if (t < p.n_items_d) kind = 1, idx = t;
+  } else {
+    int* running = &cnt[kCounterHeader + sm];
+    if (*reinterpret_cast<volatile int*>(&cnt[0]) < p.n_items_p) {
+      if (atomicAdd(running, 1) < p.max_prefill_per_sm) {
+        const int t = atomicAdd(&cnt[0], 1);
+        if (t < p.n_items_p) kind = 0, idx = t;
+      }
+      if (kind < 0) atomicSub(running, 1);
+    }
+    if (kind < 0) {
+      const int t = atomicAdd(&cnt[1], 1);
+      if (t < p.n_items_d) kind = 1, idx = t;
+    }
+    if (kind < 0) {  // decode drained: prefill may take every CTA of the SM
+      const int t = atomicAdd(&cnt[0], 1);
+      if (t < p.n_items_p) {
+        kind = 0, idx = t;
+        atomicAdd(running, 1);
+      }
+    }
+  }
+  ctl->item_kind = kind;
+  ctl->item_idx = idx;
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads, 2)
+    pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemUnion + kSmemScores);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const bool use_tmem = p.mode != kModeDecodeOnly && p.n_items_p > 0;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&ctl->q_full), 1);
+    for (int i = 0; i < kKvStages; ++i) {
+      mbar_init(smem_u32(&ctl->kv_full[i]), 1);
+      mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl->s_full[i]), 1);
+      mbar_init(smem_u32(&ctl->p_ready[i]), 128);
+    }
+    mbar_init(smem_u32(&ctl->o_done), 1);
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < kDecodeSlots; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+    if (use_tmem) {
+      prefetch_tmap(&tmq);
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+    }
+  }
+  if (use_tmem && warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const WaitCtx wc{&ctl->abort, p.status, p.timeout_ns};
+  PipeState ps;
+  const uint32_t sm_raw = smid();
+  const int sm = (int)(sm_raw % (uint32_t)p.num_sms);
+  for (;;) {
+    if (tid == 0) pick_item(p, sm, ctl);
+    __syncthreads();
+    const int kind = ctl->item_kind, idx = ctl->item_idx;
+    if (kind < 0 || ctl->abort) break;
+    const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
+    if (kind == 0)
+      prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+    else
+      decode_item<GT>(p, p.items_d + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+    if (tid == 0) {
+      if (p.records != nullptr) {
+        pod_attn_item_record* rec = p.records + (kind == 0 ? idx : p.n_items_p + idx);
+        rec->smid = (int32_t)sm_raw;
+        rec->kind = kind;
+        rec->item = idx;
+        rec->cta = blockIdx.x;
+        rec->t_start = t0;
+        rec->t_end = globaltimer();
+      }
+      if (kind == 0 && p.mode == kModeFused) atomicSub(&p.counters[kCounterHeader + sm], 1);
+    }
+  }
+  __syncthreads();
+  if (ctl->abort && tid == 0) {
+    // give copies still in flight time to land before this CTA's shared memory is released
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (use_tmem && warp == 1) tmem_dealloc(ctl->tmem_base, kTmemCols);
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&p.counters[2], 1) == (int)gridDim.x - 1) {
+      p.counters[0] = 0;
+      p.counters[1] = 0;
+      p.counters[2] = 0;
+      __threadfence();
+    }
+  }
+}
+
+__global__ void selftest_timeout_kernel(int32_t* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx wc{&abort_flag, status, timeout_ns};
+    mbar_wait(smem_u32(&bar), 0, wc);  // nobody arrives: runs into the time limit
+  }
+}
+
+// ============================================================================ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+struct CudaState {
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  CUtensorMap tmq{}, tmk{}, tmv{};
+  const void *kq = nullptr, *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
+};
+
+// Q: 3-D {dim, head, token} so one box is 128 tokens x 64 dims of one head.
+static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hq, (cuuint64_t)Tp};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Hq * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, kTileM};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// K or V pool: 2-D {dim, row} over num_blocks*Hkv*16 rows; one box is one paged block's 16 rows
+// x 64 dims.
+static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int GT>
+static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
+  static std::atomic<int> attr_set{0};
+  if (!attr_set.load()) {
+    cudaError_t e = cudaFuncSetAttribute(pod_attn_kernel<GT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+    if (e != cudaSuccess) return e;
+    attr_set.store(1);
+  }
+  pod_attn_kernel<GT><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, cs.tmk, cs.tmv);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
+  if (grid <= 0) return cudaSuccess;
+  switch (p.G) {
+    case 1: return launch_mode<1>(p, grid, st, cs);
+    case 2: return launch_mode<2>(p, grid, st, cs);
+    case 3:
+    case 4: return launch_mode<4>(p, grid, st, cs);
+    default: return launch_mode<8>(p, grid, st, cs);
+  }
+}
+
+}  // namespace pod
+
+using namespace pod;
+
+// ============================================================================ C ABI
+extern "C" {
+
+const char* pod_attn_status_string(pod_attn_status s) {
+  switch (s) {
+    case POD_ATTN_OK: return "ok";
+    case POD_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case POD_ATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case POD_ATTN_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case POD_ATTN_ERR_CUDA: return "CUDA error";
+    case POD_ATTN_ERR_BAD_INDEX: return "block-table entry out of range";
+    case POD_ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+pod_attn_status pod_attn_plan(const pod_attn_problem* problem, const int32_t* h_cu_seqlens_q,
+                              const int32_t* h_kv_lens, const pod_attn_options* options,
+                              pod_attn_plan_t* out) {
+  if (problem == nullptr || out == nullptr) return POD_ATTN_ERR_INVALID_ARG;
+  *out = nullptr;
+  pod_attn_options opt{};
+  if (options) opt = *options;
+  if (opt.variant != POD_ATTN_FUSED && opt.variant != POD_ATTN_SERIAL &&
+      opt.variant != POD_ATTN_STREAMS)
+    return POD_ATTN_ERR_INVALID_ARG;
+  int num_sms = opt.num_sms;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return POD_ATTN_ERR_CUDA;
+    }
+  }
+  pod_attn_plan_s* plan = new (std::nothrow) pod_attn_plan_s();
+  if (!plan) return POD_ATTN_ERR_INVALID_ARG;
+  pod_attn_status st;
+  try {
+    st = build_plan(*problem, h_cu_seqlens_q, h_kv_lens, opt, num_sms, plan);
+  } catch (...) {
+    st = POD_ATTN_ERR_INVALID_ARG;
+  }
+  if (st != POD_ATTN_OK) {
+    delete plan;
+    return st;
+  }
+  CudaState* cs = new (std::nothrow) CudaState();
+  if (!cs) {
+    delete plan;
+    return POD_ATTN_ERR_INVALID_ARG;
+  }
+  if (opt.variant == POD_ATTN_STREAMS) {
+    if (cudaEventCreateWithFlags(&cs->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&cs->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();  // tolerated here; run() reports it
+      cs->ev_fork = cs->ev_join = nullptr;
+    }
+  }
+  plan->cuda_state = cs;
+  *out = plan;
+  return POD_ATTN_OK;
+}
+
+size_t pod_attn_workspace_bytes(pod_attn_plan_t plan) { return plan ? plan->ws.total : 0; }
+
+pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info* info) {
+  if (!plan || !info) return POD_ATTN_ERR_INVALID_ARG;
+  pod_attn_plan_info r{};
+  r.num_prefill_items = (int32_t)(plan->items_p.size() / kItemWords);
+  r.num_decode_items = (int32_t)(plan->items_d.size() / kItemWords);
+  r.num_units = (int32_t)(plan->units.size() / kUnitWords);
+  r.num_sms = plan->num_sms;
+  r.ctas_per_sm = plan->ctas_per_sm;
+  r.max_prefill_ctas = plan->max_prefill_per_sm;
+  r.grid_fused = plan->grid_fused;
+  r.grid_prefill = plan->grid_prefill;
+  r.grid_decode = plan->grid_decode;
+  r.smem_bytes = kSmemTotal;
+  r.threads_per_cta = kThreads;
+  r.item_words = kItemWords;
+  r.workspace_bytes = plan->ws.total;
+  r.est_prefill_flops = plan->est_prefill_flops;
+  r.est_prefill_bytes = plan->est_prefill_bytes;
+  r.est_decode_bytes = plan->est_decode_bytes;
+  r.est_decode_flops = plan->est_decode_flops;
+  *info = r;
+  return POD_ATTN_OK;
+}
+
+pod_attn_status pod_attn_plan_items(pod_attn_plan_t plan, int32_t* out, size_t capacity,
+                                    size_t* count) {
+  if (!plan || !count) return POD_ATTN_ERR_INVALID_ARG;
+  const size_t n = plan->items_p.size() + plan->items_d.size() + plan->units.size();
+  *count = n;
+  if (n == 0 || out == nullptr) return POD_ATTN_OK;  // size query
+  if (capacity < n) return POD_ATTN_ERR_INVALID_ARG;
+  std::memcpy(out, plan->items_p.data(), plan->items_p.size() * 4);
+  std::memcpy(out + plan->items_p.size(), plan->items_d.data(), plan->items_d.size() * 4);
+  std::memcpy(out + plan->items_p.size() + plan->items_d.size(), plan->units.data(),
+              plan->units.size() * 4);
+  return POD_ATTN_OK;
+}
+
+static pod_attn_status check_ws(pod_attn_plan_t plan, const void* ws, size_t bytes) {
+  if (!ws) return POD_ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0 || bytes < plan->ws.total)
+    return POD_ATTN_ERR_WORKSPACE;
+  return POD_ATTN_OK;
+}
+
+pod_attn_status pod_attn_upload(pod_attn_plan_t plan, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!plan) return POD_ATTN_ERR_INVALID_ARG;
+  pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
+  if (st != POD_ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const WorkspaceLayout& w = plan->ws;
+  bool ok = cudaMemsetAsync(ws, 0, w.zero_bytes, s) == cudaSuccess;
+  if (ok && !plan->items_p.empty())
+    ok = cudaMemcpyAsync(ws + w.items_p, plan->items_p.data(), plan->items_p.size() * 4,
+                         cudaMemcpyHostToDevice, s) == cudaSuccess;
+  if (ok && !plan->items_d.empty())
+    ok = cudaMemcpyAsync(ws + w.items_d, plan->items_d.data(), plan->items_d.size() * 4,
+                         cudaMemcpyHostToDevice, s) == cudaSuccess;
+  if (ok && !plan->units.empty())
+    ok = cudaMemcpyAsync(ws + w.units, plan->units.data(), plan->units.size() * 4,
+                         cudaMemcpyHostToDevice, s) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return POD_ATTN_ERR_CUDA;
+  }
+  return POD_ATTN_OK;
+}
+
+pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const void* q_decode,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* d_block_tables, const int32_t* d_cu_seqlens_q,
+                             const int32_t* d_kv_lens, void* o_prefill, void* o_decode,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* stream2) {
+  if (!plan) return POD_ATTN_ERR_INVALID_ARG;
+  pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
+  if (st != POD_ATTN_OK) return st;
+  const pod_attn_problem& pr = plan->prob;
+  const int n_p = (int)(plan->items_p.size() / kItemWords);
+  const int n_d = (int)(plan->items_d.size() / kItemWords);
+  if (n_p + n_d == 0) return POD_ATTN_OK;
+  if (!k_pool || !v_pool || !d_block_tables || !d_kv_lens) return POD_ATTN_ERR_INVALID_ARG;
+  if (n_p > 0 && (!q_prefill || !o_prefill || !d_cu_seqlens_q)) return POD_ATTN_ERR_INVALID_ARG;
+  if (n_d > 0 && (!q_decode || !o_decode)) return POD_ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
+       reinterpret_cast<uintptr_t>(q_prefill) | reinterpret_cast<uintptr_t>(o_prefill) |
+       reinterpret_cast<uintptr_t>(q_decode)) & 15)
+    return POD_ATTN_ERR_INVALID_ARG;
+  CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
+  const int64_t pool_rows = (int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize;
+  if (n_p > 0) {
+    if (cs->kq != q_prefill) {
+      if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens))
+        return POD_ATTN_ERR_CUDA;
+      cs->kq = q_prefill;
+    }
+    if (cs->kk != k_pool) {
+      if (!encode_pool(&cs->tmk, k_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
+      cs->kk = k_pool;
+    }
+    if (cs->kv != v_pool) {
+      if (!encode_pool(&cs->tmv, v_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
+      cs->kv = v_pool;
+    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const WorkspaceLayout& w = plan->ws;
+  Params p{};
+  p.q_prefill = static_cast<const uint16_t*>(q_prefill);
+  p.q_decode = static_cast<const uint16_t*>(q_decode);
+  p.k_pool = static_cast<const uint16_t*>(k_pool);
+  p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.block_tables = d_block_tables;
+  p.cu_seqlens = d_cu_seqlens_q;
+  p.kv_lens = d_kv_lens;
+  p.o_prefill = static_cast<uint16_t*>(o_prefill);
+  p.o_decode = static_cast<uint16_t*>(o_decode);
+  p.items_p = reinterpret_cast<const int32_t*>(ws + w.items_p);
+  p.items_d = reinterpret_cast<const int32_t*>(ws + w.items_d);
+  p.units = reinterpret_cast<const int32_t*>(ws + w.units);
+  p.partial_p = reinterpret_cast<float*>(ws + w.partial_p);
+  p.partial_d = reinterpret_cast<float*>(ws + w.partial_d);
+  p.arrive = reinterpret_cast<int32_t*>(ws + w.arrive);
+  p.status = reinterpret_cast<int32_t*>(ws + w.status);
+  p.records = plan->opt.instrument ? reinterpret_cast<pod_attn_item_record*>(ws + w.records) : nullptr;
+  p.n_items_p = n_p;
+  p.n_items_d = n_d;
+  p.Hq = pr.num_q_heads;
+  p.Hkv = pr.num_kv_heads;
+  p.G = plan->group;
+  p.Np = pr.num_prefill_seqs;
+  p.Nd = pr.num_decode_seqs;
+  p.num_blocks = pr.num_blocks;
+  p.maxb = pr.max_blocks_per_seq;
+  p.pool_rows = (int32_t)pool_rows;
+  p.num_sms = plan->num_sms;
+  p.max_prefill_per_sm = plan->max_prefill_per_sm;
+  p.scale_log2 = pr.scale * 1.4426950408889634f;
+  p.timeout_ns = kWaitTimeoutNs;
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + w.counters);
+  auto counter_block = [&](int mode) { return counters + (size_t)mode * w.counter_block_words; };
+
+  cudaStream_t s1 = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  switch (plan->opt.variant) {
+    case POD_ATTN_FUSED: {
+      p.mode = kModeFused;
+      p.counters = counter_block(kModeFused);
+      e = launch(p, plan->grid_fused, s1, *cs);
+      break;
+    }
+    case POD_ATTN_SERIAL: {
+      Params a = p, b = p;
+      a.mode = kModePrefillOnly;
+      a.counters = counter_block(kModePrefillOnly);
+      b.mode = kModeDecodeOnly;
+      b.counters = counter_block(kModeDecodeOnly);
+      e = launch(a, plan->grid_prefill, s1, *cs);
+      if (e == cudaSuccess) e = launch(b, plan->grid_decode, s1, *cs);
+      break;
+    }
+    case POD_ATTN_STREAMS: {
+      if (!cs->ev_fork || !cs->ev_join) return POD_ATTN_ERR_CUDA;
+      cudaStream_t s2 = static_cast<cudaStream_t>(stream2);
+      Params a = p, b = p;
+      a.mode = kModePrefillOnly;
+      a.counters = counter_block(kModePrefillOnly);
+      b.mode = kModeDecodeOnly;
+      b.counters = counter_block(kModeDecodeOnly);
+      e = cudaEventRecord(cs->ev_fork, s1);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s2, cs->ev_fork, 0);
+      if (e == cudaSuccess) e = launch(a, plan->grid_prefill, s1, *cs);
+      if (e == cudaSuccess) e = launch(b, plan->grid_decode, s2, *cs);
+      if (e == cudaSuccess) e = cudaEventRecord(cs->ev_join, s2);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s1, cs->ev_join, 0);
+      break;
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return POD_ATTN_ERR_CUDA;
+  }
+  return POD_ATTN_OK;
+}
+
+pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspace, void* stream) {
+  (void)plan;
+  if (!workspace) return POD_ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t code = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpy(&code, workspace, sizeof code, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(workspace, 0, sizeof code) != cudaSuccess) {
+    cudaGetLastError();
+    return POD_ATTN_ERR_CUDA;
+  }
+  if (code == POD_ATTN_ERR_BAD_INDEX || code == POD_ATTN_ERR_TIMEOUT)
+    return static_cast<pod_attn_status>(code);
+  return code == 0 ? POD_ATTN_OK : POD_ATTN_ERR_CUDA;
+}
+
+pod_attn_status pod_attn_read_records(pod_attn_plan_t plan, const void* workspace,
+                                      pod_attn_item_record* out, size_t capacity, size_t* count,
+                                      void* stream) {
+  if (!plan || !workspace || !count || !plan->opt.instrument) return POD_ATTN_ERR_INVALID_ARG;
+  const size_t n = plan->items_p.size() / kItemWords + plan->items_d.size() / kItemWords;
+  *count = n;
+  if (n == 0) return POD_ATTN_OK;
+  if (!out || capacity < n) return POD_ATTN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(out, static_cast<const uint8_t*>(workspace) + plan->ws.records,
+                 n * sizeof(pod_attn_item_record), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return POD_ATTN_ERR_CUDA;
+  }
+  return POD_ATTN_OK;
+}
+
+void pod_attn_plan_destroy(pod_attn_plan_t plan) {
+  if (!plan) return;
+  CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
+  if (cs) {
+    if (cs->ev_fork) cudaEventDestroy(cs->ev_fork);
+    if (cs->ev_join) cudaEventDestroy(cs->ev_join);
+    delete cs;
+  }
+  delete plan;
+}
+
+pod_attn_status pod_attn_selftest_timeout(void* workspace, int32_t timeout_us, void* stream) {
+  if (!workspace || timeout_us < 1) return POD_ATTN_ERR_INVALID_ARG;
+  selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<int32_t*>(workspace), (uint64_t)timeout_us * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return POD_ATTN_ERR_CUDA;
+  return POD_ATTN_OK;
+}
+
+}  // extern "C"

@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
   POD_ATTN_OK = 0,
   POD_ATTN_ERR_INVALID_ARG = -1,  /* a null pointer, a bad length or an inconsistent shape */
-  POD_ATTN_ERR_UNSUPPORTED = -2,  /* head_dim != 128, block_size != 16, group size > 16, ... */
+  POD_ATTN_ERR_UNSUPPORTED = -2,  /* head_dim != 128, block_size != 16, group size > 8, ... */
   POD_ATTN_ERR_WORKSPACE = -3,    /* workspace too small or not 256-byte aligned */
   POD_ATTN_ERR_CUDA = -4,         /* a CUDA runtime call failed (no device, launch error, ...) */
   POD_ATTN_ERR_BAD_INDEX = -5,    /* device-detected: a block-table entry outside [0, num_blocks) */
@@ -82,7 +82,7 @@ typedef enum {
 /* Shapes of one hybrid batch. */
 typedef struct {
   int32_t num_q_heads;         /* Hq >= 1 */
-  int32_t num_kv_heads;        /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 16 */
+  int32_t num_kv_heads;        /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 8 */
   int32_t head_dim;            /* must be 128 */
   int32_t block_size;          /* must be 16 */
   int32_t num_prefill_seqs;    /* Np >= 0 */
@@ -204,9 +204,10 @@ pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info*
 
 /* Copy the host work lists: prefill items first, then decode items, then the unit table, each
  * item info.item_words int32 words (see DESIGN of the item encoding in the planner source).
- *   out   : host buffer of `capacity` int32 words.
- *   count : receives the number of words written.
- * Used to check the planner bit for bit. Errors: INVALID_ARG (null, capacity too small). */
+ *   out   : host buffer of `capacity` int32 words, or NULL to query the size only.
+ *   count : receives the number of words (written, or needed when out is NULL).
+ * Used to check the planner bit for bit. Errors: INVALID_ARG (null plan/count, capacity too
+ * small). */
 pod_attn_status pod_attn_plan_items(pod_attn_plan_t plan, int32_t* out, size_t capacity,
                                     size_t* count);
 
@@ -223,12 +224,14 @@ void pod_attn_plan_destroy(pod_attn_plan_t plan);
 /* Static English description of a status code. */
 const char* pod_attn_status_string(pod_attn_status status);
 
-/* Test hook for the bounded-wait failure path (no GPU fault involved): launches one CTA that
- * waits on an mbarrier nobody arrives on, with a spin limit of `spin_limit` polls, and
- * records POD_ATTN_ERR_TIMEOUT in the workspace status word when the limit runs out.
- *   workspace : device pointer with at least 256 bytes.
+/* Test hook for the bounded-wait failure path (no GPU fault involved): launches one CTA whose
+ * thread 0 waits on an mbarrier nobody arrives on, for at most `timeout_us` microseconds, and
+ * records POD_ATTN_ERR_TIMEOUT in the workspace status word when the limit runs out (the same
+ * bounded wait every pipeline wait of the attention kernels uses, there with a 4 s limit).
+ *   workspace : device pointer with at least 256 bytes, its first 8 bytes zeroed by the caller
+ *               (pod_attn_upload does this for a plan's workspace).
  * Read the outcome with pod_attn_last_device_status. Errors: INVALID_ARG, CUDA. */
-pod_attn_status pod_attn_selftest_timeout(void* workspace, int32_t spin_limit, void* stream);
+pod_attn_status pod_attn_selftest_timeout(void* workspace, int32_t timeout_us, void* stream);
 
 #ifdef __cplusplus
 }

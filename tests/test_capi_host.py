@@ -1,0 +1,219 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every declared symbol,
+validates its arguments, and its planner matches a plain Python restatement bit for bit."""
+import ctypes
+import math
+import random
+
+import pytest
+
+from hybrid_prefill_decode_gb300 import binding as B
+from hybrid_prefill_decode_gb300 import workloads as W
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return B.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = B.declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        assert lib.pod_attn_status_string(code)
+
+
+def _plan_code(Hq=4, Hkv=2, cu=(0, 5), kv=(9, 7), nd=1, nb=10, maxb=4, head_dim=128,
+               block=16, scale=0.1, variant=0):
+    lib = B.load()
+    np_ = max(0, len(cu) - 1)
+    prob = B.Problem(Hq, Hkv, head_dim, block, np_, cu[-1] if np_ else 0, nd, nb, maxb, scale)
+    opt = B.Options(148, 0, 0, 0, 0, 0, variant)
+    cua = (ctypes.c_int32 * max(1, len(cu)))(*cu)
+    kva = (ctypes.c_int32 * max(1, len(kv)))(*kv)
+    h = ctypes.c_void_p()
+    code = lib.pod_attn_plan(ctypes.byref(prob), ctypes.cast(cua, ctypes.c_void_p),
+                             ctypes.cast(kva, ctypes.c_void_p), ctypes.byref(opt),
+                             ctypes.byref(h))
+    if code == 0:
+        lib.pod_attn_plan_destroy(h)
+    return code
+
+
+def test_plan_validation(lib):
+    assert _plan_code() == B.OK
+    assert _plan_code(head_dim=64) == B.ERR_UNSUPPORTED
+    assert _plan_code(block=32) == B.ERR_UNSUPPORTED
+    assert _plan_code(Hq=18, Hkv=1) == B.ERR_UNSUPPORTED          # group 18 > 8
+    assert _plan_code(Hq=6, Hkv=4) == B.ERR_INVALID_ARG           # Hq % Hkv != 0
+    assert _plan_code(cu=(0, 5), kv=(4, 7)) == B.ERR_INVALID_ARG  # kv_len < q_len
+    assert _plan_code(cu=(1, 5), kv=(9, 7)) == B.ERR_INVALID_ARG  # cu[0] != 0
+    assert _plan_code(cu=(0, 5, 5), kv=(9, 9, 7)) == B.ERR_INVALID_ARG  # empty chunk
+    assert _plan_code(kv=(9, 0)) == B.ERR_INVALID_ARG             # decode kv_len 0
+    assert _plan_code(kv=(9, 65)) == B.ERR_INVALID_ARG            # beyond max_blocks_per_seq*16
+    assert _plan_code(variant=7) == B.ERR_INVALID_ARG
+    assert _plan_code(cu=(), kv=(), nd=0) == B.OK                  # empty batch is legal
+    assert _plan_code(cu=(), kv=(3,), nd=1) == B.OK                # decode only
+    assert _plan_code(cu=(0, 5), kv=(9,), nd=0) == B.OK            # prefill only
+    assert lib.pod_attn_plan(None, None, None, None, None) == B.ERR_INVALID_ARG
+    assert lib.pod_attn_workspace_bytes(None) == 0
+    lib.pod_attn_plan_destroy(None)
+
+
+def test_run_rejects_bad_workspace(lib):
+    p = B.Plan(4, 2, [0, 5], [9, 7], 1, 10, 4, 0.1, num_sms=148)
+    code = lib.pod_attn_run(p.handle, None, None, None, None, None, None, None, None, None,
+                            None, 0, None, None)
+    assert code == B.ERR_INVALID_ARG
+    code = lib.pod_attn_run(p.handle, None, None, None, None, None, None, None, None, None,
+                            257, 1 << 20, None, None)
+    assert code == B.ERR_WORKSPACE        # misaligned
+    code = lib.pod_attn_upload(p.handle, 256, 16, None)
+    assert code == B.ERR_WORKSPACE        # too small
+
+
+# ---- the planner restated in plain Python (integer arithmetic, same rules) -----------------
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, cps=2, psplit=0, dsplit=0, cap_opt=0):
+    np_ = len(cu) - 1 if cu else 0
+    slots = num_sms * cps
+    pu, du, total = [], [], 0
+    for s in range(np_):
+        q, L = cu[s + 1] - cu[s], kv[s]
+        P = L - q
+        for t in range(_cdiv(q, 128)):
+            kend = P + min(q, (t + 1) * 128)
+            nt = _cdiv(kend, 64)
+            for h in range(Hq):
+                pu.append((s, t, h, kend, nt))
+                total += nt * 28
+    for d in range(nd):
+        L = kv[np_ + d]
+        for g in range(Hkv):
+            du.append((d, g, L, _cdiv(L, 16)))
+            total += _cdiv(L, 16) * 8
+    target = max(1, total // (slots * 4))
+    units, lp, ld = [], [], []
+    slots_used = [0, 0]
+
+    def add_unit(ns, kind):
+        u = len(units)
+        units.append([ns, slots_used[kind], kind, 0])
+        slots_used[kind] += ns
+        return u
+
+    for s, t, h, kend, nt in pu:
+        if psplit:
+            ns = psplit
+        else:
+            ns = min(_cdiv(nt * 28, target), max(1, nt // 8), 8)
+        ns = max(1, min(ns, nt))
+        chunk = _cdiv(nt, ns)
+        ns = _cdiv(nt, chunk)
+        u = add_unit(ns, 0) if ns > 1 else -1
+        for k in range(ns):
+            t0, t1 = k * chunk, min(nt, (k + 1) * chunk)
+            lp.append(((t1 - t0) * 28, [0, s, t, h, t0 * 64, min(kend, t1 * 64), u, k]))
+    for d, g, L, nblk in du:
+        if dsplit:
+            ns = dsplit
+        else:
+            ns = min(_cdiv(nblk * 8, target), max(1, nblk // 12), 64)
+        ns = max(1, min(ns, nblk))
+        chunk = _cdiv(nblk, ns)
+        ns = _cdiv(nblk, chunk)
+        u = add_unit(ns, 1) if ns > 1 else -1
+        for k in range(ns):
+            b0, b1 = k * chunk, min(nblk, (k + 1) * chunk)
+            ld.append(((b1 - b0) * 8, [1, d, g, 0, b0 * 16, min(L, b1 * 16), u, k]))
+    lp.sort(key=lambda x: -x[0])   # stable: longest first, ties in enumeration order
+    ld.sort(key=lambda x: -x[0])
+    cap = cap_opt if cap_opt > 0 else (1 if lp and ld else 2)
+    return ([w for _, w in lp], [w for _, w in ld], units, max(1, min(cap, cps)),
+            min(slots, len(lp) + len(ld)))
+
+
+def _random_case(rng):
+    Hkv = rng.choice([1, 2, 4, 8])
+    Hq = Hkv * rng.choice([1, 2, 3, 4, 8])
+    np_ = rng.randint(0, 3)
+    nd = rng.randint(0, 40)
+    q_lens = [rng.randint(1, 700) for _ in range(np_)]
+    pkv = [q + rng.randint(0, 9000) for q in q_lens]
+    dkv = [rng.randint(1, 20000) for _ in range(nd)]
+    return Hq, Hkv, q_lens, pkv, dkv
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_planner_matches_python_restatement(lib, seed):
+    rng = random.Random(seed)
+    Hq, Hkv, q_lens, pkv, dkv = _random_case(rng)
+    cu = [0]
+    for q in q_lens:
+        cu.append(cu[-1] + q)
+    num_sms = rng.choice([148, 152, 7])
+    psplit = rng.choice([0, 0, 3])
+    dsplit = rng.choice([0, 0, 5])
+    maxb = _cdiv(max(pkv + dkv + [1]), 16)
+    p = B.Plan(Hq, Hkv, cu if q_lens else [], pkv + dkv, len(dkv), 100, maxb, 0.1,
+               num_sms=num_sms, prefill_splits=psplit, decode_splits=dsplit)
+    got_p, got_d, got_u = p.items()
+    exp_p, exp_d, exp_u, cap, grid = restated_plan(Hq, Hkv, cu if q_lens else [], pkv + dkv,
+                                                   len(dkv), num_sms, psplit=psplit,
+                                                   dsplit=dsplit)
+    assert got_p == exp_p
+    assert got_d == exp_d
+    assert got_u == exp_u
+    inf = p.info()
+    assert inf["max_prefill_ctas"] == cap and inf["grid_fused"] == grid
+
+
+@pytest.mark.parametrize("i", [1, 2, 3, 4])
+def test_planner_covers_every_key_once(lib, i):
+    """Structural invariant: the items of each output tile exactly [0, visible end) in order."""
+    Hq, Hkv, q_lens, pkv, dkv = W.config_lengths(i)
+    cu = [0]
+    for q in q_lens:
+        cu.append(cu[-1] + q)
+    p = B.Plan(Hq, Hkv, cu, pkv + dkv, len(dkv), 10, _cdiv(max(pkv + dkv), 16), 0.1,
+               num_sms=152)
+    items_p, items_d, units = p.items()
+    cover = {}
+    for it in items_p + items_d:
+        key = tuple(it[:4])
+        cover.setdefault(key, []).append((it[7], it[4], it[5], it[6]))
+    for key, parts in cover.items():
+        parts.sort()
+        assert parts[0][1] == 0
+        for a, b in zip(parts, parts[1:]):
+            assert a[2] == b[1]                      # contiguous key ranges
+        if len(parts) > 1:
+            u = parts[0][3]
+            assert all(x[3] == u for x in parts) and units[u][0] == len(parts)
+        kind, seq = key[0], key[1]
+        if kind == 1:
+            assert parts[-1][2] == dkv[seq]
+        else:
+            t = key[2]
+            q = q_lens[seq]
+            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * 128)
+    # every (token tile, head) and (decode seq, kv-head) appears
+    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, 128) for q in q_lens) * Hq
+    assert len([k for k in cover if k[0] == 1]) == len(dkv) * Hkv
+
+
+def test_workspace_grows_with_instrumentation(lib):
+    a = B.Plan(32, 8, [0, 1024], [9000] + [5000] * 10, 10, 4000, 600, 0.1, num_sms=148)
+    b = B.Plan(32, 8, [0, 1024], [9000] + [5000] * 10, 10, 4000, 600, 0.1, num_sms=148,
+               instrument=True)
+    n = a.info()["num_prefill_items"] + a.info()["num_decode_items"]
+    assert b.workspace_bytes - a.workspace_bytes >= n * ctypes.sizeof(B.ItemRecord)

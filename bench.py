@@ -43,66 +43,93 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def _workload_name(cfg: int, batch) -> str:
+def _workload_name(cfg, batch) -> str:
     from hybrid_prefill_decode_gb300 import workloads as W
-    return W.CONFIG_NAMES[cfg] + f", head_dim 128, paged block 16, bf16"
+    name = W.CONFIG_NAMES.get(cfg) or W.PROFILE_CASES[cfg][0]
+    return name + ", head_dim 128, paged block 16, bf16"
+
+
+def _make_batch(args, device):
+    from hybrid_prefill_decode_gb300 import workloads as W
+    if args.case:
+        return W.profile_case(args.case, device=device)
+    return W.config(args.config, device=device)
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event (throttle) reasons sampled while the timed region runs.
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+    Reads NVML through ctypes every ~1 ms (read-only queries), so even a timed region of a few
+    milliseconds gets samples; if NVML cannot be loaded the summary says so."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device_index: int):
+        self.dev = torch_device_index
+        self.samples = []      # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.error = None
+        self._stop = False
+        self._thread = None
+
+    def _handle(self):
+        import ctypes
+        import torch
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        props = torch.cuda.get_device_properties(self.dev)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        h = ctypes.c_void_p()
+        if nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError(f"no NVML device for bus id {bus}")
+        return nvml, h
+
+    def _loop(self, nvml, h):
+        import ctypes
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop:
+            if nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(0.001)
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
-                stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+            nvml, h = self._handle()
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._thread = threading.Thread(target=self._loop, args=(nvml, h), daemon=True)
+            self._thread.start()
+            time.sleep(0.01)
+        except Exception as e:  # no NVML: nothing sampled, say so
+            self.error = str(e)
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.f.close()
+        self._stop = True
+        if self._thread is not None:
+            self._thread.join(timeout=2)
 
     def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append(parts)
-            except Exception:
-                pass
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": [f"no samples ({self.error or 'region too short'})"],
+                    "samples": 0}
         reasons = set()
-        for r in rows:
-            for n, v in zip(names, r[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(rows)}
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "nvml"}
 
 
 def cpu_baseline(batch, target_s: float = 12.0):
@@ -156,7 +183,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     from hybrid_prefill_decode_gb300 import workloads as W
-    batch = W.config(args.config, device="cpu")
+    batch = _make_batch(args, "cpu")
     vals = []
     for k in range(args.warmup + args.steps):
         r = cpu_baseline(batch, target_s=args.ref_step_s)
@@ -167,7 +194,8 @@ def run_reference(args, rank, world):
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": _workload_name(args.config, batch), "config_index": args.config},
+           "config": {"workload": _workload_name(args.case or args.config, batch),
+                      "config_index": args.case or args.config},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
                             "kind": "oracle", "sample": vals[0]["sample"]},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -181,6 +209,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--case", default=None, help="a small profiling case instead of --config")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -211,7 +240,7 @@ def main():
     B.load()
 
     dev = torch.device(f"cuda:{local}")
-    batch = W.config(args.config, device=dev)
+    batch = _make_batch(args, dev)
     work = R.batch_work(batch.num_q_heads, batch.num_kv_heads, batch.q_lens,
                         batch.prefill_kv_lens, batch.decode_kv_lens)
     hbm, tf_burst, tf_sust, peak_src = _peaks()
@@ -358,7 +387,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us["fused"] / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": _workload_name(args.config, batch), "config_index": args.config,
+        "config": {"workload": _workload_name(args.case or args.config, batch),
+                   "config_index": args.case or args.config,
                    "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "median_us": med["fused"],

@@ -205,6 +205,25 @@ def config(i: int, device="cpu", **kw) -> HybridBatch:
     return make_batch(Hq, Hkv, ql, pkv, dkv, seed=i, device=device, name=CONFIG_NAMES[i], **kw)
 
 
+# Small single-kind cases of the same shapes, used to profile one kernel path at a time (they fit
+# a profiler's memory save/restore: at most ~1.6 GB of pool).
+PROFILE_CASES = {
+    "prefill4": ("Yi-6B prefill only (32/4, chunk 2048 @ 28672)", 4, 32, 4, [2048], [30720], 0),
+    "prefill2": ("Llama-2-7B prefill only (32/32, chunk 512 @ 3584)", 2, 32, 32, [512], [4096], 0),
+    "decode2": ("Llama-2-7B decodes only (32/32, 32 decodes ctx U[2048,4096])", 2, 32, 32, [],
+                [], 32),
+    "decode3": ("Llama-3-8B decodes only (32/8, 16 decodes ctx U[8192,16384])", 3, 32, 8, [], [],
+                16),
+}
+
+
+def profile_case(name: str, device="cpu") -> HybridBatch:
+    """A single-kind case: the prefill chunk or the first decodes of a configuration."""
+    label, cfg, Hq, Hkv, ql, pkv, nd = PROFILE_CASES[name]
+    _, _, _, _, dkv = config_lengths(cfg)
+    return make_batch(Hq, Hkv, ql, pkv, dkv[:nd], seed=cfg, device=device, name=label)
+
+
 # ----------------------------------------------------------------------------------------------
 # Mixed-kind structural example: two decodes, one extend of 8 tokens after a cached prefix,
 # one fresh prefill of 4 tokens — 14 new tokens in the step ("Week 6: Beyond PyTorch",

@@ -859,6 +859,35 @@ static cudaError_t launch(const Params& p, int grid, cudaStream_t st, const Cuda
   }
 }
 
+// ---------------------------------------------------------------- allocation-free scratch
+// The workspace of pod_attn_run_static: one array per device that loads this library, alive
+// until the process exits. Host code must not use the symbol's name as an address (it is a host
+// stand-in); static_scratch() looks up its device address per device.
+constexpr size_t kStaticScratchBytes = POD_ATTN_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+static pod_attn_status static_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return POD_ATTN_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return POD_ATTN_ERR_CUDA;
+    }
+    addr[dev] = ptr;
+  }
+  *out = addr[dev];
+  return POD_ATTN_OK;
+}
+
 }  // namespace pod
 
 using namespace pod;
@@ -1147,6 +1176,25 @@ pod_attn_status pod_attn_read_records(pod_attn_plan_t plan, const void* workspac
     return POD_ATTN_ERR_CUDA;
   }
   return POD_ATTN_OK;
+}
+
+pod_attn_status pod_attn_run_static(pod_attn_plan_t plan, const void* q_prefill,
+                                    const void* q_decode, const void* k_pool,
+                                    const void* v_pool, const int32_t* d_block_tables,
+                                    const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
+                                    void* o_prefill, void* o_decode, void* stream) {
+  if (!plan || plan->opt.variant != POD_ATTN_FUSED) return POD_ATTN_ERR_INVALID_ARG;
+  if (plan->ws.total > kStaticScratchBytes) return POD_ATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  pod_attn_status st = static_scratch(&scratch);
+  if (st != POD_ATTN_OK) return st;
+  // work lists in, status / scheduling / merge counters cleared: the array keeps the last
+  // call's contents
+  st = pod_attn_upload(plan, scratch, kStaticScratchBytes, stream);
+  if (st != POD_ATTN_OK) return st;
+  return pod_attn_run(plan, q_prefill, q_decode, k_pool, v_pool, d_block_tables,
+                      d_cu_seqlens_q, d_kv_lens, o_prefill, o_decode, scratch,
+                      kStaticScratchBytes, stream, nullptr);
 }
 
 void pod_attn_plan_destroy(pod_attn_plan_t plan) {

@@ -218,6 +218,37 @@ pod_attn_status pod_attn_read_records(pod_attn_plan_t plan, const void* workspac
                                       pod_attn_item_record* out, size_t capacity,
                                       size_t* count, void* stream);
 
+/* Allocation-free launch of the FUSED variant. The pages have no counterpart to this entry
+ * point; it exists for callers that cannot call cudaMalloc to obtain a workspace: for example a
+ * plugin running inside a host program whose device memory belongs to that program's own
+ * allocator (the plugin has no way to ask it for memory, and a private cudaMalloc would compete
+ * with it or fail once the program has reserved the device), or a latency-critical loop that
+ * cannot afford cudaMalloc's implicit device synchronisation.
+ *
+ * Instead of a caller workspace it uses one library-owned scratch array of
+ * POD_ATTN_STATIC_SCRATCH_BYTES bytes, a file-scope __device__ array: every GPU that loads the
+ * library holds it until the process exits. Each call copies the plan's work lists into that
+ * array and clears its status word, scheduling counters and merge counters (on `stream`), then
+ * launches the fused kernel exactly as pod_attn_run does. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   plan            : a plan made with variant POD_ATTN_FUSED; its pod_attn_workspace_bytes must
+ *                     not exceed POD_ATTN_STATIC_SCRATCH_BYTES.
+ *   other arguments : as for pod_attn_run (inputs read only, outputs overwritten).
+ * The first call on a device looks up the array's device address on that device (with the
+ * device current); make that first call before any stream capture on the device.
+ * All calls share the one array, which keeps the last call's contents: calls whose work
+ * overlaps on the GPU (different streams, or another host thread) race and give wrong results;
+ * serialise them. Device-detected errors (bad block index, timeout) are recorded in the shared
+ * array and are not reported by this entry point.
+ * Errors: INVALID_ARG (null plan, variant other than FUSED, null/misaligned tensors),
+ * WORKSPACE (plan needs more than POD_ATTN_STATIC_SCRATCH_BYTES), CUDA. */
+#define POD_ATTN_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+pod_attn_status pod_attn_run_static(pod_attn_plan_t plan, const void* q_prefill,
+                                    const void* q_decode, const void* k_pool,
+                                    const void* v_pool, const int32_t* d_block_tables,
+                                    const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
+                                    void* o_prefill, void* o_decode, void* stream);
+
 /* Free the plan (NULL is ignored). */
 void pod_attn_plan_destroy(pod_attn_plan_t plan);
 

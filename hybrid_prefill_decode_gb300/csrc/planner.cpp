@@ -50,7 +50,8 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   const int Hq = prob.num_q_heads, Hkv = prob.num_kv_heads;
   const int Np = prob.num_prefill_seqs, Nd = prob.num_decode_seqs;
   if (Hq < 1 || Hkv < 1 || Np < 0 || Nd < 0 || prob.num_prefill_tokens < 0 ||
-      prob.num_blocks < 0 || prob.max_blocks_per_seq < 0 || !std::isfinite(prob.scale))
+      prob.num_blocks < 0 || prob.max_blocks_per_seq < 0 || !std::isfinite(prob.scale) ||
+      !(prob.scale > 0.f))
     return POD_ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return POD_ATTN_ERR_INVALID_ARG;
   if (prob.head_dim != kHeadDim || prob.block_size != kBlockSize) return POD_ATTN_ERR_UNSUPPORTED;

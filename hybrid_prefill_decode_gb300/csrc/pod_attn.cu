@@ -70,8 +70,10 @@ struct Params {
 
 struct SmemCtl {
   uint64_t q_full;
-  uint64_t kv_full[kKvStages];
-  uint64_t kv_empty[kKvStages];
+  uint64_t k_full[kKvStages];
+  uint64_t k_empty[kKvStages];
+  uint64_t v_full[kKvStages];
+  uint64_t v_empty[kKvStages];
   uint64_t s_full[2];
   uint64_t p_ready[2];
   uint64_t o_done;
@@ -114,39 +116,71 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sKV = sQ + kSmemQ;
 
+  // K and V tiles live in separate two-stage rings with their own full/empty barriers: a K
+  // stage is released as soon as its S = Q·Kᵀ has run, a V stage after its P·V.
+  const uint32_t sKring = sKV, sVring = sKV + kKvStages * kSmemKTile;
+
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer (warp)
+    // Lane i holds the block-table entry of block i of the next 8 tiles (32 blocks): one
+    // coalesced read instead of a dependent global read per block.
+    const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
+    const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
+    const int blk0 = kb / kBlockSize;
     if (lane == 0) {
-      const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
       const uint32_t qbar = smem_u32(&ctl->q_full);
       mbar_arrive_expect_tx(qbar, kSmemQ);
       tma_load_3d(sQ, tmq, qbar, 0, h, q0 + t * kTileM);
       tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h, q0 + t * kTileM);
-      for (int j = 0; j < ntiles; ++j) {
-        const int stage = ps.kv_cnt & 1;
-        const uint32_t ph = (ps.kv_cnt >> 1) & 1;
-        if (!mbar_wait(smem_u32(&ctl->kv_empty[stage]), ph ^ 1, wc)) break;
-        const uint32_t full = smem_u32(&ctl->kv_full[stage]);
-        mbar_arrive_expect_tx(full, kSmemStage);
-        const uint32_t sK = sKV + stage * kSmemStage, sV = sK + kSmemKTile;
-        for (int b = 0; b < kTileN / kBlockSize; ++b) {
-          const int key0 = kb + j * kTileN + b * kBlockSize;
-          int y = p.pool_rows;  // past the pool: the copy lands as zeros
-          if (key0 < ke) {
-            int phys = bt_row[key0 >> 4];
-            if (phys < 0 || phys >= p.num_blocks) {
-              record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
-              phys = 0;
-            }
-            y = (phys * p.Hkv + g) * kBlockSize;
+    }
+    int btv = -1;
+    for (int j = 0; j < ntiles; ++j) {
+      if ((j & 7) == 0) {
+        const int bi = j * 4 + lane;
+        btv = -1;
+        if (bi < nblk_item) {
+          int phys = bt_row[blk0 + bi];
+          if (phys < 0 || phys >= p.num_blocks) {
+            record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+            phys = 0;
           }
-          tma_load_2d(sK + b * 2048, tmk, full, 0, y);
-          tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y);
-          tma_load_2d(sV + b * 2048, tmv, full, 0, y);
-          tma_load_2d(sV + 8192 + b * 2048, tmv, full, 64, y);
+          btv = phys;
         }
-        ps.kv_cnt++;
       }
+      int y[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int e = __shfl_sync(0xffffffffu, btv, (j & 7) * 4 + b);
+        y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
+      }
+      const int stage = ps.kv_cnt & 1;
+      const uint32_t ph = (ps.kv_cnt >> 1) & 1;
+      int okw = 1;
+      if (lane == 0) okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ph ^ 1, wc);
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      if (lane == 0) {
+        const uint32_t full = smem_u32(&ctl->k_full[stage]);
+        const uint32_t sK = sKring + stage * kSmemKTile;
+        mbar_arrive_expect_tx(full, kSmemKTile);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          tma_load_2d(sK + b * 2048, tmk, full, 0, y[b]);
+          tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y[b]);
+        }
+        okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ph ^ 1, wc);
+      }
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      if (lane == 0) {
+        const uint32_t full = smem_u32(&ctl->v_full[stage]);
+        const uint32_t sV = sVring + stage * kSmemKTile;
+        mbar_arrive_expect_tx(full, kSmemKTile);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          tma_load_2d(sV + b * 2048, tmv, full, 0, y[b]);
+          tma_load_2d(sV + 8192 + b * 2048, tmv, full, 64, y[b]);
+        }
+      }
+      ps.kv_cnt++;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -154,39 +188,20 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc);
     ps.q_cnt++;
     tc_fence_after();
-    int prev_stage = 0;
-    uint32_t prev_s = 0;
-    auto issue_pv = [&](int stage, uint32_t scnt, bool first) -> bool {
+    uint32_t prev_kv = 0, prev_s = 0;
+    int prev_j = 0;
+    // O += P_jj · V_jj, once the softmax has written P_jj and V_jj has landed
+    auto issue_pv = [&](int jj, uint32_t kvc, uint32_t scnt) -> bool {
       const uint32_t sb = scnt & 1;
+      const int stage = kvc & 1;
       if (!mbar_wait(smem_u32(&ctl->p_ready[sb]), (scnt >> 1) & 1, wc)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sV = sKV + stage * kSmemStage + kSmemKTile;
-        const uint32_t aP = tmem + kTmemS0 + sb * kTileN;
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // V tile is N-major: 64-column halves 8 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
-          const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
-          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(smem_u32(&ctl->o_done));
-        umma_commit(smem_u32(&ctl->kv_empty[stage]));
-      }
-      __syncwarp();
-      return true;
-    };
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int stage = ps.kv_cnt & 1;
-      const uint32_t ph = (ps.kv_cnt >> 1) & 1;
-      if (!mbar_wait(smem_u32(&ctl->kv_full[stage]), ph, wc)) {
-        ok = false;
-        break;
-      }
-      const int tile0 = kb + j * kTileN;
+      if (!mbar_wait(smem_u32(&ctl->v_full[stage]), (kvc >> 1) & 1, wc)) return false;
+      const int tile0 = kb + jj * kTileN;
       if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
         // Rows past the sequence end inside its last block may hold anything (even NaN); P is
         // zero there but 0 * NaN is not, so clear those V rows before the PV product.
         const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
-        uint8_t* vbase = smem + kSmemQ + stage * kSmemStage + kSmemKTile;
+        uint8_t* vbase = smem + (sVring - sQ) + stage * kSmemKTile;
         for (int c = lane; c < (r1 - r0) * 16; c += 32) {
           const int r = r0 + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
           *reinterpret_cast<uint4*>(vbase + half * 8192 + r * 128 + q16 * 16) =
@@ -196,10 +211,33 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         __syncwarp();
       }
       tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sV = sVring + stage * kSmemKTile;
+        const uint32_t aP = tmem + kTmemS0 + sb * kTileN;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          // V tile is N-major: 64-column halves 8 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
+          const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
+          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (jj == 0 && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(smem_u32(&ctl->o_done));
+        umma_commit(smem_u32(&ctl->v_empty[stage]));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int stage = ps.kv_cnt & 1;
+      if (!mbar_wait(smem_u32(&ctl->k_full[stage]), (ps.kv_cnt >> 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       const uint32_t sb = ps.s_cnt & 1;
       if (lane == 0) {
-        const uint32_t sK = sKV + stage * kSmemStage;
+        const uint32_t sK = sKring + stage * kSmemKTile;
         const uint32_t dS = tmem + kTmemS0 + sb * kTileN;
+#pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
           const uint64_t ad = sdesc_sw128(sQ + half * (kSmemQ / 2) + koff, 16, 1024);
@@ -207,18 +245,20 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&ctl->s_full[sb]));
+        umma_commit(smem_u32(&ctl->k_empty[stage]));
       }
       __syncwarp();
-      if (j > 0 && !issue_pv(prev_stage, prev_s, j == 1)) {
+      if (j > 0 && !issue_pv(prev_j, prev_kv, prev_s)) {
         ok = false;
         break;
       }
-      prev_stage = stage;
+      prev_j = j;
+      prev_kv = ps.kv_cnt;
       prev_s = ps.s_cnt;
       ps.kv_cnt++;
       ps.s_cnt++;
     }
-    if (ok && ntiles > 0) issue_pv(prev_stage, prev_s, ntiles == 1);
+    if (ok && ntiles > 0) issue_pv(prev_j, prev_kv, prev_s);
   } else {
     // ------------------------------------------------------------------ softmax (1 row/thread)
     const int quarter = warp & 3;
@@ -242,13 +282,15 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       tmem_ld32(trow + kTmemS0 + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
       const int nvis = limit - (kb + j * kTileN);
+      if (!__all_sync(0xffffffffu, nvis >= kTileN)) {  // diagonal or last tile: mask
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= nvis) sr[c] = f2u(-INFINITY);
+      }
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float x = c < nvis ? u2f(sr[c]) * p.scale_log2 : -INFINITY;
-        sr[c] = f2u(x);
-        mt = fmaxf(mt, x);
-      }
+      for (int c = 0; c < 64; ++c) mt = fmaxf(mt, u2f(sr[c]));
+      mt *= p.scale_log2;  // scale > 0: the max of the scaled scores
       // Lazy rescale: keep the old reference max while the new scores exceed it by at most
       // 2^8; exponents stay bounded and O, l remain consistent with the reference max.
       const float m_new = fmaxf(m, mt);
@@ -263,7 +305,8 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(u2f(sr[2 * c]) - mref), p1 = ex2(u2f(sr[2 * c + 1]) - mref);
+        const float p0 = ex2(fmaf(u2f(sr[2 * c]), p.scale_log2, -mref));
+        const float p1 = ex2(fmaf(u2f(sr[2 * c + 1]), p.scale_log2, -mref));
         rs += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
@@ -435,11 +478,17 @@ __device__ __forceinline__ float rowdot_scatter(float (&v)[16], int lane) {
   return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
+constexpr int kScr = kHeadDim + 4;  // shared scratch row of one warp and head: o[128], m, l
+constexpr int kRow = kHeadDim + 2;  // global partial slot row: o[128], m, l
+
+// Decode, MHA (one query head per kv-head): CUDA-core path. Each warp streams its blocks with
+// 4 KiB bulk copies; q lives in registers (4 dims per lane); q·k is reduce-scattered across the
+// warp with shuffles. Leaves the warp's (o, m, l) in the shared scratch; returns false on abort.
 template <int GT>
-__device__ void decode_item(const Params& p, const int32_t* it, uint8_t* smem, SmemCtl* ctl,
+__device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, SmemCtl* ctl,
                             PipeState& ps, const WaitCtx& wc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = it[1], g = it[2], kb = it[4], ke = it[5], unit = it[6], split = it[7];
+  const int d = it[1], g = it[2], kb = it[4], ke = it[5];
   const int G = p.G;
   const int32_t* bt_row = p.block_tables + (size_t)(p.Np + d) * p.maxb;
   const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
@@ -568,11 +617,9 @@ __device__ void decode_item(const Params& p, const int32_t* it, uint8_t* smem, S
     for (int off = 1; off < 32; off <<= 1) ls[h] += __shfl_xor_sync(0xffffffffu, ls[h], off);
   }
 
-  // ---- combine the warps' partial states (ring memory is free once every warp is done) ----
+  // ---- leave the warp's partial state (ring memory is free once every warp is done) ----
   __syncthreads();
-  float* scr = reinterpret_cast<float*>(smem);  // [kWarps][GT][kScr]: o[128], m, l (16-B rows)
-  constexpr int kScr = kHeadDim + 4;
-  constexpr int kRow = kHeadDim + 2;            // global partial slot row: o[128], m, l
+  float* scr = reinterpret_cast<float*>(smem);  // [kWarps][GT][kScr]
   if (ok) {
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
@@ -586,7 +633,179 @@ __device__ void decode_item(const Params& p, const int32_t* it, uint8_t* smem, S
       }
     }
   }
+  return ok;
+}
+
+// Decode, grouped-query attention (G >= 2 query heads per kv-head): the G heads are the rows of
+// warp-level tensor-core MMAs (m16n8k16, bf16 in, fp32 accumulate). Each warp streams its blocks
+// through TMA (one 16-row x 64-dim box per half, 128-byte swizzle, so ldmatrix reads are free of
+// bank conflicts); per 16-key block: S = Q·Kᵀ (2 x 8 MMAs), a row softmax over 16 keys with quad
+// shuffles, O += P·V (16 MMAs) with P taken straight from the S accumulators.
+template <int GT>
+__device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                          const int32_t* it, uint8_t* smem, SmemCtl* ctl, PipeState& ps,
+                          const WaitCtx& wc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = it[1], g = it[2], kb = it[4], ke = it[5];
+  const int G = p.G;
+  const int32_t* bt_row = p.block_tables + (size_t)(p.Np + d) * p.maxb;
+  const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
+  const int blk0 = kb / kBlockSize;
+  const int nmine = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* ring = smem + warp * kDecodeSlots * kSmemDecodeSlot;
+  const uint32_t ring_s = smem_u32(ring);
+  const int hr = lane >> 2, qd = lane & 3;  // fragment row (query head) and quad lane
+
+  // A fragments of Q: row hr = head g*G + hr (rows >= G and rows 8..15 are zero)
+  uint32_t qa0[8], qa2[8];
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) qa0[ks] = qa2[ks] = 0u;
+  if (hr < G) {
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(
+        p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + hr) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa0[ks] = qw[ks * 8 + qd];
+      qa2[ks] = qw[ks * 8 + qd + 4];
+    }
+  }
+  float o[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m = -INFINITY, l = 0.f;
+
+  auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
+    const int slot = i & 1;
+    int phys = bt_row[blk0 + warp + i * kWarps];
+    if (phys < 0 || phys >= p.num_blocks) {
+      record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+      phys = 0;
+    }
+    const int y = (phys * p.Hkv + g) * kBlockSize;
+    const uint32_t bar = smem_u32(&ctl->dslot[warp][slot]);
+    const uint32_t dst = ring_s + slot * kSmemDecodeSlot;
+    mbar_arrive_expect_tx(bar, kSmemDecodeSlot);
+    tma_load_2d(dst, tmk, bar, 0, y);
+    tma_load_2d(dst + 2048, tmk, bar, 64, y);
+    tma_load_2d(dst + 4096, tmv, bar, 0, y);
+    tma_load_2d(dst + 6144, tmv, bar, 64, y);
+  };
+  if (lane == 0) {
+    if (nmine > 0) issue(0);
+    if (nmine > 1) issue(1);
+  }
+  bool ok = true;
+  const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+  for (int i = 0; i < nmine; ++i) {
+    const int slot = i & 1;
+    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc)) {
+      ok = false;
+      break;
+    }
+    ps.dphase ^= 1u << slot;
+    const int key0 = kb + (warp + i * kWarps) * kBlockSize;
+    const int nv = min(kBlockSize, ke - key0);
+    const uint32_t Ks = ring_s + slot * kSmemDecodeSlot, Vs = Ks + 4096;
+    if (nv < kBlockSize) {
+      // rows past the sequence end may hold anything (even NaN): zero those V rows, since
+      // their weight 0 times NaN would not be 0
+      uint8_t* vb = ring + slot * kSmemDecodeSlot + 4096;
+      for (int c = lane; c < (kBlockSize - nv) * 16; c += 32) {
+        const int r = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+        *reinterpret_cast<uint4*>(vb + half * 2048 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    // S = Q Kᵀ: keys 0-7 in s0, keys 8-15 in s1
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int key = (mi >> 1) * 8 + mr, ch = (ks & 3) * 2 + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(Ks + (ks >> 2) * 2048 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+      const uint32_t a[4] = {qa0[ks], 0u, qa2[ks], 0u};
+      mma_16816(s0, a, b0, b1);
+      mma_16816(s1, a, b2, b3);
+    }
+    // this lane's scores: keys 2qd, 2qd+1, 8+2qd, 9+2qd of row hr
+    float x[4] = {s0[0], s0[1], s1[0], s1[1]};
+    const int kx[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = kx[e] < nv ? x[e] * p.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, x[e]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const bool resc = m_new > m + 8.f;  // lazy rescale, as in the prefill tiles
+    float alpha = 1.f;
+    if (resc) {
+      alpha = ex2(m - m_new);
+      m = m_new;
+    }
+    if (__any_sync(0xffffffffu, resc)) {
+      l *= alpha;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        o[nt][0] *= alpha;
+        o[nt][1] *= alpha;
+      }
+    }
+    const float mref = m == -INFINITY ? 0.f : m;
+    float pr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pr[e] = ex2(x[e] - mref);
+      l += pr[e];
+    }
+    const uint32_t pa[4] = {pack_bf16x2(pr[0], pr[1]), 0u, pack_bf16x2(pr[2], pr[3]), 0u};
+    // O += P V: V tiles of 16 keys x 16 dims per ldmatrix (transposed into B fragments)
+#pragma unroll
+    for (int dp = 0; dp < 8; ++dp) {
+      const int key = (mi & 1) * 8 + mr, ch = (dp & 3) * 2 + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(Vs + (dp >> 2) * 2048 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+      mma_16816(o[2 * dp], pa, b0, b1);
+      mma_16816(o[2 * dp + 1], pa, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0 && i + 2 < nmine) issue(i + 2);
+  }
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+
   __syncthreads();
+  float* scr = reinterpret_cast<float*>(smem);  // [kWarps][GT][kScr]
+  if (ok && hr < G) {
+    float* dst = scr + (warp * GT + hr) * kScr;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+      *reinterpret_cast<float2*>(dst + nt * 8 + 2 * qd) = make_float2(o[nt][0], o[nt][1]);
+    if (qd == 0) {
+      dst[kHeadDim] = m;
+      dst[kHeadDim + 1] = l;
+    }
+  }
+  return ok;
+}
+
+// Combine the warps' states of a decode item, then write the output or the split's partial and,
+// for the last split of a unit to arrive, merge all partials.
+template <int GT>
+__device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                            const int32_t* it, uint8_t* smem, SmemCtl* ctl, PipeState& ps,
+                            const WaitCtx& wc) {
+  const int d = it[1], g = it[2], unit = it[6], split = it[7];
+  const int G = p.G;
+  if constexpr (GT == 1)
+    decode_simt<GT>(p, it, smem, ctl, ps, wc);
+  else
+    decode_tc<GT>(p, tmk, tmv, it, smem, ctl, ps, wc);
+  __syncthreads();
+  const float* scr = reinterpret_cast<const float*>(smem);
   if (!ctl->abort) {
     const int nsplit = unit >= 0 ? p.units[unit * kUnitWords + 0] : 1;
     const int slot0 = unit >= 0 ? p.units[unit * kUnitWords + 1] : 0;
@@ -694,8 +913,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) {
     mbar_init(smem_u32(&ctl->q_full), 1);
     for (int i = 0; i < kKvStages; ++i) {
-      mbar_init(smem_u32(&ctl->kv_full[i]), 1);
-      mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
+      mbar_init(smem_u32(&ctl->k_full[i]), 1);
+      mbar_init(smem_u32(&ctl->k_empty[i]), 1);
+      mbar_init(smem_u32(&ctl->v_full[i]), 1);
+      mbar_init(smem_u32(&ctl->v_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
@@ -733,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (kind == 0)
       prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
     else
-      decode_item<GT>(p, p.items_d + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+      decode_item<GT>(p, &tmk, &tmv, p.items_d + (size_t)idx * kItemWords, smem, ctl, ps, wc);
     if (tid == 0) {
       if (p.records != nullptr) {
         pod_attn_item_record* rec = p.records + (kind == 0 ? idx : p.n_items_p + idx);
@@ -1050,20 +1271,19 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
     return POD_ATTN_ERR_INVALID_ARG;
   CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
   const int64_t pool_rows = (int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize;
-  if (n_p > 0) {
-    if (cs->kq != q_prefill) {
-      if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens))
-        return POD_ATTN_ERR_CUDA;
-      cs->kq = q_prefill;
-    }
-    if (cs->kk != k_pool) {
-      if (!encode_pool(&cs->tmk, k_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
-      cs->kk = k_pool;
-    }
-    if (cs->kv != v_pool) {
-      if (!encode_pool(&cs->tmv, v_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
-      cs->kv = v_pool;
-    }
+  if (n_p > 0 && cs->kq != q_prefill) {
+    if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens))
+      return POD_ATTN_ERR_CUDA;
+    cs->kq = q_prefill;
+  }
+  // the pools' maps serve the prefill tiles and the grouped-query decode path
+  if (cs->kk != k_pool) {
+    if (!encode_pool(&cs->tmk, k_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
+    cs->kk = k_pool;
+  }
+  if (cs->kv != v_pool) {
+    if (!encode_pool(&cs->tmv, v_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
+    cs->kv = v_pool;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const WorkspaceLayout& w = plan->ws;

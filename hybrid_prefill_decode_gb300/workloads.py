@@ -255,10 +255,19 @@ class TraceStep:
     q_lens: List[int]
     prefill_kv_lens: List[int]
     decode_kv_lens: List[int]
+    prefill_rids: List[int] = field(default_factory=list)   # request of each prompt chunk
+    decode_rids: List[int] = field(default_factory=list)    # request of each decode
+
+
+@dataclass
+class Trace:
+    mix: str
+    steps: List[TraceStep]
+    max_rows: List[int]          # per request id: the most cached rows it ever reaches
 
 
 def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
-          decode_targets=(19, 38, 56, 75)) -> List[TraceStep]:
+          decode_targets=(19, 38, 56, 75)) -> Trace:
     """Iteration shapes of mix 'a' (decode-heavy) or 'b' (prefill-heavy).
 
     (a) prompts log-uniform in [4096, 32768], outputs geometric with mean 256;
@@ -268,6 +277,7 @@ def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
     (19, 38, 56, 75 sequences -> 152, 304, 448, 600 decode (seq, kv-head) units for 8 KV heads:
     just above multiples of the SM count). A finished decode is replaced by a request whose
     prompt is already cached (a warm request); prompt chunks come from a FIFO of new requests.
+    Every request has an id; `max_rows[id]` sizes its blocks in a persistent pool.
     """
     assert mix in ("a", "b")
     rng = random.Random(seed * 31 + (1 if mix == "a" else 2))
@@ -286,33 +296,100 @@ def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
             n += 1
         return n
 
-    decodes = []    # [context length, tokens left]
-    fifo = []       # [prompt length, rows already prefilled]
+    max_rows: List[int] = []
+    decodes = []    # [request id, context length, tokens left]
+    fifo = []       # [request id, prompt length, rows already prefilled]
     steps = []
     for it in range(iters):
         target = decode_targets[(it * len(decode_targets)) // iters]
-        decodes = [d for d in decodes if d[1] > 0]
+        decodes = [d for d in decodes if d[2] > 0]
         while len(decodes) < target:
-            decodes.append([prompt_len(), out_len()])
+            n, o = prompt_len(), out_len()
+            decodes.append([len(max_rows), n, o])
+            max_rows.append(n + o)
         while len(fifo) < 4:
-            fifo.append([prompt_len(), 0])
-        dec_lens = []
+            n = prompt_len()
+            fifo.append([len(max_rows), n, 0])
+            max_rows.append(n)
+        dec_lens, dec_ids = [], []
         for d in decodes:
-            d[0] += 1                     # the new token's K/V is appended before attention
-            d[1] -= 1
-            dec_lens.append(d[0])
+            d[1] += 1                     # the new token's K/V is appended before attention
+            d[2] -= 1
+            dec_lens.append(d[1])
+            dec_ids.append(d[0])
         left = budget - len(dec_lens)
-        ql, pkv = [], []
+        ql, pkv, pids = [], [], []
         for r in fifo:
             if left <= 0:
                 break
-            c = min(left, r[0] - r[1])
+            c = min(left, r[1] - r[2])
             if c <= 0:
                 continue
             ql.append(c)
-            pkv.append(r[1] + c)
-            r[1] += c
+            pkv.append(r[2] + c)
+            pids.append(r[0])
+            r[2] += c
             left -= c
-        fifo = [r for r in fifo if r[1] < r[0]]
-        steps.append(TraceStep(ql, pkv, dec_lens))
-    return steps
+        fifo = [r for r in fifo if r[2] < r[1]]
+        steps.append(TraceStep(ql, pkv, dec_lens, pids, dec_ids))
+    return Trace(mix, steps, max_rows)
+
+
+class TracePool:
+    """One persistent paged K/V pool holding every request of a trace (Llama-3-8B shape:
+    32 query / 8 KV heads), and the per-iteration batches over it.
+
+    Each request owns ceil(max_rows/16) physical blocks taken in order from a random permutation
+    of the pool; K and V are seeded N(0,1) bf16 (generated once on `device`). An iteration's
+    batch references the pool's tensors (no copy) and adds its own block tables, lengths and
+    seeded queries."""
+
+    def __init__(self, tr: Trace, seed: int = 5, device="cpu", num_q_heads: int = 32,
+                 num_kv_heads: int = 8):
+        self.trace = tr
+        self.Hq, self.Hkv = num_q_heads, num_kv_heads
+        self.seed = seed
+        self.device = torch.device(device)
+        need = [_blocks(n) for n in tr.max_rows]
+        nb = sum(need)
+        g_cpu = torch.Generator().manual_seed(seed * 1_000_003 + 101)
+        perm = torch.randperm(nb, generator=g_cpu)
+        self.blocks = []
+        pos = 0
+        for n in need:
+            self.blocks.append(perm[pos:pos + n].to(torch.int32))
+            pos += n
+        self.max_blocks = max(need)
+        g = torch.Generator(device=self.device).manual_seed(seed * 1_000_003 + 103)
+        shape = (nb, num_kv_heads, BLOCK_SIZE, HEAD_DIM)
+        self.k_pool = torch.randn(*shape, generator=g, device=self.device).to(torch.bfloat16)
+        self.v_pool = torch.randn(*shape, generator=g, device=self.device).to(torch.bfloat16)
+
+    def batch(self, i: int) -> HybridBatch:
+        st = self.trace.steps[i]
+        rids = st.prefill_rids + st.decode_rids
+        lens = st.prefill_kv_lens + st.decode_kv_lens
+        maxb = max([1] + [_blocks(L) for L in lens])
+        bt = torch.zeros((max(1, len(rids)), maxb), dtype=torch.int32)
+        for r, (rid, L) in enumerate(zip(rids, lens)):
+            n = _blocks(L)
+            bt[r, :n] = self.blocks[rid][:n]
+        if not rids:
+            bt = bt[:0]
+        g = torch.Generator(device=self.device).manual_seed(self.seed * 7919 + i)
+        tp = sum(st.q_lens)
+        q_p = torch.randn(tp, self.Hq, HEAD_DIM, generator=g, device=self.device).to(torch.bfloat16)
+        q_d = torch.randn(len(st.decode_kv_lens), self.Hq, HEAD_DIM, generator=g,
+                          device=self.device).to(torch.bfloat16)
+        cu = [0]
+        for n in st.q_lens:
+            cu.append(cu[-1] + n)
+        return HybridBatch(
+            num_q_heads=self.Hq, num_kv_heads=self.Hkv, head_dim=HEAD_DIM, block_size=BLOCK_SIZE,
+            q_lens=list(st.q_lens), prefill_kv_lens=list(st.prefill_kv_lens),
+            decode_kv_lens=list(st.decode_kv_lens), scale=1.0 / math.sqrt(HEAD_DIM),
+            q_prefill=q_p, q_decode=q_d, k_pool=self.k_pool, v_pool=self.v_pool,
+            block_tables=bt.to(self.device),
+            cu_seqlens_q=torch.tensor(cu, dtype=torch.int32, device=self.device),
+            kv_lens=torch.tensor(lens, dtype=torch.int32, device=self.device), seed=self.seed,
+            name=f"trace {self.trace.mix} iteration {i}")

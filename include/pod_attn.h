@@ -90,7 +90,7 @@ typedef struct {
   int32_t num_decode_seqs;     /* Nd >= 0 */
   int32_t num_blocks;          /* physical blocks in each of k_pool and v_pool */
   int32_t max_blocks_per_seq;  /* row length of block_tables */
-  float scale;                 /* softmax scale, typically 1/sqrt(128) */
+  float scale;                 /* softmax scale, finite and > 0; typically 1/sqrt(128) */
 } pod_attn_problem;
 
 /* Planner and launch options. Zero-initialise for defaults. */
@@ -151,7 +151,7 @@ typedef struct {
  * Host only: it touches no device memory. With options->num_sms > 0 it calls no CUDA function
  * except cudaEventCreate (whose failure is tolerated; the STREAMS variant then reports
  * POD_ATTN_ERR_CUDA at run time).
- * Errors: INVALID_ARG (nulls, kv_len < q_len, q_len < 1, decode kv_len < 1, kv_len beyond
+ * Errors: INVALID_ARG (nulls, scale not finite or not > 0, kv_len < q_len, q_len < 1, decode kv_len < 1, kv_len beyond
  * max_blocks_per_seq*16, cu_seqlens not starting at 0 or not non-decreasing, token total
  * mismatch), UNSUPPORTED (head_dim, block size, group size), CUDA (num_sms == 0 and no device). */
 pod_attn_status pod_attn_plan(const pod_attn_problem* problem, const int32_t* h_cu_seqlens_q,

@@ -58,6 +58,9 @@ def test_plan_validation(lib):
     assert _plan_code(kv=(9, 0)) == B.ERR_INVALID_ARG             # decode kv_len 0
     assert _plan_code(kv=(9, 65)) == B.ERR_INVALID_ARG            # beyond max_blocks_per_seq*16
     assert _plan_code(variant=7) == B.ERR_INVALID_ARG
+    assert _plan_code(scale=0.0) == B.ERR_INVALID_ARG               # scale must be > 0
+    assert _plan_code(scale=-0.1) == B.ERR_INVALID_ARG
+    assert _plan_code(scale=float("inf")) == B.ERR_INVALID_ARG
     assert _plan_code(cu=(), kv=(), nd=0) == B.OK                  # empty batch is legal
     assert _plan_code(cu=(), kv=(3,), nd=1) == B.OK                # decode only
     assert _plan_code(cu=(0, 5), kv=(9,), nd=0) == B.OK            # prefill only

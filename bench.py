@@ -49,6 +49,14 @@ def _workload_name(cfg, batch) -> str:
     return name + ", head_dim 128, paged block 16, bf16"
 
 
+def _config_dict(args, batch, world):
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": _workload_name(args.case or args.config, batch),
+            "config_index": args.case or args.config,
+            "l2": "flushed between steps (256 MiB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
 def _make_batch(args, device):
     from hybrid_prefill_decode_gb300 import workloads as W
     if args.case:
@@ -194,8 +202,7 @@ def run_reference(args, rank, world):
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": _workload_name(args.case or args.config, batch),
-                      "config_index": args.case or args.config},
+           "config": _config_dict(args, batch, world),
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
                             "kind": "oracle", "sample": vals[0]["sample"]},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -215,6 +222,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default=None, help="profile mode: run only this variant, no extras")
+    ap.add_argument("--trace", default=None, choices=["a", "b"],
+                    help="the 200-iteration hybrid-batching trace (mix a or b) instead of --config")
+    ap.add_argument("--trace-iters", type=int, default=200)
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -240,6 +250,9 @@ def main():
     B.load()
 
     dev = torch.device(f"cuda:{local}")
+    if args.trace:
+        run_trace(args, dev, B, R, W, rank, world, dist)
+        return
     batch = _make_batch(args, dev)
     work = R.batch_work(batch.num_q_heads, batch.num_kv_heads, batch.q_lens,
                         batch.prefill_kv_lens, batch.decode_kv_lens)
@@ -387,10 +400,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us["fused"] / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": _workload_name(args.case or args.config, batch),
-                   "config_index": args.case or args.config,
-                   "l2": "flushed between steps (256 MiB write)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "config": _config_dict(args, batch, world),
         "median_us": med["fused"],
         "hybrid_roofline": {"t_star_us": tstar * 1e6, "frac_of_t_star": tstar / t_fused,
                             "bytes": work.bytes, "prefill_flops": work.prefill_flops,
@@ -416,6 +426,73 @@ def main():
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def run_trace(args, dev, B, R, W, rank, world, dist):
+    """Configuration 5: every iteration of a seeded hybrid-batching trace is one step. The plan
+    and upload of each iteration happen before its timed events (they are host work of the
+    serving loop); the events time pod_attn_run. Reports mean/p50/p99 us/iter per variant and
+    the sum of measured times over the sum of per-iteration hybrid rooflines."""
+    import torch
+    hbm, tf_burst, _, _ = _peaks()
+    tr = W.trace(args.trace, iters=args.trace_iters)
+    pool = W.TracePool(tr, device=dev)
+    batches = [pool.batch(i) for i in range(len(tr.steps))]
+    variants = ["fused", "serial", "streams"]
+    plans = {v: [B.Plan.for_batch(b, variant=v) for b in batches] for v in variants}
+    wsb = max(pl.workspace_bytes for v in variants for pl in plans[v])
+    ws = {v: torch.empty(max(256, wsb), dtype=torch.uint8, device=dev) for v in variants}
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    outs = [(torch.empty_like(b.q_prefill), torch.empty_like(b.q_decode)) for b in batches]
+    tstar = [R.batch_work(b.num_q_heads, b.num_kv_heads, b.q_lens, b.prefill_kv_lens,
+                          b.decode_kv_lens).t_star(hbm, tf_burst) * 1e6 for b in batches]
+    times = {}
+    for v in variants:
+        for i in range(min(args.warmup, len(batches))):            # warm-up iterations
+            plans[v][i].upload(ws[v], stream)
+            B.run_batch(plans[v][i], batches[i], ws[v], *outs[i], stream=stream, stream2=side)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in batches]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i, b in enumerate(batches):
+            plans[v][i].upload(ws[v], stream)
+            flush.fill_(1)
+            evs[i][0].record(stream)
+            B.run_batch(plans[v][i], b, ws[v], *outs[i], stream=stream, stream2=side)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        times[v] = [a.elapsed_time(e) * 1e3 for a, e in evs]
+        assert plans[v][-1].device_status(ws[v]) == B.OK, v
+    if rank != 0:
+        return
+
+    def stats(xs):
+        xs = sorted(xs)
+        return {"mean": statistics.mean(xs), "p50": xs[len(xs) // 2],
+                "p99": xs[min(len(xs) - 1, int(round(0.99 * (len(xs) - 1))))]}
+
+    f = stats(times["fused"])
+    out = {"metric": METRIC, "value": f["mean"], "unit": UNIT, "n_gpus": world,
+           "steps": len(batches), "warmup": args.warmup, "ms_per_step": f["mean"] / 1e3,
+           "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic",
+           "config": {"workload": f"hybrid-batching trace mix {args.trace}: Llama-3-8B attention "
+                                  f"(32/8, head_dim 128, paged block 16), 2048-token budget, "
+                                  f"decodes first, {len(batches)} iterations",
+                      "l2": "flushed between steps (256 MiB write)"},
+           "fused": f, "serial": stats(times["serial"]), "streams": stats(times["streams"]),
+           "sum_measured_over_sum_tstar": sum(times["fused"]) / sum(tstar),
+           "frac_of_t_star": sum(tstar) / sum(times["fused"]),
+           "speedup_vs_serial": sum(times["serial"]) / sum(times["fused"]),
+           "speedup_vs_streams": sum(times["streams"]) / sum(times["fused"]),
+           "mean_t_star_us": statistics.mean(tstar),
+           "pool_gb": pool.k_pool.numel() * 4 / 1e9}
+    print(json.dumps(out), flush=True)
 
 
 def _traffic_from_profiles(cfg):

@@ -38,6 +38,9 @@ namespace pod {
 using namespace ptx;
 
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: no healthy wait comes close
+// Longest hardware sleep of one poll for roles off the softmax's critical path; a completed
+// phase wakes the thread earlier.
+constexpr uint32_t kSleepNs = 20000;
 
 struct Params {
   const uint16_t* q_prefill;
@@ -76,7 +79,7 @@ struct SmemCtl {
   uint64_t v_empty[kKvStages];
   uint64_t s_full[2];
   uint64_t p_ready[2];
-  uint64_t o_done;
+  uint64_t pv_done[2];  // P·V of the tile held in S buffer b has completed
   uint64_t dslot[kWarps][kDecodeSlots];
   uint32_t tmem_base;
   int abort;
@@ -88,7 +91,7 @@ static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 
 // Pipeline positions; each role advances the fields it owns, across items.
 struct PipeState {
-  uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, o_cnt = 0;
+  uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0;
   uint32_t dphase = 0;  // decode ring: one parity bit per slot
 };
 
@@ -156,7 +159,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const int stage = ps.kv_cnt & 1;
       const uint32_t ph = (ps.kv_cnt >> 1) & 1;
       int okw = 1;
-      if (lane == 0) okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ph ^ 1, wc);
+      if (lane == 0) okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ph ^ 1, wc, kSleepNs);
       if (!__shfl_sync(0xffffffffu, okw, 0)) break;
       if (lane == 0) {
         const uint32_t full = smem_u32(&ctl->k_full[stage]);
@@ -167,7 +170,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           tma_load_2d(sK + b * 2048, tmk, full, 0, y[b]);
           tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y[b]);
         }
-        okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ph ^ 1, wc);
+        okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ph ^ 1, wc, kSleepNs);
       }
       if (!__shfl_sync(0xffffffffu, okw, 0)) break;
       if (lane == 0) {
@@ -185,7 +188,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t tmem = ctl->tmem_base;
-    bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc);
+    bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc, kSleepNs);
     ps.q_cnt++;
     tc_fence_after();
     uint32_t prev_kv = 0, prev_s = 0;
@@ -194,8 +197,8 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     auto issue_pv = [&](int jj, uint32_t kvc, uint32_t scnt) -> bool {
       const uint32_t sb = scnt & 1;
       const int stage = kvc & 1;
-      if (!mbar_wait(smem_u32(&ctl->p_ready[sb]), (scnt >> 1) & 1, wc)) return false;
-      if (!mbar_wait(smem_u32(&ctl->v_full[stage]), (kvc >> 1) & 1, wc)) return false;
+      if (!mbar_wait(smem_u32(&ctl->p_ready[sb]), (scnt >> 1) & 1, wc, kSleepNs)) return false;
+      if (!mbar_wait(smem_u32(&ctl->v_full[stage]), (kvc >> 1) & 1, wc, kSleepNs)) return false;
       const int tile0 = kb + jj * kTileN;
       if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
         // Rows past the sequence end inside its last block may hold anything (even NaN); P is
@@ -220,7 +223,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
           umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (jj == 0 && kk == 0) ? 0u : 1u);
         }
-        umma_commit(smem_u32(&ctl->o_done));
+        umma_commit(smem_u32(&ctl->pv_done[sb]));
         umma_commit(smem_u32(&ctl->v_empty[stage]));
       }
       __syncwarp();
@@ -228,7 +231,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     };
     for (int j = 0; ok && j < ntiles; ++j) {
       const int stage = ps.kv_cnt & 1;
-      if (!mbar_wait(smem_u32(&ctl->k_full[stage]), (ps.kv_cnt >> 1) & 1, wc)) {
+      if (!mbar_wait(smem_u32(&ctl->k_full[stage]), (ps.kv_cnt >> 1) & 1, wc, kSleepNs)) {
         ok = false;
         break;
       }
@@ -278,19 +281,33 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       }
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld32(trow + kTmemS0 + sb * kTileN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(trow + kTmemS0 + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld_wait();
       const int nvis = limit - (kb + j * kTileN);
-      if (!__all_sync(0xffffffffu, nvis >= kTileN)) {  // diagonal or last tile: mask
+      const bool full_tile = __all_sync(0xffffffffu, nvis >= kTileN);
+      // first half of the row; the second half's load overlaps the first half's max
+      tmem_ld32(trow + kTmemS0 + sb * kTileN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld_wait();
+      tmem_ld32(trow + kTmemS0 + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      float mx[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      if (!full_tile) {  // diagonal or last tile: mask
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
           if (c >= nvis) sr[c] = f2u(-INFINITY);
       }
-      float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mt = fmaxf(mt, u2f(sr[c]));
-      mt *= p.scale_log2;  // scale > 0: the max of the scaled scores
+      for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
+      tmem_ld_wait();
+      if (!full_tile) {
+#pragma unroll
+        for (int c = 32; c < 64; ++c)
+          if (c >= nvis) sr[c] = f2u(-INFINITY);
+      }
+#pragma unroll
+      for (int c = 32; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                       p.scale_log2;  // scale > 0: the max of the scaled scores
       // Lazy rescale: keep the old reference max while the new scores exceed it by at most
       // 2^8; exponents stay bounded and O, l remain consistent with the reference max.
       const float m_new = fmaxf(m, mt);
@@ -301,36 +318,41 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         m = m_new;
       }
       const float mref = m == -INFINITY ? 0.f : m;
-      float rs = 0.f;
+      float2 sum[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
       uint32_t pk[32];
+      const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-mref, -mref);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(u2f(sr[2 * c]), p.scale_log2, -mref));
-        const float p1 = ex2(fmaf(u2f(sr[2 * c + 1]), p.scale_log2, -mref));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        const float2 x = ffma2(make_float2(u2f(sr[2 * c]), u2f(sr[2 * c + 1])), c2, nm2);
+        const float2 e = make_float2(ex2(x.x), ex2(x.y));
+        sum[c & 3] = fadd2(sum[c & 3], e);
+        pk[c] = pack_bf16x2(e.x, e.y);
       }
+      const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
+      const float rs = s01.x + s01.y;
       l = l * alpha + rs;
-      if (j > 0) {
-        // O holds PV of the previous tile once that MMA is done; rescale it if any row needs.
-        if (!mbar_wait(smem_u32(&ctl->o_done), ps.o_cnt & 1, wc)) {
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O holds P·V of the previous tiles once the previous tile's MMA is done (the one
+        // before it finished ahead of S_j). At most one completion of that buffer's barrier can
+        // be pending, so waiting on its parity only when a rescale is due stays unambiguous.
+        const uint32_t pn = ps.s_cnt - 1;
+        if (!mbar_wait(smem_u32(&ctl->pv_done[pn & 1]), (pn >> 1) & 1, wc)) {
           ok = false;
           break;
         }
-        ps.o_cnt++;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-          for (int ch = 0; ch < kHeadDim / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(trow + kTmemO + ch * 32, o);
-            tmem_ld_wait();
+        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(trow + kTmemO + ch * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-            tmem_st32(trow + kTmemO + ch * 32, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+          tmem_st32(trow + kTmemO + ch * 32, o);
         }
+        tmem_st_wait();
       }
       tmem_st32(trow + kTmemS0 + sb * kTileN, pk);  // P (bf16 pairs) over S's first 32 columns
       tmem_st_wait();
@@ -338,9 +360,9 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       mbar_arrive(smem_u32(&ctl->p_ready[sb]));
       ps.s_cnt++;
     }
-    if (ok && ntiles > 0) {
-      ok = mbar_wait(smem_u32(&ctl->o_done), ps.o_cnt & 1, wc);
-      ps.o_cnt++;
+    if (ok && ntiles > 0) {  // the last tile's P·V (all earlier ones completed before it)
+      const uint32_t pn = ps.s_cnt - 1;
+      ok = mbar_wait(smem_u32(&ctl->pv_done[pn & 1]), (pn >> 1) & 1, wc);
       tc_fence_after();
     }
     // ------------------------------------------------------------------ epilogue
@@ -538,7 +560,7 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, S
   const int r = lane >> 1;  // the row whose full score this lane holds after the reduction
   for (int i = 0; i < nmine; ++i) {
     const int slot = i & 1;
-    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc)) {
+    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc, kSleepNs)) {
       ok = false;
       break;
     }
@@ -698,7 +720,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
   const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
   for (int i = 0; i < nmine; ++i) {
     const int slot = i & 1;
-    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc)) {
+    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc, kSleepNs)) {
       ok = false;
       break;
     }
@@ -922,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
       mbar_init(smem_u32(&ctl->p_ready[i]), 128);
     }
-    mbar_init(smem_u32(&ctl->o_done), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kDecodeSlots; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);
     ctl->abort = 0;

@@ -220,3 +220,4 @@ def test_workspace_grows_with_instrumentation(lib):
                instrument=True)
     n = a.info()["num_prefill_items"] + a.info()["num_decode_items"]
     assert b.workspace_bytes - a.workspace_bytes >= n * ctypes.sizeof(B.ItemRecord)
+

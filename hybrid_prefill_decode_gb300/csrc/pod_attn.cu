@@ -136,55 +136,68 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       tma_load_3d(sQ, tmq, qbar, 0, h, q0 + t * kTileM);
       tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h, q0 + t * kTileM);
     }
+    // K runs one tile ahead of V: K_j is requested as soon as S_{j-2} has freed its stage,
+    // without waiting behind the V stage that P·V_{j-2} frees later.
     int btv = -1;
-    for (int j = 0; j < ntiles; ++j) {
-      if ((j & 7) == 0) {
-        const int bi = j * 4 + lane;
-        btv = -1;
-        if (bi < nblk_item) {
-          int phys = bt_row[blk0 + bi];
-          if (phys < 0 || phys >= p.num_blocks) {
-            record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
-            phys = 0;
+    int yv[4] = {0, 0, 0, 0};  // rows of the tile whose V is due next
+    const uint32_t base = ps.kv_cnt;
+    for (int j = 0; j <= ntiles; ++j) {
+      int y[4] = {0, 0, 0, 0};
+      if (j < ntiles) {
+        if ((j & 7) == 0) {
+          const int bi = j * 4 + lane;
+          btv = -1;
+          if (bi < nblk_item) {
+            int phys = bt_row[blk0 + bi];
+            if (phys < 0 || phys >= p.num_blocks) {
+              record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+              phys = 0;
+            }
+            btv = phys;
           }
-          btv = phys;
         }
-      }
-      int y[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int e = __shfl_sync(0xffffffffu, btv, (j & 7) * 4 + b);
-        y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
-      }
-      const int stage = ps.kv_cnt & 1;
-      const uint32_t ph = (ps.kv_cnt >> 1) & 1;
-      int okw = 1;
-      if (lane == 0) okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ph ^ 1, wc, kSleepNs);
-      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-      if (lane == 0) {
-        const uint32_t full = smem_u32(&ctl->k_full[stage]);
-        const uint32_t sK = sKring + stage * kSmemKTile;
-        mbar_arrive_expect_tx(full, kSmemKTile);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          tma_load_2d(sK + b * 2048, tmk, full, 0, y[b]);
-          tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y[b]);
+          const int e = __shfl_sync(0xffffffffu, btv, (j & 7) * 4 + b);
+          y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
         }
-        okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ph ^ 1, wc, kSleepNs);
-      }
-      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-      if (lane == 0) {
-        const uint32_t full = smem_u32(&ctl->v_full[stage]);
-        const uint32_t sV = sVring + stage * kSmemKTile;
-        mbar_arrive_expect_tx(full, kSmemKTile);
+        const uint32_t cnt = base + j;
+        const int stage = cnt & 1;
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ((cnt >> 1) & 1) ^ 1, wc, kSleepNs);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&ctl->k_full[stage]);
+          const uint32_t sK = sKring + stage * kSmemKTile;
+          mbar_arrive_expect_tx(full, kSmemKTile);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          tma_load_2d(sV + b * 2048, tmv, full, 0, y[b]);
-          tma_load_2d(sV + 8192 + b * 2048, tmv, full, 64, y[b]);
+          for (int b = 0; b < 4; ++b) {
+            tma_load_2d(sK + b * 2048, tmk, full, 0, y[b]);
+            tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y[b]);
+          }
         }
       }
-      ps.kv_cnt++;
+      if (j >= 1) {
+        const uint32_t cnt = base + j - 1;
+        const int stage = cnt & 1;
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ((cnt >> 1) & 1) ^ 1, wc, kSleepNs);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&ctl->v_full[stage]);
+          const uint32_t sV = sVring + stage * kSmemKTile;
+          mbar_arrive_expect_tx(full, kSmemKTile);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            tma_load_2d(sV + b * 2048, tmv, full, 0, yv[b]);
+            tma_load_2d(sV + 8192 + b * 2048, tmv, full, 64, yv[b]);
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) yv[b] = y[b];
     }
+    ps.kv_cnt = base + ntiles;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t tmem = ctl->tmem_base;

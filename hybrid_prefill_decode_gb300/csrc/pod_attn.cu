@@ -73,10 +73,10 @@ struct Params {
 
 struct SmemCtl {
   uint64_t q_full;
-  uint64_t k_full[kKvStages];
-  uint64_t k_empty[kKvStages];
-  uint64_t v_full[kKvStages];
-  uint64_t v_empty[kKvStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t p_ready[2];
   uint64_t pv_done[2];  // P·V of the tile held in S buffer b has completed
@@ -119,9 +119,9 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sKV = sQ + kSmemQ;
 
-  // K and V tiles live in separate two-stage rings with their own full/empty barriers: a K
-  // stage is released as soon as its S = Q·Kᵀ has run, a V stage after its P·V.
-  const uint32_t sKring = sKV, sVring = sKV + kKvStages * kSmemKTile;
+  // K and V tiles live in separate rings (3 K stages, 2 V stages) with their own full/empty
+  // barriers: a K stage is released as soon as its S = Q·Kᵀ has run, a V stage after its P·V.
+  const uint32_t sKring = sKV, sVring = sKV + kKStages * kSmemKTile;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (warp)
@@ -162,9 +162,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
         }
         const uint32_t cnt = base + j;
-        const int stage = cnt & 1;
+        const int stage = cnt % kKStages;
         int okw = 1;
-        if (lane == 0) okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ((cnt >> 1) & 1) ^ 1, wc, kSleepNs);
+        if (lane == 0)
+          okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ((cnt / kKStages) & 1) ^ 1, wc, kSleepNs);
         if (!__shfl_sync(0xffffffffu, okw, 0)) break;
         if (lane == 0) {
           const uint32_t full = smem_u32(&ctl->k_full[stage]);
@@ -179,9 +180,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       }
       if (j >= 1) {
         const uint32_t cnt = base + j - 1;
-        const int stage = cnt & 1;
+        const int stage = cnt % kVStages;
         int okw = 1;
-        if (lane == 0) okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ((cnt >> 1) & 1) ^ 1, wc, kSleepNs);
+        if (lane == 0)
+          okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ((cnt / kVStages) & 1) ^ 1, wc, kSleepNs);
         if (!__shfl_sync(0xffffffffu, okw, 0)) break;
         if (lane == 0) {
           const uint32_t full = smem_u32(&ctl->v_full[stage]);
@@ -209,9 +211,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     // O += P_jj · V_jj, once the softmax has written P_jj and V_jj has landed
     auto issue_pv = [&](int jj, uint32_t kvc, uint32_t scnt) -> bool {
       const uint32_t sb = scnt & 1;
-      const int stage = kvc & 1;
+      const int stage = kvc % kVStages;
       if (!mbar_wait(smem_u32(&ctl->p_ready[sb]), (scnt >> 1) & 1, wc, kSleepNs)) return false;
-      if (!mbar_wait(smem_u32(&ctl->v_full[stage]), (kvc >> 1) & 1, wc, kSleepNs)) return false;
+      if (!mbar_wait(smem_u32(&ctl->v_full[stage]), (kvc / kVStages) & 1, wc, kSleepNs))
+        return false;
       const int tile0 = kb + jj * kTileN;
       if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
         // Rows past the sequence end inside its last block may hold anything (even NaN); P is
@@ -243,8 +246,8 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       return true;
     };
     for (int j = 0; ok && j < ntiles; ++j) {
-      const int stage = ps.kv_cnt & 1;
-      if (!mbar_wait(smem_u32(&ctl->k_full[stage]), (ps.kv_cnt >> 1) & 1, wc, kSleepNs)) {
+      const int stage = ps.kv_cnt % kKStages;
+      if (!mbar_wait(smem_u32(&ctl->k_full[stage]), (ps.kv_cnt / kKStages) & 1, wc, kSleepNs)) {
         ok = false;
         break;
       }
@@ -530,7 +533,7 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, S
   const int blk0 = kb / kBlockSize;
   const int nmine = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
   uint8_t* ring = smem + warp * kDecodeSlots * kSmemDecodeSlot;
-  float* ps_x = reinterpret_cast<float*>(smem + kSmemUnion) + warp * kMaxGroup * kBlockSize;
+  float* ps_x = reinterpret_cast<float*>(smem + kSmemDecodeRing) + warp * kMaxGroup * kBlockSize;
 
   // q in registers: 4 consecutive dims per lane, premultiplied by scale*log2(e)
   float q[GT][4], o[GT][4], m[GT], ls[GT];
@@ -939,17 +942,22 @@ template <int GT>
 __global__ void __launch_bounds__(kThreads, 2)
     pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemUnion + kSmemScores);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemUnion);
+  if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte-aligned tiles
+    if (threadIdx.x == 0) record_error(p.status, POD_ATTN_ERR_CUDA);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool use_tmem = p.mode != kModeDecodeOnly && p.n_items_p > 0;
 
   if (tid == 0) {
     mbar_init(smem_u32(&ctl->q_full), 1);
-    for (int i = 0; i < kKvStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(smem_u32(&ctl->k_full[i]), 1);
       mbar_init(smem_u32(&ctl->k_empty[i]), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(smem_u32(&ctl->v_full[i]), 1);
       mbar_init(smem_u32(&ctl->v_empty[i]), 1);
     }

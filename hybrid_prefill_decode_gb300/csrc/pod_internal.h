@@ -19,7 +19,8 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 // Prefill tile: 128 query rows x 64 keys per step; QKᵀ and PV on the tcgen05 tensor cores.
 constexpr int kTileM = 128;
 constexpr int kTileN = 64;
-constexpr int kKvStages = 2;
+constexpr int kKStages = 3;             // K tiles in flight (needed first, by S = Q·Kᵀ)
+constexpr int kVStages = 2;             // V tiles in flight (needed a softmax later, by P·V)
 
 // One CTA shape serves both item kinds ("POD-Attention" digest, §"가상 CTA와 SM별 균형": one
 // shared-memory configuration for both operations).
@@ -27,16 +28,19 @@ constexpr int kThreads = 192;           // 6 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp
 
-// Shared-memory map (bytes from a 1024-aligned base).
+// Shared-memory map (bytes from the dynamic shared-memory base, which the hardware places at
+// a 1024-byte boundary; the kernel checks this and reports an error otherwise).
 constexpr int kSmemQ = kTileM * kHeadDim * 2;                  // 32 KiB
-constexpr int kSmemKTile = kTileN * kHeadDim * 2;              // 16 KiB
-constexpr int kSmemStage = 2 * kSmemKTile;                     // K + V tile
-constexpr int kSmemUnion = kSmemQ + kKvStages * kSmemStage;    // 96 KiB
+constexpr int kSmemKTile = kTileN * kHeadDim * 2;              // 16 KiB (K or V tile)
+constexpr int kSmemUnion = kSmemQ + (kKStages + kVStages) * kSmemKTile;  // 112 KiB
 constexpr int kSmemDecodeSlot = 2 * kBlockSize * kHeadDim * 2; // 8 KiB (K block + V block)
-static_assert(kWarps * kDecodeSlots * kSmemDecodeSlot <= kSmemUnion, "decode ring too big");
+constexpr int kSmemDecodeRing = kWarps * kDecodeSlots * kSmemDecodeSlot;  // 96 KiB
 constexpr int kSmemScores = kWarps * kMaxGroup * kBlockSize * 4;   // per-warp p exchange
+static_assert(kSmemDecodeRing + kSmemScores <= kSmemUnion, "decode ring too big");
 constexpr int kSmemBarriers = 256;                                   // mbarriers + scalars
-constexpr int kSmemTotal = 1024 /*alignment slack*/ + kSmemUnion + kSmemScores + kSmemBarriers;
+constexpr int kSmemTotal = kSmemUnion + kSmemBarriers;
+// Two CTAs per SM: 2 x (kSmemTotal + 1 KiB the driver reserves per CTA) <= 228 KiB.
+static_assert(2 * (kSmemTotal + 1024) <= 228 * 1024, "two CTAs per SM must fit");
 
 // TMEM columns per CTA: O (128 fp32 columns) + two S buffers of 64 columns. Two CTAs per SM
 // fit the 512 columns of an SM.

@@ -6,18 +6,20 @@
 // count just above a multiple of what the SMs hold at once costs a whole extra wave.
 //
 // This file turns one hybrid batch into two work lists (virtual CTAs):
-//   prefill item = (chunk s, 128-row query tile t, query head h, KV split k)
+//   prefill item = (chunk s, pair t of 128-row query tiles, query head h, KV split k)
 //   decode item  = (sequence d, kv-head g, KV split k)   — one item serves all G query heads
 //                  of the kv-head (GQA grouping, "LLMSO - W4", §"KV 헤드 줄이기")
-// and sizes the persistent grid: num_sms x ctas_per_sm CTAs that pull items from the two lists.
+// and sizes the persistent grid: one CTA per SM, each with a prefill slot and a decode slot
+// that pull items from the two lists.
 //
 // Split planning. Every item gets a cost (decode: 8 per 16-row K/V block, i.e. its bytes in
-// KiB; prefill: 28 per 128x64 tile, its tensor-core time expressed in the same byte-time units
-// at a 6.8 TB/s : 1 PFLOP/s balance). With W the total cost and S the CTA slots, an output whose
-// cost exceeds W / (4 S) is split along the keys ("LLMSO - W4", §"FlashDecoding — decode 단계의
-// 병렬성 확보") into at most 64 (decode) or 8 (prefill) parts of at least 12 blocks / 8 tiles, so
-// no single item can leave a long tail after the others finish. Items are then ordered longest
-// first. All arithmetic is integer, so the plan is reproducible bit for bit.
+// KiB; prefill: 114 per 256x128 step, its tensor-core time expressed in the same byte-time
+// units at a 6.8 TB/s : 1 PFLOP/s balance). With W the total cost and S the item slots, an
+// output whose cost exceeds W / (4 S) is split along the keys ("LLMSO - W4", §"FlashDecoding —
+// decode 단계의 병렬성 확보") into at most 64 (decode) or 8 (prefill) parts of at least
+// 12 blocks / 4 steps, so no single item can leave a long tail after the others finish. Items
+// are then ordered longest first. All arithmetic is integer, so the plan is reproducible bit
+// for bit.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -28,10 +30,10 @@ namespace pod {
 namespace {
 
 constexpr int64_t kDecodeBlockCost = 8;   // 16 rows x (K + V) x 128 x bf16 = 8 KiB
-constexpr int64_t kPrefillTileCost = 28;  // 4*128*64*128 FLOPs at the byte-time balance
+constexpr int64_t kPrefillTileCost = 114;  // 4*256*128*128 FLOPs at the byte-time balance
 constexpr int kMinDecodeBlocksPerSplit = 12;
 constexpr int kMaxDecodeSplits = 64;
-constexpr int kMinPrefillTilesPerSplit = 8;
+constexpr int kMinPrefillTilesPerSplit = 4;
 constexpr int kMaxPrefillSplits = 8;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -80,10 +82,10 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->opt = opt;
   plan->group = G;
   plan->num_sms = num_sms;
-  plan->ctas_per_sm = opt.ctas_per_sm > 0 ? std::min(opt.ctas_per_sm, 2) : 2;
+  plan->ctas_per_sm = 1;  // one CTA per SM holds both slots (and all 512 TMEM columns)
   plan->cu.assign(cu ? cu : nullptr, cu ? cu + Np + 1 : nullptr);
   plan->kv.assign(kv ? kv : nullptr, kv ? kv + Np + Nd : nullptr);
-  const int64_t slots = (int64_t)num_sms * plan->ctas_per_sm;
+  const int64_t slots = (int64_t)num_sms * 2;  // a prefill slot and a decode slot per SM
 
   // ---- enumerate outputs (before splitting) and their costs --------------------------------
   struct PUnit { int s, t, h; int64_t kend; int64_t ntiles; };
@@ -97,8 +99,8 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
     pf += 4.0 * kHeadDim * Hq * (double)(q * P + q * (q + 1) / 2);
     pb += (double)L * row_bytes + 4.0 * q * Hq * kHeadDim;
-    for (int64_t t = 0; t < ceil_div(q, kTileM); ++t) {
-      const int64_t kend = P + std::min(q, (t + 1) * kTileM);
+    for (int64_t t = 0; t < ceil_div(q, kPairM); ++t) {
+      const int64_t kend = P + std::min(q, (t + 1) * kPairM);
       const int64_t nt = ceil_div(kend, kTileN);
       for (int h = 0; h < Hq; ++h) {
         pu.push_back({s, (int)t, h, kend, nt});
@@ -186,11 +188,10 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->num_d_slots = d_slots;
 
   const int n_p = (int)lp.size(), n_d = (int)ld.size();
-  int cap = opt.max_prefill_ctas > 0 ? opt.max_prefill_ctas : (n_p > 0 && n_d > 0 ? 1 : 2);
-  plan->max_prefill_per_sm = std::max(1, std::min(cap, plan->ctas_per_sm));
-  plan->grid_fused = (int)std::min<int64_t>(slots, n_p + n_d);
-  plan->grid_prefill = (int)std::min<int64_t>(slots, n_p);
-  plan->grid_decode = (int)std::min<int64_t>(slots, n_d);
+  plan->max_prefill_per_sm = 1;  // one prefill pipeline per SM
+  plan->grid_fused = (int)std::min<int64_t>(num_sms, n_p + n_d);
+  plan->grid_prefill = (int)std::min<int64_t>(num_sms, n_p);
+  plan->grid_decode = (int)std::min<int64_t>(num_sms, n_d);
 
   // ---- workspace layout --------------------------------------------------------------------
   WorkspaceLayout& w = plan->ws;

@@ -72,27 +72,39 @@ struct Params {
 };
 
 struct SmemCtl {
-  uint64_t q_full;
+  uint64_t q_full;                 // both query tiles of a prefill item landed
   uint64_t k_full[kKStages];
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full[2];
-  uint64_t p_ready[2];
-  uint64_t pv_done[2];  // P·V of the tile held in S buffer b has completed
-  uint64_t dslot[kWarps][kDecodeSlots];
+  uint64_t s_full[2];              // S of query tile A / B computed
+  uint64_t p_ready[2];             // P of tile A / B written (128 arrivals each)
+  uint64_t pv_done[2];             // P·V of tile A / B completed
+  uint64_t dslot[kWarps][kDecodeSlots];  // decode rings, by absolute warp
   uint32_t tmem_base;
   int abort;
-  int item_kind;
-  int item_idx;
-  int merge_last;
+  int item_kind[2];                // per slot: 0 = prefill slot, 1 = decode slot
+  int item_idx[2];
+  int merge_last[2];
 };
 static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 
 // Pipeline positions; each role advances the fields it owns, across items.
 struct PipeState {
-  uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0;
-  uint32_t dphase = 0;  // decode ring: one parity bit per slot
+  uint32_t q_cnt = 0;   // prefill items (query-tile loads)
+  uint32_t kv_cnt = 0;  // 128-key steps loaded (producer) / consumed (MMA issuer)
+  uint32_t t_cnt = 0;   // 128-key steps whose S, P and P·V barriers have turned over
+  uint32_t dphase = 0;  // decode ring: one parity bit per slot of this warp
+};
+
+// Where a decode item runs: `nw` warps from absolute warp `w0` (the decode slot's warps, or the
+// prefill slot's softmax warps when it borrows decode work), their rings and score areas, and
+// the named barrier of the slot that runs it.
+struct DecodeCtx {
+  int w0, nw;
+  uint8_t* ring;        // nw * kDecodeSlots * kSmemDecodeSlot bytes; also the combine scratch
+  float* scores;        // nw * kMaxGroup * kBlockSize floats
+  int bar_id, bar_threads, first_thread, slot;
 };
 
 constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, 0, 0);     // S = Q Kᵀ, both K-major
@@ -105,6 +117,10 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 }
 
 // ============================================================================ prefill item
+// One prefill item: query tiles A = rows 256t..256t+127 and B = rows 256t+128..256t+255 of a
+// chunk, one head, a range of keys in 128-key steps. Both tiles share every K and V tile.
+// Issue order on the tensor cores: S_A(0), S_B(0), then per step j: P·V_A(j), S_A(j+1),
+// P·V_B(j), S_B(j+1) — while one tile's softmax runs, the tensor cores work for the other.
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
                              const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
                              SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
@@ -116,36 +132,39 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   const int L = p.kv_lens[s];
   const int P = L - qlen;  // cached prefix rows before this chunk
   const int ntiles = (ke - kb + kTileN - 1) / kTileN;
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sKV = sQ + kSmemQ;
-
-  // K and V tiles live in separate rings (3 K stages, 2 V stages) with their own full/empty
-  // barriers: a K stage is released as soon as its S = Q·Kᵀ has run, a V stage after its P·V.
-  const uint32_t sKring = sKV, sVring = sKV + kKStages * kSmemKTile;
+  const uint32_t sQ = smem_u32(smem);                 // tile A at sQ, tile B at sQ + kSmemQ
+  const uint32_t sKring = sQ + 2 * kSmemQ;
+  const uint32_t sVring = sKring + kKStages * kSmemKTile;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (warp)
-    // Lane i holds the block-table entry of block i of the next 8 tiles (32 blocks): one
-    // coalesced read instead of a dependent global read per block.
+    // Lane i holds the block-table entry of block i of the next 4 steps (32 blocks): one
+    // coalesced read instead of a dependent global read per block. K runs one step ahead of V.
     const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
     const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
     const int blk0 = kb / kBlockSize;
+    constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
     if (lane == 0) {
       const uint32_t qbar = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qbar, kSmemQ);
-      tma_load_3d(sQ, tmq, qbar, 0, h, q0 + t * kTileM);
-      tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h, q0 + t * kTileM);
+      mbar_arrive_expect_tx(qbar, 2 * kSmemQ);
+      for (int x = 0; x < 2; ++x) {
+        const int row0 = q0 + t * kPairM + x * kTileM;
+        tma_load_3d(sQ + x * kSmemQ, tmq, qbar, 0, h, row0);
+        tma_load_3d(sQ + x * kSmemQ + kSmemQ / 2, tmq, qbar, 64, h, row0);
+      }
     }
-    // K runs one tile ahead of V: K_j is requested as soon as S_{j-2} has freed its stage,
-    // without waiting behind the V stage that P·V_{j-2} frees later.
     int btv = -1;
-    int yv[4] = {0, 0, 0, 0};  // rows of the tile whose V is due next
+    int yv[kBlocksPerTile];
+#pragma unroll
+    for (int b = 0; b < kBlocksPerTile; ++b) yv[b] = 0;
     const uint32_t base = ps.kv_cnt;
     for (int j = 0; j <= ntiles; ++j) {
-      int y[4] = {0, 0, 0, 0};
+      int y[kBlocksPerTile];
+#pragma unroll
+      for (int b = 0; b < kBlocksPerTile; ++b) y[b] = 0;
       if (j < ntiles) {
-        if ((j & 7) == 0) {
-          const int bi = j * 4 + lane;
+        if ((j & 3) == 0) {
+          const int bi = j * kBlocksPerTile + lane;
           btv = -1;
           if (bi < nblk_item) {
             int phys = bt_row[blk0 + bi];
@@ -157,8 +176,8 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           }
         }
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int e = __shfl_sync(0xffffffffu, btv, (j & 7) * 4 + b);
+        for (int b = 0; b < kBlocksPerTile; ++b) {
+          const int e = __shfl_sync(0xffffffffu, btv, (j & 3) * kBlocksPerTile + b);
           y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
         }
         const uint32_t cnt = base + j;
@@ -172,9 +191,9 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           const uint32_t sK = sKring + stage * kSmemKTile;
           mbar_arrive_expect_tx(full, kSmemKTile);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int b = 0; b < kBlocksPerTile; ++b) {
             tma_load_2d(sK + b * 2048, tmk, full, 0, y[b]);
-            tma_load_2d(sK + 8192 + b * 2048, tmk, full, 64, y[b]);
+            tma_load_2d(sK + kSmemKTile / 2 + b * 2048, tmk, full, 64, y[b]);
           }
         }
       }
@@ -190,142 +209,152 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           const uint32_t sV = sVring + stage * kSmemKTile;
           mbar_arrive_expect_tx(full, kSmemKTile);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int b = 0; b < kBlocksPerTile; ++b) {
             tma_load_2d(sV + b * 2048, tmv, full, 0, yv[b]);
-            tma_load_2d(sV + 8192 + b * 2048, tmv, full, 64, yv[b]);
+            tma_load_2d(sV + kSmemKTile / 2 + b * 2048, tmv, full, 64, yv[b]);
           }
         }
       }
 #pragma unroll
-      for (int b = 0; b < 4; ++b) yv[b] = y[b];
+      for (int b = 0; b < kBlocksPerTile; ++b) yv[b] = y[b];
     }
     ps.kv_cnt = base + ntiles;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     const uint32_t tmem = ctl->tmem_base;
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc, kSleepNs);
-    ps.q_cnt++;
     tc_fence_after();
-    uint32_t prev_kv = 0, prev_s = 0;
-    int prev_j = 0;
-    // O += P_jj · V_jj, once the softmax has written P_jj and V_jj has landed
-    auto issue_pv = [&](int jj, uint32_t kvc, uint32_t scnt) -> bool {
-      const uint32_t sb = scnt & 1;
-      const int stage = kvc % kVStages;
-      if (!mbar_wait(smem_u32(&ctl->p_ready[sb]), (scnt >> 1) & 1, wc, kSleepNs)) return false;
-      if (!mbar_wait(smem_u32(&ctl->v_full[stage]), (kvc / kVStages) & 1, wc, kSleepNs))
-        return false;
-      const int tile0 = kb + jj * kTileN;
+    const uint32_t base = ps.kv_cnt;
+    auto issue_s = [&](int x, uint32_t cnt) {  // S_x = Q_x · Kᵀ of step cnt (lane 0 issues)
+      if (lane == 0) {
+        const uint32_t sK = sKring + (cnt % kKStages) * kSmemKTile;
+        const uint32_t sq = sQ + x * kSmemQ;
+        const uint32_t dS = tmem + kTmemS + x * 128;
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sq + half * (kSmemQ / 2) + koff, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + half * (kSmemKTile / 2) + koff, 16, 1024);
+          umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&ctl->s_full[x]));
+        if (x == 1) umma_commit(smem_u32(&ctl->k_empty[cnt % kKStages]));
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int x, int j, uint32_t cnt) {  // O_x += P_x · V of step cnt
+      if (lane == 0) {
+        const uint32_t sV = sVring + (cnt % kVStages) * kSmemKTile;
+        const uint32_t aP = tmem + kTmemS + x * 128;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          // V tile is N-major: 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart
+          const uint64_t bd = sdesc_sw128(sV + kk * 2048, kSmemKTile / 2, 1024);
+          umma_ts(tmem + kTmemO + x * 128, aP + kk * 8, bd, kIdescPV,
+                  (j == 0 && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(smem_u32(&ctl->pv_done[x]));
+        if (x == 1) umma_commit(smem_u32(&ctl->v_empty[cnt % kVStages]));
+      }
+      __syncwarp();
+    };
+    if (ok && ntiles > 0) {
+      ok = mbar_wait(smem_u32(&ctl->k_full[base % kKStages]), (base / kKStages) & 1, wc, kSleepNs);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, base);
+        issue_s(1, base);
+      }
+    }
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const uint32_t cnt = base + j, n = ps.t_cnt + j;
+      // P·V_A(j): P_A written and V_j landed
+      if (!mbar_wait(smem_u32(&ctl->p_ready[0]), n & 1, wc, kSleepNs) ||
+          !mbar_wait(smem_u32(&ctl->v_full[cnt % kVStages]), (cnt / kVStages) & 1, wc, kSleepNs)) {
+        ok = false;
+        break;
+      }
+      const int tile0 = kb + j * kTileN;
       if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
         // Rows past the sequence end inside its last block may hold anything (even NaN); P is
-        // zero there but 0 * NaN is not, so clear those V rows before the PV product.
+        // zero there but 0 * NaN is not, so clear those V rows before the P·V products.
         const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
-        uint8_t* vbase = smem + (sVring - sQ) + stage * kSmemKTile;
+        uint8_t* vbase = smem + (sVring - sQ) + (cnt % kVStages) * kSmemKTile;
         for (int c = lane; c < (r1 - r0) * 16; c += 32) {
           const int r = r0 + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
-          *reinterpret_cast<uint4*>(vbase + half * 8192 + r * 128 + q16 * 16) =
+          *reinterpret_cast<uint4*>(vbase + half * (kSmemKTile / 2) + r * 128 + q16 * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sV = sVring + stage * kSmemKTile;
-        const uint32_t aP = tmem + kTmemS0 + sb * kTileN;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // V tile is N-major: 64-column halves 8 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
-          const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
-          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (jj == 0 && kk == 0) ? 0u : 1u);
+      issue_pv(0, j, cnt);
+      const bool more = j + 1 < ntiles;
+      if (more) {
+        if (!mbar_wait(smem_u32(&ctl->k_full[(cnt + 1) % kKStages]), ((cnt + 1) / kKStages) & 1,
+                       wc, kSleepNs)) {
+          ok = false;
+          break;
         }
-        umma_commit(smem_u32(&ctl->pv_done[sb]));
-        umma_commit(smem_u32(&ctl->v_empty[stage]));
+        tc_fence_after();
+        issue_s(0, cnt + 1);
       }
-      __syncwarp();
-      return true;
-    };
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int stage = ps.kv_cnt % kKStages;
-      if (!mbar_wait(smem_u32(&ctl->k_full[stage]), (ps.kv_cnt / kKStages) & 1, wc, kSleepNs)) {
+      // P·V_B(j)
+      if (!mbar_wait(smem_u32(&ctl->p_ready[1]), n & 1, wc, kSleepNs)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sb = ps.s_cnt & 1;
-      if (lane == 0) {
-        const uint32_t sK = sKring + stage * kSmemKTile;
-        const uint32_t dS = tmem + kTmemS0 + sb * kTileN;
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + half * (kSmemQ / 2) + koff, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + half * (kSmemKTile / 2) + koff, 16, 1024);
-          umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&ctl->s_full[sb]));
-        umma_commit(smem_u32(&ctl->k_empty[stage]));
-      }
-      __syncwarp();
-      if (j > 0 && !issue_pv(prev_j, prev_kv, prev_s)) {
-        ok = false;
-        break;
-      }
-      prev_j = j;
-      prev_kv = ps.kv_cnt;
-      prev_s = ps.s_cnt;
-      ps.kv_cnt++;
-      ps.s_cnt++;
+      issue_pv(1, j, cnt);
+      if (more) issue_s(1, cnt + 1);
     }
-    if (ok && ntiles > 0) issue_pv(prev_j, prev_kv, prev_s);
-  } else {
+    ps.kv_cnt = base + ntiles;
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
     // ------------------------------------------------------------------ softmax (1 row/thread)
+    const int x = (warp - kSoftmaxWarp0) >> 2;  // query tile: 0 = A, 1 = B
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int qi = t * kTileM + row;  // local index of this thread's query in the chunk
+    const uint32_t tS = trow + kTmemS + x * 128, tO = trow + kTmemO + x * 128;
+    const int qi = t * kPairM + x * kTileM + row;  // local index of this thread's query
     const bool valid = qi < qlen;
     const int limit = min(P + qi + 1, ke);  // keys [kb, limit) are visible to this row
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     for (int j = 0; j < ntiles; ++j) {
-      const uint32_t sb = ps.s_cnt & 1;
-      if (!mbar_wait(smem_u32(&ctl->s_full[sb]), (ps.s_cnt >> 1) & 1, wc)) {
+      const uint32_t n = ps.t_cnt + j;
+      if (!mbar_wait(smem_u32(&ctl->s_full[x]), n & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[64];
       const int nvis = limit - (kb + j * kTileN);
       const bool full_tile = __all_sync(0xffffffffu, nvis >= kTileN);
-      // first half of the row; the second half's load overlaps the first half's max
-      tmem_ld32(trow + kTmemS0 + sb * kTileN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld_wait();
-      tmem_ld32(trow + kTmemS0 + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      // pass 1: the row max over the 128 columns, 32 at a time (TMEM reads are cheap)
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-      if (!full_tile) {  // diagonal or last tile: mask
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32];
+        tmem_ld32(tS + ch * 32, sr);
+        tmem_ld_wait();
+        if (!full_tile) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c >= nvis) sr[c] = f2u(-INFINITY);
+          for (int c = 0; c < 32; ++c)
+            if (ch * 32 + c >= nvis) sr[c] = f2u(-INFINITY);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
       }
-#pragma unroll
-      for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
-      tmem_ld_wait();
-      if (!full_tile) {
-#pragma unroll
-        for (int c = 32; c < 64; ++c)
-          if (c >= nvis) sr[c] = f2u(-INFINITY);
-      }
-#pragma unroll
-      for (int c = 32; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
                        p.scale_log2;  // scale > 0: the max of the scaled scores
-      // Lazy rescale: keep the old reference max while the new scores exceed it by at most
-      // 2^8; exponents stay bounded and O, l remain consistent with the reference max.
+      // Lazy rescale: the reference max moves only when a score exceeds it by more than 2^8;
+      // O and l stay consistent with whichever reference is current.
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + 8.f;
       float alpha = 1.f;
@@ -333,28 +362,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         alpha = ex2(m - m_new);
         m = m_new;
       }
-      const float mref = m == -INFINITY ? 0.f : m;
-      float2 sum[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
-      uint32_t pk[32];
-      const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-mref, -mref);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 x = ffma2(make_float2(u2f(sr[2 * c]), u2f(sr[2 * c + 1])), c2, nm2);
-        const float2 e = make_float2(ex2(x.x), ex2(x.y));
-        sum[c & 3] = fadd2(sum[c & 3], e);
-        pk[c] = pack_bf16x2(e.x, e.y);
-      }
-      const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
-      const float rs = s01.x + s01.y;
-      l = l * alpha + rs;
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // O holds P·V of the previous tiles once the previous tile's MMA is done (the one
-        // before it finished ahead of S_j). At most one completion of that buffer's barrier can
-        // be pending, so waiting on its parity only when a rescale is due stays unambiguous.
-        const uint32_t pn = ps.s_cnt - 1;
-        if (!mbar_wait(smem_u32(&ctl->pv_done[pn & 1]), (pn >> 1) & 1, wc)) {
+        // O holds P·V of the earlier steps once step j-1's product completed (the one before
+        // finished ahead of S of step j); at most one completion of that barrier is pending.
+        if (!mbar_wait(smem_u32(&ctl->pv_done[x]), (n - 1) & 1, wc)) {
           ok = false;
           break;
         }
@@ -362,26 +373,53 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
 #pragma unroll 1
         for (int ch = 0; ch < kHeadDim / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(trow + kTmemO + ch * 32, o);
+          tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-          tmem_st32(trow + kTmemO + ch * 32, o);
+          tmem_st32(tO + ch * 32, o);
         }
         tmem_st_wait();
       }
-      tmem_st32(trow + kTmemS0 + sb * kTileN, pk);  // P (bf16 pairs) over S's first 32 columns
+      const float mref = m == -INFINITY ? 0.f : m;
+      const float2 nm2 = make_float2(-mref, -mref);
+      // pass 2: exponentials, row sum, and P (bf16 pairs) written over S's first 64 columns;
+      // chunk ch writes columns 16ch..16ch+15, all of which earlier chunks have already read
+      float2 sum[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32];
+        tmem_ld32(tS + ch * 32, sr);
+        tmem_ld_wait();
+        if (!full_tile) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (ch * 32 + c >= nvis) sr[c] = f2u(-INFINITY);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float2 xv = ffma2(make_float2(u2f(sr[2 * c]), u2f(sr[2 * c + 1])), c2, nm2);
+          const float2 e = make_float2(ex2(xv.x), ex2(xv.y));
+          sum[c & 3] = fadd2(sum[c & 3], e);
+          pk[c] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st16(tS + ch * 16, pk);
+      }
+      const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
+      l = l * alpha + (s01.x + s01.y);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->p_ready[sb]));
-      ps.s_cnt++;
+      mbar_arrive(smem_u32(&ctl->p_ready[x]));
     }
-    if (ok && ntiles > 0) {  // the last tile's P·V (all earlier ones completed before it)
-      const uint32_t pn = ps.s_cnt - 1;
-      ok = mbar_wait(smem_u32(&ctl->pv_done[pn & 1]), (pn >> 1) & 1, wc);
+    if (ok && ntiles > 0) {  // the last step's P·V (all earlier ones completed before it)
+      ok = mbar_wait(smem_u32(&ctl->pv_done[x]), (ps.t_cnt + ntiles - 1) & 1, wc);
       tc_fence_after();
     }
     // ------------------------------------------------------------------ epilogue
+    const int prow = x * kTileM + row;  // row within the pair
     if (ok) {
       if (unit < 0) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -389,7 +427,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
 #pragma unroll 1
         for (int ch = 0; ch < kHeadDim / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(trow + kTmemO + ch * 32, o);
+          tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
           if (valid) {
             uint32_t w[16];
@@ -407,32 +445,32 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
 #pragma unroll 1
         for (int ch = 0; ch < kHeadDim / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(trow + kTmemO + ch * 32, o);
+          tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
-          float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + ch * 32);
+          float4* d4 = reinterpret_cast<float4*>(slot + prow * kHeadDim + ch * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             d4[i] = make_float4(u2f(o[4 * i]), u2f(o[4 * i + 1]), u2f(o[4 * i + 2]), u2f(o[4 * i + 3]));
         }
-        slot[kTileM * kHeadDim + row] = m;
-        slot[kTileM * kHeadDim + kTileM + row] = l;
+        slot[kPairM * kHeadDim + prow] = m;
+        slot[kPairM * kHeadDim + kPairM + prow] = l;
         __threadfence();
-        named_bar_sync(1, 128);
-        if (row == 0) ctl->merge_last = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
-        named_bar_sync(1, 128);
-        if (ctl->merge_last) {
+        named_bar_sync(2, 256);
+        if (prow == 0) ctl->merge_last[0] = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+        named_bar_sync(2, 256);
+        if (ctl->merge_last[0]) {
           __threadfence();
           if (valid) {
             float mx = -INFINITY;
             for (int k = 0; k < nsplit; ++k) {
               const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-              mx = fmaxf(mx, __ldcg(sl + kTileM * kHeadDim + row));
+              mx = fmaxf(mx, __ldcg(sl + kPairM * kHeadDim + prow));
             }
             float den = 0.f;
             for (int k = 0; k < nsplit; ++k) {
               const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-              const float mk = __ldcg(sl + kTileM * kHeadDim + row);
-              if (mk != -INFINITY) den += ex2(mk - mx) * __ldcg(sl + kTileM * kHeadDim + kTileM + row);
+              const float mk = __ldcg(sl + kPairM * kHeadDim + prow);
+              if (mk != -INFINITY) den += ex2(mk - mx) * __ldcg(sl + kPairM * kHeadDim + kPairM + prow);
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
             uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim;
@@ -443,10 +481,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
               for (int c = 0; c < 32; ++c) acc[c] = 0.f;
               for (int k = 0; k < nsplit; ++k) {
                 const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-                const float mk = __ldcg(sl + kTileM * kHeadDim + row);
+                const float mk = __ldcg(sl + kPairM * kHeadDim + prow);
                 if (mk == -INFINITY) continue;
                 const float f = ex2(mk - mx) * inv;
-                const float4* src = reinterpret_cast<const float4*>(sl + row * kHeadDim + ch * 32);
+                const float4* src = reinterpret_cast<const float4*>(sl + prow * kHeadDim + ch * 32);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                   const float4 v = __ldcg(src + c);
@@ -465,13 +503,17 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
                                    pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
             }
           }
-          if (row == 0) p.arrive[unit] = 0;  // ready for the next run
+          if (prow == 0) p.arrive[unit] = 0;  // ready for the next run
         }
       }
     }
     tc_fence_before();
   }
-  __syncthreads();
+  // every thread of the prefill slot keeps the same pipeline positions
+  ps.q_cnt++;
+  ps.t_cnt += ntiles;
+  if (warp != 0 && warp != 1) ps.kv_cnt += ntiles;
+  named_bar_sync(1, kPrefillThreads);
 }
 
 // ============================================================================ decode item
@@ -523,17 +565,19 @@ constexpr int kRow = kHeadDim + 2;  // global partial slot row: o[128], m, l
 // 4 KiB bulk copies; q lives in registers (4 dims per lane); q·k is reduce-scattered across the
 // warp with shuffles. Leaves the warp's (o, m, l) in the shared scratch; returns false on abort.
 template <int GT>
-__device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, SmemCtl* ctl,
-                            PipeState& ps, const WaitCtx& wc) {
+__device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx& dc,
+                            SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wl = warp - dc.w0;  // this warp's index among the item's warps
   const int d = it[1], g = it[2], kb = it[4], ke = it[5];
   const int G = p.G;
   const int32_t* bt_row = p.block_tables + (size_t)(p.Np + d) * p.maxb;
   const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
   const int blk0 = kb / kBlockSize;
-  const int nmine = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
-  uint8_t* ring = smem + warp * kDecodeSlots * kSmemDecodeSlot;
-  float* ps_x = reinterpret_cast<float*>(smem + kSmemDecodeRing) + warp * kMaxGroup * kBlockSize;
+  const bool mine = wl >= 0 && wl < dc.nw;
+  const int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  uint8_t* ring = dc.ring + (mine ? wl : 0) * kDecodeSlots * kSmemDecodeSlot;
+  float* ps_x = dc.scores + (mine ? wl : 0) * kMaxGroup * kBlockSize;
 
   // q in registers: 4 consecutive dims per lane, premultiplied by scale*log2(e)
   float q[GT][4], o[GT][4], m[GT], ls[GT];
@@ -556,7 +600,7 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, S
   const uint64_t pol = policy_evict_first();
   auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
     const int slot = i & 1;
-    int phys = bt_row[blk0 + warp + i * kWarps];
+    int phys = bt_row[blk0 + wl + i * dc.nw];
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
@@ -581,7 +625,7 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, S
       break;
     }
     ps.dphase ^= 1u << slot;
-    const int key0 = kb + (warp + i * kWarps) * kBlockSize;
+    const int key0 = kb + (wl + i * dc.nw) * kBlockSize;
     const int nv = min(kBlockSize, ke - key0);
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(ring + slot * kSmemDecodeSlot);
     const uint16_t* Vs = Ks + kBlockSize * kHeadDim;
@@ -656,13 +700,13 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, S
   }
 
   // ---- leave the warp's partial state (ring memory is free once every warp is done) ----
-  __syncthreads();
-  float* scr = reinterpret_cast<float*>(smem);  // [kWarps][GT][kScr]
-  if (ok) {
+  named_bar_sync(dc.bar_id, dc.bar_threads);
+  float* scr = reinterpret_cast<float*>(dc.ring);  // [nw][GT][kScr]
+  if (ok && mine) {
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
       if (h < G) {
-        float* dst = scr + (warp * GT + h) * kScr;
+        float* dst = scr + (wl * GT + h) * kScr;
         *reinterpret_cast<float4*>(dst + lane * 4) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
         if (lane == 0) {
           dst[kHeadDim] = m[h];
@@ -674,23 +718,26 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, uint8_t* smem, S
   return ok;
 }
 
-// Decode, grouped-query attention (G >= 2 query heads per kv-head): the G heads are the rows of
-// warp-level tensor-core MMAs (m16n8k16, bf16 in, fp32 accumulate). Each warp streams its blocks
-// through TMA (one 16-row x 64-dim box per half, 128-byte swizzle, so ldmatrix reads are free of
-// bank conflicts); per 16-key block: S = Q·Kᵀ (2 x 8 MMAs), a row softmax over 16 keys with quad
-// shuffles, O += P·V (16 MMAs) with P taken straight from the S accumulators.
+// Decode, grouped-query attention (G >= 2 query heads per kv-head): warp-level tensor-core MMAs
+// (m16n8k16, bf16 in, fp32 accumulate). Each warp streams its blocks through TMA (one 16-row x
+// 64-dim box per half, 128-byte swizzle, so ldmatrix reads are free of bank conflicts); per
+// 16-key block: S = Q·Kᵀ with the G heads as rows (2 x 8 MMAs), a row softmax over 16 keys with
+// quad shuffles, then Oᵀ += Vᵀ·Pᵀ (8 MMAs) with the heads as columns, so P goes from the S
+// accumulators straight into the B operand and the accumulator needs only 32 registers.
 template <int GT>
 __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                          const int32_t* it, uint8_t* smem, SmemCtl* ctl, PipeState& ps,
+                          const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl, PipeState& ps,
                           const WaitCtx& wc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wl = warp - dc.w0;  // this warp's index among the item's warps
   const int d = it[1], g = it[2], kb = it[4], ke = it[5];
   const int G = p.G;
   const int32_t* bt_row = p.block_tables + (size_t)(p.Np + d) * p.maxb;
   const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
   const int blk0 = kb / kBlockSize;
-  const int nmine = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
-  uint8_t* ring = smem + warp * kDecodeSlots * kSmemDecodeSlot;
+  const bool mine = wl >= 0 && wl < dc.nw;
+  const int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  uint8_t* ring = dc.ring + (mine ? wl : 0) * kDecodeSlots * kSmemDecodeSlot;
   const uint32_t ring_s = smem_u32(ring);
   const int hr = lane >> 2, qd = lane & 3;  // fragment row (query head) and quad lane
 
@@ -707,14 +754,14 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       qa2[ks] = qw[ks * 8 + qd + 4];
     }
   }
-  float o[16][4];
+  float ot[8][4];  // Oᵀ: dims 16mt + hr (+8) x heads 2qd, 2qd+1
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  for (int mt = 0; mt < 8; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
   float m = -INFINITY, l = 0.f;
 
   auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
     const int slot = i & 1;
-    int phys = bt_row[blk0 + warp + i * kWarps];
+    int phys = bt_row[blk0 + wl + i * dc.nw];
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
@@ -741,7 +788,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       break;
     }
     ps.dphase ^= 1u << slot;
-    const int key0 = kb + (warp + i * kWarps) * kBlockSize;
+    const int key0 = kb + (wl + i * dc.nw) * kBlockSize;
     const int nv = min(kBlockSize, ke - key0);
     const uint32_t Ks = ring_s + slot * kSmemDecodeSlot, Vs = Ks + 4096;
     if (nv < kBlockSize) {
@@ -786,10 +833,15 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
     }
     if (__any_sync(0xffffffffu, resc)) {
       l *= alpha;
+      // Oᵀ columns are heads 2qd and 2qd+1: their factors live in rows (lanes) 8qd and 8qd+4
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * qd);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * qd + 4);
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        o[nt][0] *= alpha;
-        o[nt][1] *= alpha;
+      for (int mt = 0; mt < 8; ++mt) {
+        ot[mt][0] *= a0;
+        ot[mt][1] *= a1;
+        ot[mt][2] *= a0;
+        ot[mt][3] *= a1;
       }
     }
     const float mref = m == -INFINITY ? 0.f : m;
@@ -799,15 +851,16 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       pr[e] = ex2(x[e] - mref);
       l += pr[e];
     }
-    const uint32_t pa[4] = {pack_bf16x2(pr[0], pr[1]), 0u, pack_bf16x2(pr[2], pr[3]), 0u};
-    // O += P V: V tiles of 16 keys x 16 dims per ldmatrix (transposed into B fragments)
+    // Pᵀ as the B operand (keys x heads): exactly this lane's S values, packed
+    const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]), pb1 = pack_bf16x2(pr[2], pr[3]);
+    // Oᵀ += Vᵀ Pᵀ: A = Vᵀ tiles of 16 dims x 16 keys, ldmatrix-transposed from the V slot
 #pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      const int key = (mi & 1) * 8 + mr, ch = (dp & 3) * 2 + (mi >> 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(Vs + (dp >> 2) * 2048 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-      mma_16816(o[2 * dp], pa, b0, b1);
-      mma_16816(o[2 * dp + 1], pa, b2, b3);
+    for (int mt = 0; mt < 8; ++mt) {
+      const int key = (mi >> 1) * 8 + mr, ch = (mt & 3) * 2 + (mi & 1);
+      uint32_t a[4];
+      ldsm_x4_t(Vs + (mt >> 2) * 2048 + key * 128 + ((ch ^ (key & 7)) << 4), a[0], a[1], a[2],
+                a[3]);
+      mma_16816(ot[mt], a, pb0, pb1);
     }
     __syncwarp();
     if (lane == 0 && i + 2 < nmine) issue(i + 2);
@@ -815,14 +868,23 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
 
-  __syncthreads();
-  float* scr = reinterpret_cast<float*>(smem);  // [kWarps][GT][kScr]
-  if (ok && hr < G) {
-    float* dst = scr + (warp * GT + hr) * kScr;
+  named_bar_sync(dc.bar_id, dc.bar_threads);
+  float* scr = reinterpret_cast<float*>(dc.ring);  // [nw][GT][kScr]
+  if (ok && mine) {
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-      *reinterpret_cast<float2*>(dst + nt * 8 + 2 * qd) = make_float2(o[nt][0], o[nt][1]);
-    if (qd == 0) {
+    for (int e = 0; e < 2; ++e) {
+      const int head = 2 * qd + e;
+      if (head < G) {
+        float* dst = scr + (wl * GT + head) * kScr;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          dst[mt * 16 + hr] = ot[mt][e];
+          dst[mt * 16 + hr + 8] = ot[mt][2 + e];
+        }
+      }
+    }
+    if (hr < G && qd == 0) {
+      float* dst = scr + (wl * GT + hr) * kScr;
       dst[kHeadDim] = m;
       dst[kHeadDim + 1] = l;
     }
@@ -834,28 +896,27 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 // for the last split of a unit to arrive, merge all partials.
 template <int GT>
 __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                            const int32_t* it, uint8_t* smem, SmemCtl* ctl, PipeState& ps,
-                            const WaitCtx& wc) {
+                            const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl,
+                            PipeState& ps, const WaitCtx& wc) {
   const int d = it[1], g = it[2], unit = it[6], split = it[7];
   const int G = p.G;
+  const int ltid = threadIdx.x - dc.first_thread;
   if constexpr (GT == 1)
-    decode_simt<GT>(p, it, smem, ctl, ps, wc);
+    decode_simt<GT>(p, it, dc, ctl, ps, wc);
   else
-    decode_tc<GT>(p, tmk, tmv, it, smem, ctl, ps, wc);
-  __syncthreads();
-  const float* scr = reinterpret_cast<const float*>(smem);
+    decode_tc<GT>(p, tmk, tmv, it, dc, ctl, ps, wc);
+  named_bar_sync(dc.bar_id, dc.bar_threads);
+  const float* scr = reinterpret_cast<const float*>(dc.ring);
   if (!ctl->abort) {
     const int nsplit = unit >= 0 ? p.units[unit * kUnitWords + 0] : 1;
     const int slot0 = unit >= 0 ? p.units[unit * kUnitWords + 1] : 0;
     float* slot = unit >= 0 ? p.partial_d + (size_t)(slot0 + split) * decode_slot_floats(G) : nullptr;
-    for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kThreads) {
+    for (int idx = ltid; idx < G * kHeadDim; idx += dc.bar_threads) {
       const int h = idx / kHeadDim, c = idx % kHeadDim;
       float mx = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, scr[(w * GT + h) * kScr + kHeadDim]);
+      for (int w = 0; w < dc.nw; ++w) mx = fmaxf(mx, scr[(w * GT + h) * kScr + kHeadDim]);
       float num = 0.f, den = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < dc.nw; ++w) {
         const float* src = scr + (w * GT + h) * kScr;
         const float mw = src[kHeadDim];
         if (mw == -INFINITY) continue;
@@ -875,12 +936,12 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
     }
     if (unit >= 0) {
       __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) ctl->merge_last = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
-      __syncthreads();
-      if (ctl->merge_last) {
+      named_bar_sync(dc.bar_id, dc.bar_threads);
+      if (ltid == 0) ctl->merge_last[dc.slot] = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+      named_bar_sync(dc.bar_id, dc.bar_threads);
+      if (ctl->merge_last[dc.slot]) {
         __threadfence();
-        for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kThreads) {
+        for (int idx = ltid; idx < G * kHeadDim; idx += dc.bar_threads) {
           const int h = idx / kHeadDim, c = idx % kHeadDim;
           float mx = -INFINITY;
           for (int k = 0; k < nsplit; ++k)
@@ -896,54 +957,54 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
           }
           p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + c] = f2bf(num / den);
         }
-        if (threadIdx.x == 0) p.arrive[unit] = 0;
+        if (ltid == 0) p.arrive[unit] = 0;
       }
     }
   }
-  __syncthreads();
+  named_bar_sync(dc.bar_id, dc.bar_threads);
 }
 
 // ============================================================================ scheduler
-__device__ __forceinline__ void pick_item(const Params& p, int sm, SmemCtl* ctl) {
+// Next item for a slot. The prefill slot takes prefill tickets, and decode tickets once the
+// prefill list is drained (or in a decode-only launch); the decode slot takes decode tickets
+// only. Per-SM counters record how many decode items each SM's prefill slot took over.
+__device__ __forceinline__ void pick_item(const Params& p, int slot, int sm, SmemCtl* ctl) {
   int32_t* cnt = p.counters;
   int kind = -1, idx = 0;
-  if (p.mode == kModePrefillOnly) {
+  const bool may_prefill = slot == 0 && p.mode != kModeDecodeOnly;
+  const bool may_decode = p.mode != kModePrefillOnly;
+  if (may_prefill) {
     const int t = atomicAdd(&cnt[0], 1);
     if (t < p.n_items_p) kind = 0, idx = t;
-  } else if (p.mode == kModeDecodeOnly) {
+  }
+  if (kind < 0 && may_decode) {
     const int t = atomicAdd(&cnt[1], 1);
-    if (t < p.n_items_d) kind = 1, idx = t;
-  } else {
-    int* running = &cnt[kCounterHeader + sm];
-    if (*reinterpret_cast<volatile int*>(&cnt[0]) < p.n_items_p) {
-      if (atomicAdd(running, 1) < p.max_prefill_per_sm) {
-        const int t = atomicAdd(&cnt[0], 1);
-        if (t < p.n_items_p) kind = 0, idx = t;
-      }
-      if (kind < 0) atomicSub(running, 1);
-    }
-    if (kind < 0) {
-      const int t = atomicAdd(&cnt[1], 1);
-      if (t < p.n_items_d) kind = 1, idx = t;
-    }
-    if (kind < 0) {  // decode drained: prefill may take every CTA of the SM
-      const int t = atomicAdd(&cnt[0], 1);
-      if (t < p.n_items_p) {
-        kind = 0, idx = t;
-        atomicAdd(running, 1);
-      }
+    if (t < p.n_items_d) {
+      kind = 1, idx = t;
+      if (slot == 0) atomicAdd(&cnt[kCounterHeader + sm], 1);
     }
   }
-  ctl->item_kind = kind;
-  ctl->item_idx = idx;
+  ctl->item_kind[slot] = kind;
+  ctl->item_idx[slot] = idx;
+}
+
+__device__ __forceinline__ void record_item(const Params& p, int kind, int idx, uint32_t sm_raw,
+                                            uint64_t t0) {
+  pod_attn_item_record* rec = p.records + (kind == 0 ? idx : p.n_items_p + idx);
+  rec->smid = (int32_t)sm_raw;
+  rec->kind = kind;
+  rec->item = idx;
+  rec->cta = blockIdx.x;
+  rec->t_start = t0;
+  rec->t_end = globaltimer();
 }
 
 template <int GT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemUnion);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemCtlOff);
   if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte-aligned tiles
     if (threadIdx.x == 0) record_error(p.status, POD_ATTN_ERR_CUDA);
     return;
@@ -964,17 +1025,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
       mbar_init(smem_u32(&ctl->p_ready[i]), 128);
+      mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kDecodeSlots; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);
     ctl->abort = 0;
     fence_barrier_init();
-    if (use_tmem) {
-      prefetch_tmap(&tmq);
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-    }
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+    if (use_tmem) prefetch_tmap(&tmq);
   }
   if (use_tmem && warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -988,36 +1047,46 @@ __global__ void __launch_bounds__(kThreads, 2)
   PipeState ps;
   const uint32_t sm_raw = smid();
   const int sm = (int)(sm_raw % (uint32_t)p.num_sms);
-  for (;;) {
-    if (tid == 0) pick_item(p, sm, ctl);
-    __syncthreads();
-    const int kind = ctl->item_kind, idx = ctl->item_idx;
-    if (kind < 0 || ctl->abort) break;
-    const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
-    if (kind == 0)
-      prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
-    else
-      decode_item<GT>(p, &tmk, &tmv, p.items_d + (size_t)idx * kItemWords, smem, ctl, ps, wc);
-    if (tid == 0) {
-      if (p.records != nullptr) {
-        pod_attn_item_record* rec = p.records + (kind == 0 ? idx : p.n_items_p + idx);
-        rec->smid = (int32_t)sm_raw;
-        rec->kind = kind;
-        rec->item = idx;
-        rec->cta = blockIdx.x;
-        rec->t_start = t0;
-        rec->t_end = globaltimer();
-      }
-      if (kind == 0 && p.mode == kModeFused) atomicSub(&p.counters[kCounterHeader + sm], 1);
+  if (warp < kDecodeWarp0) {
+    // ------------------------------------------------------------------ prefill slot
+    const DecodeCtx dc{kBorrowWarp0, kBorrowWarps, smem,
+                       reinterpret_cast<float*>(smem + kBorrowWarps * kDecodeSlots * kSmemDecodeSlot),
+                       1, kPrefillThreads, 0, 0};
+    for (;;) {
+      if (tid == 0) pick_item(p, 0, sm, ctl);
+      named_bar_sync(1, kPrefillThreads);
+      const int kind = ctl->item_kind[0], idx = ctl->item_idx[0];
+      if (kind < 0 || ctl->abort) break;
+      const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
+      if (kind == 0)
+        prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+      else
+        decode_item<GT>(p, &tmk, &tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
+      if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
+    }
+  } else {
+    // ------------------------------------------------------------------ decode slot
+    const int first = kDecodeWarp0 * 32;
+    const DecodeCtx dc{kDecodeWarp0, kDecodeWarps, smem + kSmemDecodeOff,
+                       reinterpret_cast<float*>(smem + kSmemScoresOff), 3,
+                       kDecodeWarps * 32, first, 1};
+    for (;;) {
+      if (tid == first) pick_item(p, 1, sm, ctl);
+      named_bar_sync(3, kDecodeWarps * 32);
+      const int kind = ctl->item_kind[1], idx = ctl->item_idx[1];
+      if (kind < 0 || ctl->abort) break;
+      const uint64_t t0 = (p.records != nullptr && tid == first) ? globaltimer() : 0;
+      decode_item<GT>(p, &tmk, &tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
+      if (p.records != nullptr && tid == first) record_item(p, kind, idx, sm_raw, t0);
     }
   }
+  tc_fence_before();
   __syncthreads();
   if (ctl->abort && tid == 0) {
     // give copies still in flight time to land before this CTA's shared memory is released
     const uint64_t t0 = globaltimer();
     while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
   }
-  tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (use_tmem && warp == 1) tmem_dealloc(ctl->tmem_base, kTmemCols);

@@ -16,44 +16,64 @@ constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;          // tokens per paged K/V block
 constexpr int kMaxGroup = 8;            // query heads per KV head handled by the decode path
 
-// Prefill tile: 128 query rows x 64 keys per step; QKᵀ and PV on the tcgen05 tensor cores.
-constexpr int kTileM = 128;
-constexpr int kTileN = 64;
-constexpr int kKStages = 3;             // K tiles in flight (needed first, by S = Q·Kᵀ)
-constexpr int kVStages = 2;             // V tiles in flight (needed a softmax later, by P·V)
-
-// One CTA shape serves both item kinds ("POD-Attention" digest, §"가상 CTA와 SM별 균형": one
-// shared-memory configuration for both operations).
-constexpr int kThreads = 192;           // 6 warps
+// One persistent CTA per SM holds two concurrent virtual-CTA slots ("POD-Attention" digest,
+// §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
+//  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns — warp 0 issues
+//    TMA, warp 1 issues tcgen05 MMAs, warps 4-7 and 8-11 are the softmax warpgroups of two
+//    128-row query tiles that take turns on the tensor cores (warps 2-3 are idle in prefill);
+//  * the decode slot (warps 12-15): decode items, on their own ticket loop.
+// When one kind's queue is empty the prefill slot's warps 4-11 also run decode items.
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kPrefillThreads = 384;    // warps 0-11
+constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (tile A: 4-7, tile B: 8-11)
+constexpr int kDecodeWarp0 = 12;        // decode slot: warps 12-15
+constexpr int kDecodeWarps = 4;
+constexpr int kBorrowWarp0 = 4;         // prefill slot running decode items: warps 4-11
+constexpr int kBorrowWarps = 8;
 constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp
+
+// Prefill step: two 128-row query tiles (same sequence and head, consecutive) x 128 keys.
+constexpr int kTileM = 128;
+constexpr int kPairM = 2 * kTileM;
+constexpr int kTileN = 128;
+// K of step j+1 is requested once both tiles' S of step j are done, and is needed only after
+// tile A's softmax of step j; V of step j+1 is requested once tile B's P·V of step j-1 is done
+// and needed a whole step later — so one K stage and two V stages keep both ahead.
+constexpr int kKStages = 1;
+constexpr int kVStages = 2;
 
 // Shared-memory map (bytes from the dynamic shared-memory base, which the hardware places at
 // a 1024-byte boundary; the kernel checks this and reports an error otherwise).
-constexpr int kSmemQ = kTileM * kHeadDim * 2;                  // 32 KiB
-constexpr int kSmemKTile = kTileN * kHeadDim * 2;              // 16 KiB (K or V tile)
-constexpr int kSmemUnion = kSmemQ + (kKStages + kVStages) * kSmemKTile;  // 112 KiB
-constexpr int kSmemDecodeSlot = 2 * kBlockSize * kHeadDim * 2; // 8 KiB (K block + V block)
-constexpr int kSmemDecodeRing = kWarps * kDecodeSlots * kSmemDecodeSlot;  // 96 KiB
-constexpr int kSmemScores = kWarps * kMaxGroup * kBlockSize * 4;   // per-warp p exchange
-static_assert(kSmemDecodeRing + kSmemScores <= kSmemUnion, "decode ring too big");
-constexpr int kSmemBarriers = 256;                                   // mbarriers + scalars
-constexpr int kSmemTotal = kSmemUnion + kSmemBarriers;
-// Two CTAs per SM: 2 x (kSmemTotal + 1 KiB the driver reserves per CTA) <= 228 KiB.
-static_assert(2 * (kSmemTotal + 1024) <= 228 * 1024, "two CTAs per SM must fit");
+constexpr int kSmemQ = kTileM * kHeadDim * 2;                      // 32 KiB per query tile
+constexpr int kSmemKTile = kTileN * kHeadDim * 2;                  // 32 KiB (K or V tile)
+constexpr int kSmemPrefill = 2 * kSmemQ + (kKStages + kVStages) * kSmemKTile;  // 160 KiB
+constexpr int kSmemDecodeSlot = 2 * kBlockSize * kHeadDim * 2;     // 8 KiB (K block + V block)
+constexpr int kSmemDecodeRing = kDecodeWarps * kDecodeSlots * kSmemDecodeSlot;  // 64 KiB
+constexpr int kSmemScoresPerWarp = kMaxGroup * kBlockSize * 4;     // p exchange of one warp
+constexpr int kSmemDecodeOff = kSmemPrefill;                       // decode slot's region
+constexpr int kSmemScoresOff = kSmemDecodeOff + kSmemDecodeRing;   // its score exchange
+constexpr int kSmemCtlOff = kSmemScoresOff + kDecodeWarps * kSmemScoresPerWarp;
+constexpr int kSmemBarriers = 512;                                  // mbarriers + scalars
+constexpr int kSmemTotal = kSmemCtlOff + kSmemBarriers;
+static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
+// the prefill slot's region also serves as the borrowed decode warps' rings and score areas
+static_assert(kBorrowWarps * (kDecodeSlots * kSmemDecodeSlot + kSmemScoresPerWarp) <=
+                  kSmemPrefill, "borrowed decode rings must fit the prefill region");
 
-// TMEM columns per CTA: O (128 fp32 columns) + two S buffers of 64 columns. Two CTAs per SM
-// fit the 512 columns of an SM.
-constexpr int kTmemCols = 256;
-constexpr int kTmemO = 0;
-constexpr int kTmemS0 = 128;
+// TMEM columns (the whole SM): O of tile A, O of tile B, S of tile A, S of tile B (fp32);
+// P of a tile (bf16 pairs) overwrites the first 64 columns of its S.
+constexpr int kTmemCols = 512;
+constexpr int kTmemO = 0;      // + 128 * tile
+constexpr int kTmemS = 256;    // + 128 * tile
 
 // Work item: kItemWords int32 words.
 //   [0] kind         0 = prefill, 1 = decode
 //   [1] seq          prefill: chunk index s in [0, Np); decode: d in [0, Nd)
-//   [2] tile / kvh   prefill: 128-row query tile index t; decode: kv-head g
+//   [2] tile / kvh   prefill: index t of the pair of 128-row query tiles (rows 256t ..
+//                    256t + 255 of the chunk); decode: kv-head g
 //   [3] head         prefill: query head h; decode: 0
-//   [4] key_begin    first key row of this split (prefill: multiple of 64; decode: of 16)
+//   [4] key_begin    first key row of this split (prefill: multiple of 128; decode: of 16)
 //   [5] key_end      one past the last key row this split may read
 //   [6] unit         -1 = the only split (write the output directly), else the unit index
 //   [7] split        split index within the unit
@@ -63,7 +83,7 @@ constexpr int kItemWords = 8;
 constexpr int kUnitWords = 4;
 
 // Partial-result slots: fp32 o[rows][128] then m[rows] then l[rows] (m, l in log2 units).
-constexpr int kPrefillSlotFloats = kTileM * (kHeadDim + 2);
+constexpr int kPrefillSlotFloats = kPairM * (kHeadDim + 2);
 #ifdef __CUDACC__
 __host__ __device__
 #endif
@@ -71,7 +91,7 @@ inline int decode_slot_floats(int group) { return group * (kHeadDim + 2); }
 
 // Counter block of one launch mode (fused, prefill-only, decode-only), int32 words:
 //   [0] prefill ticket  [1] decode ticket  [2] exited CTAs  [3] unused
-//   [4 .. 4+num_sms)    prefill items running on each SM
+//   [4 .. 4+num_sms)    decode items the prefill slot of each SM has taken (diagnostics)
 constexpr int kCounterHeader = 4;
 
 enum LaunchMode { kModeFused = 0, kModePrefillOnly = 1, kModeDecodeOnly = 2 };

@@ -6,14 +6,14 @@
 // count just above a multiple of what the SMs hold at once costs a whole extra wave.
 //
 // This file turns one hybrid batch into two work lists (virtual CTAs):
-//   prefill item = (chunk s, pair t of 128-row query tiles, query head h, KV split k)
+//   prefill item = (chunk s, 128-row query tile t, query head h, KV split k)
 //   decode item  = (sequence d, kv-head g, KV split k)   — one item serves all G query heads
 //                  of the kv-head (GQA grouping, "LLMSO - W4", §"KV 헤드 줄이기")
 // and sizes the persistent grid: one CTA per SM, each with a prefill slot and a decode slot
 // that pull items from the two lists.
 //
 // Split planning. Every item gets a cost (decode: 8 per 16-row K/V block, i.e. its bytes in
-// KiB; prefill: 114 per 256x128 step, its tensor-core time expressed in the same byte-time
+// KiB; prefill: 57 per 128x128 step, its tensor-core time expressed in the same byte-time
 // units at a 6.8 TB/s : 1 PFLOP/s balance). With W the total cost and S the item slots, an
 // output whose cost exceeds W / (4 S) is split along the keys ("LLMSO - W4", §"FlashDecoding —
 // decode 단계의 병렬성 확보") into at most 64 (decode) or 8 (prefill) parts of at least
@@ -30,7 +30,7 @@ namespace pod {
 namespace {
 
 constexpr int64_t kDecodeBlockCost = 8;   // 16 rows x (K + V) x 128 x bf16 = 8 KiB
-constexpr int64_t kPrefillTileCost = 114;  // 4*256*128*128 FLOPs at the byte-time balance
+constexpr int64_t kPrefillTileCost = 57;  // 4*128*128*128 FLOPs at the byte-time balance
 constexpr int kMinDecodeBlocksPerSplit = 12;
 constexpr int kMaxDecodeSplits = 64;
 constexpr int kMinPrefillTilesPerSplit = 4;
@@ -99,8 +99,8 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
     pf += 4.0 * kHeadDim * Hq * (double)(q * P + q * (q + 1) / 2);
     pb += (double)L * row_bytes + 4.0 * q * Hq * kHeadDim;
-    for (int64_t t = 0; t < ceil_div(q, kPairM); ++t) {
-      const int64_t kend = P + std::min(q, (t + 1) * kPairM);
+    for (int64_t t = 0; t < ceil_div(q, kTileM); ++t) {
+      const int64_t kend = P + std::min(q, (t + 1) * kTileM);
       const int64_t nt = ceil_div(kend, kTileN);
       for (int h = 0; h < Hq; ++h) {
         pu.push_back({s, (int)t, h, kend, nt});

@@ -8,17 +8,17 @@
 //    through the paged block table, causal mask and online softmax (running max m and sum l,
 //    rescale by 2^(m_old - m_new); "Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
 //    §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를 줄이는 방향").
-//    Warp 0 issues TMA, warp 1 issues MMAs, warps 2-5 (one per TMEM lane quarter) do the softmax
-//    with one query row per thread.
+//    Warps 0 and 2 issue TMA (Q and K / V), warp 1 issues MMAs, and two warpgroups (4-7, 8-11)
+//    do the softmax, one query row per thread and 64 of each step's 128 keys per warpgroup.
 //  * decode item — one sequence, one kv-head with its G query heads, a range of 16-row paged
 //    blocks: each warp streams its blocks into a private two-slot shared-memory ring with 4 KiB
 //    bulk copies, holds q in registers (4 dims per lane), reduces q·k across the warp with
 //    shuffles, and keeps an online softmax per head ("LLMSO - W4", §"FlashDecoding — decode 단계의
 //    병렬성 확보", §"KV 헤드 줄이기").
 //
-// Each hardware CTA reads %smid and a per-SM counter of running prefill items, and takes the
-// next prefill ticket while its SM is under the prefill cap, else the next decode ticket, so both
-// kinds share every SM (§"가상 CTA와 SM별 균형"). Outputs split along the keys are merged exactly
+// One hardware CTA per SM runs a prefill slot and a decode slot side by side, each pulling
+// tickets from its own list, so both kinds share every SM (§"가상 CTA와 SM별 균형"); %smid is
+// recorded per item. Outputs split along the keys are merged exactly
 // by log-sum-exp by whichever split finishes last (no CTA ever waits for another CTA, so the two
 // kinds cannot deadlock; §"가상 CTA와 SM별 균형": exact synchronisation where partials meet).
 #include <cuda.h>
@@ -72,20 +72,20 @@ struct Params {
 };
 
 struct SmemCtl {
-  uint64_t q_full;                 // both query tiles of a prefill item landed
+  uint64_t q_full;                 // the query tile of a prefill item landed
   uint64_t k_full[kKStages];
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full[2];              // S of query tile A / B computed
-  uint64_t p_ready[2];             // P of tile A / B written (128 arrivals each)
-  uint64_t pv_done[2];             // P·V of tile A / B completed
+  uint64_t s_full[2];              // S buffer 0 / 1 computed
+  uint64_t p_ready[2];             // P of S buffer 0 / 1 written (256 softmax arrivals each)
+  uint64_t pv_done[2];             // P·V reading S buffer 0 / 1 completed
   uint64_t dslot[kWarps][kDecodeSlots];  // decode rings, by absolute warp
   uint32_t tmem_base;
   int abort;
-  int item_kind[2];                // per slot: 0 = prefill slot, 1 = decode slot
-  int item_idx[2];
-  int merge_last[2];
+  int item_kind[4];                // per slot: 0 = prefill, 1 = decode, 2-3 = the prefill slot's
+  int item_idx[4];                 //   warps 4-7 / 8-11 once prefill work is drained
+  int merge_last[4];
 };
 static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 
@@ -97,9 +97,8 @@ struct PipeState {
   uint32_t dphase = 0;  // decode ring: one parity bit per slot of this warp
 };
 
-// Where a decode item runs: `nw` warps from absolute warp `w0` (the decode slot's warps, or the
-// prefill slot's softmax warps when it borrows decode work), their rings and score areas, and
-// the named barrier of the slot that runs it.
+// Where a decode item runs: `nw` (= 4) warps from absolute warp `w0`, their rings and score
+// areas, the named barrier of the slot that runs it and the slot's index in the control block.
 struct DecodeCtx {
   int w0, nw;
   uint8_t* ring;        // nw * kDecodeSlots * kSmemDecodeSlot bytes; also the combine scratch
@@ -117,10 +116,11 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 }
 
 // ============================================================================ prefill item
-// One prefill item: query tiles A = rows 256t..256t+127 and B = rows 256t+128..256t+255 of a
-// chunk, one head, a range of keys in 128-key steps. Both tiles share every K and V tile.
-// Issue order on the tensor cores: S_A(0), S_B(0), then per step j: P·V_A(j), S_A(j+1),
-// P·V_B(j), S_B(j+1) — while one tile's softmax runs, the tensor cores work for the other.
+// One prefill item: a 128-row query tile of a chunk, one head, a range of keys in 128-key
+// steps. The MMA issuer keeps the tensor cores one step ahead: S of step j+1 (into the other TMEM
+// buffer) runs while the softmax of step j runs; P·V of step j follows the softmax. The two
+// softmax warpgroups split each 128x128 score tile by columns (64 keys each) and agree on the
+// row max through the TMEM exchange columns.
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
                              const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
                              SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
@@ -132,91 +132,68 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   const int L = p.kv_lens[s];
   const int P = L - qlen;  // cached prefix rows before this chunk
   const int ntiles = (ke - kb + kTileN - 1) / kTileN;
-  const uint32_t sQ = smem_u32(smem);                 // tile A at sQ, tile B at sQ + kSmemQ
-  const uint32_t sKring = sQ + 2 * kSmemQ;
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sKring = sQ + kSmemQ;
   const uint32_t sVring = sKring + kKStages * kSmemKTile;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer (warp)
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 0 loads Q and the K tiles, warp 2 the V tiles: the two rings advance independently.
     // Lane i holds the block-table entry of block i of the next 4 steps (32 blocks): one
-    // coalesced read instead of a dependent global read per block. K runs one step ahead of V.
+    // coalesced read instead of a dependent global read per block.
+    const bool is_k = warp == 0;
     const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
     const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
     const int blk0 = kb / kBlockSize;
     constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
-    if (lane == 0) {
+    if (is_k && lane == 0) {
       const uint32_t qbar = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qbar, 2 * kSmemQ);
-      for (int x = 0; x < 2; ++x) {
-        const int row0 = q0 + t * kPairM + x * kTileM;
-        tma_load_3d(sQ + x * kSmemQ, tmq, qbar, 0, h, row0);
-        tma_load_3d(sQ + x * kSmemQ + kSmemQ / 2, tmq, qbar, 64, h, row0);
-      }
+      mbar_arrive_expect_tx(qbar, kSmemQ);
+      tma_load_3d(sQ, tmq, qbar, 0, h, q0 + t * kTileM);
+      tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h, q0 + t * kTileM);
     }
+    const int nst = is_k ? kKStages : kVStages;
+    uint64_t* empty_bar = is_k ? ctl->k_empty : ctl->v_empty;
+    uint64_t* full_bar = is_k ? ctl->k_full : ctl->v_full;
+    const uint32_t ring = is_k ? sKring : sVring;
+    const CUtensorMap* tm = is_k ? tmk : tmv;
     int btv = -1;
-    int yv[kBlocksPerTile];
-#pragma unroll
-    for (int b = 0; b < kBlocksPerTile; ++b) yv[b] = 0;
     const uint32_t base = ps.kv_cnt;
-    for (int j = 0; j <= ntiles; ++j) {
+    for (int j = 0; j < ntiles; ++j) {
+      if ((j & 3) == 0) {
+        const int bi = j * kBlocksPerTile + lane;
+        btv = -1;
+        if (bi < nblk_item) {
+          int phys = bt_row[blk0 + bi];
+          if (phys < 0 || phys >= p.num_blocks) {
+            record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+            phys = 0;
+          }
+          btv = phys;
+        }
+      }
       int y[kBlocksPerTile];
 #pragma unroll
-      for (int b = 0; b < kBlocksPerTile; ++b) y[b] = 0;
-      if (j < ntiles) {
-        if ((j & 3) == 0) {
-          const int bi = j * kBlocksPerTile + lane;
-          btv = -1;
-          if (bi < nblk_item) {
-            int phys = bt_row[blk0 + bi];
-            if (phys < 0 || phys >= p.num_blocks) {
-              record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
-              phys = 0;
-            }
-            btv = phys;
-          }
-        }
+      for (int b = 0; b < kBlocksPerTile; ++b) {
+        const int e = __shfl_sync(0xffffffffu, btv, (j & 3) * kBlocksPerTile + b);
+        y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
+      }
+      const uint32_t cnt = base + j;
+      const int stage = cnt % nst;
+      int okw = 1;
+      if (lane == 0)
+        okw = mbar_wait(smem_u32(&empty_bar[stage]), ((cnt / nst) & 1) ^ 1, wc, kSleepNs);
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      if (lane == 0) {
+        const uint32_t full = smem_u32(&full_bar[stage]);
+        const uint32_t dst = ring + stage * kSmemKTile;
+        mbar_arrive_expect_tx(full, kSmemKTile);
 #pragma unroll
         for (int b = 0; b < kBlocksPerTile; ++b) {
-          const int e = __shfl_sync(0xffffffffu, btv, (j & 3) * kBlocksPerTile + b);
-          y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
-        }
-        const uint32_t cnt = base + j;
-        const int stage = cnt % kKStages;
-        int okw = 1;
-        if (lane == 0)
-          okw = mbar_wait(smem_u32(&ctl->k_empty[stage]), ((cnt / kKStages) & 1) ^ 1, wc, kSleepNs);
-        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-        if (lane == 0) {
-          const uint32_t full = smem_u32(&ctl->k_full[stage]);
-          const uint32_t sK = sKring + stage * kSmemKTile;
-          mbar_arrive_expect_tx(full, kSmemKTile);
-#pragma unroll
-          for (int b = 0; b < kBlocksPerTile; ++b) {
-            tma_load_2d(sK + b * 2048, tmk, full, 0, y[b]);
-            tma_load_2d(sK + kSmemKTile / 2 + b * 2048, tmk, full, 64, y[b]);
-          }
+          tma_load_2d(dst + b * 2048, tm, full, 0, y[b]);
+          tma_load_2d(dst + kSmemKTile / 2 + b * 2048, tm, full, 64, y[b]);
         }
       }
-      if (j >= 1) {
-        const uint32_t cnt = base + j - 1;
-        const int stage = cnt % kVStages;
-        int okw = 1;
-        if (lane == 0)
-          okw = mbar_wait(smem_u32(&ctl->v_empty[stage]), ((cnt / kVStages) & 1) ^ 1, wc, kSleepNs);
-        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-        if (lane == 0) {
-          const uint32_t full = smem_u32(&ctl->v_full[stage]);
-          const uint32_t sV = sVring + stage * kSmemKTile;
-          mbar_arrive_expect_tx(full, kSmemKTile);
-#pragma unroll
-          for (int b = 0; b < kBlocksPerTile; ++b) {
-            tma_load_2d(sV + b * 2048, tmv, full, 0, yv[b]);
-            tma_load_2d(sV + kSmemKTile / 2 + b * 2048, tmv, full, 64, yv[b]);
-          }
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kBlocksPerTile; ++b) yv[b] = y[b];
     }
     ps.kv_cnt = base + ntiles;
   } else if (warp == 1) {
@@ -225,51 +202,33 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc, kSleepNs);
     tc_fence_after();
     const uint32_t base = ps.kv_cnt;
-    auto issue_s = [&](int x, uint32_t cnt) {  // S_x = Q_x · Kᵀ of step cnt (lane 0 issues)
+    // S of step j (global step n = t_cnt + j) into TMEM buffer n mod 2
+    auto issue_s = [&](int j) -> bool {
+      const uint32_t cnt = base + j, n = ps.t_cnt + j;
+      if (!mbar_wait(smem_u32(&ctl->k_full[cnt % kKStages]), (cnt / kKStages) & 1, wc, kSleepNs))
+        return false;
+      tc_fence_after();
       if (lane == 0) {
         const uint32_t sK = sKring + (cnt % kKStages) * kSmemKTile;
-        const uint32_t sq = sQ + x * kSmemQ;
-        const uint32_t dS = tmem + kTmemS + x * 128;
+        const uint32_t dS = tmem + kTmemS + (n & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sq + half * (kSmemQ / 2) + koff, 16, 1024);
+          const uint64_t ad = sdesc_sw128(sQ + half * (kSmemQ / 2) + koff, 16, 1024);
           const uint64_t bd = sdesc_sw128(sK + half * (kSmemKTile / 2) + koff, 16, 1024);
           umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(smem_u32(&ctl->s_full[x]));
-        if (x == 1) umma_commit(smem_u32(&ctl->k_empty[cnt % kKStages]));
+        umma_commit(smem_u32(&ctl->s_full[n & 1]));
+        umma_commit(smem_u32(&ctl->k_empty[cnt % kKStages]));
       }
       __syncwarp();
+      return true;
     };
-    auto issue_pv = [&](int x, int j, uint32_t cnt) {  // O_x += P_x · V of step cnt
-      if (lane == 0) {
-        const uint32_t sV = sVring + (cnt % kVStages) * kSmemKTile;
-        const uint32_t aP = tmem + kTmemS + x * 128;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // V tile is N-major: 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart
-          const uint64_t bd = sdesc_sw128(sV + kk * 2048, kSmemKTile / 2, 1024);
-          umma_ts(tmem + kTmemO + x * 128, aP + kk * 8, bd, kIdescPV,
-                  (j == 0 && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(smem_u32(&ctl->pv_done[x]));
-        if (x == 1) umma_commit(smem_u32(&ctl->v_empty[cnt % kVStages]));
-      }
-      __syncwarp();
-    };
-    if (ok && ntiles > 0) {
-      ok = mbar_wait(smem_u32(&ctl->k_full[base % kKStages]), (base / kKStages) & 1, wc, kSleepNs);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, base);
-        issue_s(1, base);
-      }
-    }
+    if (ok && ntiles > 0) ok = issue_s(0);
+    if (ok && ntiles > 1) ok = issue_s(1);
     for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t cnt = base + j, n = ps.t_cnt + j;
-      // P·V_A(j): P_A written and V_j landed
-      if (!mbar_wait(smem_u32(&ctl->p_ready[0]), n & 1, wc, kSleepNs) ||
+      if (!mbar_wait(smem_u32(&ctl->p_ready[n & 1]), (n >> 1) & 1, wc, kSleepNs) ||
           !mbar_wait(smem_u32(&ctl->v_full[cnt % kVStages]), (cnt / kVStages) & 1, wc, kSleepNs)) {
         ok = false;
         break;
@@ -277,7 +236,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const int tile0 = kb + j * kTileN;
       if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
         // Rows past the sequence end inside its last block may hold anything (even NaN); P is
-        // zero there but 0 * NaN is not, so clear those V rows before the P·V products.
+        // zero there but 0 * NaN is not, so clear those V rows before the P·V product.
         const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
         uint8_t* vbase = smem + (sVring - sQ) + (cnt % kVStages) * kSmemKTile;
         for (int c = lane; c < (r1 - r0) * 16; c += 32) {
@@ -289,56 +248,57 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         __syncwarp();
       }
       tc_fence_after();
-      issue_pv(0, j, cnt);
-      const bool more = j + 1 < ntiles;
-      if (more) {
-        if (!mbar_wait(smem_u32(&ctl->k_full[(cnt + 1) % kKStages]), ((cnt + 1) / kKStages) & 1,
-                       wc, kSleepNs)) {
-          ok = false;
-          break;
+      if (lane == 0) {
+        const uint32_t sV = sVring + (cnt % kVStages) * kSmemKTile;
+        const uint32_t aP = tmem + kTmemS + (n & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          // P of keys 16kk.. sits at column 64*(kk/4) + 8*(kk%4) of its S buffer; V is N-major:
+          // 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
+          const uint64_t bd = sdesc_sw128(sV + kk * 2048, kSmemKTile / 2, 1024);
+          umma_ts(tmem + kTmemO, aP + (kk >> 2) * 64 + (kk & 3) * 8, bd, kIdescPV,
+                  (j == 0 && kk == 0) ? 0u : 1u);
         }
-        tc_fence_after();
-        issue_s(0, cnt + 1);
+        umma_commit(smem_u32(&ctl->pv_done[n & 1]));
+        umma_commit(smem_u32(&ctl->v_empty[cnt % kVStages]));
       }
-      // P·V_B(j)
-      if (!mbar_wait(smem_u32(&ctl->p_ready[1]), n & 1, wc, kSleepNs)) {
+      __syncwarp();
+      // S of step j+2 reuses this buffer: it is issued after the P·V just issued, which reads it
+      if (j + 2 < ntiles && !issue_s(j + 2)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      issue_pv(1, j, cnt);
-      if (more) issue_s(1, cnt + 1);
     }
     ps.kv_cnt = base + ntiles;
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
     // ------------------------------------------------------------------ softmax (1 row/thread)
-    const int x = (warp - kSoftmaxWarp0) >> 2;  // query tile: 0 = A, 1 = B
+    const int grp = (warp - kSoftmaxWarp0) >> 2;  // columns 64*grp .. 64*grp + 63 of each S
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tS = trow + kTmemS + x * 128, tO = trow + kTmemO + x * 128;
-    const int qi = t * kPairM + x * kTileM + row;  // local index of this thread's query
+    const uint32_t tO = trow + kTmemO + grp * 64, tX = trow + kTmemX;
+    const int qi = t * kTileM + row;  // local index of this thread's query in the chunk
     const bool valid = qi < qlen;
-    const int limit = min(P + qi + 1, ke);  // keys [kb, limit) are visible to this row
+    const int limit = min(P + qi + 1, ke) - grp * 64;  // keys visible to this group: [.., limit)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     for (int j = 0; j < ntiles; ++j) {
       const uint32_t n = ps.t_cnt + j;
-      if (!mbar_wait(smem_u32(&ctl->s_full[x]), n & 1, wc)) {
-        ok = false;
-        break;
-      }
+      const uint32_t tS = trow + kTmemS + (n & 1) * 128 + grp * 64;
+      // After a failed wait the loop still runs (every wait then fails at once), so that both
+      // warpgroups pass the same named barriers whatever happened.
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[n & 1]), (n >> 1) & 1, wc));
       tc_fence_after();
       const int nvis = limit - (kb + j * kTileN);
-      const bool full_tile = __all_sync(0xffffffffu, nvis >= kTileN);
-      // pass 1: the row max over the 128 columns, 32 at a time (TMEM reads are cheap)
+      const bool full_tile = __all_sync(0xffffffffu, nvis >= 64);
+      // pass 1: this group's partial row max, swapped with the other group through TMEM
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32];
         tmem_ld32(tS + ch * 32, sr);
         tmem_ld_wait();
@@ -350,11 +310,19 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
 #pragma unroll
         for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
       }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                       p.scale_log2;  // scale > 0: the max of the scaled scores
+      const float mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      tmem_st1(tX + (n & 1) * 2 + grp, f2u(mine));
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_sync(2, 256);
+      tc_fence_after();
+      const float other = u2f(tmem_ld1(tX + (n & 1) * 2 + (grp ^ 1)));
+      tmem_ld_wait();
+      const float mt = fmaxf(mine, other) * p.scale_log2;  // scale > 0: max of scaled scores
       // Lazy rescale: the reference max moves only when a score exceeds it by more than 2^8;
-      // O and l stay consistent with whichever reference is current.
+      // O and l stay consistent with whichever reference is current. Both groups see the same
+      // row max and history, so they decide alike.
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + 8.f;
       float alpha = 1.f;
@@ -364,14 +332,12 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         // O holds P·V of the earlier steps once step j-1's product completed (the one before
-        // finished ahead of S of step j); at most one completion of that barrier is pending.
-        if (!mbar_wait(smem_u32(&ctl->pv_done[x]), (n - 1) & 1, wc)) {
-          ok = false;
-          break;
-        }
+        // finished ahead of it); at most one completion of that barrier is pending.
+        ok = __all_sync(0xffffffffu,
+                        ok && mbar_wait(smem_u32(&ctl->pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1, wc));
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {  // this group's 64 columns of O
           uint32_t o[32];
           tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
@@ -383,13 +349,13 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       }
       const float mref = m == -INFINITY ? 0.f : m;
       const float2 nm2 = make_float2(-mref, -mref);
-      // pass 2: exponentials, row sum, and P (bf16 pairs) written over S's first 64 columns;
-      // chunk ch writes columns 16ch..16ch+15, all of which earlier chunks have already read
+      // pass 2: exponentials, partial row sum, and P (bf16 pairs) written over the group's own,
+      // already read S columns (chunk ch writes columns 16ch..16ch+15 of the group's range)
       float2 sum[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32];
         tmem_ld32(tS + ch * 32, sr);
         tmem_ld_wait();
@@ -409,27 +375,35 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         tmem_st16(tS + ch * 16, pk);
       }
       const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
-      l = l * alpha + (s01.x + s01.y);
+      l = l * alpha + (s01.x + s01.y);  // this group's share of the row sum
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->p_ready[x]));
+      mbar_arrive(smem_u32(&ctl->p_ready[n & 1]));
     }
     if (ok && ntiles > 0) {  // the last step's P·V (all earlier ones completed before it)
-      ok = mbar_wait(smem_u32(&ctl->pv_done[x]), (ps.t_cnt + ntiles - 1) & 1, wc);
+      const uint32_t nl = ps.t_cnt + ntiles - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[nl & 1]), (nl >> 1) & 1, wc));
       tc_fence_after();
     }
+    // the full row sum: swap the two groups' shares through TMEM
+    tmem_st1(tX + 4 + grp, f2u(l));
+    tmem_st_wait();
+    tc_fence_before();
+    named_bar_sync(2, 256);
+    tc_fence_after();
+    const float lt = l + u2f(tmem_ld1(tX + 4 + (grp ^ 1)));
+    tmem_ld_wait();
     // ------------------------------------------------------------------ epilogue
-    const int prow = x * kTileM + row;  // row within the pair
-    if (ok) {
+    {
       if (unit < 0) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim + grp * 64;
 #pragma unroll 1
-        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {
           uint32_t o[32];
           tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
-          if (valid) {
+          if (valid && ok) {
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
@@ -443,48 +417,51 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         const int slot0 = p.units[unit * kUnitWords + 1];
         float* slot = p.partial_p + (size_t)(slot0 + split) * kPrefillSlotFloats;
 #pragma unroll 1
-        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+        for (int ch = 0; ch < 2 && ok; ++ch) {
           uint32_t o[32];
           tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
-          float4* d4 = reinterpret_cast<float4*>(slot + prow * kHeadDim + ch * 32);
+          float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + grp * 64 + ch * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             d4[i] = make_float4(u2f(o[4 * i]), u2f(o[4 * i + 1]), u2f(o[4 * i + 2]), u2f(o[4 * i + 3]));
         }
-        slot[kPairM * kHeadDim + prow] = m;
-        slot[kPairM * kHeadDim + kPairM + prow] = l;
+        if (grp == 0 && ok) {
+          slot[kTileM * kHeadDim + row] = m;
+          slot[kTileM * kHeadDim + kTileM + row] = lt;
+        }
         __threadfence();
         named_bar_sync(2, 256);
-        if (prow == 0) ctl->merge_last[0] = (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+        if (grp == 0 && row == 0)
+          ctl->merge_last[0] = ok && (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
         named_bar_sync(2, 256);
-        if (ctl->merge_last[0]) {
+        if (ctl->merge_last[0] && ok) {
           __threadfence();
           if (valid) {
             float mx = -INFINITY;
             for (int k = 0; k < nsplit; ++k) {
               const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-              mx = fmaxf(mx, __ldcg(sl + kPairM * kHeadDim + prow));
+              mx = fmaxf(mx, __ldcg(sl + kTileM * kHeadDim + row));
             }
             float den = 0.f;
             for (int k = 0; k < nsplit; ++k) {
               const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-              const float mk = __ldcg(sl + kPairM * kHeadDim + prow);
-              if (mk != -INFINITY) den += ex2(mk - mx) * __ldcg(sl + kPairM * kHeadDim + kPairM + prow);
+              const float mk = __ldcg(sl + kTileM * kHeadDim + row);
+              if (mk != -INFINITY) den += ex2(mk - mx) * __ldcg(sl + kTileM * kHeadDim + kTileM + row);
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim;
+            uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim + grp * 64;
 #pragma unroll 1
-            for (int ch = 0; ch < kHeadDim / 32; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
               float acc[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) acc[c] = 0.f;
               for (int k = 0; k < nsplit; ++k) {
                 const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-                const float mk = __ldcg(sl + kPairM * kHeadDim + prow);
+                const float mk = __ldcg(sl + kTileM * kHeadDim + row);
                 if (mk == -INFINITY) continue;
                 const float f = ex2(mk - mx) * inv;
-                const float4* src = reinterpret_cast<const float4*>(sl + prow * kHeadDim + ch * 32);
+                const float4* src = reinterpret_cast<const float4*>(sl + row * kHeadDim + grp * 64 + ch * 32);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                   const float4 v = __ldcg(src + c);
@@ -503,7 +480,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
                                    pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
             }
           }
-          if (prow == 0) p.arrive[unit] = 0;  // ready for the next run
+          if (grp == 0 && row == 0) p.arrive[unit] = 0;  // ready for the next run
         }
       }
     }
@@ -512,7 +489,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   // every thread of the prefill slot keeps the same pipeline positions
   ps.q_cnt++;
   ps.t_cnt += ntiles;
-  if (warp != 0 && warp != 1) ps.kv_cnt += ntiles;
+  if (warp != 0 && warp != 1 && warp != 2) ps.kv_cnt += ntiles;
   named_bar_sync(1, kPrefillThreads);
 }
 
@@ -965,9 +942,10 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
 }
 
 // ============================================================================ scheduler
-// Next item for a slot. The prefill slot takes prefill tickets, and decode tickets once the
-// prefill list is drained (or in a decode-only launch); the decode slot takes decode tickets
-// only. Per-SM counters record how many decode items each SM's prefill slot took over.
+// Next item for a slot. The prefill slot (0) takes prefill tickets, and a decode ticket once the
+// prefill list is drained (or in a decode-only launch); the decode slot (1) and the prefill
+// warps' two decode slots (2, 3) take decode tickets only. Per-SM counters record how many
+// decode items each SM's prefill warps took over.
 __device__ __forceinline__ void pick_item(const Params& p, int slot, int sm, SmemCtl* ctl) {
   int32_t* cnt = p.counters;
   int kind = -1, idx = 0;
@@ -981,7 +959,7 @@ __device__ __forceinline__ void pick_item(const Params& p, int slot, int sm, Sme
     const int t = atomicAdd(&cnt[1], 1);
     if (t < p.n_items_d) {
       kind = 1, idx = t;
-      if (slot == 0) atomicAdd(&cnt[kCounterHeader + sm], 1);
+      if (slot != 1) atomicAdd(&cnt[kCounterHeader + sm], 1);
     }
   }
   ctl->item_kind[slot] = kind;
@@ -997,6 +975,31 @@ __device__ __forceinline__ void record_item(const Params& p, int kind, int idx, 
   rec->cta = blockIdx.x;
   rec->t_start = t0;
   rec->t_end = globaltimer();
+}
+
+// A decode slot's ticket loop; `first` >= 0 is an item already taken for it.
+template <int GT>
+__device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                            const DecodeCtx& dc, int first, int sm, uint32_t sm_raw, SmemCtl* ctl,
+                            PipeState& ps, const WaitCtx& wc) {
+  const bool leader = threadIdx.x == dc.first_thread;
+  for (;;) {
+    if (leader) {
+      if (first >= 0) {
+        ctl->item_kind[dc.slot] = 1;
+        ctl->item_idx[dc.slot] = first;
+      } else {
+        pick_item(p, dc.slot, sm, ctl);
+      }
+    }
+    first = -1;
+    named_bar_sync(dc.bar_id, dc.bar_threads);
+    const int kind = ctl->item_kind[dc.slot], idx = ctl->item_idx[dc.slot];
+    if (kind < 0 || ctl->abort) break;
+    const uint64_t t0 = (p.records != nullptr && leader) ? globaltimer() : 0;
+    decode_item<GT>(p, tmk, tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
+    if (p.records != nullptr && leader) record_item(p, kind, idx, sm_raw, t0);
+  }
 }
 
 template <int GT>
@@ -1024,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctl->p_ready[i]), 128);
+      mbar_init(smem_u32(&ctl->p_ready[i]), 256);
       mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     }
     for (int w = 0; w < kWarps; ++w)
@@ -1049,36 +1052,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int sm = (int)(sm_raw % (uint32_t)p.num_sms);
   if (warp < kDecodeWarp0) {
     // ------------------------------------------------------------------ prefill slot
-    const DecodeCtx dc{kBorrowWarp0, kBorrowWarps, smem,
-                       reinterpret_cast<float*>(smem + kBorrowWarps * kDecodeSlots * kSmemDecodeSlot),
-                       1, kPrefillThreads, 0, 0};
+    int handoff = -1;  // a decode item taken once the prefill list ran dry
     for (;;) {
       if (tid == 0) pick_item(p, 0, sm, ctl);
       named_bar_sync(1, kPrefillThreads);
       const int kind = ctl->item_kind[0], idx = ctl->item_idx[0];
       if (kind < 0 || ctl->abort) break;
+      if (kind == 1) {
+        handoff = idx;
+        break;
+      }
       const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
-      if (kind == 0)
-        prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
-      else
-        decode_item<GT>(p, &tmk, &tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
+      prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
       if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
+    }
+    if (handoff >= 0 && warp >= kSoftmaxWarp0) {
+      // the softmax warps become two 4-warp decode slots over the prefill region
+      const int sub = (warp - kSoftmaxWarp0) / kDecodeWarps;
+      const int w0 = kSoftmaxWarp0 + sub * kDecodeWarps;
+      const DecodeCtx dc{w0, kDecodeWarps, smem + sub * kSmemDecodeRing,
+                         reinterpret_cast<float*>(smem + 2 * kSmemDecodeRing +
+                                                  sub * kDecodeWarps * kSmemScoresPerWarp),
+                         4 + sub, kDecodeWarps * 32, w0 * 32, 2 + sub};
+      decode_loop<GT>(p, &tmk, &tmv, dc, sub == 0 ? handoff : -1, sm, sm_raw, ctl, ps, wc);
     }
   } else {
     // ------------------------------------------------------------------ decode slot
-    const int first = kDecodeWarp0 * 32;
     const DecodeCtx dc{kDecodeWarp0, kDecodeWarps, smem + kSmemDecodeOff,
-                       reinterpret_cast<float*>(smem + kSmemScoresOff), 3,
-                       kDecodeWarps * 32, first, 1};
-    for (;;) {
-      if (tid == first) pick_item(p, 1, sm, ctl);
-      named_bar_sync(3, kDecodeWarps * 32);
-      const int kind = ctl->item_kind[1], idx = ctl->item_idx[1];
-      if (kind < 0 || ctl->abort) break;
-      const uint64_t t0 = (p.records != nullptr && tid == first) ? globaltimer() : 0;
-      decode_item<GT>(p, &tmk, &tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
-      if (p.records != nullptr && tid == first) record_item(p, kind, idx, sm_raw, t0);
-    }
+                       reinterpret_cast<float*>(smem + kSmemScoresOff), 3, kDecodeWarps * 32,
+                       kDecodeWarp0 * 32, 1};
+    decode_loop<GT>(p, &tmk, &tmv, dc, -1, sm, sm_raw, ctl, ps, wc);
   }
   tc_fence_before();
   __syncthreads();

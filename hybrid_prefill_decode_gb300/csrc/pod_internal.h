@@ -19,35 +19,33 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 // One persistent CTA per SM holds two concurrent virtual-CTA slots ("POD-Attention" digest,
 // §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
 //  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns — warp 0 issues
-//    TMA, warp 1 issues tcgen05 MMAs, warps 4-7 and 8-11 are the softmax warpgroups of two
-//    128-row query tiles that take turns on the tensor cores (warps 2-3 are idle in prefill);
+//    the TMA loads of Q and K, warp 2 those of V, warp 1 issues tcgen05 MMAs, and warps 4-7 and
+//    8-11 are two softmax warpgroups that share each 128x128 score tile (64 columns each);
 //  * the decode slot (warps 12-15): decode items, on their own ticket loop.
-// When one kind's queue is empty the prefill slot's warps 4-11 also run decode items.
+// Once the prefill list is drained, the prefill slot's warps 4-7 and 8-11 become two more
+// 4-warp decode slots. Every decode item thus runs on exactly 4 warps, whichever slot takes it,
+// so its arithmetic (and result) does not depend on where it ran.
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPrefillThreads = 384;    // warps 0-11
-constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (tile A: 4-7, tile B: 8-11)
+constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (column group 0: 4-7, 1: 8-11)
 constexpr int kDecodeWarp0 = 12;        // decode slot: warps 12-15
 constexpr int kDecodeWarps = 4;
-constexpr int kBorrowWarp0 = 4;         // prefill slot running decode items: warps 4-11
-constexpr int kBorrowWarps = 8;
 constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp
 
-// Prefill step: two 128-row query tiles (same sequence and head, consecutive) x 128 keys.
+// Prefill step: one 128-row query tile x 128 keys. S is double-buffered in TMEM, so S of step
+// j+1 runs on the tensor cores while the softmax of step j runs; two K and two V stages keep
+// the loads one step ahead of both.
 constexpr int kTileM = 128;
-constexpr int kPairM = 2 * kTileM;
 constexpr int kTileN = 128;
-// K of step j+1 is requested once both tiles' S of step j are done, and is needed only after
-// tile A's softmax of step j; V of step j+1 is requested once tile B's P·V of step j-1 is done
-// and needed a whole step later — so one K stage and two V stages keep both ahead.
-constexpr int kKStages = 1;
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 
 // Shared-memory map (bytes from the dynamic shared-memory base, which the hardware places at
 // a 1024-byte boundary; the kernel checks this and reports an error otherwise).
-constexpr int kSmemQ = kTileM * kHeadDim * 2;                      // 32 KiB per query tile
+constexpr int kSmemQ = kTileM * kHeadDim * 2;                      // 32 KiB query tile
 constexpr int kSmemKTile = kTileN * kHeadDim * 2;                  // 32 KiB (K or V tile)
-constexpr int kSmemPrefill = 2 * kSmemQ + (kKStages + kVStages) * kSmemKTile;  // 160 KiB
+constexpr int kSmemPrefill = kSmemQ + (kKStages + kVStages) * kSmemKTile;  // 160 KiB
 constexpr int kSmemDecodeSlot = 2 * kBlockSize * kHeadDim * 2;     // 8 KiB (K block + V block)
 constexpr int kSmemDecodeRing = kDecodeWarps * kDecodeSlots * kSmemDecodeSlot;  // 64 KiB
 constexpr int kSmemScoresPerWarp = kMaxGroup * kBlockSize * 4;     // p exchange of one warp
@@ -57,21 +55,23 @@ constexpr int kSmemCtlOff = kSmemScoresOff + kDecodeWarps * kSmemScoresPerWarp;
 constexpr int kSmemBarriers = 512;                                  // mbarriers + scalars
 constexpr int kSmemTotal = kSmemCtlOff + kSmemBarriers;
 static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
-// the prefill slot's region also serves as the borrowed decode warps' rings and score areas
-static_assert(kBorrowWarps * (kDecodeSlots * kSmemDecodeSlot + kSmemScoresPerWarp) <=
-                  kSmemPrefill, "borrowed decode rings must fit the prefill region");
+// the prefill slot's region also serves as the rings and score areas of its two decode slots
+static_assert(2 * (kSmemDecodeRing + kDecodeWarps * kSmemScoresPerWarp) <= kSmemPrefill,
+              "the two decode slots of the prefill warps must fit the prefill region");
 
-// TMEM columns (the whole SM): O of tile A, O of tile B, S of tile A, S of tile B (fp32);
-// P of a tile (bf16 pairs) overwrites the first 64 columns of its S.
+// TMEM columns (the whole SM): O (fp32, 128 columns), then two S buffers (fp32, 128 columns
+// each); P of a step (bf16 pairs) overwrites the S columns its own warpgroup has read. Columns
+// from kTmemX are the two softmax warpgroups' exchange of per-row partial maxima and sums.
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 0;      // + 128 * tile
-constexpr int kTmemS = 256;    // + 128 * tile
+constexpr int kTmemO = 0;
+constexpr int kTmemS = 128;    // + 128 * buffer
+constexpr int kTmemX = 384;    // + 2 * (step parity) + group: partial max; + 4 + group: sum
 
 // Work item: kItemWords int32 words.
 //   [0] kind         0 = prefill, 1 = decode
 //   [1] seq          prefill: chunk index s in [0, Np); decode: d in [0, Nd)
-//   [2] tile / kvh   prefill: index t of the pair of 128-row query tiles (rows 256t ..
-//                    256t + 255 of the chunk); decode: kv-head g
+//   [2] tile / kvh   prefill: index t of the 128-row query tile (rows 128t .. 128t + 127
+//                    of the chunk); decode: kv-head g
 //   [3] head         prefill: query head h; decode: 0
 //   [4] key_begin    first key row of this split (prefill: multiple of 128; decode: of 16)
 //   [5] key_end      one past the last key row this split may read
@@ -83,7 +83,7 @@ constexpr int kItemWords = 8;
 constexpr int kUnitWords = 4;
 
 // Partial-result slots: fp32 o[rows][128] then m[rows] then l[rows] (m, l in log2 units).
-constexpr int kPrefillSlotFloats = kPairM * (kHeadDim + 2);
+constexpr int kPrefillSlotFloats = kTileM * (kHeadDim + 2);
 #ifdef __CUDACC__
 __host__ __device__
 #endif

@@ -87,8 +87,8 @@ def _cdiv(a, b):
 
 
 def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
-    """Items: prefill = (chunk, pair of 128-row query tiles, head, split) over 128-key steps
-    (cost 114 each), decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
+    """Items: prefill = (chunk, 128-row query tile, head, split) over 128-key steps
+    (cost 57 each), decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
     item slots per SM; split when an output costs more than a quarter of a slot's share."""
     np_ = len(cu) - 1 if cu else 0
     slots = num_sms * 2
@@ -96,12 +96,12 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
     for s in range(np_):
         q, L = cu[s + 1] - cu[s], kv[s]
         P = L - q
-        for t in range(_cdiv(q, 256)):
-            kend = P + min(q, (t + 1) * 256)
+        for t in range(_cdiv(q, 128)):
+            kend = P + min(q, (t + 1) * 128)
             nt = _cdiv(kend, 128)
             for h in range(Hq):
                 pu.append((s, t, h, kend, nt))
-                total += nt * 114
+                total += nt * 57
     for d in range(nd):
         L = kv[np_ + d]
         for g in range(Hkv):
@@ -121,14 +121,14 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
         if psplit:
             ns = psplit
         else:
-            ns = min(_cdiv(nt * 114, target), max(1, nt // 4), 8)
+            ns = min(_cdiv(nt * 57, target), max(1, nt // 4), 8)
         ns = max(1, min(ns, nt))
         chunk = _cdiv(nt, ns)
         ns = _cdiv(nt, chunk)
         u = add_unit(ns, 0) if ns > 1 else -1
         for k in range(ns):
             t0, t1 = k * chunk, min(nt, (k + 1) * chunk)
-            lp.append(((t1 - t0) * 114, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
+            lp.append(((t1 - t0) * 57, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
     for d, g, L, nblk in du:
         if dsplit:
             ns = dsplit
@@ -210,9 +210,9 @@ def test_planner_covers_every_key_once(lib, i):
         else:
             t = key[2]
             q = q_lens[seq]
-            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * 256)
-    # every (pair of query tiles, head) and (decode seq, kv-head) appears
-    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, 256) for q in q_lens) * Hq
+            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * 128)
+    # every (query tile, head) and (decode seq, kv-head) appears
+    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, 128) for q in q_lens) * Hq
     assert len([k for k in cover if k[0] == 1]) == len(dkv) * Hkv
 
 

@@ -6,7 +6,9 @@
 // count just above a multiple of what the SMs hold at once costs a whole extra wave.
 //
 // This file turns one hybrid batch into two work lists (virtual CTAs):
-//   prefill item = (chunk s, 128-row query tile t, query head h, KV split k)
+//   prefill item = (chunk s, query tile t, block of hp query heads, KV split k) — a tile is
+//                  128 rows = 128/hp tokens x hp heads of one kv-head group, so every K/V tile
+//                  it loads serves hp heads
 //   decode item  = (sequence d, kv-head g, KV split k)   — one item serves all G query heads
 //                  of the kv-head (GQA grouping, "LLMSO - W4", §"KV 헤드 줄이기")
 // and sizes the persistent grid: one CTA per SM, each with a prefill slot and a decode slot
@@ -15,7 +17,8 @@
 // Split planning. Every item gets a cost (decode: 8 per 16-row K/V block, i.e. its bytes in
 // KiB; prefill: 57 per 128x128 step, its tensor-core time expressed in the same byte-time
 // units at a 6.8 TB/s : 1 PFLOP/s balance). With W the total cost and S the item slots, an
-// output whose cost exceeds W / (4 S) is split along the keys ("LLMSO - W4", §"FlashDecoding —
+// output whose cost exceeds W / (4 S) (prefill: also W_prefill / (4 x SMs), as only the SMs'
+// prefill slots run it) is split along the keys ("LLMSO - W4", §"FlashDecoding —
 // decode 단계의 병렬성 확보") into at most 64 (decode) or 8 (prefill) parts of at least
 // 12 blocks / 4 steps, so no single item can leave a long tail after the others finish. Items
 // are then ordered longest first. All arithmetic is integer, so the plan is reproducible bit
@@ -34,7 +37,6 @@ constexpr int64_t kPrefillTileCost = 57;  // 4*128*128*128 FLOPs at the byte-tim
 constexpr int kMinDecodeBlocksPerSplit = 12;
 constexpr int kMaxDecodeSplits = 64;
 constexpr int kMinPrefillTilesPerSplit = 4;
-constexpr int kMaxPrefillSplits = 8;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -81,6 +83,10 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->prob = prob;
   plan->opt = opt;
   plan->group = G;
+  const int hp = G & -G;  // largest power of two dividing G (G <= 8)
+  const int tq = kTileM / hp;
+  plan->head_pack = hp;
+  plan->tile_tokens = tq;
   plan->num_sms = num_sms;
   plan->ctas_per_sm = 1;  // one CTA per SM holds both slots (and all 512 TMEM columns)
   plan->cu.assign(cu ? cu : nullptr, cu ? cu + Np + 1 : nullptr);
@@ -99,11 +105,11 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
     pf += 4.0 * kHeadDim * Hq * (double)(q * P + q * (q + 1) / 2);
     pb += (double)L * row_bytes + 4.0 * q * Hq * kHeadDim;
-    for (int64_t t = 0; t < ceil_div(q, kTileM); ++t) {
-      const int64_t kend = P + std::min(q, (t + 1) * kTileM);
+    for (int64_t t = 0; t < ceil_div(q, tq); ++t) {
+      const int64_t kend = P + std::min(q, (t + 1) * tq);
       const int64_t nt = ceil_div(kend, kTileN);
-      for (int h = 0; h < Hq; ++h) {
-        pu.push_back({s, (int)t, h, kend, nt});
+      for (int h0 = 0; h0 < Hq; h0 += hp) {
+        pu.push_back({s, (int)t, h0, kend, nt});
         total += nt * kPrefillTileCost;
       }
     }
@@ -122,6 +128,11 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->est_decode_bytes = db;
   plan->est_decode_flops = df;
   const int64_t target = std::max<int64_t>(1, total / (slots * 4));
+  // prefill items run only on the prefill slots (one per SM): size them against that capacity
+  // too, so a prefill-heavy batch is not cut into more splits (each with a merge) than needed
+  int64_t total_p = 0;
+  for (const auto& x : pu) total_p += x.ntiles * kPrefillTileCost;
+  const int64_t target_p = std::max<int64_t>(target, total_p / ((int64_t)num_sms * 4));
 
   // ---- split and emit ----------------------------------------------------------------------
   std::vector<Pending> lp, ld;
@@ -139,11 +150,10 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     if (opt.prefill_splits > 0) {
       ns = opt.prefill_splits;
     } else {
-      ns = ceil_div(x.ntiles * kPrefillTileCost, target);
+      ns = ceil_div(x.ntiles * kPrefillTileCost, target_p);
       ns = std::min<int64_t>(ns, std::max<int64_t>(1, x.ntiles / kMinPrefillTilesPerSplit));
-      ns = std::min<int64_t>(ns, kMaxPrefillSplits);
     }
-    ns = std::max<int64_t>(1, std::min(ns, x.ntiles));
+    ns = std::max<int64_t>(1, std::min<int64_t>({ns, x.ntiles, (int64_t)kMaxPrefillSplits}));
     const int64_t chunk = ceil_div(x.ntiles, ns);
     ns = ceil_div(x.ntiles, chunk);
     const int u = ns > 1 ? add_unit((int)ns, 0) : -1;

@@ -8,8 +8,9 @@
 //    through the paged block table, causal mask and online softmax (running max m and sum l,
 //    rescale by 2^(m_old - m_new); "Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
 //    §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를 줄이는 방향").
-//    Warps 0 and 2 issue TMA (Q and K / V), warp 1 issues MMAs, and two warpgroups (4-7, 8-11)
-//    do the softmax, one query row per thread and 64 of each step's 128 keys per warpgroup.
+//    Warps 0 and 2 issue TMA (Q and K / V), warps 1 and 3 issue the S and P·V MMAs, and two
+//    warpgroups (4-7, 8-11) do the softmax, one query row per thread and 64 of each step's 128
+//    keys per warpgroup.
 //  * decode item — one sequence, one kv-head with its G query heads, a range of 16-row paged
 //    blocks: each warp streams its blocks into a private two-slot shared-memory ring with 4 KiB
 //    bulk copies, holds q in registers (4 dims per lane), reduces q·k across the warp with
@@ -66,6 +67,8 @@ struct Params {
   int32_t pool_rows;  // num_blocks * Hkv * 16: first row past the pools (TMA fills zeros)
   int32_t num_sms;
   int32_t max_prefill_per_sm;
+  int32_t hp_log2;    // prefill tile: 2^hp_log2 heads x tq tokens
+  int32_t tq;
   int32_t mode;
   float scale_log2;   // scale * log2(e): scores are kept in base-2 units
   uint64_t timeout_ns;
@@ -74,12 +77,11 @@ struct Params {
 struct SmemCtl {
   uint64_t q_full;                 // the query tile of a prefill item landed
   uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];
+  uint64_t k_empty[kKStages];      // S of the stage's last step completed
   uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];
   uint64_t s_full[2];              // S buffer 0 / 1 computed
-  uint64_t p_ready[2];             // P of S buffer 0 / 1 written (256 softmax arrivals each)
-  uint64_t pv_done[2];             // P·V reading S buffer 0 / 1 completed
+  uint64_t p_ready[2];             // P buffer 0 / 1 written (256 softmax arrivals each)
+  uint64_t pv_done[2];             // P·V of P buffer 0 / 1 done (also frees V stage 0 / 1)
   uint64_t dslot[kWarps][kDecodeSlots];  // decode rings, by absolute warp
   uint32_t tmem_base;
   int abort;
@@ -92,7 +94,6 @@ static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 // Pipeline positions; each role advances the fields it owns, across items.
 struct PipeState {
   uint32_t q_cnt = 0;   // prefill items (query-tile loads)
-  uint32_t kv_cnt = 0;  // 128-key steps loaded (producer) / consumed (MMA issuer)
   uint32_t t_cnt = 0;   // 128-key steps whose S, P and P·V barriers have turned over
   uint32_t dphase = 0;  // decode ring: one parity bit per slot of this warp
 };
@@ -117,30 +118,37 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 
 // ============================================================================ prefill item
 // One prefill item: a 128-row query tile of a chunk, one head, a range of keys in 128-key
-// steps. The MMA issuer keeps the tensor cores one step ahead: S of step j+1 (into the other TMEM
-// buffer) runs while the softmax of step j runs; P·V of step j follows the softmax. The two
-// softmax warpgroups split each 128x128 score tile by columns (64 keys each) and agree on the
-// row max through the TMEM exchange columns.
+// steps. Steps are numbered n by a counter that runs on across items; step n uses K/V stage,
+// S buffer and P buffer n & 1. Two warps feed the tensor cores, whose instruction queue is only
+// a few MMAs deep: warp 1 issues S(j) as soon as the softmax of step j-2 has read its buffer,
+// warp 3 issues P·V(j) as soon as P(j) is written, so one issuer's waits do not idle the pipe.
+// The two softmax warpgroups split each score tile by columns (64 keys each) and keep one
+// reference max per row in common: when no score of the step exceeds it by more than 2^8 (the
+// lazy-rescale threshold) — which a vote over both groups establishes — nothing is exchanged;
+// otherwise both groups read the whole row of S and move the reference alike.
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
                              const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
                              SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
+  static_assert(kVStages == 2, "V stages and TMEM buffers are indexed by n & 1");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int s = it[1], t = it[2], h = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
-  const int g = h / p.G;
+  const int s = it[1], t = it[2], h0 = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
+  const int g = h0 / p.G;  // the tile's heads h0 .. h0 + hp - 1 share kv-head g
   const int q0 = p.cu_seqlens[s];
   const int qlen = p.cu_seqlens[s + 1] - q0;
   const int L = p.kv_lens[s];
   const int P = L - qlen;  // cached prefix rows before this chunk
   const int ntiles = (ke - kb + kTileN - 1) / kTileN;
+  const uint32_t n0 = ps.t_cnt;  // this item's first step
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sKring = sQ + kSmemQ;
   const uint32_t sVring = sKring + kKStages * kSmemKTile;
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA producers
-    // Warp 0 loads Q and the K tiles, warp 2 the V tiles: the two rings advance independently.
-    // Lane i holds the block-table entry of block i of the next 4 steps (32 blocks): one
-    // coalesced read instead of a dependent global read per block.
+    // Warp 0 loads Q and the K tiles, warp 2 the V tiles. Lane i holds the block-table entry of
+    // block i of the next 4 steps (32 blocks): one coalesced read instead of a dependent global
+    // read per block. A K stage is free once the S that read it completed (k_empty); V stage
+    // n & 1 once P·V of step n-2 completed (pv_done, which the softmax also waits on).
     const bool is_k = warp == 0;
     const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
     const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
@@ -149,28 +157,31 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     if (is_k && lane == 0) {
       const uint32_t qbar = smem_u32(&ctl->q_full);
       mbar_arrive_expect_tx(qbar, kSmemQ);
-      tma_load_3d(sQ, tmq, qbar, 0, h, q0 + t * kTileM);
-      tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h, q0 + t * kTileM);
+      // box {64 dims, hp heads, tq tokens}: tile row r = token r / hp, head h0 + r % hp
+      tma_load_3d(sQ, tmq, qbar, 0, h0, q0 + t * p.tq);
+      tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h0, q0 + t * p.tq);
     }
-    const int nst = is_k ? kKStages : kVStages;
-    uint64_t* empty_bar = is_k ? ctl->k_empty : ctl->v_empty;
+    uint64_t* free_bar = is_k ? ctl->k_empty : ctl->pv_done;
+    const uint32_t nst = is_k ? kKStages : kVStages;
     uint64_t* full_bar = is_k ? ctl->k_full : ctl->v_full;
     const uint32_t ring = is_k ? sKring : sVring;
     const CUtensorMap* tm = is_k ? tmk : tmv;
-    int btv = -1;
-    const uint32_t base = ps.kv_cnt;
+    // entries of the next group of 4 steps are requested one group ahead
+    auto bt_fetch = [&](int j4) -> int {
+      const int bi = j4 * kBlocksPerTile + lane;
+      return bi < nblk_item ? bt_row[blk0 + bi] : -1;
+    };
+    int bt_next = bt_fetch(0), btv = -1;
     for (int j = 0; j < ntiles; ++j) {
       if ((j & 3) == 0) {
-        const int bi = j * kBlocksPerTile + lane;
-        btv = -1;
-        if (bi < nblk_item) {
-          int phys = bt_row[blk0 + bi];
-          if (phys < 0 || phys >= p.num_blocks) {
-            record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
-            phys = 0;
-          }
-          btv = phys;
+        const bool in_range = j * kBlocksPerTile + lane < nblk_item;
+        btv = bt_next;
+        if (j + 4 < ntiles) bt_next = bt_fetch(j + 4);
+        if (in_range && (btv < 0 || btv >= p.num_blocks)) {
+          record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+          btv = 0;
         }
+        if (!in_range) btv = -1;
       }
       int y[kBlocksPerTile];
 #pragma unroll
@@ -178,11 +189,11 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         const int e = __shfl_sync(0xffffffffu, btv, (j & 3) * kBlocksPerTile + b);
         y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
       }
-      const uint32_t cnt = base + j;
-      const int stage = cnt % nst;
+      const uint32_t n = n0 + j;
+      const uint32_t stage = n % nst;
       int okw = 1;
-      if (lane == 0)
-        okw = mbar_wait(smem_u32(&empty_bar[stage]), ((cnt / nst) & 1) ^ 1, wc, kSleepNs);
+      if (lane == 0)  // completion n/nst - 1 of the stage's barrier; a fresh barrier passes
+        okw = mbar_wait(smem_u32(&free_bar[stage]), ((n / nst) & 1) ^ 1, wc, kSleepNs);
       if (!__shfl_sync(0xffffffffu, okw, 0)) break;
       if (lane == 0) {
         const uint32_t full = smem_u32(&full_bar[stage]);
@@ -195,21 +206,27 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         }
       }
     }
-    ps.kv_cnt = base + ntiles;
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S issuer
+    // S(j) = Q K(j)ᵀ into S buffer n & 1, once the softmax of step j-2 has read that buffer.
     const uint32_t tmem = ctl->tmem_base;
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc, kSleepNs);
     tc_fence_after();
-    const uint32_t base = ps.kv_cnt;
-    // S of step j (global step n = t_cnt + j) into TMEM buffer n mod 2
-    auto issue_s = [&](int j) -> bool {
-      const uint32_t cnt = base + j, n = ps.t_cnt + j;
-      if (!mbar_wait(smem_u32(&ctl->k_full[cnt % kKStages]), (cnt / kKStages) & 1, wc, kSleepNs))
-        return false;
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const uint32_t n = n0 + j;
+      // completion (n-2)/2 of p_ready[n & 1]; the steps before this item's first two are done
+      if (j >= 2 && !mbar_wait(smem_u32(&ctl->p_ready[n & 1]), ((n >> 1) & 1) ^ 1, wc)) {
+        ok = false;
+        break;
+      }
+      const uint32_t ks = n % kKStages;
+      if (!mbar_wait(smem_u32(&ctl->k_full[ks]), (n / kKStages) & 1, wc)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t sK = sKring + (cnt % kKStages) * kSmemKTile;
+        const uint32_t sK = sKring + ks * kSmemKTile;
         const uint32_t dS = tmem + kTmemS + (n & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
@@ -219,17 +236,21 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&ctl->s_full[n & 1]));
-        umma_commit(smem_u32(&ctl->k_empty[cnt % kKStages]));
+        umma_commit(smem_u32(&ctl->k_empty[ks]));
       }
       __syncwarp();
-      return true;
-    };
-    if (ok && ntiles > 0) ok = issue_s(0);
-    if (ok && ntiles > 1) ok = issue_s(1);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ P·V issuer
+    // O += P(j) V(j) once the softmax of step j has written P(j). S and P·V use disjoint TMEM
+    // columns, so the two issuers need no order between them; each commit tracks only its own
+    // thread's MMAs.
+    const uint32_t tmem = ctl->tmem_base;
+    bool ok = true;
     for (int j = 0; ok && j < ntiles; ++j) {
-      const uint32_t cnt = base + j, n = ps.t_cnt + j;
-      if (!mbar_wait(smem_u32(&ctl->p_ready[n & 1]), (n >> 1) & 1, wc, kSleepNs) ||
-          !mbar_wait(smem_u32(&ctl->v_full[cnt % kVStages]), (cnt / kVStages) & 1, wc, kSleepNs)) {
+      const uint32_t n = n0 + j;
+      if (!mbar_wait(smem_u32(&ctl->p_ready[n & 1]), (n >> 1) & 1, wc) ||
+          !mbar_wait(smem_u32(&ctl->v_full[n & 1]), (n >> 1) & 1, wc)) {
         ok = false;
         break;
       }
@@ -238,7 +259,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         // Rows past the sequence end inside its last block may hold anything (even NaN); P is
         // zero there but 0 * NaN is not, so clear those V rows before the P·V product.
         const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
-        uint8_t* vbase = smem + (sVring - sQ) + (cnt % kVStages) * kSmemKTile;
+        uint8_t* vbase = smem + (sVring - sQ) + (n & 1) * kSmemKTile;
         for (int c = lane; c < (r1 - r0) * 16; c += 32) {
           const int r = r0 + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
           *reinterpret_cast<uint4*>(vbase + half * (kSmemKTile / 2) + r * 128 + q16 * 16) =
@@ -249,149 +270,168 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t sV = sVring + (cnt % kVStages) * kSmemKTile;
-        const uint32_t aP = tmem + kTmemS + (n & 1) * 128;
+        const uint32_t sV = sVring + (n & 1) * kSmemKTile;
+        const uint32_t aP = tmem + kTmemP + (n & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // P of keys 16kk.. sits at column 64*(kk/4) + 8*(kk%4) of its S buffer; V is N-major:
-          // 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
+          // P of keys 16kk.. at column 8kk of its buffer; V is N-major: 64-column halves
+          // 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
           const uint64_t bd = sdesc_sw128(sV + kk * 2048, kSmemKTile / 2, 1024);
-          umma_ts(tmem + kTmemO, aP + (kk >> 2) * 64 + (kk & 3) * 8, bd, kIdescPV,
-                  (j == 0 && kk == 0) ? 0u : 1u);
+          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (j == 0 && kk == 0) ? 0u : 1u);
         }
         umma_commit(smem_u32(&ctl->pv_done[n & 1]));
-        umma_commit(smem_u32(&ctl->v_empty[cnt % kVStages]));
       }
       __syncwarp();
-      // S of step j+2 reuses this buffer: it is issued after the P·V just issued, which reads it
-      if (j + 2 < ntiles && !issue_s(j + 2)) {
-        ok = false;
-        break;
-      }
     }
-    ps.kv_cnt = base + ntiles;
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
     // ------------------------------------------------------------------ softmax (1 row/thread)
-    const int grp = (warp - kSoftmaxWarp0) >> 2;  // columns 64*grp .. 64*grp + 63 of each S
+    const int grp = (warp - kSoftmaxWarp0) >> 2;  // keys 64*grp .. 64*grp + 63 of each step
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tO = trow + kTmemO + grp * 64, tX = trow + kTmemX;
-    const int qi = t * kTileM + row;  // local index of this thread's query in the chunk
+    const uint32_t tO = trow + kTmemO + grp * 64;
+    const int qi = t * p.tq + (row >> p.hp_log2);  // this row's token (index in the chunk)
+    const int h = h0 + (row & ((1 << p.hp_log2) - 1));  // and query head
     const bool valid = qi < qlen;
-    const int limit = min(P + qi + 1, ke) - grp * 64;  // keys visible to this group: [.., limit)
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    for (int j = 0; j < ntiles; ++j) {
-      const uint32_t n = ps.t_cnt + j;
-      const uint32_t tS = trow + kTmemS + (n & 1) * 128 + grp * 64;
-      // After a failed wait the loop still runs (every wait then fails at once), so that both
-      // warpgroups pass the same named barriers whatever happened.
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[n & 1]), (n >> 1) & 1, wc));
-      tc_fence_after();
-      const int nvis = limit - (kb + j * kTileN);
-      const bool full_tile = __all_sync(0xffffffffu, nvis >= 64);
-      // pass 1: this group's partial row max, swapped with the other group through TMEM
+    const int lim = min(P + qi + 1, ke);  // keys [.., lim) are visible to this row
+    // max over 64 columns of S from `taddr`, of which the first `vis` are visible
+    auto rowmax64 = [&](uint32_t taddr, int vis) -> float {
+      const bool full = __all_sync(0xffffffffu, vis >= 64);
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll 1
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32];
-        tmem_ld32(tS + ch * 32, sr);
+        tmem_ld32(taddr + ch * 32, sr);
         tmem_ld_wait();
-        if (!full_tile) {
+        if (!full) {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (ch * 32 + c >= nvis) sr[c] = f2u(-INFINITY);
+            if (ch * 32 + c >= vis) sr[c] = f2u(-INFINITY);
         }
 #pragma unroll
         for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
       }
-      const float mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      tmem_st1(tX + (n & 1) * 2 + grp, f2u(mine));
-      tmem_st_wait();
-      tc_fence_before();
-      named_bar_sync(2, 256);
+      return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    };
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    for (int j = 0; j < ntiles; ++j) {
+      const uint32_t n = n0 + j;
+      const uint32_t tS = trow + kTmemS + (n & 1) * 128;
+      const uint32_t tP = trow + kTmemP + (n & 1) * 64 + grp * 32;
+      // After a failed wait the loop still runs (every wait then fails at once), so that both
+      // warpgroups pass the same named barriers whatever happened.
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[n & 1]), (n >> 1) & 1, wc));
       tc_fence_after();
-      const float other = u2f(tmem_ld1(tX + (n & 1) * 2 + (grp ^ 1)));
+      const int nvis = lim - (kb + j * kTileN);  // visible columns of this step: [0, nvis)
+      const int vis = nvis - grp * 64;            // visible columns of this group: [0, vis)
+      const bool full = __all_sync(0xffffffffu, vis >= 64);
+      // this group's 64 scores stay in registers from the max to the exponentials
+      uint32_t sa[32], sb[32];
+      tmem_ld32(tS + grp * 64, sa);
+      tmem_ld32(tS + grp * 64 + 32, sb);
       tmem_ld_wait();
-      const float mt = fmaxf(mine, other) * p.scale_log2;  // scale > 0: max of scaled scores
-      // Lazy rescale: the reference max moves only when a score exceeds it by more than 2^8;
-      // O and l stay consistent with whichever reference is current. Both groups see the same
-      // row max and history, so they decide alike.
-      const float m_new = fmaxf(m, mt);
-      const bool resc = m_new > m + 8.f;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2(m - m_new);
-        m = m_new;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // O holds P·V of the earlier steps once step j-1's product completed (the one before
-        // finished ahead of it); at most one completion of that barrier is pending.
-        ok = __all_sync(0xffffffffu,
-                        ok && mbar_wait(smem_u32(&ctl->pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1, wc));
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {  // this group's 64 columns of O
-          uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
-          tmem_ld_wait();
+      if (!full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-          tmem_st32(tO + ch * 32, o);
+        for (int c = 0; c < 32; ++c) {
+          if (c >= vis) sa[c] = f2u(-INFINITY);
+          if (c + 32 >= vis) sb[c] = f2u(-INFINITY);
         }
-        tmem_st_wait();
       }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(u2f(sa[i]), u2f(sa[i + 8]), u2f(sa[i + 16]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], u2f(sa[i + 24]), u2f(sb[i]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], u2f(sb[i + 8]), u2f(sb[i + 16]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], u2f(sb[i + 24]));
+      const float mine = fmaxf(fmax3(mx[0], mx[1], mx[2]),
+                               fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+      // scale > 0, so the max of the scaled scores is the scaled max
+      const bool need = mine * p.scale_log2 > m + 8.f;
+      float alpha = 1.f;
+      if (bar_red_or(2, 256, need)) {
+        // some row moves its reference: both groups take the max of the whole row, so they move
+        // it alike (m, O and l stay consistent with whichever reference is current)
+        const float other = rowmax64(tS + (grp ^ 1) * 64, nvis - (grp ^ 1) * 64);
+        const float m_new = fmaxf(m, fmaxf(mine, other) * p.scale_log2);
+        const bool resc = m_new > m + 8.f;
+        if (resc) {
+          alpha = ex2(m - m_new);
+          m = m_new;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // O holds P·V of the earlier steps once step j-1's product completed (all before it
+          // completed first); at most one completion of that barrier is pending.
+          ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done[(n - 1) & 1]),
+                                                       ((n - 1) >> 1) & 1, wc));
+          tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < 2; ++ch) {  // this group's 64 columns of O
+            uint32_t o[32];
+            tmem_ld32(tO + ch * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+            tmem_st32(tO + ch * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P buffer n & 1 is free once P·V of step n-2 completed (a fresh barrier passes)
+      ok = __all_sync(0xffffffffu,
+                      ok && mbar_wait(smem_u32(&ctl->pv_done[n & 1]), ((n >> 1) & 1) ^ 1, wc));
+      tc_fence_after();
       const float mref = m == -INFINITY ? 0.f : m;
       const float2 nm2 = make_float2(-mref, -mref);
-      // pass 2: exponentials, partial row sum, and P (bf16 pairs) written over the group's own,
-      // already read S columns (chunk ch writes columns 16ch..16ch+15 of the group's range)
+      // exponentials of this group's 64 columns, their sum, and P as bf16 pairs
       float2 sum[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sr[32];
-        tmem_ld32(tS + ch * 32, sr);
-        tmem_ld_wait();
-        if (!full_tile) {
+      uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (ch * 32 + c >= nvis) sr[c] = f2u(-INFINITY);
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float2 xv = ffma2(make_float2(u2f(sr[2 * c]), u2f(sr[2 * c + 1])), c2, nm2);
-          const float2 e = make_float2(ex2(xv.x), ex2(xv.y));
-          sum[c & 3] = fadd2(sum[c & 3], e);
-          pk[c] = pack_bf16x2(e.x, e.y);
-        }
-        tmem_st16(tS + ch * 16, pk);
+      for (int c = 0; c < 16; ++c) {
+        const float2 xv = ffma2(make_float2(u2f(sa[2 * c]), u2f(sa[2 * c + 1])), c2, nm2);
+        const float2 e = make_float2(ex2(xv.x), ex2(xv.y));
+        sum[c & 3] = fadd2(sum[c & 3], e);
+        pk[c] = pack_bf16x2(e.x, e.y);
       }
+      tmem_st16(tP, pk);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float2 xv = ffma2(make_float2(u2f(sb[2 * c]), u2f(sb[2 * c + 1])), c2, nm2);
+        const float2 e = make_float2(ex2(xv.x), ex2(xv.y));
+        sum[c & 3] = fadd2(sum[c & 3], e);
+        pk[c] = pack_bf16x2(e.x, e.y);
+      }
+      tmem_st16(tP + 16, pk);
       const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
       l = l * alpha + (s01.x + s01.y);  // this group's share of the row sum
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl->p_ready[n & 1]));
     }
-    if (ok && ntiles > 0) {  // the last step's P·V (all earlier ones completed before it)
-      const uint32_t nl = ps.t_cnt + ntiles - 1;
+    if (ok && ntiles > 0) {  // the last P·V; every S completed before the softmax that fed it
+      const uint32_t nl = n0 + ntiles - 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[nl & 1]), (nl >> 1) & 1, wc));
       tc_fence_after();
     }
-    // the full row sum: swap the two groups' shares through TMEM
-    tmem_st1(tX + 4 + grp, f2u(l));
+    // the full row sum: swap the two groups' shares through two columns of the last step's P
+    // buffer, whose P·V has completed (and every MMA of the item before it)
+    const uint32_t tX = trow + kTmemP + ((n0 + (ntiles > 0 ? ntiles : 1) - 1) & 1) * 64;
+    tmem_st1(tX + grp, f2u(l));
     tmem_st_wait();
     tc_fence_before();
     named_bar_sync(2, 256);
     tc_fence_after();
-    const float lt = l + u2f(tmem_ld1(tX + 4 + (grp ^ 1)));
+    const float lt = l + u2f(tmem_ld1(tX + (grp ^ 1)));
     tmem_ld_wait();
     // ------------------------------------------------------------------ epilogue
     {
@@ -438,42 +478,50 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         if (ctl->merge_last[0] && ok) {
           __threadfence();
           if (valid) {
+            // the planner makes at most kMaxPrefillSplits splits; all loads of one pass are
+            // independent, so each pass costs one memory latency rather than one per split
+            const float* ml = p.partial_p + (size_t)slot0 * kPrefillSlotFloats + kTileM * kHeadDim;
+            float f[kMaxPrefillSplits];
             float mx = -INFINITY;
-            for (int k = 0; k < nsplit; ++k) {
-              const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-              mx = fmaxf(mx, __ldcg(sl + kTileM * kHeadDim + row));
+#pragma unroll
+            for (int k = 0; k < kMaxPrefillSplits; ++k) {
+              f[k] = k < nsplit ? __ldcg(ml + (size_t)k * kPrefillSlotFloats + row) : -INFINITY;
+              mx = fmaxf(mx, f[k]);
             }
             float den = 0.f;
-            for (int k = 0; k < nsplit; ++k) {
-              const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-              const float mk = __ldcg(sl + kTileM * kHeadDim + row);
-              if (mk != -INFINITY) den += ex2(mk - mx) * __ldcg(sl + kTileM * kHeadDim + kTileM + row);
+#pragma unroll
+            for (int k = 0; k < kMaxPrefillSplits; ++k) {
+              const float lk = k < nsplit ? __ldcg(ml + (size_t)k * kPrefillSlotFloats + kTileM + row) : 0.f;
+              f[k] = f[k] == -INFINITY ? 0.f : ex2(f[k] - mx);  // weight of split k
+              den += f[k] * lk;
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
             uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim + grp * 64;
+            const float* ob = p.partial_p + (size_t)slot0 * kPrefillSlotFloats + row * kHeadDim + grp * 64;
 #pragma unroll 1
-            for (int ch = 0; ch < 2; ++ch) {
-              float acc[32];
+            for (int ch = 0; ch < 4; ++ch) {  // 16 columns at a time
+              float acc[16];
 #pragma unroll
-              for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-              for (int k = 0; k < nsplit; ++k) {
-                const float* sl = p.partial_p + (size_t)(slot0 + k) * kPrefillSlotFloats;
-                const float mk = __ldcg(sl + kTileM * kHeadDim + row);
-                if (mk == -INFINITY) continue;
-                const float f = ex2(mk - mx) * inv;
-                const float4* src = reinterpret_cast<const float4*>(sl + row * kHeadDim + grp * 64 + ch * 32);
+              for (int c = 0; c < 16; ++c) acc[c] = 0.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                  const float4 v = __ldcg(src + c);
-                  acc[4 * c] += f * v.x;
-                  acc[4 * c + 1] += f * v.y;
-                  acc[4 * c + 2] += f * v.z;
-                  acc[4 * c + 3] += f * v.w;
+              for (int k = 0; k < kMaxPrefillSplits; ++k) {
+                if (k < nsplit) {
+                  const float4* src =
+                      reinterpret_cast<const float4*>(ob + (size_t)k * kPrefillSlotFloats + ch * 16);
+                  const float fk = f[k] * inv;
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) {
+                    const float4 v = __ldcg(src + c);
+                    acc[4 * c] += fk * v.x;
+                    acc[4 * c + 1] += fk * v.y;
+                    acc[4 * c + 2] += fk * v.z;
+                    acc[4 * c + 3] += fk * v.w;
+                  }
                 }
               }
-              uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+              uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 16);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
+              for (int i = 0; i < 2; ++i)
                 d4[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
                                    pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
                                    pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
@@ -489,7 +537,6 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   // every thread of the prefill slot keeps the same pipeline positions
   ps.q_cnt++;
   ps.t_cnt += ntiles;
-  if (warp != 0 && warp != 1 && warp != 2) ps.kv_cnt += ntiles;
   named_bar_sync(1, kPrefillThreads);
 }
 
@@ -1021,10 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->k_full[i]), 1);
       mbar_init(smem_u32(&ctl->k_empty[i]), 1);
     }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(smem_u32(&ctl->v_full[i]), 1);
-      mbar_init(smem_u32(&ctl->v_empty[i]), 1);
-    }
+    for (int i = 0; i < kVStages; ++i) mbar_init(smem_u32(&ctl->v_full[i]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
       mbar_init(smem_u32(&ctl->p_ready[i]), 256);
@@ -1145,13 +1189,14 @@ struct CudaState {
   const void *kq = nullptr, *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
 };
 
-// Q: 3-D {dim, head, token} so one box is 128 tokens x 64 dims of one head.
-static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp) {
+// Q: 3-D {dim, head, token} so one box is 64 dims of hp heads x 128/hp tokens: the 128 rows of
+// a prefill tile, token-major.
+static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp, int hp) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hq, (cuuint64_t)Tp};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Hq * kHeadDim * 2};
-  cuuint32_t box[3] = {64, 1, kTileM};
+  cuuint32_t box[3] = {64, (cuuint32_t)hp, (cuuint32_t)(kTileM / hp)};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1387,7 +1432,7 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
   CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
   const int64_t pool_rows = (int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize;
   if (n_p > 0 && cs->kq != q_prefill) {
-    if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens))
+    if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens, plan->head_pack))
       return POD_ATTN_ERR_CUDA;
     cs->kq = q_prefill;
   }
@@ -1432,6 +1477,8 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
   p.pool_rows = (int32_t)pool_rows;
   p.num_sms = plan->num_sms;
   p.max_prefill_per_sm = plan->max_prefill_per_sm;
+  p.hp_log2 = __builtin_ctz((unsigned)plan->head_pack);
+  p.tq = plan->tile_tokens;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.timeout_ns = kWaitTimeoutNs;
   int32_t* counters = reinterpret_cast<int32_t*>(ws + w.counters);

@@ -19,8 +19,9 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 // One persistent CTA per SM holds two concurrent virtual-CTA slots ("POD-Attention" digest,
 // §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
 //  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns — warp 0 issues
-//    the TMA loads of Q and K, warp 2 those of V, warp 1 issues tcgen05 MMAs, and warps 4-7 and
-//    8-11 are two softmax warpgroups that share each 128x128 score tile (64 columns each);
+//    the TMA loads of Q and K, warp 2 those of V, warps 1 and 3 issue the S and P·V tcgen05
+//    MMAs, and warps 4-7 and 8-11 are two softmax warpgroups that share each 128x128 score
+//    tile (64 columns each);
 //  * the decode slot (warps 12-15): decode items, on their own ticket loop.
 // Once the prefill list is drained, the prefill slot's warps 4-7 and 8-11 become two more
 // 4-warp decode slots. Every decode item thus runs on exactly 4 warps, whichever slot takes it,
@@ -33,9 +34,13 @@ constexpr int kDecodeWarp0 = 12;        // decode slot: warps 12-15
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp
 
-// Prefill step: one 128-row query tile x 128 keys. S is double-buffered in TMEM, so S of step
-// j+1 runs on the tensor cores while the softmax of step j runs; two K and two V stages keep
-// the loads one step ahead of both.
+// Prefill tile: 128 query rows = T tokens x hp query heads of one kv-head group (hp = the largest
+// power of two dividing the group size, T = 128 / hp; row r is token r / hp, head h0 + r % hp).
+// All hp heads read the same K and V, so one K/V tile serves hp heads ("LLMSO - W4", §"KV 헤드
+// 줄이기": the heads of a group share their K/V).
+// Prefill step: one 128-row query tile x 128 keys. S and P are double-buffered in TMEM, so the
+// tensor cores compute S of the next steps while the softmax of this one runs; K stages
+// (step % kKStages) and V stages (step & 1) keep the loads ahead of both.
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 constexpr int kKStages = 2;
@@ -59,20 +64,21 @@ static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
 static_assert(2 * (kSmemDecodeRing + kDecodeWarps * kSmemScoresPerWarp) <= kSmemPrefill,
               "the two decode slots of the prefill warps must fit the prefill region");
 
-// TMEM columns (the whole SM): O (fp32, 128 columns), then two S buffers (fp32, 128 columns
-// each); P of a step (bf16 pairs) overwrites the S columns its own warpgroup has read. Columns
-// from kTmemX are the two softmax warpgroups' exchange of per-row partial maxima and sums.
+// TMEM columns (the whole SM): O (fp32, 128 columns), two S buffers (fp32, 128 columns each)
+// and two P buffers (bf16 pairs, 64 columns each). P has its own columns so that S of step j+2
+// can be computed into the buffer of step j as soon as the softmax of step j has read it, before
+// P·V of step j.
 constexpr int kTmemCols = 512;
 constexpr int kTmemO = 0;
-constexpr int kTmemS = 128;    // + 128 * buffer
-constexpr int kTmemX = 384;    // + 2 * (step parity) + group: partial max; + 4 + group: sum
+constexpr int kTmemS = 128;    // + 128 * (step & 1)
+constexpr int kTmemP = 384;    // + 64 * (step & 1)
 
 // Work item: kItemWords int32 words.
 //   [0] kind         0 = prefill, 1 = decode
 //   [1] seq          prefill: chunk index s in [0, Np); decode: d in [0, Nd)
-//   [2] tile / kvh   prefill: index t of the 128-row query tile (rows 128t .. 128t + 127
-//                    of the chunk); decode: kv-head g
-//   [3] head         prefill: query head h; decode: 0
+//   [2] tile / kvh   prefill: index t of the query tile (chunk tokens T t .. T t + T - 1, with
+//                    T = 128 / hp tokens per tile); decode: kv-head g
+//   [3] head         prefill: first query head h0 of the tile's hp heads; decode: 0
 //   [4] key_begin    first key row of this split (prefill: multiple of 128; decode: of 16)
 //   [5] key_end      one past the last key row this split may read
 //   [6] unit         -1 = the only split (write the output directly), else the unit index
@@ -81,6 +87,9 @@ constexpr int kItemWords = 8;
 // Unit (an output assembled from several splits): kUnitWords int32 words.
 //   [0] nsplit  [1] first partial slot  [2] kind  [3] unused
 constexpr int kUnitWords = 4;
+
+// Most splits of one prefill output (the planner's cap; the merge keeps one weight per split).
+constexpr int kMaxPrefillSplits = 8;
 
 // Partial-result slots: fp32 o[rows][128] then m[rows] then l[rows] (m, l in log2 units).
 constexpr int kPrefillSlotFloats = kTileM * (kHeadDim + 2);
@@ -119,6 +128,8 @@ struct pod_attn_plan_s {
   pod_attn_problem prob{};
   pod_attn_options opt{};
   int group = 1;
+  int head_pack = 1;                      // hp: query heads per prefill tile
+  int tile_tokens = pod::kTileM;          // T = 128 / hp: tokens per prefill tile
   int num_sms = 0, ctas_per_sm = 2, max_prefill_per_sm = 1;
   int grid_fused = 0, grid_prefill = 0, grid_decode = 0;
   std::vector<int32_t> cu, kv;            // host copies of the lengths

@@ -87,19 +87,22 @@ def _cdiv(a, b):
 
 
 def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
-    """Items: prefill = (chunk, 128-row query tile, head, split) over 128-key steps
-    (cost 57 each), decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
+    """Items: prefill = (chunk, query tile of 128/hp tokens x hp heads, first head, split) over
+    128-key steps (cost 57 each), with hp the largest power of two dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
     item slots per SM; split when an output costs more than a quarter of a slot's share."""
     np_ = len(cu) - 1 if cu else 0
     slots = num_sms * 2
+    G = Hq // Hkv
+    hp = max(x for x in (1, 2, 4, 8) if G % x == 0)
+    tq = 128 // hp
     pu, du, total = [], [], 0
     for s in range(np_):
         q, L = cu[s + 1] - cu[s], kv[s]
         P = L - q
-        for t in range(_cdiv(q, 128)):
-            kend = P + min(q, (t + 1) * 128)
+        for t in range(_cdiv(q, tq)):
+            kend = P + min(q, (t + 1) * tq)
             nt = _cdiv(kend, 128)
-            for h in range(Hq):
+            for h in range(0, Hq, hp):
                 pu.append((s, t, h, kend, nt))
                 total += nt * 57
     for d in range(nd):
@@ -108,6 +111,8 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
             du.append((d, g, L, _cdiv(L, 16)))
             total += _cdiv(L, 16) * 8
     target = max(1, total // (slots * 4))
+    total_p = sum(nt * 57 for *_, nt in pu)
+    target_p = max(target, total_p // (num_sms * 4))
     units, lp, ld = [], [], []
     slots_used = [0, 0]
 
@@ -121,8 +126,8 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
         if psplit:
             ns = psplit
         else:
-            ns = min(_cdiv(nt * 57, target), max(1, nt // 4), 8)
-        ns = max(1, min(ns, nt))
+            ns = min(_cdiv(nt * 57, target_p), max(1, nt // 4))
+        ns = max(1, min(ns, nt, 8))
         chunk = _cdiv(nt, ns)
         ns = _cdiv(nt, chunk)
         u = add_unit(ns, 0) if ns > 1 else -1
@@ -191,6 +196,8 @@ def test_planner_covers_every_key_once(lib, i):
         cu.append(cu[-1] + q)
     p = B.Plan(Hq, Hkv, cu, pkv + dkv, len(dkv), 10, _cdiv(max(pkv + dkv), 16), 0.1,
                num_sms=152)
+    hp = max(x for x in (1, 2, 4, 8) if (Hq // Hkv) % x == 0)   # heads per prefill tile
+    tq = 128 // hp                                                # tokens per prefill tile
     items_p, items_d, units = p.items()
     cover = {}
     for it in items_p + items_d:
@@ -210,9 +217,10 @@ def test_planner_covers_every_key_once(lib, i):
         else:
             t = key[2]
             q = q_lens[seq]
-            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * 128)
-    # every (query tile, head) and (decode seq, kv-head) appears
-    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, 128) for q in q_lens) * Hq
+            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * tq)
+            assert key[3] % hp == 0
+    # every (query tile, block of hp heads) and (decode seq, kv-head) appears
+    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, tq) for q in q_lens) * (Hq // hp)
     assert len([k for k in cover if k[0] == 1]) == len(dkv) * Hkv
 
 

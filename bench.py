@@ -496,13 +496,16 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
 
 
 def _traffic_from_profiles(cfg):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if present."""
-    path = os.path.join(ROOT, "profiles", f"traffic_config{cfg}.json")
+    """DRAM bytes (read + write) per launch of the fused kernel, from the committed ncu summary
+    `profiles/traffic_config<cfg>.md` (its line `dram_bytes_per_launch: N`), if present."""
+    path = os.path.join(ROOT, "profiles", f"traffic_config{cfg}.md")
     try:
-        d = json.load(open(path))
-        return d.get("dram_bytes_per_launch")
-    except Exception:
-        return None
+        for line in open(path):
+            if line.strip().startswith("dram_bytes_per_launch:"):
+                return int(line.split(":", 1)[1].strip())
+    except (OSError, ValueError):
+        pass
+    return None
 
 
 if __name__ == "__main__":

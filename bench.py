@@ -51,10 +51,13 @@ def _workload_name(cfg, batch) -> str:
 
 def _config_dict(args, batch, world):
     """The workload description both arms print (identical keys and values)."""
-    return {"workload": _workload_name(args.case or args.config, batch),
-            "config_index": args.case or args.config,
-            "l2": "flushed between steps (256 MiB write)",
-            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+    d = {"workload": _workload_name(args.case or args.config, batch),
+         "config_index": args.case or args.config,
+         "l2": "flushed between steps (256 MiB write)",
+         "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+    if getattr(args, "append", False):
+        d["kv_append"] = "new K/V rows written into the pools inside each step"
+    return d
 
 
 def _make_batch(args, device):
@@ -225,6 +228,9 @@ def main():
     ap.add_argument("--trace", default=None, choices=["a", "b"],
                     help="the 200-iteration hybrid-batching trace (mix a or b) instead of --config")
     ap.add_argument("--trace-iters", type=int, default=200)
+    ap.add_argument("--append", action="store_true",
+                    help="every step also writes the iteration's new K/V rows into the pools "
+                         "(pod_attn_run_append); the metric then includes that step")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -271,9 +277,19 @@ def main():
         plan.upload(ws, stream)
         plans[v] = (plan, ws)
 
+    if args.append:
+        # the new rows come separately; the pools start without them (NaN) and every step
+        # writes them again (the same bytes: the step's work does not change)
+        k_new, v_new, batch.k_pool, batch.v_pool = W.split_off_new_rows(batch)
+
     def step(v):
         plan, ws = plans[v]
-        B.run_batch(plan, batch, ws, o_p, o_d, stream=stream, stream2=side)
+        if args.append:
+            plan.run_append(batch.q_prefill, batch.q_decode, k_new, v_new, batch.k_pool,
+                            batch.v_pool, batch.block_tables, batch.cu_seqlens_q, batch.kv_lens,
+                            o_p, o_d, ws, stream=stream, stream2=side)
+        else:
+            B.run_batch(plan, batch, ws, o_p, o_d, stream=stream, stream2=side)
 
     if args.only:                    # profiling mode: warm-up + K plain steps, nothing else
         for _ in range(args.warmup + args.steps):

@@ -90,6 +90,8 @@ def load():
     lib.pod_attn_upload.argtypes = [P, P, SZ, P]
     lib.pod_attn_run.restype = I32
     lib.pod_attn_run.argtypes = [P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+    lib.pod_attn_run_append.restype = I32
+    lib.pod_attn_run_append.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
     lib.pod_attn_last_device_status.restype = I32
     lib.pod_attn_last_device_status.argtypes = [P, P, P]
     lib.pod_attn_get_plan_info.restype = I32
@@ -219,6 +221,18 @@ class Plan:
             _ptr(o_decode), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream),
             _stream_ptr(stream2) if stream2 is not None else None)
         _check(code, "pod_attn_run")
+
+    def run_append(self, q_prefill, q_decode, k_new, v_new, k_pool, v_pool, block_tables,
+                   cu_seqlens_q, kv_lens, o_prefill, o_decode, workspace, stream=None,
+                   stream2=None):
+        """pod_attn_run_append: write the new tokens' K/V rows (`k_new`, `v_new`, bf16
+        [T_p + Nd][Hkv][128]) into the pools, then run the attention."""
+        code = load().pod_attn_run_append(
+            self.handle, _ptr(q_prefill), _ptr(q_decode), _ptr(k_new), _ptr(v_new),
+            _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(kv_lens),
+            _ptr(o_prefill), _ptr(o_decode), workspace.data_ptr(), workspace.numel(),
+            _stream_ptr(stream), _stream_ptr(stream2) if stream2 is not None else None)
+        _check(code, "pod_attn_run_append")
 
     def device_status(self, workspace, stream=None) -> int:
         return int(load().pod_attn_last_device_status(self.handle, workspace.data_ptr(),

@@ -195,6 +195,16 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   for (auto& it : lp) plan->items_p.insert(plan->items_p.end(), it.w, it.w + kItemWords);
   for (auto& it : ld) plan->items_d.insert(plan->items_d.end(), it.w, it.w + kItemWords);
   plan->num_p_slots = p_slots;
+  // where each token of this iteration sits in its sequence (the KV append writes its K/V
+  // row there): chunk token i of prefill sequence s at kv_len - q_len + i, a decode token at
+  // kv_len - 1 ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM", §"한 스텝에 여러 종류의 request
+  // 섞기": an extend token follows the cached rows, a decode token is the last row)
+  plan->new_rows.clear();
+  for (int s = 0; s < Np; ++s) {
+    const int32_t q = cu[s + 1] - cu[s], P = kv[s] - q;
+    for (int32_t i = 0; i < q; ++i) plan->new_rows.insert(plan->new_rows.end(), {s, P + i});
+  }
+  for (int d = 0; d < Nd; ++d) plan->new_rows.insert(plan->new_rows.end(), {Np + d, kv[Np + d] - 1});
   plan->num_d_slots = d_slots;
 
   const int n_p = (int)lp.size(), n_d = (int)ld.size();
@@ -210,7 +220,7 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   off += 256;
   w.counters = off;
   w.counter_block_words = kCounterHeader + (size_t)num_sms;
-  off = align256(off + 3 * w.counter_block_words * 4);
+  off = align256(off + kNumModes * w.counter_block_words * 4);
   w.arrive = off;
   off = align256(off + plan->units.size() / kUnitWords * 4);
   w.zero_bytes = off;
@@ -220,6 +230,8 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   off = align256(off + plan->items_d.size() * 4);
   w.units = off;
   off = align256(off + plan->units.size() * 4);
+  w.new_rows = off;
+  off = align256(off + plan->new_rows.size() * 4);
   w.partial_p = off;
   off = align256(off + (size_t)p_slots * kPrefillSlotFloats * 4);
   w.partial_d = off;

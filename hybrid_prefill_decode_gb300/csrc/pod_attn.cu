@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -62,6 +63,15 @@ struct Params {
   int32_t* arrive;
   int32_t* status;    // [0] status word, [1] unused
   pod_attn_item_record* records;
+  // KV append (pod_attn_run_append): the new K/V rows and where they go
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_pool_w;
+  uint16_t* v_pool_w;
+  const int32_t* new_rows;  // (sequence, position) per new token
+  int32_t n_new;            // new tokens this launch appends (0 = no append)
+  int32_t new_first;        // index of the first of them in k_new / v_new / new_rows
+  int32_t wait_append;      // items wait until every CTA has done its share of the append
   int32_t n_items_p, n_items_d;
   int32_t Hq, Hkv, G, Np, Nd, num_blocks, maxb;
   int32_t pool_rows;  // num_blocks * Hkv * 16: first row past the pools (TMA fills zeros)
@@ -94,6 +104,7 @@ static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 // Pipeline positions; each role advances the fields it owns, across items.
 struct PipeState {
   uint32_t q_cnt = 0;   // prefill items (query-tile loads)
+  bool appended = false;  // this thread has seen the launch's KV append complete
   uint32_t t_cnt = 0;   // 128-key steps whose S, P and P·V barriers have turned over
   uint32_t dphase = 0;  // decode ring: one parity bit per slot of this warp
 };
@@ -114,6 +125,52 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ uint16_t f2bf(float f) {
   return static_cast<uint16_t>(pack_bf16x2(f, 0.f) & 0xFFFFu);
+}
+
+// ============================================================================ KV append
+// The step before attention ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM", §"PagedAttention":
+// the cache is append-only; §"한 스텝에 여러 종류의 request 섞기"): every new token's K and V row
+// of each kv-head is written into its paged block. One warp per (token, kv-head): lanes 0-15 copy
+// the K row, lanes 16-31 the V row, 16 bytes each (coalesced 256-byte rows).
+__device__ void append_rows(const Params& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = p.n_new * p.Hkv;
+  for (int u = blockIdx.x * kWarps + warp; u < units; u += gridDim.x * kWarps) {
+    const int tok = p.new_first + u / p.Hkv, g = u % p.Hkv;
+    const int seq = p.new_rows[2 * tok], pos = p.new_rows[2 * tok + 1];
+    const int phys = p.block_tables[(size_t)seq * p.maxb + pos / kBlockSize];
+    if (phys < 0 || phys >= p.num_blocks) {
+      if (lane == 0) record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+      continue;
+    }
+    const size_t row = ((size_t)phys * p.Hkv + g) * kBlockSize + pos % kBlockSize;
+    const uint16_t* src = (lane < 16 ? p.k_new : p.v_new) + ((size_t)tok * p.Hkv + g) * kHeadDim;
+    uint16_t* dst = (lane < 16 ? p.k_pool_w : p.v_pool_w) + row * kHeadDim;
+    reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
+  }
+}
+
+// Before a thread issues copies of pool rows that the launch appends: wait (bounded) until every
+// CTA has finished its share, then order those generic-proxy writes before this thread's
+// async-proxy (TMA, bulk copy) reads. Returns false on timeout or abort.
+__device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc) {
+  if (!p.wait_append || ps.appended) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    int done;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(p.counters + 3) : "memory");
+    if (done >= (int)gridDim.x) break;
+    if (*wc.abort) return false;
+    if (globaltimer() - t0 > wc.timeout_ns) {
+      *wc.abort = 1;
+      record_error(wc.status, POD_ATTN_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(200);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  ps.appended = true;
+  return true;
 }
 
 // ============================================================================ prefill item
@@ -172,7 +229,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       return bi < nblk_item ? bt_row[blk0 + bi] : -1;
     };
     int bt_next = bt_fetch(0), btv = -1;
-    for (int j = 0; j < ntiles; ++j) {
+    // the chunk's own rows [P, P + qlen) may be appended by this launch
+    int oka = 1;
+    if (lane == 0 && ke > P) oka = wait_appended(p, ps, wc);
+    for (int j = 0; __shfl_sync(0xffffffffu, oka, 0) && j < ntiles; ++j) {
       if ((j & 3) == 0) {
         const bool in_range = j * kBlocksPerTile + lane < nblk_item;
         btv = bt_next;
@@ -599,7 +659,12 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
   const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
   const int blk0 = kb / kBlockSize;
   const bool mine = wl >= 0 && wl < dc.nw;
-  const int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  {  // the sequence's last row (this step's token) may be appended by this launch
+    int oka = 1;
+    if (lane == 0 && nmine > 0 && ke >= p.kv_lens[p.Np + d]) oka = wait_appended(p, ps, wc);
+    if (!__shfl_sync(0xffffffffu, oka, 0)) nmine = 0;
+  }
   uint8_t* ring = dc.ring + (mine ? wl : 0) * kDecodeSlots * kSmemDecodeSlot;
   float* ps_x = dc.scores + (mine ? wl : 0) * kMaxGroup * kBlockSize;
 
@@ -760,7 +825,12 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
   const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
   const int blk0 = kb / kBlockSize;
   const bool mine = wl >= 0 && wl < dc.nw;
-  const int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  {  // the sequence's last row (this step's token) may be appended by this launch
+    int oka = 1;
+    if (lane == 0 && nmine > 0 && ke >= p.kv_lens[p.Np + d]) oka = wait_appended(p, ps, wc);
+    if (!__shfl_sync(0xffffffffu, oka, 0)) nmine = 0;
+  }
   uint8_t* ring = dc.ring + (mine ? wl : 0) * kDecodeSlots * kSmemDecodeSlot;
   const uint32_t ring_s = smem_u32(ring);
   const int hr = lane >> 2, qd = lane & 3;  // fragment row (query head) and quad lane
@@ -1092,6 +1162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const WaitCtx wc{&ctl->abort, p.status, p.timeout_ns};
   PipeState ps;
+  if (p.n_new > 0) {
+    // this CTA's share of the KV append, then one arrival; readers of appended rows wait for all
+    append_rows(p);
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(&p.counters[3], 1);
+    }
+  }
   const uint32_t sm_raw = smid();
   const int sm = (int)(sm_raw % (uint32_t)p.num_sms);
   if (warp < kDecodeWarp0) {
@@ -1143,6 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.counters[0] = 0;
       p.counters[1] = 0;
       p.counters[2] = 0;
+      p.counters[3] = 0;
       __threadfence();
     }
   }
@@ -1225,8 +1305,23 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
     if (e != cudaSuccess) return e;
     attr_set.store(1);
   }
-  pod_attn_kernel<GT><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, cs.tmk, cs.tmv);
-  return cudaGetLastError();
+  if (!p.wait_append) {
+    pod_attn_kernel<GT><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, cs.tmk, cs.tmv);
+    return cudaGetLastError();
+  }
+  // Items wait for every CTA's share of the append: a cooperative launch guarantees that all
+  // CTAs are resident at once (or fails to launch), so the wait cannot starve.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemTotal;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT>, p, cs.tmq, cs.tmk, cs.tmv);
 }
 
 static cudaError_t launch(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
@@ -1402,6 +1497,9 @@ pod_attn_status pod_attn_upload(pod_attn_plan_t plan, void* workspace, size_t wo
   if (ok && !plan->units.empty())
     ok = cudaMemcpyAsync(ws + w.units, plan->units.data(), plan->units.size() * 4,
                          cudaMemcpyHostToDevice, s) == cudaSuccess;
+  if (ok && !plan->new_rows.empty())
+    ok = cudaMemcpyAsync(ws + w.new_rows, plan->new_rows.data(), plan->new_rows.size() * 4,
+                         cudaMemcpyHostToDevice, s) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     return POD_ATTN_ERR_CUDA;
@@ -1409,12 +1507,15 @@ pod_attn_status pod_attn_upload(pod_attn_plan_t plan, void* workspace, size_t wo
   return POD_ATTN_OK;
 }
 
-pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const void* q_decode,
-                             const void* k_pool, const void* v_pool,
-                             const int32_t* d_block_tables, const int32_t* d_cu_seqlens_q,
-                             const int32_t* d_kv_lens, void* o_prefill, void* o_decode,
-                             void* workspace, size_t workspace_bytes, void* stream,
-                             void* stream2) {
+}  // extern "C"
+
+// pod_attn_run and pod_attn_run_append; k_new == nullptr: no append.
+static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, const void* q_decode,
+                                const void* k_new, const void* v_new, const void* k_pool,
+                                const void* v_pool, const int32_t* d_block_tables,
+                                const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
+                                void* o_prefill, void* o_decode, void* workspace,
+                                size_t workspace_bytes, void* stream, void* stream2) {
   if (!plan) return POD_ATTN_ERR_INVALID_ARG;
   pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
   if (st != POD_ATTN_OK) return st;
@@ -1427,7 +1528,8 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
   if (n_d > 0 && (!q_decode || !o_decode)) return POD_ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
        reinterpret_cast<uintptr_t>(q_prefill) | reinterpret_cast<uintptr_t>(o_prefill) |
-       reinterpret_cast<uintptr_t>(q_decode)) & 15)
+       reinterpret_cast<uintptr_t>(q_decode) | reinterpret_cast<uintptr_t>(k_new) |
+       reinterpret_cast<uintptr_t>(v_new)) & 15)
     return POD_ATTN_ERR_INVALID_ARG;
   CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
   const int64_t pool_rows = (int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize;
@@ -1483,6 +1585,24 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
   p.timeout_ns = kWaitTimeoutNs;
   int32_t* counters = reinterpret_cast<int32_t*>(ws + w.counters);
   auto counter_block = [&](int mode) { return counters + (size_t)mode * w.counter_block_words; };
+  const bool append = k_new != nullptr;
+  const int n_new = (int)(plan->new_rows.size() / 2);
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.k_pool_w = static_cast<uint16_t*>(const_cast<void*>(k_pool));
+  p.v_pool_w = static_cast<uint16_t*>(const_cast<void*>(v_pool));
+  p.new_rows = reinterpret_cast<const int32_t*>(ws + w.new_rows);
+  p.n_new = 0;
+  p.new_first = 0;
+  p.wait_append = 0;
+  // SERIAL and STREAMS: the append runs as a launch of its own, ahead of both kinds of items
+  Params ap = p;
+  ap.mode = kModeAppendOnly;
+  ap.counters = counter_block(kModeAppendOnly);
+  ap.n_items_p = ap.n_items_d = 0;
+  ap.n_new = n_new;
+  const int grid_append =
+      std::max(1, std::min(plan->num_sms, (n_new * pr.num_kv_heads + kWarps - 1) / kWarps));
 
   cudaStream_t s1 = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -1490,6 +1610,10 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
     case POD_ATTN_FUSED: {
       p.mode = kModeFused;
       p.counters = counter_block(kModeFused);
+      if (append) {  // in the same launch, ahead of the items that read the new rows
+        p.n_new = n_new;
+        p.wait_append = 1;
+      }
       e = launch(p, plan->grid_fused, s1, *cs);
       break;
     }
@@ -1499,7 +1623,8 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
       a.counters = counter_block(kModePrefillOnly);
       b.mode = kModeDecodeOnly;
       b.counters = counter_block(kModeDecodeOnly);
-      e = launch(a, plan->grid_prefill, s1, *cs);
+      if (append && n_new > 0) e = launch(ap, grid_append, s1, *cs);
+      if (e == cudaSuccess) e = launch(a, plan->grid_prefill, s1, *cs);
       if (e == cudaSuccess) e = launch(b, plan->grid_decode, s1, *cs);
       break;
     }
@@ -1511,7 +1636,8 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
       a.counters = counter_block(kModePrefillOnly);
       b.mode = kModeDecodeOnly;
       b.counters = counter_block(kModeDecodeOnly);
-      e = cudaEventRecord(cs->ev_fork, s1);
+      if (append && n_new > 0) e = launch(ap, grid_append, s1, *cs);
+      if (e == cudaSuccess) e = cudaEventRecord(cs->ev_fork, s1);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(s2, cs->ev_fork, 0);
       if (e == cudaSuccess) e = launch(a, plan->grid_prefill, s1, *cs);
       if (e == cudaSuccess) e = launch(b, plan->grid_decode, s2, *cs);
@@ -1525,6 +1651,31 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
     return POD_ATTN_ERR_CUDA;
   }
   return POD_ATTN_OK;
+}
+
+extern "C" {
+
+pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const void* q_decode,
+                             const void* k_pool, const void* v_pool,
+                             const int32_t* d_block_tables, const int32_t* d_cu_seqlens_q,
+                             const int32_t* d_kv_lens, void* o_prefill, void* o_decode,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* stream2) {
+  return run_impl(plan, q_prefill, q_decode, nullptr, nullptr, k_pool, v_pool, d_block_tables,
+                  d_cu_seqlens_q, d_kv_lens, o_prefill, o_decode, workspace, workspace_bytes,
+                  stream, stream2);
+}
+
+pod_attn_status pod_attn_run_append(pod_attn_plan_t plan, const void* q_prefill,
+                                    const void* q_decode, const void* k_new, const void* v_new,
+                                    void* k_pool, void* v_pool, const int32_t* d_block_tables,
+                                    const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
+                                    void* o_prefill, void* o_decode, void* workspace,
+                                    size_t workspace_bytes, void* stream, void* stream2) {
+  if (!k_new || !v_new) return POD_ATTN_ERR_INVALID_ARG;
+  return run_impl(plan, q_prefill, q_decode, k_new, v_new, k_pool, v_pool, d_block_tables,
+                  d_cu_seqlens_q, d_kv_lens, o_prefill, o_decode, workspace, workspace_bytes,
+                  stream, stream2);
 }
 
 pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspace, void* stream) {

@@ -98,22 +98,25 @@ __host__ __device__
 #endif
 inline int decode_slot_floats(int group) { return group * (kHeadDim + 2); }
 
-// Counter block of one launch mode (fused, prefill-only, decode-only), int32 words:
-//   [0] prefill ticket  [1] decode ticket  [2] exited CTAs  [3] unused
+// Counter block of one launch mode (fused, prefill-only, decode-only, append-only), int32 words:
+//   [0] prefill ticket  [1] decode ticket  [2] exited CTAs
+//   [3] CTAs that have finished their share of the KV append (pod_attn_run_append)
 //   [4 .. 4+num_sms)    decode items the prefill slot of each SM has taken (diagnostics)
 constexpr int kCounterHeader = 4;
 
-enum LaunchMode { kModeFused = 0, kModePrefillOnly = 1, kModeDecodeOnly = 2 };
+enum LaunchMode { kModeFused = 0, kModePrefillOnly = 1, kModeDecodeOnly = 2, kModeAppendOnly = 3 };
+constexpr int kNumModes = 4;
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct WorkspaceLayout {
   size_t status = 0;        // int32 status word, int32 abort word
-  size_t counters = 0;      // 3 counter blocks
+  size_t counters = 0;      // kNumModes counter blocks
   size_t counter_block_words = 0;
   size_t arrive = 0;        // int32 per unit
   size_t items_p = 0;       // prefill items
   size_t items_d = 0;       // decode items
   size_t units = 0;         // unit table
+  size_t new_rows = 0;      // (sequence, position) of each appended token (KV append)
   size_t partial_p = 0;     // prefill partial slots
   size_t partial_d = 0;     // decode partial slots
   size_t records = 0;       // instrumentation records (0 bytes when off)
@@ -135,6 +138,8 @@ struct pod_attn_plan_s {
   std::vector<int32_t> cu, kv;            // host copies of the lengths
   std::vector<int32_t> items_p, items_d;  // kItemWords each
   std::vector<int32_t> units;             // kUnitWords each
+  std::vector<int32_t> new_rows;          // 2 words per new token: prefill chunk tokens in
+                                          // order, then one per decode sequence
   int num_p_slots = 0, num_d_slots = 0;
   pod::WorkspaceLayout ws;
   double est_prefill_flops = 0, est_prefill_bytes = 0, est_decode_bytes = 0,

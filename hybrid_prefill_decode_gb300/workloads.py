@@ -93,6 +93,34 @@ class HybridBatch:
         return HybridBatch(**kw)
 
 
+def split_off_new_rows(batch: HybridBatch):
+    """The inputs of an iteration whose new tokens' K/V are not yet in the pool: returns
+    (k_new, v_new, k_pool, v_pool) where k_new / v_new (bf16 [T_p + Nd][Hkv][D]) hold the rows of
+    the iteration's tokens — chunk token i of prefill sequence s at position
+    kv_len - q_len + i, then each decode sequence's token at kv_len - 1 — and the returned pools
+    are copies of the batch's with exactly those rows set to bf16 NaN (so a read before they are
+    written shows up in the output)."""
+    seq, pos = [], []
+    for s, (q, L) in enumerate(zip(batch.q_lens, batch.prefill_kv_lens)):
+        seq += [s] * q
+        pos += list(range(L - q, L))
+    for d, L in enumerate(batch.decode_kv_lens):
+        seq.append(batch.num_prefill_seqs + d)
+        pos.append(L - 1)
+    dev = batch.k_pool.device
+    seq_t = torch.tensor(seq, dtype=torch.long, device=dev)
+    pos_t = torch.tensor(pos, dtype=torch.long, device=dev)
+    phys = batch.block_tables.to(dev).long()[seq_t, pos_t // BLOCK_SIZE]
+    off = pos_t % BLOCK_SIZE
+    k_new = batch.k_pool[phys, :, off, :].contiguous()
+    v_new = batch.v_pool[phys, :, off, :].contiguous()
+    nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+    k_pool, v_pool = batch.k_pool.clone(), batch.v_pool.clone()
+    k_pool[phys, :, off, :] = nan
+    v_pool[phys, :, off, :] = nan
+    return k_new, v_new, k_pool, v_pool
+
+
 def _blocks(n: int) -> int:
     return (n + BLOCK_SIZE - 1) // BLOCK_SIZE
 

@@ -193,6 +193,29 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
                              void* workspace, size_t workspace_bytes, void* stream,
                              void* stream2);
 
+/* pod_attn_run with the iteration's KV append in front: the K and V rows of this iteration's new
+ * tokens are written into the paged pools, then the attention reads them — the step that
+ * precedes attention in a serving iteration ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
+ * §"PagedAttention": the paged cache grows by appending; §"한 스텝에 여러 종류의 request 섞기").
+ *   k_new, v_new : device bf16 [T_p + Nd][Hkv][128], 16-byte aligned: row i < T_p is prefill
+ *                  token i (chunks in cu_seqlens order), row T_p + d is decode sequence d's token.
+ *                  Token i of chunk s is written at position kv_len[s] - q_len(s) + i of sequence
+ *                  s, decode d's token at position kv_len[Np + d] - 1, through the block tables
+ *                  (whose blocks for those positions must exist).
+ *   k_pool, v_pool : written at exactly those rows; every other row is only read.
+ * Other arguments as pod_attn_run. FUSED does the append inside its one launch (each CTA writes
+ * a share, then the items that read new rows wait, bounded, until all shares are done; the
+ * launch is cooperative, so all CTAs are resident); SERIAL and STREAMS run the append as a
+ * launch of its own ahead of theirs. Results equal pod_attn_run on pools that already hold the
+ * rows. Errors: as pod_attn_run; INVALID_ARG also for NULL or misaligned k_new / v_new; a
+ * block-table entry outside the pool is reported as BAD_INDEX (the row is not written). */
+pod_attn_status pod_attn_run_append(pod_attn_plan_t plan, const void* q_prefill,
+                                    const void* q_decode, const void* k_new, const void* v_new,
+                                    void* k_pool, void* v_pool, const int32_t* d_block_tables,
+                                    const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
+                                    void* o_prefill, void* o_decode, void* workspace,
+                                    size_t workspace_bytes, void* stream, void* stream2);
+
 /* Synchronise `stream`, read and clear the device status word of `workspace`.
  * Returns OK, BAD_INDEX, TIMEOUT, or CUDA if the synchronisation itself failed. After
  * BAD_INDEX or TIMEOUT the outputs of that run are unspecified and the workspace must be

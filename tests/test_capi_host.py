@@ -69,6 +69,14 @@ def test_plan_validation(lib):
     lib.pod_attn_plan_destroy(None)
 
 
+def test_run_append_rejects_missing_rows(lib):
+    p = B.Plan(4, 2, [0, 5], [9, 7], 1, 10, 4, 0.1, num_sms=148)
+    for kn, vn in ((None, 16), (16, None), (None, None)):
+        code = lib.pod_attn_run_append(p.handle, None, None, kn, vn, None, None, None, None,
+                                       None, None, None, None, 0, None, None)
+        assert code == B.ERR_INVALID_ARG
+
+
 def test_run_rejects_bad_workspace(lib):
     p = B.Plan(4, 2, [0, 5], [9, 7], 1, 10, 4, 0.1, num_sms=148)
     code = lib.pod_attn_run(p.handle, None, None, None, None, None, None, None, None, None,

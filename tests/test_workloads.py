@@ -101,3 +101,25 @@ def test_trace_pool_maps_requests_to_disjoint_blocks():
         n = (L + 15) // 16
         assert b.block_tables[r, :n].tolist() == pool.blocks[
             (tr.steps[2].prefill_rids + tr.steps[2].decode_rids)[r]][:n].tolist()
+
+
+def test_split_off_new_rows_is_a_gather_of_the_iteration_tokens():
+    b = W.make_batch(4, 2, [5, 9], [20, 9], [33, 1, 16], seed=11)
+    k_new, v_new, kp, vp = W.split_off_new_rows(b)
+    # positions written out by hand: chunk tokens follow the cached prefix, a decode token is
+    # the sequence's last row
+    want = [(0, p) for p in range(15, 20)] + [(1, p) for p in range(0, 9)] + \
+        [(2, 32), (3, 0), (4, 15)]
+    assert k_new.shape == (len(want), 2, 128)
+    bt = b.block_tables
+    holes = torch.zeros(b.k_pool.shape[:3], dtype=torch.bool)
+    for i, (s, p) in enumerate(want):
+        blk = int(bt[s, p // 16])
+        for g in range(2):
+            assert torch.equal(k_new[i, g].view(torch.int16), b.k_pool[blk, g, p % 16].view(torch.int16))
+            assert torch.equal(v_new[i, g].view(torch.int16), b.v_pool[blk, g, p % 16].view(torch.int16))
+        holes[blk, :, p % 16] = True
+    # the returned pools differ from the batch's exactly at those rows, which are NaN there
+    assert _nan(kp[holes]).all() and _nan(vp[holes]).all()
+    assert torch.equal(kp[~holes].view(torch.int16), b.k_pool[~holes].view(torch.int16))
+    assert torch.equal(vp[~holes].view(torch.int16), b.v_pool[~holes].view(torch.int16))

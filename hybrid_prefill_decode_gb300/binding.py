@@ -56,6 +56,15 @@ class PlanInfo(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class Bucket(ctypes.Structure):
+    _fields_ = [("prefill_flops", ctypes.c_int64), ("read_bytes", ctypes.c_int64),
+                ("prefill_ctas", ctypes.c_int32), ("decode_ctas", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("smem_per_cta", ctypes.c_int32),
+                ("tmem_cols_per_cta", ctypes.c_int32), ("bucket_flops", ctypes.c_int32),
+                ("bucket_bytes", ctypes.c_int32), ("bucket_ctas", ctypes.c_int32),
+                ("intensity", ctypes.c_double)]
+
+
 class ItemRecord(ctypes.Structure):
     _fields_ = [("smid", ctypes.c_int32), ("kind", ctypes.c_int32), ("item", ctypes.c_int32),
                 ("cta", ctypes.c_int32), ("t_start", ctypes.c_uint64),
@@ -90,6 +99,8 @@ def load():
     lib.pod_attn_upload.argtypes = [P, P, SZ, P]
     lib.pod_attn_run.restype = I32
     lib.pod_attn_run.argtypes = [P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+    lib.pod_attn_plan_bucket.restype = I32
+    lib.pod_attn_plan_bucket.argtypes = [P, ctypes.POINTER(Bucket)]
     lib.pod_attn_run_append.restype = I32
     lib.pod_attn_run_append.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
     lib.pod_attn_last_device_status.restype = I32
@@ -221,6 +232,12 @@ class Plan:
             _ptr(o_decode), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream),
             _stream_ptr(stream2) if stream2 is not None else None)
         _check(code, "pod_attn_run")
+
+    def bucket(self) -> dict:
+        """pod_attn_plan_bucket: the plan's resource features and buckets."""
+        b = Bucket()
+        _check(load().pod_attn_plan_bucket(self.handle, ctypes.byref(b)), "pod_attn_plan_bucket")
+        return {name: getattr(b, name) for name, _ in Bucket._fields_}
 
     def run_append(self, q_prefill, q_decode, k_new, v_new, k_pool, v_pool, block_tables,
                    cu_seqlens_q, kv_lens, o_prefill, o_decode, workspace, stream=None,

@@ -1434,6 +1434,37 @@ pod_attn_status pod_attn_plan(const pod_attn_problem* problem, const int32_t* h_
 
 size_t pod_attn_workspace_bytes(pod_attn_plan_t plan) { return plan ? plan->ws.total : 0; }
 
+pod_attn_status pod_attn_plan_bucket(pod_attn_plan_t plan, pod_attn_bucket* out) {
+  if (!plan || !out) return POD_ATTN_ERR_INVALID_ARG;
+  const pod_attn_problem& pr = plan->prob;
+  const int Np = pr.num_prefill_seqs, Nd = pr.num_decode_seqs;
+  const int64_t row = 4 * kHeadDim;  // K + V (or q + o) of one row, bf16
+  int64_t flops = 0, bytes = 0;
+  for (int s = 0; s < Np; ++s) {
+    const int64_t q = plan->cu[s + 1] - plan->cu[s], L = plan->kv[s], P = L - q;
+    flops += 4 * kHeadDim * (int64_t)pr.num_q_heads * (q * P + q * (q + 1) / 2);
+    bytes += L * pr.num_kv_heads * row + q * pr.num_q_heads * row;
+  }
+  for (int d = 0; d < Nd; ++d)
+    bytes += (int64_t)plan->kv[Np + d] * pr.num_kv_heads * row + (int64_t)pr.num_q_heads * row;
+  auto bit_length = [](int64_t x) { int b = 0; while (x > 0) { ++b; x >>= 1; } return b; };
+  auto bucket = [&](int64_t x, int64_t unit) { return x > 0 ? bit_length((x + unit - 1) / unit) : 0; };
+  pod_attn_bucket r{};
+  r.prefill_flops = flops;
+  r.read_bytes = bytes;
+  r.prefill_ctas = (int32_t)(plan->items_p.size() / kItemWords);
+  r.decode_ctas = (int32_t)(plan->items_d.size() / kItemWords);
+  r.grid = plan->grid_fused;
+  r.smem_per_cta = kSmemTotal;
+  r.tmem_cols_per_cta = r.prefill_ctas > 0 ? kTmemCols : 0;
+  r.bucket_flops = bucket(flops, int64_t(1) << 30);
+  r.bucket_bytes = bucket(bytes, int64_t(1) << 20);
+  r.bucket_ctas = bit_length((int64_t)r.prefill_ctas + r.decode_ctas);
+  r.intensity = bytes > 0 ? (double)flops / (double)bytes : 0.0;
+  *out = r;
+  return POD_ATTN_OK;
+}
+
 pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info* info) {
   if (!plan || !info) return POD_ATTN_ERR_INVALID_ARG;
   pod_attn_plan_info r{};

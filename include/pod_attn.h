@@ -96,12 +96,15 @@ typedef struct {
 /* Planner and launch options. Zero-initialise for defaults. */
 typedef struct {
   int32_t num_sms;          /* SMs the planner sizes the grid for; 0 = query the current device */
-  int32_t ctas_per_sm;      /* resident CTAs per SM; 0 = auto (2: one TMEM half each) */
-  int32_t max_prefill_ctas; /* prefill items allowed to run at once on one SM while decode work
-                               remains ([POD] §"가상 CTA와 SM별 균형": cap prefill so it does not
-                               crowd out decode); 0 = auto */
+  int32_t ctas_per_sm;      /* accepted and ignored: one persistent CTA per SM, which holds a
+                               prefill slot and a decode slot side by side */
+  int32_t max_prefill_ctas; /* accepted and ignored: the prefill work of an SM is capped at one
+                               item at a time by construction (its one prefill slot), so decode
+                               is never crowded out ("POD-Attention" digest, §"가상 CTA와 SM별
+                               균형") */
   int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head); 0 = auto */
-  int32_t prefill_splits;   /* force this many KV splits per prefill (tile, head); 0 = auto */
+  int32_t prefill_splits;   /* force this many KV splits per prefill (tile, head block), at
+                               most 8; 0 = auto */
   int32_t instrument;       /* nonzero: record (SM, kind, start, end) per work item */
   pod_attn_variant variant; /* launch variant, see above */
 } pod_attn_options;
@@ -110,7 +113,8 @@ typedef struct pod_attn_plan_s* pod_attn_plan_t;
 
 /* Summary of a plan (what the planner decided). */
 typedef struct {
-  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, 128-row tile, q-head, kv-split) */
+  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, 128-row tile = 128/hp tokens x hp
+                                 q-heads of one kv-head group, kv-split) */
   int32_t num_decode_items;   /* virtual decode CTAs: (seq, kv-head, kv-split) */
   int32_t num_units;          /* outputs assembled from more than one split */
   int32_t num_sms;            /* SM count the grid was sized for */
@@ -224,6 +228,32 @@ pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspac
 
 /* Fill *info with the plan summary. Errors: INVALID_ARG. */
 pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info* info);
+
+/* Resource features of a plan and their buckets. No counterpart in code on the pages: the
+ * "POD-Attention" digest (§"스케줄링 입력으로 쓰는 자원 특성") proposes describing prefill chunks
+ * and decode groups by CTA count, shared memory, arithmetic intensity and bytes read, in coarse
+ * buckets, so that the kernel can publish a few validated (bucket, latency) pairs from which an
+ * outer scheduler chooses (e.g. the largest prefill chunk whose measured tail latency fits a
+ * token-to-token budget, §"예측 가능한 지연시간과 진단"). Host only, integer arithmetic: equal
+ * batches give equal buckets, bit for bit. */
+typedef struct {
+  int64_t prefill_flops;     /* 4*128*Hq per visible (query, key) pair of the prefill chunks */
+  int64_t read_bytes;        /* algorithmic bytes: each sequence's K/V rows once per kv-head
+                                (512 B per row and kv-head), q in and o out (512 B per token and
+                                q-head) */
+  int32_t prefill_ctas;      /* virtual prefill CTAs (work items) */
+  int32_t decode_ctas;       /* virtual decode CTAs */
+  int32_t grid;              /* hardware CTAs of the fused launch */
+  int32_t smem_per_cta;      /* dynamic shared memory of one CTA, bytes */
+  int32_t tmem_cols_per_cta; /* TMEM columns one CTA allocates (0: decode-only plan) */
+  int32_t bucket_flops;      /* 0 without prefill, else bit length of ceil(prefill_flops / 2^30) */
+  int32_t bucket_bytes;      /* 0 without work, else bit length of ceil(read_bytes / 2^20) */
+  int32_t bucket_ctas;       /* bit length of prefill_ctas + decode_ctas */
+  double intensity;          /* prefill_flops / read_bytes (FLOP per byte) */
+} pod_attn_bucket;
+
+/* Fill `out` for `plan`. Errors: INVALID_ARG (null plan or out). */
+pod_attn_status pod_attn_plan_bucket(pod_attn_plan_t plan, pod_attn_bucket* out);
 
 /* Copy the host work lists: prefill items first, then decode items, then the unit table, each
  * item info.item_words int32 words (see DESIGN of the item encoding in the planner source).

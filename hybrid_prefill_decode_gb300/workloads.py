@@ -52,6 +52,7 @@ class HybridBatch:
     seed: int = 0
     name: str = ""
     meta: dict = field(default_factory=dict)
+    causal: bool = True             # False: chunk tokens see every row of their sequence
 
     @property
     def num_prefill_seqs(self) -> int:
@@ -129,7 +130,7 @@ def make_batch(num_q_heads: int, num_kv_heads: int, q_lens: Sequence[int],
                prefill_kv_lens: Sequence[int], decode_kv_lens: Sequence[int], seed: int,
                device="cpu", scale: Optional[float] = None, permute: bool = True,
                spare_frac: float = 0.05, poison: bool = True, std: float = 1.0,
-               name: str = "") -> HybridBatch:
+               name: str = "", causal: bool = True) -> HybridBatch:
     """Build one seeded hybrid batch (see the module docstring for the recipe)."""
     q_lens = [int(x) for x in q_lens]
     prefill_kv_lens = [int(x) for x in prefill_kv_lens]
@@ -195,7 +196,8 @@ def make_batch(num_q_heads: int, num_kv_heads: int, q_lens: Sequence[int],
         scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
         q_prefill=q_prefill, q_decode=q_decode, k_pool=k_pool, v_pool=v_pool,
         block_tables=bt.to(dev), cu_seqlens_q=torch.tensor(cu, dtype=torch.int32, device=dev),
-        kv_lens=torch.tensor(lens, dtype=torch.int32, device=dev), seed=seed, name=name)
+        kv_lens=torch.tensor(lens, dtype=torch.int32, device=dev), seed=seed, name=name,
+        causal=causal)
 
 
 # ----------------------------------------------------------------------------------------------

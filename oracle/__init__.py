@@ -63,10 +63,10 @@ def _load():
             lib.oracle_attend_row.argtypes = [P, P, L, I, I, I, I, P, P, L, D, P, P]
             lib.oracle_rows.restype = I
             lib.oracle_rows.argtypes = [I, I, I, I, I, I, L, I, D, P, P, P, P, P, P, P,
-                                        L, P, P, P, P]
+                                        L, P, P, P, P, I]
             lib.oracle_hybrid_attention.restype = I
             lib.oracle_hybrid_attention.argtypes = [I, I, I, I, I, I, L, I, D, P, P, P, P,
-                                                    P, P, P, P, P]
+                                                    P, P, P, P, P, I]
             _lib = lib
     return _lib
 
@@ -115,6 +115,7 @@ class _Batch:
         self.num_blocks = int(self.k_pool.shape[0])
         self.maxb = int(self.block_tables.shape[1]) if self.block_tables.ndim == 2 else 0
         self.tp = int(self.cu[-1]) if self.Np > 0 else 0
+        self.causal = 1 if getattr(b, "causal", True) else 0
 
     def common(self):
         return (self.Hq, self.Hkv, self.D, self.BS, self.Np, self.Nd, self.num_blocks,
@@ -131,7 +132,7 @@ def hybrid_attention(batch):
     b = _Batch(batch)
     o_p = np.zeros((b.tp, b.Hq, b.D), dtype=np.float64)
     o_d = np.zeros((b.Nd, b.Hq, b.D), dtype=np.float64)
-    rc = _load().oracle_hybrid_attention(*b.common(), _ptr(o_p), _ptr(o_d))
+    rc = _load().oracle_hybrid_attention(*b.common(), _ptr(o_p), _ptr(o_d), b.causal)
     if rc != 0:
         raise ValueError(f"oracle_hybrid_attention failed with code {rc}")
     return o_p, o_d
@@ -146,7 +147,7 @@ def rows(batch, kinds, indices, heads) -> np.ndarray:
     n = int(kinds.shape[0])
     out = np.zeros((n, b.D), dtype=np.float64)
     rc = _load().oracle_rows(*b.common(), n, _ptr(kinds), _ptr(indices), _ptr(heads),
-                             _ptr(out))
+                             _ptr(out), b.causal)
     if rc != 0:
         raise ValueError(f"oracle_rows failed with code {rc}")
     return out

@@ -4,7 +4,8 @@ An implementation independent of ``oracle.c``, for tiny cases: for each sequence
 gathers the sequence's K and V rows into contiguous arrays through the block table
 ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM", §"PagedAttention"), then forms the whole
 [q_len x kv_len] score matrix, applies the causal mask with an explicit position comparison
-(§"Non-Causal vs. Causal Attention"; chunk tokens sit after the cached prefix,
+unless the batch is non-causal (§"Non-Causal vs. Causal Attention"; chunk tokens sit after the
+cached prefix,
 §"한 스텝에 여러 종류의 request 섞기"), and takes a row softmax and a matrix product
 (§"Attention에 적용하기"). Everything is float64.
 """
@@ -27,12 +28,14 @@ def _gather(pool: np.ndarray, bt_row: np.ndarray, n: int, g: int) -> np.ndarray:
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray,
-              scale: float) -> np.ndarray:
-    """Masked attention of query rows q[t] at absolute positions q_pos[t] over keys 0..n-1."""
+              scale: float, causal: bool = True) -> np.ndarray:
+    """Attention of query rows q[t] at absolute positions q_pos[t] over keys 0..n-1, masked
+    (causal: key j visible iff j <= p) or not (every key visible)."""
     n = k.shape[0]
     s = scale * (q @ k.T)                                   # [t][n]
-    key_pos = np.arange(n)[None, :]
-    s = np.where(key_pos <= q_pos[:, None], s, -np.inf)    # causal: key j visible iff j <= p
+    if causal:
+        key_pos = np.arange(n)[None, :]
+        s = np.where(key_pos <= q_pos[:, None], s, -np.inf)
     s = s - s.max(axis=1, keepdims=True)
     w = np.exp(s)
     w = w / w.sum(axis=1, keepdims=True)
@@ -69,7 +72,8 @@ def hybrid_attention(batch):
         for h in range(Hq):
             g = h // group
             K, V = _gather(kp, bt[s], L, g), _gather(vp, bt[s], L, g)
-            o_p[t0:t1, h, :] = attention(qp[t0:t1, h, :], K, V, pos, float(batch.scale))
+            o_p[t0:t1, h, :] = attention(qp[t0:t1, h, :], K, V, pos, float(batch.scale),
+                                         causal=getattr(batch, "causal", True))
     for d in range(Nd):
         s = Np + d
         L = int(kvl[s])

@@ -9,7 +9,8 @@
  *   "Week 6: Beyond PyTorch: Custom Kernel과 vLLM" (core-sig.pytorch.kr)
  *     §"Attention에 적용하기"            out = softmax(q·Kᵀ / sqrt(d_k)) · V (scale passed in)
  *     §"Safe softmax (3-pass, 수치 안정성 확보)"   max pass, exp-sum pass, normalise pass
- *     §"Non-Causal vs. Causal Attention"  a token sees itself and earlier tokens only
+ *     §"Non-Causal vs. Causal Attention"  causal: a token sees itself and earlier tokens only;
+ *                                         non-causal: a token sees every token of its sequence
  *     §"한 스텝에 여러 종류의 request 섞기"      extend: a chunk token sees the cached prefix and
  *                                         the earlier tokens of its own chunk; decode is an
  *                                         extend of one token
@@ -165,6 +166,7 @@ typedef struct {
   double scale;
   const uint16_t *q_prefill, *q_decode, *k_pool, *v_pool;
   const int32_t *block_tables, *cu_seqlens_q, *kv_lens;
+  int causal; /* nonzero: chunk tokens see rows 0..p; zero: all kv_len rows */
 } oracle_batch;
 
 /* Locate the sequence, visible row count and query vector of one requested row. */
@@ -179,7 +181,7 @@ static int resolve_row(const oracle_batch* b, int kind, int64_t index, int h, co
     int64_t i = index - b->cu_seqlens_q[s];
     int64_t prefix = (int64_t)b->kv_lens[s] - qlen;
     if (prefix < 0) return -3;
-    *nvis = prefix + i + 1; /* sees rows 0..prefix+i */
+    *nvis = b->causal ? prefix + i + 1 : b->kv_lens[s]; /* rows 0..prefix+i, or all */
     *bt_row = b->block_tables + (int64_t)s * b->max_blocks_per_seq;
     *q = b->q_prefill + (index * b->Hq + h) * (int64_t)b->D;
   } else {
@@ -202,10 +204,11 @@ int oracle_rows(int Hq, int Hkv, int D, int BS, int Np, int Nd, int64_t num_bloc
                 const uint16_t* q_decode, const uint16_t* k_pool, const uint16_t* v_pool,
                 const int32_t* block_tables, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
                 int64_t n, const int32_t* kinds, const int64_t* indices, const int32_t* heads,
-                double* out) {
+                double* out, int causal) {
   if (Hkv < 1 || Hq % Hkv != 0) return -3;
   oracle_batch b = {Hq, Hkv, D, BS, Np, Nd, num_blocks, max_blocks_per_seq, scale,
-                    q_prefill, q_decode, k_pool, v_pool, block_tables, cu_seqlens_q, kv_lens};
+                    q_prefill, q_decode, k_pool, v_pool, block_tables, cu_seqlens_q, kv_lens,
+                    causal};
   int group = Hq / Hkv;
   int err = 0;
   int64_t max_rows = (int64_t)max_blocks_per_seq * BS;
@@ -240,10 +243,11 @@ int oracle_hybrid_attention(int Hq, int Hkv, int D, int BS, int Np, int Nd, int6
                             const uint16_t* q_decode, const uint16_t* k_pool,
                             const uint16_t* v_pool, const int32_t* block_tables,
                             const int32_t* cu_seqlens_q, const int32_t* kv_lens,
-                            double* o_prefill, double* o_decode) {
+                            double* o_prefill, double* o_decode, int causal) {
   if (Hkv < 1 || Hq % Hkv != 0) return -3;
   oracle_batch b = {Hq, Hkv, D, BS, Np, Nd, num_blocks, max_blocks_per_seq, scale,
-                    q_prefill, q_decode, k_pool, v_pool, block_tables, cu_seqlens_q, kv_lens};
+                    q_prefill, q_decode, k_pool, v_pool, block_tables, cu_seqlens_q, kv_lens,
+                    causal};
   int64_t tp = Np > 0 ? cu_seqlens_q[Np] : 0;
   int64_t total = (tp + Nd) * Hq;
   int group = Hq / Hkv;

@@ -246,3 +246,60 @@ def test_mixed_kind_worked_example_structure():
     r_p, r_d = bruteforce.hybrid_attention(b)
     np.testing.assert_allclose(o_p, r_p, rtol=0, atol=1e-12)
     np.testing.assert_allclose(o_d, r_d, rtol=0, atol=1e-12)
+
+
+# ---- the non-causal reading ("Week 6: Beyond PyTorch", §"Non-Causal vs. Causal Attention":
+# without the mask every token of the sequence is visible, including later tokens of the chunk)
+
+def test_noncausal_uniform_scores_give_mean_of_all_rows():
+    b = _small(seed=31, causal=False)
+    b.q_prefill.zero_()
+    o_p, _ = oracle.hybrid_attention(b)
+    cu, group = b.host_cu_seqlens, b.num_q_heads // b.num_kv_heads
+    for s in range(b.num_prefill_seqs):
+        L = b.host_kv_lens[s]
+        for h in range(b.num_q_heads):
+            want = _rows(b, s, h // group, L).mean(axis=0)      # every row, whatever the token
+            for t in range(cu[s], cu[s + 1]):
+                assert np.abs(o_p[t, h] - want).max() <= 1e-12
+
+
+def test_noncausal_later_rows_change_earlier_outputs():
+    b = W.make_batch(2, 1, [6], [10], [], seed=32, causal=False)
+    o1, _ = oracle.hybrid_attention(b)
+    bt = b.block_tables
+    b.v_pool[int(bt[0, 9 // 16]), 0, 9 % 16] += 1.0            # the chunk's last row
+    o2, _ = oracle.hybrid_attention(b)
+    assert np.abs(o2[0] - o1[0]).max() > 1e-3                # the chunk's first token sees it
+    b.causal = True
+    o3, _ = oracle.hybrid_attention(b)
+    o4_first = o3[0].copy()
+    b.v_pool[int(bt[0, 9 // 16]), 0, 9 % 16] -= 1.0
+    o5, _ = oracle.hybrid_attention(b)
+    assert np.array_equal(o4_first, o5[0])                   # causal: it does not
+
+
+def test_noncausal_equal_queries_give_equal_rows():
+    b = W.make_batch(4, 2, [7], [30], [], seed=33, causal=False)
+    b.q_prefill[:] = b.q_prefill[0:1].clone()                # one query repeated on every token
+    o_p, _ = oracle.hybrid_attention(b)
+    for t in range(1, 7):
+        assert np.array_equal(o_p[t], o_p[0])
+
+
+def test_noncausal_chunk_row_equals_a_decode_over_the_sequence():
+    b = W.make_batch(4, 2, [5], [21], [21], seed=34, causal=False)
+    b.block_tables[1] = b.block_tables[0]                    # the decode reads the same rows
+    for i in range(5):
+        b.q_decode[0] = b.q_prefill[i]
+        o_p, o_d = oracle.hybrid_attention(b)
+        assert np.array_equal(o_d[0], o_p[i])
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_bruteforce_agrees_noncausal(case):
+    q_lens, pkv = [(4, 4), (4, 9), (1, 3, 4)][case], [(4, 4), (4, 20), (1, 7, 40)][case]
+    b = W.make_batch(4, 2, list(q_lens), list(pkv), [3, 17], seed=40 + case, causal=False)
+    o_p, o_d = oracle.hybrid_attention(b)
+    r_p, r_d = bruteforce.hybrid_attention(b)
+    assert np.abs(o_p - r_p).max() <= 1e-12 and np.abs(o_d - r_d).max() <= 1e-12

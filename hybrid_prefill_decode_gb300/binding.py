@@ -38,7 +38,7 @@ class Options(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("max_prefill_ctas", ctypes.c_int32), ("decode_splits", ctypes.c_int32),
                 ("prefill_splits", ctypes.c_int32), ("instrument", ctypes.c_int32),
-                ("variant", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("non_causal", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -162,14 +162,16 @@ class Plan:
                  kv_lens: Sequence[int], num_decode_seqs: int, num_blocks: int,
                  max_blocks_per_seq: int, scale: float, variant: str = "fused",
                  num_sms: int = 0, ctas_per_sm: int = 0, max_prefill_ctas: int = 0,
-                 decode_splits: int = 0, prefill_splits: int = 0, instrument: bool = False):
+                 decode_splits: int = 0, prefill_splits: int = 0, instrument: bool = False,
+                 non_causal: bool = False):
         lib = load()
         np_ = len(cu_seqlens) - 1 if len(cu_seqlens) > 0 else 0
         self.problem = Problem(num_q_heads, num_kv_heads, 128, 16, np_,
                                int(cu_seqlens[-1]) if np_ > 0 else 0, num_decode_seqs,
                                num_blocks, max_blocks_per_seq, scale)
         self.options = Options(num_sms, ctas_per_sm, max_prefill_ctas, decode_splits,
-                               prefill_splits, 1 if instrument else 0, VARIANTS[variant])
+                               prefill_splits, 1 if instrument else 0, VARIANTS[variant],
+                               1 if non_causal else 0)
         self.variant = variant
         cu = _i32_array(list(cu_seqlens) if np_ > 0 else [0])
         kv = _i32_array(list(kv_lens))
@@ -182,6 +184,7 @@ class Plan:
 
     @classmethod
     def for_batch(cls, batch, variant="fused", **kw) -> "Plan":
+        kw.setdefault("non_causal", not getattr(batch, "causal", True))
         return cls(batch.num_q_heads, batch.num_kv_heads, batch.host_cu_seqlens,
                    batch.host_kv_lens, batch.num_decode_seqs, batch.num_blocks,
                    batch.max_blocks_per_seq, batch.scale, variant=variant, **kw)

@@ -101,12 +101,14 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   int64_t total = 0;
   double pf = 0, pb = 0, db = 0, df = 0;
   const double row_bytes = 4.0 * Hkv * kHeadDim;  // K + V, bf16
+  const bool causal = opt.non_causal == 0;
   for (int s = 0; s < Np; ++s) {
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
-    pf += 4.0 * kHeadDim * Hq * (double)(q * P + q * (q + 1) / 2);
+    pf += 4.0 * kHeadDim * Hq * (double)(causal ? q * P + q * (q + 1) / 2 : q * L);
     pb += (double)L * row_bytes + 4.0 * q * Hq * kHeadDim;
     for (int64_t t = 0; t < ceil_div(q, tq); ++t) {
-      const int64_t kend = P + std::min(q, (t + 1) * tq);
+      // causal: the tile's last token sees up to its own position; otherwise every row
+      const int64_t kend = causal ? P + std::min(q, (t + 1) * tq) : L;
       const int64_t nt = ceil_div(kend, kTileN);
       for (int h0 = 0; h0 < Hq; h0 += hp) {
         pu.push_back({s, (int)t, h0, kend, nt});

@@ -78,6 +78,7 @@ struct Params {
   int32_t num_sms;
   int32_t max_prefill_per_sm;
   int32_t hp_log2;    // prefill tile: 2^hp_log2 heads x tq tokens
+  int32_t causal;     // 0: chunk tokens see every row of their sequence
   int32_t tq;
   int32_t mode;
   float scale_log2;   // scale * log2(e): scores are kept in base-2 units
@@ -354,7 +355,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     const int qi = t * p.tq + (row >> p.hp_log2);  // this row's token (index in the chunk)
     const int h = h0 + (row & ((1 << p.hp_log2) - 1));  // and query head
     const bool valid = qi < qlen;
-    const int lim = min(P + qi + 1, ke);  // keys [.., lim) are visible to this row
+    const int lim = p.causal ? min(P + qi + 1, ke) : ke;  // keys [.., lim) are visible
     // max over 64 columns of S from `taddr`, of which the first `vis` are visible
     auto rowmax64 = [&](uint32_t taddr, int vis) -> float {
       const bool full = __all_sync(0xffffffffu, vis >= 64);
@@ -1442,7 +1443,8 @@ pod_attn_status pod_attn_plan_bucket(pod_attn_plan_t plan, pod_attn_bucket* out)
   int64_t flops = 0, bytes = 0;
   for (int s = 0; s < Np; ++s) {
     const int64_t q = plan->cu[s + 1] - plan->cu[s], L = plan->kv[s], P = L - q;
-    flops += 4 * kHeadDim * (int64_t)pr.num_q_heads * (q * P + q * (q + 1) / 2);
+    flops += 4 * kHeadDim * (int64_t)pr.num_q_heads *
+             (plan->opt.non_causal == 0 ? q * P + q * (q + 1) / 2 : q * L);
     bytes += L * pr.num_kv_heads * row + q * pr.num_q_heads * row;
   }
   for (int d = 0; d < Nd; ++d)
@@ -1611,6 +1613,7 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   p.num_sms = plan->num_sms;
   p.max_prefill_per_sm = plan->max_prefill_per_sm;
   p.hp_log2 = __builtin_ctz((unsigned)plan->head_pack);
+  p.causal = plan->opt.non_causal == 0;
   p.tq = plan->tile_tokens;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.timeout_ns = kWaitTimeoutNs;

@@ -53,14 +53,15 @@ class Work:
 
 def batch_work(num_q_heads: int, num_kv_heads: int, q_lens: Sequence[int],
                prefill_kv_lens: Sequence[int], decode_kv_lens: Sequence[int],
-               head_dim: int = 128) -> Work:
-    """Algorithmic FLOPs and bytes of one hybrid batch (see the module docstring)."""
+               head_dim: int = 128, causal: bool = True) -> Work:
+    """Algorithmic FLOPs and bytes of one hybrid batch (see the module docstring); with
+    causal=False every chunk token pairs with every row of its sequence."""
     d, Hq, Hkv = head_dim, num_q_heads, num_kv_heads
     row = kv_bytes_per_token(1, Hkv, d, 2)
     pf = pb = 0.0
     for C, L in zip(q_lens, prefill_kv_lens):
         P = L - C
-        pairs = C * P + C * (C + 1) // 2
+        pairs = C * P + C * (C + 1) // 2 if causal else C * L
         pf += 4.0 * d * Hq * pairs
         pb += float(L) * row + 2.0 * C * Hq * d * 2
     db = sum(float(L) * row for L in decode_kv_lens) + 2.0 * len(decode_kv_lens) * Hq * d * 2

@@ -107,6 +107,10 @@ typedef struct {
                                most 8; 0 = auto */
   int32_t instrument;       /* nonzero: record (SM, kind, start, end) per work item */
   pod_attn_variant variant; /* launch variant, see above */
+  int32_t non_causal;       /* nonzero: prefill chunk tokens attend to every row of their
+                               sequence, later chunk tokens included ("Week 6: Beyond PyTorch:
+                               Custom Kernel과 vLLM", §"Non-Causal vs. Causal Attention");
+                               0 = causal (default) */
 } pod_attn_options;
 
 typedef struct pod_attn_plan_s* pod_attn_plan_t;

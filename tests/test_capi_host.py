@@ -94,7 +94,7 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
-def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
+def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True):
     """Items: prefill = (chunk, query tile of 128/hp tokens x hp heads, first head, split) over
     128-key steps (cost 57 each), with hp the largest power of two dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
     item slots per SM; split when an output costs more than a quarter of a slot's share."""
@@ -108,7 +108,7 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0):
         q, L = cu[s + 1] - cu[s], kv[s]
         P = L - q
         for t in range(_cdiv(q, tq)):
-            kend = P + min(q, (t + 1) * tq)
+            kend = P + min(q, (t + 1) * tq) if causal else L      # non-causal: every row
             nt = _cdiv(kend, 128)
             for h in range(0, Hq, hp):
                 pu.append((s, t, h, kend, nt))
@@ -193,6 +193,26 @@ def test_planner_matches_python_restatement(lib, seed):
     assert got_u == exp_u
     inf = p.info()
     assert inf["max_prefill_ctas"] == cap and inf["grid_fused"] == grid
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_planner_matches_python_restatement_non_causal(lib, seed):
+    rng = random.Random(100 + seed)
+    Hq, Hkv, q_lens, pkv, dkv = _random_case(rng)
+    cu = [0]
+    for q in q_lens:
+        cu.append(cu[-1] + q)
+    maxb = _cdiv(max(pkv + dkv + [1]), 16)
+    p = B.Plan(Hq, Hkv, cu if q_lens else [], pkv + dkv, len(dkv), 100, maxb, 0.1,
+               num_sms=152, non_causal=True)
+    got_p, got_d, got_u = p.items()
+    exp_p, exp_d, exp_u, _, _ = restated_plan(Hq, Hkv, cu if q_lens else [], pkv + dkv,
+                                              len(dkv), 152, causal=False)
+    assert (got_p, got_d, got_u) == (exp_p, exp_d, exp_u)
+    ends = {}                                         # every prefill tile reads all rows
+    for it in got_p:
+        ends[(it[1], it[2], it[3])] = max(ends.get((it[1], it[2], it[3]), 0), it[5])
+    assert all(e == pkv[k[0]] for k, e in ends.items())
 
 
 @pytest.mark.parametrize("i", [1, 2, 3, 4])

@@ -15,10 +15,12 @@ def built():
     __graft_entry__.build()
 
 
-def _restated_bucket(Hq, Hkv, q_lens, pkv, dkv):
-    """prefill FLOPs = 4*128*Hq per visible (query, key) pair; bytes = 512 per (row, kv-head) of
-    every sequence plus 512 per (token, q-head); buckets = bit length of ceil(x / unit)."""
-    flops = sum(4 * 128 * Hq * (q * (L - q) + q * (q + 1) // 2) for q, L in zip(q_lens, pkv))
+def _restated_bucket(Hq, Hkv, q_lens, pkv, dkv, causal=True):
+    """prefill FLOPs = 4*128*Hq per visible (query, key) pair (all q*L pairs when non-causal);
+    bytes = 512 per (row, kv-head) of every sequence plus 512 per (token, q-head); buckets = bit
+    length of ceil(x / unit)."""
+    flops = sum(4 * 128 * Hq * ((q * (L - q) + q * (q + 1) // 2) if causal else q * L)
+                for q, L in zip(q_lens, pkv))
     by = sum(L * Hkv * 512 + q * Hq * 512 for q, L in zip(q_lens, pkv))
     by += sum(L * Hkv * 512 + Hq * 512 for L in dkv)
 
@@ -37,13 +39,15 @@ def test_plan_bucket_matches_restatement(seed):
     dkv = [rng.randint(1, 40000) for _ in range(rng.randint(0, 80))]
     if not q_lens and not dkv:
         dkv = [5]
+    causal = rng.random() < 0.7
     cu = [0]
     for q in q_lens:
         cu.append(cu[-1] + q)
     maxb = max(-(-x // 16) for x in pkv + dkv)
-    p = B.Plan(Hq, Hkv, cu if q_lens else [], pkv + dkv, len(dkv), 10, maxb, 0.1, num_sms=152)
+    p = B.Plan(Hq, Hkv, cu if q_lens else [], pkv + dkv, len(dkv), 10, maxb, 0.1, num_sms=152,
+               non_causal=not causal)
     b = p.bucket()
-    flops, by, bf, bb = _restated_bucket(Hq, Hkv, q_lens, pkv, dkv)
+    flops, by, bf, bb = _restated_bucket(Hq, Hkv, q_lens, pkv, dkv, causal)
     assert (b["prefill_flops"], b["read_bytes"], b["bucket_flops"], b["bucket_bytes"]) == \
         (flops, by, bf, bb)
     inf = p.info()

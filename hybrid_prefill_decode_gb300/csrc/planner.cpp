@@ -26,6 +26,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <functional>
+#include <numeric>
 
 #include "pod_internal.h"
 
@@ -41,11 +43,6 @@ constexpr int kMinPrefillTilesPerSplit = 4;
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-struct Pending {
-  int64_t cost;
-  int32_t w[kItemWords];
-};
 
 }  // namespace
 
@@ -137,17 +134,10 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   const int64_t target_p = std::max<int64_t>(target, total_p / ((int64_t)num_sms * 4));
 
   // ---- split and emit ----------------------------------------------------------------------
-  std::vector<Pending> lp, ld;
-  plan->units.clear();
-  int p_slots = 0, d_slots = 0;
-  auto add_unit = [&](int nsplit, int kind) {
-    int u = (int)(plan->units.size() / kUnitWords);
-    int first = kind == 0 ? p_slots : d_slots;
-    (kind == 0 ? p_slots : d_slots) += nsplit;
-    plan->units.insert(plan->units.end(), {nsplit, first, kind, 0});
-    return u;
-  };
-  for (const PUnit& x : pu) {
+  // Items are written in enumeration order into flat arrays (cost, 8 words), then ordered
+  // longest first; ties keep enumeration order (the sort key carries the item's index).
+  struct Split { int64_t ns, chunk; };
+  auto split_p = [&](const PUnit& x) {
     int64_t ns;
     if (opt.prefill_splits > 0) {
       ns = opt.prefill_splits;
@@ -157,17 +147,9 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     }
     ns = std::max<int64_t>(1, std::min<int64_t>({ns, x.ntiles, (int64_t)kMaxPrefillSplits}));
     const int64_t chunk = ceil_div(x.ntiles, ns);
-    ns = ceil_div(x.ntiles, chunk);
-    const int u = ns > 1 ? add_unit((int)ns, 0) : -1;
-    for (int64_t k = 0; k < ns; ++k) {
-      const int64_t t0 = k * chunk, t1 = std::min(x.ntiles, (k + 1) * chunk);
-      Pending it{(t1 - t0) * kPrefillTileCost,
-                 {0, x.s, x.t, x.h, (int32_t)(t0 * kTileN),
-                  (int32_t)std::min(x.kend, t1 * kTileN), u, (int32_t)k}};
-      lp.push_back(it);
-    }
-  }
-  for (const DUnit& x : du) {
+    return Split{ceil_div(x.ntiles, chunk), chunk};
+  };
+  auto split_d = [&](const DUnit& x) {
     int64_t ns;
     if (opt.decode_splits > 0) {
       ns = opt.decode_splits;
@@ -178,42 +160,110 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     }
     ns = std::max<int64_t>(1, std::min(ns, x.nblk));
     const int64_t chunk = ceil_div(x.nblk, ns);
-    ns = ceil_div(x.nblk, chunk);
-    const int u = ns > 1 ? add_unit((int)ns, 1) : -1;
-    for (int64_t k = 0; k < ns; ++k) {
-      const int64_t b0 = k * chunk, b1 = std::min(x.nblk, (k + 1) * chunk);
-      Pending it{(b1 - b0) * kDecodeBlockCost,
-                 {1, x.d, x.g, 0, (int32_t)(b0 * kBlockSize),
-                  (int32_t)std::min(x.L, b1 * kBlockSize), u, (int32_t)k}};
-      ld.push_back(it);
+    return Split{ceil_div(x.nblk, chunk), chunk};
+  };
+  std::vector<Split> sp(pu.size()), sd(du.size());
+  size_t n_p = 0, n_d = 0, n_units = 0;
+  for (size_t i = 0; i < pu.size(); ++i) {
+    sp[i] = split_p(pu[i]);
+    n_p += (size_t)sp[i].ns;
+    n_units += sp[i].ns > 1;
+  }
+  for (size_t i = 0; i < du.size(); ++i) {
+    sd[i] = split_d(du[i]);
+    n_d += (size_t)sd[i].ns;
+    n_units += sd[i].ns > 1;
+  }
+  std::vector<int64_t> cost_p(n_p), cost_d(n_d);
+  std::vector<int32_t> words_p(n_p * kItemWords), words_d(n_d * kItemWords);
+  plan->units.clear();
+  plan->units.reserve(n_units * kUnitWords);
+  int p_slots = 0, d_slots = 0;
+  auto add_unit = [&](int nsplit, int kind) {
+    int u = (int)(plan->units.size() / kUnitWords);
+    int first = kind == 0 ? p_slots : d_slots;
+    (kind == 0 ? p_slots : d_slots) += nsplit;
+    plan->units.push_back(nsplit);
+    plan->units.push_back(first);
+    plan->units.push_back(kind);
+    plan->units.push_back(0);
+    return u;
+  };
+  size_t ip = 0, id = 0;
+  for (size_t i = 0; i < pu.size(); ++i) {
+    const PUnit& x = pu[i];
+    const int64_t ns = sp[i].ns, chunk = sp[i].chunk;
+    const int u = ns > 1 ? add_unit((int)ns, 0) : -1;
+    for (int64_t k = 0; k < ns; ++k, ++ip) {
+      const int64_t t0 = k * chunk, t1 = std::min(x.ntiles, (k + 1) * chunk);
+      cost_p[ip] = (t1 - t0) * kPrefillTileCost;
+      const int32_t w[kItemWords] = {0, x.s, x.t, x.h, (int32_t)(t0 * kTileN),
+                                     (int32_t)std::min(x.kend, t1 * kTileN), u, (int32_t)k};
+      std::memcpy(&words_p[ip * kItemWords], w, sizeof(w));
     }
   }
-  // longest first (stable: ties keep enumeration order)
-  auto by_cost = [](const Pending& a, const Pending& b) { return a.cost > b.cost; };
-  std::stable_sort(lp.begin(), lp.end(), by_cost);
-  std::stable_sort(ld.begin(), ld.end(), by_cost);
-  plan->items_p.clear();
-  plan->items_d.clear();
-  for (auto& it : lp) plan->items_p.insert(plan->items_p.end(), it.w, it.w + kItemWords);
-  for (auto& it : ld) plan->items_d.insert(plan->items_d.end(), it.w, it.w + kItemWords);
+  for (size_t i = 0; i < du.size(); ++i) {
+    const DUnit& x = du[i];
+    const int64_t ns = sd[i].ns, chunk = sd[i].chunk;
+    const int u = ns > 1 ? add_unit((int)ns, 1) : -1;
+    for (int64_t k = 0; k < ns; ++k, ++id) {
+      const int64_t b0 = k * chunk, b1 = std::min(x.nblk, (k + 1) * chunk);
+      cost_d[id] = (b1 - b0) * kDecodeBlockCost;
+      const int32_t w[kItemWords] = {1, x.d, x.g, 0, (int32_t)(b0 * kBlockSize),
+                                     (int32_t)std::min(x.L, b1 * kBlockSize), u, (int32_t)k};
+      std::memcpy(&words_d[id * kItemWords], w, sizeof(w));
+    }
+  }
+  // longest first, ties in enumeration order: a stable counting sort over the few distinct
+  // costs (items of one split size share a cost)
+  auto order = [](const std::vector<int64_t>& cost, const std::vector<int32_t>& words,
+                  std::vector<int32_t>& out) {
+    const size_t n = cost.size();
+    std::vector<int64_t> distinct;
+    for (size_t i = 0; i < n; ++i)  // few distinct values: a scan from the last one found
+      if (distinct.empty() || (distinct.back() != cost[i] &&
+                               std::find(distinct.begin(), distinct.end(), cost[i]) == distinct.end()))
+        distinct.push_back(cost[i]);
+    std::sort(distinct.begin(), distinct.end(), std::greater<int64_t>());
+    std::vector<size_t> start(distinct.size() + 1, 0);
+    std::vector<uint32_t> bucket(n);
+    for (size_t i = 0; i < n; ++i) {  // bucket = rank of the cost, largest first
+      bucket[i] = (uint32_t)(std::lower_bound(distinct.begin(), distinct.end(), cost[i],
+                                              std::greater<int64_t>()) - distinct.begin());
+      ++start[bucket[i] + 1];
+    }
+    for (size_t b = 1; b < start.size(); ++b) start[b] += start[b - 1];
+    out.resize(n * kItemWords);
+    for (size_t i = 0; i < n; ++i)
+      std::memcpy(&out[(start[bucket[i]]++) * kItemWords], &words[i * kItemWords],
+                  kItemWords * sizeof(int32_t));
+  };
+  order(cost_p, words_p, plan->items_p);
+  order(cost_d, words_d, plan->items_d);
   plan->num_p_slots = p_slots;
   // where each token of this iteration sits in its sequence (the KV append writes its K/V
   // row there): chunk token i of prefill sequence s at kv_len - q_len + i, a decode token at
   // kv_len - 1 ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM", §"한 스텝에 여러 종류의 request
   // 섞기": an extend token follows the cached rows, a decode token is the last row)
-  plan->new_rows.clear();
+  plan->new_rows.resize(2 * ((size_t)prob.num_prefill_tokens + Nd));
+  size_t r = 0;
   for (int s = 0; s < Np; ++s) {
     const int32_t q = cu[s + 1] - cu[s], P = kv[s] - q;
-    for (int32_t i = 0; i < q; ++i) plan->new_rows.insert(plan->new_rows.end(), {s, P + i});
+    for (int32_t i = 0; i < q; ++i, r += 2) {
+      plan->new_rows[r] = s;
+      plan->new_rows[r + 1] = P + i;
+    }
   }
-  for (int d = 0; d < Nd; ++d) plan->new_rows.insert(plan->new_rows.end(), {Np + d, kv[Np + d] - 1});
+  for (int d = 0; d < Nd; ++d, r += 2) {
+    plan->new_rows[r] = Np + d;
+    plan->new_rows[r + 1] = kv[Np + d] - 1;
+  }
   plan->num_d_slots = d_slots;
 
-  const int n_p = (int)lp.size(), n_d = (int)ld.size();
   plan->max_prefill_per_sm = 1;  // one prefill pipeline per SM
-  plan->grid_fused = (int)std::min<int64_t>(num_sms, n_p + n_d);
-  plan->grid_prefill = (int)std::min<int64_t>(num_sms, n_p);
-  plan->grid_decode = (int)std::min<int64_t>(num_sms, n_d);
+  plan->grid_fused = (int)std::min<int64_t>(num_sms, (int64_t)(n_p + n_d));
+  plan->grid_prefill = (int)std::min<int64_t>(num_sms, (int64_t)n_p);
+  plan->grid_decode = (int)std::min<int64_t>(num_sms, (int64_t)n_d);
 
   // ---- workspace layout --------------------------------------------------------------------
   WorkspaceLayout& w = plan->ws;

@@ -163,10 +163,10 @@ class Plan:
                  max_blocks_per_seq: int, scale: float, variant: str = "fused",
                  num_sms: int = 0, ctas_per_sm: int = 0, max_prefill_ctas: int = 0,
                  decode_splits: int = 0, prefill_splits: int = 0, instrument: bool = False,
-                 non_causal: bool = False):
+                 non_causal: bool = False, head_dim: int = 128):
         lib = load()
         np_ = len(cu_seqlens) - 1 if len(cu_seqlens) > 0 else 0
-        self.problem = Problem(num_q_heads, num_kv_heads, 128, 16, np_,
+        self.problem = Problem(num_q_heads, num_kv_heads, head_dim, 16, np_,
                                int(cu_seqlens[-1]) if np_ > 0 else 0, num_decode_seqs,
                                num_blocks, max_blocks_per_seq, scale)
         self.options = Options(num_sms, ctas_per_sm, max_prefill_ctas, decode_splits,
@@ -185,6 +185,7 @@ class Plan:
     @classmethod
     def for_batch(cls, batch, variant="fused", **kw) -> "Plan":
         kw.setdefault("non_causal", not getattr(batch, "causal", True))
+        kw.setdefault("head_dim", int(batch.head_dim))
         return cls(batch.num_q_heads, batch.num_kv_heads, batch.host_cu_seqlens,
                    batch.host_kv_lens, batch.num_decode_seqs, batch.num_blocks,
                    batch.max_blocks_per_seq, batch.scale, variant=variant, **kw)

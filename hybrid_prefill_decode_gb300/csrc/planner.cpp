@@ -55,7 +55,10 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
       !(prob.scale > 0.f))
     return POD_ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return POD_ATTN_ERR_INVALID_ARG;
-  if (prob.head_dim != kHeadDim || prob.block_size != kBlockSize) return POD_ATTN_ERR_UNSUPPORTED;
+  // head dims 128 and 64 (the layouts are sized for 128; 64 uses their first half)
+  if ((prob.head_dim != kHeadDim && prob.head_dim != 64) || prob.block_size != kBlockSize)
+    return POD_ATTN_ERR_UNSUPPORTED;
+  const int D = prob.head_dim;
   const int G = Hq / Hkv;
   if (G > kMaxGroup) return POD_ATTN_ERR_UNSUPPORTED;
   if ((Np == 0) != (prob.num_prefill_tokens == 0)) return POD_ATTN_ERR_INVALID_ARG;
@@ -97,12 +100,12 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   std::vector<DUnit> du;
   int64_t total = 0;
   double pf = 0, pb = 0, db = 0, df = 0;
-  const double row_bytes = 4.0 * Hkv * kHeadDim;  // K + V, bf16
+  const double row_bytes = 4.0 * Hkv * D;  // K + V, bf16
   const bool causal = opt.non_causal == 0;
   for (int s = 0; s < Np; ++s) {
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
-    pf += 4.0 * kHeadDim * Hq * (double)(causal ? q * P + q * (q + 1) / 2 : q * L);
-    pb += (double)L * row_bytes + 4.0 * q * Hq * kHeadDim;
+    pf += 4.0 * D * Hq * (double)(causal ? q * P + q * (q + 1) / 2 : q * L);
+    pb += (double)L * row_bytes + 4.0 * q * Hq * D;
     for (int64_t t = 0; t < ceil_div(q, tq); ++t) {
       // causal: the tile's last token sees up to its own position; otherwise every row
       const int64_t kend = causal ? P + std::min(q, (t + 1) * tq) : L;
@@ -115,8 +118,8 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   }
   for (int d = 0; d < Nd; ++d) {
     const int64_t L = kv[Np + d];
-    db += (double)L * row_bytes + 4.0 * Hq * kHeadDim;
-    df += 4.0 * kHeadDim * Hq * (double)L;
+    db += (double)L * row_bytes + 4.0 * Hq * D;
+    df += 4.0 * D * Hq * (double)L;
     for (int g = 0; g < Hkv; ++g) {
       du.push_back({d, g, L, ceil_div(L, kBlockSize)});
       total += ceil_div(L, kBlockSize) * kDecodeBlockCost;

@@ -79,6 +79,7 @@ struct Params {
   int32_t max_prefill_per_sm;
   int32_t hp_log2;    // prefill tile: 2^hp_log2 heads x tq tokens
   int32_t causal;     // 0: chunk tokens see every row of their sequence
+  int32_t head_dim;   // 128 or 64 (selects the kernel instantiation)
   int32_t tq;
   int32_t mode;
   float scale_log2;   // scale * log2(e): scores are kept in base-2 units
@@ -120,7 +121,6 @@ struct DecodeCtx {
 };
 
 constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, 0, 0);     // S = Q Kᵀ, both K-major
-constexpr uint32_t kIdescPV = idesc_bf16(kTileM, kHeadDim, 0, 1);  // O += P V, V is N-major
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
@@ -133,7 +133,9 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 // the cache is append-only; §"한 스텝에 여러 종류의 request 섞기"): every new token's K and V row
 // of each kv-head is written into its paged block. One warp per (token, kv-head): lanes 0-15 copy
 // the K row, lanes 16-31 the V row, 16 bytes each (coalesced 256-byte rows).
+template <int HD>
 __device__ void append_rows(const Params& p) {
+  constexpr int kVec = HD / 8;  // 16-byte vectors per row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = p.n_new * p.Hkv;
   for (int u = blockIdx.x * kWarps + warp; u < units; u += gridDim.x * kWarps) {
@@ -145,9 +147,12 @@ __device__ void append_rows(const Params& p) {
       continue;
     }
     const size_t row = ((size_t)phys * p.Hkv + g) * kBlockSize + pos % kBlockSize;
-    const uint16_t* src = (lane < 16 ? p.k_new : p.v_new) + ((size_t)tok * p.Hkv + g) * kHeadDim;
-    uint16_t* dst = (lane < 16 ? p.k_pool_w : p.v_pool_w) + row * kHeadDim;
-    reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
+    if (lane >= 2 * kVec) continue;  // lanes [0, kVec) copy the K row, [kVec, 2 kVec) the V row
+    const bool is_k = lane < kVec;
+    const int v = lane % kVec;
+    const uint16_t* src = (is_k ? p.k_new : p.v_new) + ((size_t)tok * p.Hkv + g) * HD;
+    uint16_t* dst = (is_k ? p.k_pool_w : p.v_pool_w) + row * HD;
+    reinterpret_cast<uint4*>(dst)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
   }
 }
 
@@ -184,10 +189,18 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 // reference max per row in common: when no score of the step exceeds it by more than 2^8 (the
 // lazy-rescale threshold) — which a vote over both groups establishes — nothing is exchanged;
 // otherwise both groups read the whole row of S and move the reference alike.
+// HD (head dim) is 128 or 64; shared memory and TMEM keep the layout of 128 (a 64-dim head
+// uses the first 64-column half of every tile and the first 64 columns of O).
+template <int HD>
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
                              const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
                              SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
   static_assert(kVStages == 2, "V stages and TMEM buffers are indexed by n & 1");
+  static_assert(HD == 64 || HD == 128, "head dim");
+  constexpr int kHalves = HD / 64;                  // 64-dim halves (128-byte swizzle atoms)
+  constexpr int kOG = HD / 2;                       // O columns of one softmax group
+  constexpr uint32_t kIdescPVh = idesc_bf16(kTileM, HD, 0, 1);  // O += P V, V N-major
+  constexpr uint32_t kQBytes = kTileM * HD * 2, kTileBytes = kTileN * HD * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = it[1], t = it[2], h0 = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
   const int g = h0 / p.G;  // the tile's heads h0 .. h0 + hp - 1 share kv-head g
@@ -214,10 +227,11 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
     if (is_k && lane == 0) {
       const uint32_t qbar = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qbar, kSmemQ);
+      mbar_arrive_expect_tx(qbar, kQBytes);
       // box {64 dims, hp heads, tq tokens}: tile row r = token r / hp, head h0 + r % hp
-      tma_load_3d(sQ, tmq, qbar, 0, h0, q0 + t * p.tq);
-      tma_load_3d(sQ + kSmemQ / 2, tmq, qbar, 64, h0, q0 + t * p.tq);
+#pragma unroll
+      for (int hf = 0; hf < kHalves; ++hf)
+        tma_load_3d(sQ + hf * (kSmemQ / 2), tmq, qbar, 64 * hf, h0, q0 + t * p.tq);
     }
     uint64_t* free_bar = is_k ? ctl->k_empty : ctl->pv_done;
     const uint32_t nst = is_k ? kKStages : kVStages;
@@ -259,12 +273,12 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       if (lane == 0) {
         const uint32_t full = smem_u32(&full_bar[stage]);
         const uint32_t dst = ring + stage * kSmemKTile;
-        mbar_arrive_expect_tx(full, kSmemKTile);
+        mbar_arrive_expect_tx(full, kTileBytes);
 #pragma unroll
-        for (int b = 0; b < kBlocksPerTile; ++b) {
-          tma_load_2d(dst + b * 2048, tm, full, 0, y[b]);
-          tma_load_2d(dst + kSmemKTile / 2 + b * 2048, tm, full, 64, y[b]);
-        }
+        for (int b = 0; b < kBlocksPerTile; ++b)
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_load_2d(dst + hf * (kSmemKTile / 2) + b * 2048, tm, full, 64 * hf, y[b]);
       }
     }
   } else if (warp == 1) {
@@ -290,7 +304,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         const uint32_t sK = sKring + ks * kSmemKTile;
         const uint32_t dS = tmem + kTmemS + (n & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
           const uint64_t ad = sdesc_sw128(sQ + half * (kSmemQ / 2) + koff, 16, 1024);
           const uint64_t bd = sdesc_sw128(sK + half * (kSmemKTile / 2) + koff, 16, 1024);
@@ -321,8 +335,8 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         // zero there but 0 * NaN is not, so clear those V rows before the P·V product.
         const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
         uint8_t* vbase = smem + (sVring - sQ) + (n & 1) * kSmemKTile;
-        for (int c = lane; c < (r1 - r0) * 16; c += 32) {
-          const int r = r0 + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
+        for (int c = lane; c < (r1 - r0) * 8 * kHalves; c += 32) {  // 16-byte chunks
+          const int r = r0 + c / (8 * kHalves), half = (c >> 3) % kHalves, q16 = c & 7;
           *reinterpret_cast<uint4*>(vbase + half * (kSmemKTile / 2) + r * 128 + q16 * 16) =
               make_uint4(0, 0, 0, 0);
         }
@@ -338,7 +352,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           // P of keys 16kk.. at column 8kk of its buffer; V is N-major: 64-column halves
           // 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
           const uint64_t bd = sdesc_sw128(sV + kk * 2048, kSmemKTile / 2, 1024);
-          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPV, (j == 0 && kk == 0) ? 0u : 1u);
+          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPVh, (j == 0 && kk == 0) ? 0u : 1u);
         }
         umma_commit(smem_u32(&ctl->pv_done[n & 1]));
       }
@@ -351,7 +365,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     const int row = quarter * 32 + lane;
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tO = trow + kTmemO + grp * 64;
+    const uint32_t tO = trow + kTmemO + grp * kOG;  // this group's O columns
     const int qi = t * p.tq + (row >> p.hp_log2);  // this row's token (index in the chunk)
     const int h = h0 + (row & ((1 << p.hp_log2) - 1));  // and query head
     const bool valid = qi < qlen;
@@ -435,7 +449,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
                                                        ((n - 1) >> 1) & 1, wc));
           tc_fence_after();
 #pragma unroll 1
-          for (int ch = 0; ch < 2; ++ch) {  // this group's 64 columns of O
+          for (int ch = 0; ch < kOG / 32; ++ch) {  // this group's columns of O
             uint32_t o[32];
             tmem_ld32(tO + ch * 32, o);
             tmem_ld_wait();
@@ -498,9 +512,9 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     {
       if (unit < 0) {
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim + grp * 64;
+        uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD + grp * kOG;
 #pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int ch = 0; ch < kOG / 32; ++ch) {
           uint32_t o[32];
           tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
@@ -518,11 +532,12 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         const int slot0 = p.units[unit * kUnitWords + 1];
         float* slot = p.partial_p + (size_t)(slot0 + split) * kPrefillSlotFloats;
 #pragma unroll 1
-        for (int ch = 0; ch < 2 && ok; ++ch) {
+        for (int ch = 0; ch < kOG / 32 && ok; ++ch) {
           uint32_t o[32];
           tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait();
-          float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + grp * 64 + ch * 32);
+          // slot rows keep a stride of 128 columns whatever the head dim
+          float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + grp * kOG + ch * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             d4[i] = make_float4(u2f(o[4 * i]), u2f(o[4 * i + 1]), u2f(o[4 * i + 2]), u2f(o[4 * i + 3]));
@@ -557,10 +572,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
               den += f[k] * lk;
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * kHeadDim + grp * 64;
-            const float* ob = p.partial_p + (size_t)slot0 * kPrefillSlotFloats + row * kHeadDim + grp * 64;
+            uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD + grp * kOG;
+            const float* ob = p.partial_p + (size_t)slot0 * kPrefillSlotFloats + row * kHeadDim + grp * kOG;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {  // 16 columns at a time
+            for (int ch = 0; ch < kOG / 16; ++ch) {  // 16 columns at a time
               float acc[16];
 #pragma unroll
               for (int c = 0; c < 16; ++c) acc[c] = 0.f;
@@ -646,12 +661,32 @@ __device__ __forceinline__ float rowdot_scatter(float (&v)[16], int lane) {
 constexpr int kScr = kHeadDim + 4;  // shared scratch row of one warp and head: o[128], m, l
 constexpr int kRow = kHeadDim + 2;  // global partial slot row: o[128], m, l
 
+// DL consecutive bf16 values of one lane (DL = head dim / 32: 4 or 2), as one vector load.
+template <int DL> struct LaneVec;
+template <> struct LaneVec<4> {
+  uint2 v;
+  __device__ __forceinline__ void load(const uint16_t* src) { v = *reinterpret_cast<const uint2*>(src); }
+  __device__ __forceinline__ float operator[](int i) const {
+    return i == 0 ? bf16lo(v.x) : i == 1 ? bf16hi(v.x) : i == 2 ? bf16lo(v.y) : bf16hi(v.y);
+  }
+  __device__ __forceinline__ void zero() { v = make_uint2(0, 0); }
+};
+template <> struct LaneVec<2> {
+  uint32_t v;
+  __device__ __forceinline__ void load(const uint16_t* src) { v = *reinterpret_cast<const uint32_t*>(src); }
+  __device__ __forceinline__ float operator[](int i) const { return i == 0 ? bf16lo(v) : bf16hi(v); }
+  __device__ __forceinline__ void zero() { v = 0; }
+};
+
 // Decode, MHA (one query head per kv-head): CUDA-core path. Each warp streams its blocks with
-// 4 KiB bulk copies; q lives in registers (4 dims per lane); q·k is reduce-scattered across the
-// warp with shuffles. Leaves the warp's (o, m, l) in the shared scratch; returns false on abort.
-template <int GT>
+// bulk copies of whole (block, kv-head) units; q lives in registers (HD/32 dims per lane); q·k is
+// reduce-scattered across the warp with shuffles. Leaves the warp's (o, m, l) in the shared
+// scratch; returns false on abort.
+template <int GT, int HD>
 __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx& dc,
                             SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
+  constexpr int DL = HD / 32;                    // dims per lane
+  constexpr uint32_t kUnit = kBlockSize * HD * 2;  // bytes of one (block, kv-head) K or V unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wl = warp - dc.w0;  // this warp's index among the item's warps
   const int d = it[1], g = it[2], kb = it[4], ke = it[5];
@@ -669,21 +704,19 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
   uint8_t* ring = dc.ring + (mine ? wl : 0) * kDecodeSlots * kSmemDecodeSlot;
   float* ps_x = dc.scores + (mine ? wl : 0) * kMaxGroup * kBlockSize;
 
-  // q in registers: 4 consecutive dims per lane, premultiplied by scale*log2(e)
-  float q[GT][4], o[GT][4], m[GT], ls[GT];
+  // q in registers: DL consecutive dims per lane, premultiplied by scale*log2(e)
+  float q[GT][DL], o[GT][DL], m[GT], ls[GT];
 #pragma unroll
   for (int h = 0; h < GT; ++h) {
     m[h] = -INFINITY;
     ls[h] = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[h][k] = q[h][k] = 0.f;
+    for (int k = 0; k < DL; ++k) o[h][k] = q[h][k] = 0.f;
     if (h < G) {
-      const uint2 r = *reinterpret_cast<const uint2*>(
-          p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + lane * 4);
-      q[h][0] = bf16lo(r.x) * p.scale_log2;
-      q[h][1] = bf16hi(r.x) * p.scale_log2;
-      q[h][2] = bf16lo(r.y) * p.scale_log2;
-      q[h][3] = bf16hi(r.y) * p.scale_log2;
+      LaneVec<DL> r;
+      r.load(p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + h) * HD + lane * DL);
+#pragma unroll
+      for (int k = 0; k < DL; ++k) q[h][k] = r[k] * p.scale_log2;
     }
   }
 
@@ -695,12 +728,12 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
     }
-    const size_t off = ((size_t)phys * p.Hkv + g) * (kBlockSize * kHeadDim);
+    const size_t off = ((size_t)phys * p.Hkv + g) * (kBlockSize * HD);
     const uint32_t bar = smem_u32(&ctl->dslot[warp][slot]);
     const uint32_t dst = smem_u32(ring + slot * kSmemDecodeSlot);
-    mbar_arrive_expect_tx(bar, kSmemDecodeSlot);
-    bulk_load(dst, p.k_pool + off, kSmemDecodeSlot / 2, bar, pol);
-    bulk_load(dst + kSmemDecodeSlot / 2, p.v_pool + off, kSmemDecodeSlot / 2, bar, pol);
+    mbar_arrive_expect_tx(bar, 2 * kUnit);
+    bulk_load(dst, p.k_pool + off, kUnit, bar, pol);
+    bulk_load(dst + kSmemDecodeSlot / 2, p.v_pool + off, kUnit, bar, pol);
   };
   if (lane == 0) {
     if (nmine > 0) issue(0);
@@ -719,17 +752,19 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
     const int nv = min(kBlockSize, ke - key0);
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(ring + slot * kSmemDecodeSlot);
     const uint16_t* Vs = Ks + kBlockSize * kHeadDim;
-    uint2 kr[16];
+    LaneVec<DL> kr[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) kr[c] = *reinterpret_cast<const uint2*>(Ks + c * kHeadDim + lane * 4);
+    for (int c = 0; c < 16; ++c) kr[c].load(Ks + c * HD + lane * DL);
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
       if (h < G) {
         float part[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          part[c] = q[h][0] * bf16lo(kr[c].x) + q[h][1] * bf16hi(kr[c].x) +
-                    q[h][2] * bf16lo(kr[c].y) + q[h][3] * bf16hi(kr[c].y);
+        for (int c = 0; c < 16; ++c) {
+          part[c] = 0.f;
+#pragma unroll
+          for (int k = 0; k < DL; ++k) part[c] += q[h][k] * kr[c][k];
+        }
         float sc = rowdot_scatter(part, lane);
         sc = r < nv ? sc : -INFINITY;
         float bm = sc;
@@ -742,7 +777,7 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
           m[h] = bm;
           ls[h] *= alpha;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) o[h][k] *= alpha;
+          for (int k = 0; k < DL; ++k) o[h][k] *= alpha;
         }
         const float pv = r < nv ? ex2(sc - m[h]) : 0.f;
         if ((lane & 1) == 0) {
@@ -752,14 +787,14 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
       }
     }
     __syncwarp();
-    uint2 vr[16];
+    LaneVec<DL> vr[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) vr[c] = *reinterpret_cast<const uint2*>(Vs + c * kHeadDim + lane * 4);
+    for (int c = 0; c < 16; ++c) vr[c].load(Vs + c * HD + lane * DL);
     if (nv < kBlockSize) {
       // rows past the sequence end may hold anything; their weight is 0 and so is their value
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        if (c >= nv) vr[c] = make_uint2(0, 0);
+        if (c >= nv) vr[c].zero();
     }
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
@@ -770,13 +805,9 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
           const float4 w = pp[c4];
           const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint2 v = vr[c4 * 4 + e];
-            o[h][0] += wv[e] * bf16lo(v.x);
-            o[h][1] += wv[e] * bf16hi(v.x);
-            o[h][2] += wv[e] * bf16lo(v.y);
-            o[h][3] += wv[e] * bf16hi(v.y);
-          }
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int k = 0; k < DL; ++k) o[h][k] += wv[e] * vr[c4 * 4 + e][k];
         }
       }
     }
@@ -797,7 +828,8 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
     for (int h = 0; h < GT; ++h) {
       if (h < G) {
         float* dst = scr + (wl * GT + h) * kScr;
-        *reinterpret_cast<float4*>(dst + lane * 4) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+#pragma unroll
+        for (int k = 0; k < DL; ++k) dst[lane * DL + k] = o[h][k];
         if (lane == 0) {
           dst[kHeadDim] = m[h];
           dst[kHeadDim + 1] = ls[h];
@@ -814,10 +846,12 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
 // 16-key block: S = Q·Kᵀ with the G heads as rows (2 x 8 MMAs), a row softmax over 16 keys with
 // quad shuffles, then Oᵀ += Vᵀ·Pᵀ (8 MMAs) with the heads as columns, so P goes from the S
 // accumulators straight into the B operand and the accumulator needs only 32 registers.
-template <int GT>
+template <int GT, int HD>
 __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                           const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl, PipeState& ps,
                           const WaitCtx& wc) {
+  constexpr int kKS = HD / 16;     // k-steps of S = Q Kᵀ and 16-dim tiles of Oᵀ
+  constexpr int kHalves = HD / 64; // 64-dim halves of a K or V block in the slot
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wl = warp - dc.w0;  // this warp's index among the item's warps
   const int d = it[1], g = it[2], kb = it[4], ke = it[5];
@@ -837,21 +871,21 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
   const int hr = lane >> 2, qd = lane & 3;  // fragment row (query head) and quad lane
 
   // A fragments of Q: row hr = head g*G + hr (rows >= G and rows 8..15 are zero)
-  uint32_t qa0[8], qa2[8];
+  uint32_t qa0[kKS], qa2[kKS];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) qa0[ks] = qa2[ks] = 0u;
+  for (int ks = 0; ks < kKS; ++ks) qa0[ks] = qa2[ks] = 0u;
   if (hr < G) {
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(
-        p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + hr) * kHeadDim);
+        p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + hr) * HD);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < kKS; ++ks) {
       qa0[ks] = qw[ks * 8 + qd];
       qa2[ks] = qw[ks * 8 + qd + 4];
     }
   }
-  float ot[8][4];  // Oᵀ: dims 16mt + hr (+8) x heads 2qd, 2qd+1
+  float ot[kKS][4];  // Oᵀ: dims 16mt + hr (+8) x heads 2qd, 2qd+1
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+  for (int mt = 0; mt < kKS; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
   float m = -INFINITY, l = 0.f;
 
   auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
@@ -864,11 +898,12 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
     const int y = (phys * p.Hkv + g) * kBlockSize;
     const uint32_t bar = smem_u32(&ctl->dslot[warp][slot]);
     const uint32_t dst = ring_s + slot * kSmemDecodeSlot;
-    mbar_arrive_expect_tx(bar, kSmemDecodeSlot);
-    tma_load_2d(dst, tmk, bar, 0, y);
-    tma_load_2d(dst + 2048, tmk, bar, 64, y);
-    tma_load_2d(dst + 4096, tmv, bar, 0, y);
-    tma_load_2d(dst + 6144, tmv, bar, 64, y);
+    mbar_arrive_expect_tx(bar, 2 * kBlockSize * HD * 2);
+#pragma unroll
+    for (int hf = 0; hf < kHalves; ++hf) {  // K at +0, V at +4 KiB; 64-dim halves 2 KiB apart
+      tma_load_2d(dst + hf * 2048, tmk, bar, 64 * hf, y);
+      tma_load_2d(dst + 4096 + hf * 2048, tmv, bar, 64 * hf, y);
+    }
   };
   if (lane == 0) {
     if (nmine > 0) issue(0);
@@ -890,8 +925,8 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       // rows past the sequence end may hold anything (even NaN): zero those V rows, since
       // their weight 0 times NaN would not be 0
       uint8_t* vb = ring + slot * kSmemDecodeSlot + 4096;
-      for (int c = lane; c < (kBlockSize - nv) * 16; c += 32) {
-        const int r = nv + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+      for (int c = lane; c < (kBlockSize - nv) * 8 * kHalves; c += 32) {
+        const int r = nv + c / (8 * kHalves), half = (c >> 3) % kHalves, ch = c & 7;
         *reinterpret_cast<uint4*>(vb + half * 2048 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
@@ -900,7 +935,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
     // S = Q Kᵀ: keys 0-7 in s0, keys 8-15 in s1
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < kKS; ++ks) {
       const int key = (mi >> 1) * 8 + mr, ch = (ks & 3) * 2 + (mi & 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(Ks + (ks >> 2) * 2048 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
@@ -932,7 +967,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * qd);
       const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * qd + 4);
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
+      for (int mt = 0; mt < kKS; ++mt) {
         ot[mt][0] *= a0;
         ot[mt][1] *= a1;
         ot[mt][2] *= a0;
@@ -950,7 +985,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
     const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]), pb1 = pack_bf16x2(pr[2], pr[3]);
     // Oᵀ += Vᵀ Pᵀ: A = Vᵀ tiles of 16 dims x 16 keys, ldmatrix-transposed from the V slot
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+    for (int mt = 0; mt < kKS; ++mt) {
       const int key = (mi >> 1) * 8 + mr, ch = (mt & 3) * 2 + (mi & 1);
       uint32_t a[4];
       ldsm_x4_t(Vs + (mt >> 2) * 2048 + key * 128 + ((ch ^ (key & 7)) << 4), a[0], a[1], a[2],
@@ -972,7 +1007,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       if (head < G) {
         float* dst = scr + (wl * GT + head) * kScr;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
+        for (int mt = 0; mt < kKS; ++mt) {
           dst[mt * 16 + hr] = ot[mt][e];
           dst[mt * 16 + hr + 8] = ot[mt][2 + e];
         }
@@ -989,7 +1024,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 
 // Combine the warps' states of a decode item, then write the output or the split's partial and,
 // for the last split of a unit to arrive, merge all partials.
-template <int GT>
+template <int GT, int HD>
 __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                             const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl,
                             PipeState& ps, const WaitCtx& wc) {
@@ -997,17 +1032,17 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
   const int G = p.G;
   const int ltid = threadIdx.x - dc.first_thread;
   if constexpr (GT == 1)
-    decode_simt<GT>(p, it, dc, ctl, ps, wc);
+    decode_simt<GT, HD>(p, it, dc, ctl, ps, wc);
   else
-    decode_tc<GT>(p, tmk, tmv, it, dc, ctl, ps, wc);
+    decode_tc<GT, HD>(p, tmk, tmv, it, dc, ctl, ps, wc);
   named_bar_sync(dc.bar_id, dc.bar_threads);
   const float* scr = reinterpret_cast<const float*>(dc.ring);
   if (!ctl->abort) {
     const int nsplit = unit >= 0 ? p.units[unit * kUnitWords + 0] : 1;
     const int slot0 = unit >= 0 ? p.units[unit * kUnitWords + 1] : 0;
     float* slot = unit >= 0 ? p.partial_d + (size_t)(slot0 + split) * decode_slot_floats(G) : nullptr;
-    for (int idx = ltid; idx < G * kHeadDim; idx += dc.bar_threads) {
-      const int h = idx / kHeadDim, c = idx % kHeadDim;
+    for (int idx = ltid; idx < G * HD; idx += dc.bar_threads) {
+      const int h = idx / HD, c = idx % HD;
       float mx = -INFINITY;
       for (int w = 0; w < dc.nw; ++w) mx = fmaxf(mx, scr[(w * GT + h) * kScr + kHeadDim]);
       float num = 0.f, den = 0.f;
@@ -1020,7 +1055,7 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
         den += f * src[kHeadDim + 1];
       }
       if (unit < 0) {
-        p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + c] = f2bf(num / den);
+        p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * HD + c] = f2bf(num / den);
       } else {
         slot[h * kRow + c] = num;
         if (c == 0) {
@@ -1036,8 +1071,8 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
       named_bar_sync(dc.bar_id, dc.bar_threads);
       if (ctl->merge_last[dc.slot]) {
         __threadfence();
-        for (int idx = ltid; idx < G * kHeadDim; idx += dc.bar_threads) {
-          const int h = idx / kHeadDim, c = idx % kHeadDim;
+        for (int idx = ltid; idx < G * HD; idx += dc.bar_threads) {
+          const int h = idx / HD, c = idx % HD;
           float mx = -INFINITY;
           for (int k = 0; k < nsplit; ++k)
             mx = fmaxf(mx, __ldcg(p.partial_d + (size_t)(slot0 + k) * decode_slot_floats(G) + h * kRow + kHeadDim));
@@ -1050,7 +1085,7 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
             num += f * __ldcg(sl + c);
             den += f * __ldcg(sl + kHeadDim + 1);
           }
-          p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * kHeadDim + c] = f2bf(num / den);
+          p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * HD + c] = f2bf(num / den);
         }
         if (ltid == 0) p.arrive[unit] = 0;
       }
@@ -1096,7 +1131,7 @@ __device__ __forceinline__ void record_item(const Params& p, int kind, int idx, 
 }
 
 // A decode slot's ticket loop; `first` >= 0 is an item already taken for it.
-template <int GT>
+template <int GT, int HD>
 __device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                             const DecodeCtx& dc, int first, int sm, uint32_t sm_raw, SmemCtl* ctl,
                             PipeState& ps, const WaitCtx& wc) {
@@ -1115,12 +1150,12 @@ __device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUten
     const int kind = ctl->item_kind[dc.slot], idx = ctl->item_idx[dc.slot];
     if (kind < 0 || ctl->abort) break;
     const uint64_t t0 = (p.records != nullptr && leader) ? globaltimer() : 0;
-    decode_item<GT>(p, tmk, tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
+    decode_item<GT, HD>(p, tmk, tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
     if (p.records != nullptr && leader) record_item(p, kind, idx, sm_raw, t0);
   }
 }
 
-template <int GT>
+template <int GT, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -1165,7 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   PipeState ps;
   if (p.n_new > 0) {
     // this CTA's share of the KV append, then one arrival; readers of appended rows wait for all
-    append_rows(p);
+    append_rows<HD>(p);
     __syncthreads();
     if (tid == 0) {
       __threadfence();
@@ -1187,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
-      prefill_item(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+      prefill_item<HD>(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
       if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
     }
     if (handoff >= 0 && warp >= kSoftmaxWarp0) {
@@ -1198,14 +1233,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                          reinterpret_cast<float*>(smem + 2 * kSmemDecodeRing +
                                                   sub * kDecodeWarps * kSmemScoresPerWarp),
                          4 + sub, kDecodeWarps * 32, w0 * 32, 2 + sub};
-      decode_loop<GT>(p, &tmk, &tmv, dc, sub == 0 ? handoff : -1, sm, sm_raw, ctl, ps, wc);
+      decode_loop<GT, HD>(p, &tmk, &tmv, dc, sub == 0 ? handoff : -1, sm, sm_raw, ctl, ps, wc);
     }
   } else {
     // ------------------------------------------------------------------ decode slot
     const DecodeCtx dc{kDecodeWarp0, kDecodeWarps, smem + kSmemDecodeOff,
                        reinterpret_cast<float*>(smem + kSmemScoresOff), 3, kDecodeWarps * 32,
                        kDecodeWarp0 * 32, 1};
-    decode_loop<GT>(p, &tmk, &tmv, dc, -1, sm, sm_raw, ctl, ps, wc);
+    decode_loop<GT, HD>(p, &tmk, &tmv, dc, -1, sm, sm_raw, ctl, ps, wc);
   }
   tc_fence_before();
   __syncthreads();
@@ -1272,11 +1307,11 @@ struct CudaState {
 
 // Q: 3-D {dim, head, token} so one box is 64 dims of hp heads x 128/hp tokens: the 128 rows of
 // a prefill tile, token-major.
-static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp, int hp) {
+static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp, int hp, int hd) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hq, (cuuint64_t)Tp};
-  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Hq * kHeadDim * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)Hq, (cuuint64_t)Tp};
+  cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)Hq * hd * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)hp, (cuuint32_t)(kTileM / hp)};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
@@ -1285,11 +1320,11 @@ static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp, int hp) {
 }
 // K or V pool: 2-D {dim, row} over num_blocks*Hkv*16 rows; one box is one paged block's 16 rows
 // x 64 dims.
-static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows) {
+static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows, int hd) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
@@ -1297,17 +1332,17 @@ static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int GT>
+template <int GT, int HD>
 static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
   static std::atomic<int> attr_set{0};
   if (!attr_set.load()) {
-    cudaError_t e = cudaFuncSetAttribute(pod_attn_kernel<GT>,
+    cudaError_t e = cudaFuncSetAttribute(pod_attn_kernel<GT, HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
     if (e != cudaSuccess) return e;
     attr_set.store(1);
   }
   if (!p.wait_append) {
-    pod_attn_kernel<GT><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, cs.tmk, cs.tmv);
+    pod_attn_kernel<GT, HD><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, cs.tmk, cs.tmv);
     return cudaGetLastError();
   }
   // Items wait for every CTA's share of the append: a cooperative launch guarantees that all
@@ -1322,18 +1357,23 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT>, p, cs.tmq, cs.tmk, cs.tmv);
+  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD>, p, cs.tmq, cs.tmk, cs.tmv);
+}
+
+template <int HD>
+static cudaError_t launch_hd(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
+  switch (p.G) {
+    case 1: return launch_mode<1, HD>(p, grid, st, cs);
+    case 2: return launch_mode<2, HD>(p, grid, st, cs);
+    case 3:
+    case 4: return launch_mode<4, HD>(p, grid, st, cs);
+    default: return launch_mode<8, HD>(p, grid, st, cs);
+  }
 }
 
 static cudaError_t launch(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
   if (grid <= 0) return cudaSuccess;
-  switch (p.G) {
-    case 1: return launch_mode<1>(p, grid, st, cs);
-    case 2: return launch_mode<2>(p, grid, st, cs);
-    case 3:
-    case 4: return launch_mode<4>(p, grid, st, cs);
-    default: return launch_mode<8>(p, grid, st, cs);
-  }
+  return p.head_dim == 64 ? launch_hd<64>(p, grid, st, cs) : launch_hd<128>(p, grid, st, cs);
 }
 
 // ---------------------------------------------------------------- allocation-free scratch
@@ -1439,11 +1479,12 @@ pod_attn_status pod_attn_plan_bucket(pod_attn_plan_t plan, pod_attn_bucket* out)
   if (!plan || !out) return POD_ATTN_ERR_INVALID_ARG;
   const pod_attn_problem& pr = plan->prob;
   const int Np = pr.num_prefill_seqs, Nd = pr.num_decode_seqs;
-  const int64_t row = 4 * kHeadDim;  // K + V (or q + o) of one row, bf16
+  const int64_t hd = pr.head_dim;
+  const int64_t row = 4 * hd;  // K + V (or q + o) of one row, bf16
   int64_t flops = 0, bytes = 0;
   for (int s = 0; s < Np; ++s) {
     const int64_t q = plan->cu[s + 1] - plan->cu[s], L = plan->kv[s], P = L - q;
-    flops += 4 * kHeadDim * (int64_t)pr.num_q_heads *
+    flops += 4 * hd * (int64_t)pr.num_q_heads *
              (plan->opt.non_causal == 0 ? q * P + q * (q + 1) / 2 : q * L);
     bytes += L * pr.num_kv_heads * row + q * pr.num_q_heads * row;
   }
@@ -1567,17 +1608,18 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
   const int64_t pool_rows = (int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize;
   if (n_p > 0 && cs->kq != q_prefill) {
-    if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens, plan->head_pack))
+    if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens, plan->head_pack,
+                  pr.head_dim))
       return POD_ATTN_ERR_CUDA;
     cs->kq = q_prefill;
   }
   // the pools' maps serve the prefill tiles and the grouped-query decode path
   if (cs->kk != k_pool) {
-    if (!encode_pool(&cs->tmk, k_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
+    if (!encode_pool(&cs->tmk, k_pool, pool_rows, pr.head_dim)) return POD_ATTN_ERR_CUDA;
     cs->kk = k_pool;
   }
   if (cs->kv != v_pool) {
-    if (!encode_pool(&cs->tmv, v_pool, pool_rows)) return POD_ATTN_ERR_CUDA;
+    if (!encode_pool(&cs->tmv, v_pool, pool_rows, pr.head_dim)) return POD_ATTN_ERR_CUDA;
     cs->kv = v_pool;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1614,6 +1656,7 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   p.max_prefill_per_sm = plan->max_prefill_per_sm;
   p.hp_log2 = __builtin_ctz((unsigned)plan->head_pack);
   p.causal = plan->opt.non_causal == 0;
+  p.head_dim = pr.head_dim;
   p.tq = plan->tile_tokens;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.timeout_ns = kWaitTimeoutNs;

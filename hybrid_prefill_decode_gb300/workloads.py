@@ -130,13 +130,13 @@ def make_batch(num_q_heads: int, num_kv_heads: int, q_lens: Sequence[int],
                prefill_kv_lens: Sequence[int], decode_kv_lens: Sequence[int], seed: int,
                device="cpu", scale: Optional[float] = None, permute: bool = True,
                spare_frac: float = 0.05, poison: bool = True, std: float = 1.0,
-               name: str = "", causal: bool = True) -> HybridBatch:
+               name: str = "", causal: bool = True, head_dim: int = HEAD_DIM) -> HybridBatch:
     """Build one seeded hybrid batch (see the module docstring for the recipe)."""
     q_lens = [int(x) for x in q_lens]
     prefill_kv_lens = [int(x) for x in prefill_kv_lens]
     decode_kv_lens = [int(x) for x in decode_kv_lens]
     assert len(q_lens) == len(prefill_kv_lens)
-    D = HEAD_DIM
+    D = int(head_dim)
     Hq, Hkv = int(num_q_heads), int(num_kv_heads)
     lens = prefill_kv_lens + decode_kv_lens
     nseq = len(lens)

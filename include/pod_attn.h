@@ -24,14 +24,14 @@
  *   it does not change the mathematical result.
  *
  * Conventions shared by every entry point:
- *   - head_dim is 128, the paged block size is 16 tokens, all tensors are bf16 (IEEE bfloat16,
- *     little-endian), accumulation is fp32, outputs are rounded once to bf16 (nearest-even).
+ *   - head_dim D is 128 or 64, the paged block size is 16 tokens, all tensors are bf16 (IEEE
+ *     bfloat16, little-endian), accumulation is fp32, outputs are rounded once to bf16.
  *   - Layouts (row-major, innermost last, no padding):
- *       q_prefill, o_prefill : [num_prefill_tokens][num_q_heads][128]   (tokens of all chunks,
- *                                                                        concatenated)
- *       q_decode,  o_decode  : [num_decode_seqs][num_q_heads][128]
- *       k_pool, v_pool       : [num_blocks][num_kv_heads][16][128]      (one (block, kv-head)
- *                                                                        is 4 KiB contiguous)
+ *       q_prefill, o_prefill : [num_prefill_tokens][num_q_heads][D]   (tokens of all chunks,
+ *                                                                      concatenated)
+ *       q_decode,  o_decode  : [num_decode_seqs][num_q_heads][D]
+ *       k_pool, v_pool       : [num_blocks][num_kv_heads][16][D]      (one (block, kv-head)
+ *                                                                      is 32*D bytes contiguous)
  *       block_tables         : int32 [num_prefill_seqs + num_decode_seqs][max_blocks_per_seq];
  *                              row s maps logical block j of sequence s to a physical block
  *                              ([BEYOND] §"PagedAttention", [LLMSO] §"PagedAttention —
@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
   POD_ATTN_OK = 0,
   POD_ATTN_ERR_INVALID_ARG = -1,  /* a null pointer, a bad length or an inconsistent shape */
-  POD_ATTN_ERR_UNSUPPORTED = -2,  /* head_dim != 128, block_size != 16, group size > 8, ... */
+  POD_ATTN_ERR_UNSUPPORTED = -2,  /* head_dim not 128 or 64, block_size != 16, group size > 8 */
   POD_ATTN_ERR_WORKSPACE = -3,    /* workspace too small or not 256-byte aligned */
   POD_ATTN_ERR_CUDA = -4,         /* a CUDA runtime call failed (no device, launch error, ...) */
   POD_ATTN_ERR_BAD_INDEX = -5,    /* device-detected: a block-table entry outside [0, num_blocks) */
@@ -83,7 +83,7 @@ typedef enum {
 typedef struct {
   int32_t num_q_heads;         /* Hq >= 1 */
   int32_t num_kv_heads;        /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 8 */
-  int32_t head_dim;            /* must be 128 */
+  int32_t head_dim;            /* 128 or 64 */
   int32_t block_size;          /* must be 16 */
   int32_t num_prefill_seqs;    /* Np >= 0 */
   int32_t num_prefill_tokens;  /* sum of chunk lengths; 0 iff Np == 0 */
@@ -205,7 +205,7 @@ pod_attn_status pod_attn_run(pod_attn_plan_t plan, const void* q_prefill, const 
  * tokens are written into the paged pools, then the attention reads them — the step that
  * precedes attention in a serving iteration ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
  * §"PagedAttention": the paged cache grows by appending; §"한 스텝에 여러 종류의 request 섞기").
- *   k_new, v_new : device bf16 [T_p + Nd][Hkv][128], 16-byte aligned: row i < T_p is prefill
+ *   k_new, v_new : device bf16 [T_p + Nd][Hkv][D], 16-byte aligned: row i < T_p is prefill
  *                  token i (chunks in cu_seqlens order), row T_p + d is decode sequence d's token.
  *                  Token i of chunk s is written at position kv_len[s] - q_len(s) + i of sequence
  *                  s, decode d's token at position kv_len[Np + d] - 1, through the block tables
@@ -241,9 +241,9 @@ pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info*
  * token-to-token budget, §"예측 가능한 지연시간과 진단"). Host only, integer arithmetic: equal
  * batches give equal buckets, bit for bit. */
 typedef struct {
-  int64_t prefill_flops;     /* 4*128*Hq per visible (query, key) pair of the prefill chunks */
+  int64_t prefill_flops;     /* 4*D*Hq per visible (query, key) pair of the prefill chunks */
   int64_t read_bytes;        /* algorithmic bytes: each sequence's K/V rows once per kv-head
-                                (512 B per row and kv-head), q in and o out (512 B per token and
+                                (4*D B per row and kv-head), q in and o out (4*D B per token and
                                 q-head) */
   int32_t prefill_ctas;      /* virtual prefill CTAs (work items) */
   int32_t decode_ctas;       /* virtual decode CTAs */

@@ -48,7 +48,9 @@ def _plan_code(Hq=4, Hkv=2, cu=(0, 5), kv=(9, 7), nd=1, nb=10, maxb=4, head_dim=
 
 def test_plan_validation(lib):
     assert _plan_code() == B.OK
-    assert _plan_code(head_dim=64) == B.ERR_UNSUPPORTED
+    assert _plan_code(head_dim=64) == B.OK                          # 128 and 64 supported
+    assert _plan_code(head_dim=96) == B.ERR_UNSUPPORTED
+    assert _plan_code(head_dim=256) == B.ERR_UNSUPPORTED
     assert _plan_code(block=32) == B.ERR_UNSUPPORTED
     assert _plan_code(Hq=18, Hkv=1) == B.ERR_UNSUPPORTED          # group 18 > 8
     assert _plan_code(Hq=6, Hkv=4) == B.ERR_INVALID_ARG           # Hq % Hkv != 0

@@ -423,3 +423,88 @@ class TracePool:
             cu_seqlens_q=torch.tensor(cu, dtype=torch.int32, device=self.device),
             kv_lens=torch.tensor(lens, dtype=torch.int32, device=self.device), seed=self.seed,
             name=f"trace {self.trace.mix} iteration {i}")
+
+
+# ----------------------------------------------------------------------------------------------
+# FP8 (e4m3) KV cache for the decode-only FP8 path: K with one scale per kv-head and channel,
+# V with one scale per cached token and kv-head (quantised from a seeded bf16 batch).
+# ----------------------------------------------------------------------------------------------
+
+@dataclass
+class Fp8DecodeBatch:
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    decode_kv_lens: List[int]
+    scale: float
+    q_decode: torch.Tensor          # bf16 [Nd][Hq][D]
+    k8: torch.Tensor                # uint8 e4m3 [NB][Hkv][16][D]
+    v8: torch.Tensor                # uint8 e4m3 [NB][Hkv][16][D]
+    k_scale: torch.Tensor           # fp32 [Hkv][D]
+    v_scale: torch.Tensor           # fp32 [NB][Hkv][16]
+    block_tables: torch.Tensor      # int32 [Nd][max_blocks_per_seq]
+    kv_lens: torch.Tensor           # int32 [Nd]
+    seed: int = 0
+
+    @property
+    def num_decode_seqs(self) -> int:
+        return len(self.decode_kv_lens)
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k8.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    def to(self, device) -> "Fp8DecodeBatch":
+        kw = dict(self.__dict__)
+        for k, v in list(kw.items()):
+            if isinstance(v, torch.Tensor):
+                kw[k] = v.to(device)
+        return Fp8DecodeBatch(**kw)
+
+
+def make_fp8_decode_batch(num_q_heads: int, num_kv_heads: int, decode_kv_lens: Sequence[int],
+                          seed: int, device="cpu", pow2_scales: bool = False) -> Fp8DecodeBatch:
+    """Quantise the pools of a seeded bf16 decode batch to e4m3: k_scale = max |K| over the
+    finite cached rows of each (kv-head, channel) / 448, v_scale = max |V| over each row / 448
+    (1 where that max is 0 or the row is poison), values rounded to nearest e4m3 by torch's
+    float8 conversion. NaN-poisoned rows stay NaN. With pow2_scales every scale is rounded up to
+    a power of two, so each dequantised value is exactly a bf16 value."""
+    b = make_batch(num_q_heads, num_kv_heads, [], [], list(decode_kv_lens), seed=seed,
+                   device=device)
+    k = b.k_pool.float()
+    v = b.v_pool.float()
+    fk = torch.nan_to_num(k.abs(), nan=0.0)
+    ks = fk.amax(dim=(0, 2)) / 448.0                          # [Hkv][D]
+    vs = torch.nan_to_num(v.abs(), nan=0.0).amax(dim=3) / 448.0   # [NB][Hkv][16]
+    ks = torch.where(ks > 0, ks, torch.ones_like(ks))
+    vs = torch.where(vs > 0, vs, torch.ones_like(vs))
+    if pow2_scales:
+        ks = torch.exp2(torch.ceil(torch.log2(ks)))
+        vs = torch.exp2(torch.ceil(torch.log2(vs)))
+    k8 = (k / ks[None, :, None, :]).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (v / vs[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return Fp8DecodeBatch(num_q_heads, num_kv_heads, b.head_dim, b.block_size,
+                          list(decode_kv_lens), b.scale, b.q_decode, k8.contiguous(),
+                          v8.contiguous(), ks.float().contiguous(), vs.float().contiguous(),
+                          b.block_tables, b.kv_lens, seed=seed)
+
+
+def dequantised_batch(fb: Fp8DecodeBatch) -> HybridBatch:
+    """The bf16 decode batch holding the dequantised cache e4m3(bits) * scale, rounded to bf16
+    (exact when the scales are powers of two)."""
+    k = fb.k8.view(torch.float8_e4m3fn).float() * fb.k_scale[None, :, None, :]
+    v = fb.v8.view(torch.float8_e4m3fn).float() * fb.v_scale[..., None]
+    dev = fb.q_decode.device
+    return HybridBatch(
+        num_q_heads=fb.num_q_heads, num_kv_heads=fb.num_kv_heads, head_dim=fb.head_dim,
+        block_size=fb.block_size, q_lens=[], prefill_kv_lens=[],
+        decode_kv_lens=list(fb.decode_kv_lens), scale=fb.scale,
+        q_prefill=torch.zeros((0, fb.num_q_heads, fb.head_dim), dtype=torch.bfloat16, device=dev),
+        q_decode=fb.q_decode, k_pool=k.to(torch.bfloat16), v_pool=v.to(torch.bfloat16),
+        block_tables=fb.block_tables, cu_seqlens_q=torch.zeros((1,), dtype=torch.int32, device=dev),
+        kv_lens=fb.kv_lens, seed=fb.seed)

@@ -67,6 +67,10 @@ def _load():
             lib.oracle_hybrid_attention.restype = I
             lib.oracle_hybrid_attention.argtypes = [I, I, I, I, I, I, L, I, D, P, P, P, P,
                                                     P, P, P, P, P, I]
+            lib.oracle_e4m3_to_double.restype = D
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_decode_fp8.restype = I
+            lib.oracle_decode_fp8.argtypes = [I, I, I, I, I, L, I, D, P, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -182,4 +186,32 @@ def merge(ms, ls, os_) -> np.ndarray:
     n, D = os_.shape
     out = np.zeros(D, dtype=np.float64)
     _load().oracle_merge(n, _ptr(ms), _ptr(ls), _ptr(os_), D, _ptr(out))
+    return out
+
+
+def e4m3_to_double(bits: int) -> float:
+    """The value of one e4m3 bit pattern (see oracle.c)."""
+    return float(_load().oracle_e4m3_to_double(int(bits) & 0xFF))
+
+
+def decode_fp8(batch):
+    """Decode outputs [Nd][Hq][D] (float64) over an FP8 cache. ``batch`` has the fields of
+    ``hybrid_prefill_decode_gb300.workloads.Fp8DecodeBatch`` (q_decode bf16, k8 / v8 uint8
+    pools, k_scale [Hkv][D] and v_scale [NB][Hkv][16] float32, block tables and kv lengths of
+    the decode sequences)."""
+    q = _u16(batch.q_decode)
+    k8 = np.ascontiguousarray(batch.k8.cpu().numpy(), dtype=np.uint8)
+    v8 = np.ascontiguousarray(batch.v8.cpu().numpy(), dtype=np.uint8)
+    ks = np.ascontiguousarray(batch.k_scale.cpu().numpy(), dtype=np.float32)
+    vs = np.ascontiguousarray(batch.v_scale.cpu().numpy(), dtype=np.float32)
+    bt = _i32(batch.block_tables)
+    kv = _i32(batch.kv_lens)
+    Nd, Hq, D = int(q.shape[0]), int(batch.num_q_heads), int(batch.head_dim)
+    out = np.zeros((Nd, Hq, D), dtype=np.float64)
+    rc = _load().oracle_decode_fp8(Hq, int(batch.num_kv_heads), D, int(batch.block_size), Nd,
+                                   int(k8.shape[0]), int(bt.shape[1]) if bt.ndim == 2 else 0,
+                                   float(batch.scale), _ptr(q), _ptr(k8), _ptr(v8), _ptr(ks),
+                                   _ptr(vs), _ptr(bt), _ptr(kv), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_fp8 failed with code {rc}")
     return out

@@ -279,3 +279,89 @@ int oracle_hybrid_attention(int Hq, int Hkv, int D, int BS, int Np, int Nd, int6
   }
   return err;
 }
+
+/*
+ * FP8 KV cache (the 8-bit cache of "Week 6: Beyond PyTorch: Custom Kernel과 vLLM" and "LLMSO -
+ * W4", §"KV 헤드 줄이기": the cache shrinks when each element takes fewer bytes).
+ *
+ * e4m3 (the 8-bit floating-point format with 4 exponent and 3 mantissa bits and no
+ * infinities): bit 7 sign; bits 6..3 exponent E (bias 7); bits 2..0 mantissa M.
+ *   E = 0:            (-1)^s * M/8 * 2^(1-7)      (subnormal, and zero)
+ *   E = 15, M = 7:    NaN
+ *   otherwise:        (-1)^s * (1 + M/8) * 2^(E-7)   (largest: 448)
+ */
+double oracle_e4m3_to_double(uint8_t bits) {
+  int s = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, 1 - 7);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/*
+ * Decode attention over an FP8 cache. K row j, channel c of kv-head g is
+ * e4m3(k8[row j][c]) * k_scale[g][c] (one scale per kv-head and channel); V row j is
+ * e4m3(v8[row j][c]) * v_scale[row j] (one scale per cached token and kv-head). Every decode
+ * token attends to all kv_len rows of its sequence, as in oracle_attend_row. Pools are
+ * [num_blocks][Hkv][BS][D] bytes, v_scale is [num_blocks][Hkv][BS], block_tables is
+ * [Nd][max_blocks_per_seq]; o_decode is [Nd][Hq][D] doubles. OpenMP over (sequence, head).
+ * Returns 0, -1 on a bad table entry, -3 on bad shapes.
+ */
+int oracle_decode_fp8(int Hq, int Hkv, int D, int BS, int Nd, int64_t num_blocks,
+                      int max_blocks_per_seq, double scale, const uint16_t* q_decode,
+                      const uint8_t* k8, const uint8_t* v8, const float* k_scale,
+                      const float* v_scale, const int32_t* block_tables, const int32_t* kv_lens,
+                      double* o_decode) {
+  if (Hkv < 1 || Hq % Hkv != 0) return -3;
+  int group = Hq / Hkv;
+  int err = 0;
+  int64_t max_rows = (int64_t)max_blocks_per_seq * BS;
+#pragma omp parallel
+  {
+    double* x = (double*)malloc(sizeof(double) * (size_t)(max_rows > 0 ? max_rows : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t t = 0; t < (int64_t)Nd * Hq; ++t) {
+      int64_t d = t / Hq;
+      int h = (int)(t % Hq), g = h / group;
+      int64_t nvis = kv_lens[d];
+      const int32_t* bt_row = block_tables + d * (int64_t)max_blocks_per_seq;
+      const uint16_t* q = q_decode + (d * Hq + h) * (int64_t)D;
+      double* out = o_decode + (d * Hq + h) * (int64_t)D;
+      int rc = 0;
+      if (nvis < 1 || nvis > max_rows) rc = -3;
+      double m = -INFINITY;
+      for (int64_t j = 0; rc == 0 && j < nvis; ++j) {
+        int64_t r = pool_row(bt_row, j, g, Hkv, D, BS, num_blocks);
+        if (r < 0) {
+          rc = -1;
+          break;
+        }
+        double dot = 0.0;
+        for (int c = 0; c < D; ++c)
+          dot += widen_bf16(q[c]) * (oracle_e4m3_to_double(k8[r + c]) * (double)k_scale[g * D + c]);
+        x[j] = scale * dot;
+        if (x[j] > m) m = x[j];
+      }
+      if (rc == 0) {
+        double den = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) den += exp(x[j] - m);
+        for (int c = 0; c < D; ++c) out[c] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+          double p = exp(x[j] - m) / den;
+          int64_t r = pool_row(bt_row, j, g, Hkv, D, BS, num_blocks);
+          double vs = (double)v_scale[r / D];
+          for (int c = 0; c < D; ++c) out[c] += p * (oracle_e4m3_to_double(v8[r + c]) * vs);
+        }
+      }
+      if (rc != 0) {
+#pragma omp critical
+        if (err == 0) err = rc;
+      }
+    }
+    free(x);
+  }
+  return err;
+}

@@ -303,3 +303,51 @@ def test_bruteforce_agrees_noncausal(case):
     o_p, o_d = oracle.hybrid_attention(b)
     r_p, r_d = bruteforce.hybrid_attention(b)
     assert np.abs(o_p - r_p).max() <= 1e-12 and np.abs(o_d - r_d).max() <= 1e-12
+
+
+# ---- the FP8 (e4m3) cache of the decode path
+
+def test_e4m3_decoding_matches_its_definition_and_torch():
+    by_hand = {0x00: 0.0, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0,
+               0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0xB8: -1.0}
+    for bits, val in by_hand.items():
+        assert oracle.e4m3_to_double(bits) == val, hex(bits)
+    assert math.isnan(oracle.e4m3_to_double(0x7F)) and math.isnan(oracle.e4m3_to_double(0xFF))
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double()
+    for bits in range(256):
+        got, want = oracle.e4m3_to_double(bits), float(ref[bits])
+        assert (math.isnan(got) and math.isnan(want)) or got == want, hex(bits)
+
+
+def test_fp8_decode_equals_bf16_oracle_on_exact_dequantised_cache():
+    fb = W.make_fp8_decode_batch(8, 2, [1, 17, 100, 333], seed=81, pow2_scales=True)
+    deq = W.dequantised_batch(fb)
+    # power-of-two scales: every dequantised value is exactly representable in bf16
+    k_exact = fb.k8.view(torch.float8_e4m3fn).double() * fb.k_scale[None, :, None, :].double()
+    assert torch.equal(deq.k_pool.double()[~torch.isnan(k_exact)], k_exact[~torch.isnan(k_exact)])
+    _, ref = oracle.hybrid_attention(deq)
+    got = oracle.decode_fp8(fb)
+    assert np.abs(got - ref).max() <= 1e-12
+
+
+def test_fp8_decode_scales_act_linearly():
+    fb = W.make_fp8_decode_batch(4, 4, [40, 257], seed=82)
+    base = oracle.decode_fp8(fb)
+    fb.v_scale *= 2.0                                      # every V row doubles
+    assert np.abs(oracle.decode_fp8(fb) - 2.0 * base).max() <= 1e-12 * max(1.0, np.abs(base).max())
+    fb.v_scale /= 2.0
+    fb.k_scale *= 2.0                                      # K doubles, q halves: same scores
+    fb.q_decode = (fb.q_decode.double() * 0.5).to(torch.bfloat16)
+    assert np.abs(oracle.decode_fp8(fb) - base).max() <= 1e-12
+
+
+def test_fp8_decode_zero_query_gives_mean_of_dequantised_rows():
+    fb = W.make_fp8_decode_batch(2, 1, [5, 70], seed=83)
+    fb.q_decode.zero_()
+    out = oracle.decode_fp8(fb)
+    v = fb.v8.view(torch.float8_e4m3fn).double() * fb.v_scale[..., None].double()
+    bt = fb.block_tables
+    for d, L in enumerate(fb.decode_kv_lens):
+        rows = torch.stack([v[int(bt[d, j // 16]), 0, j % 16] for j in range(L)])
+        for h in range(2):
+            assert np.abs(out[d, h] - rows.mean(dim=0).numpy()).max() <= 1e-12

@@ -6,10 +6,12 @@ layer of one serving iteration). Default workload: the Llama-2-7B attention shap
 32 KV heads, head_dim 128, one 512-token chunk after a 3584-token prefix, 32 decodes with
 contexts uniform in [2048, 4096], paged block 16), synthetic N(0,1) bf16 inputs.
 
-Timing: CUDA events on the launching stream around each step; a 256 MiB buffer is written
-between steps (outside the events) so every step starts with a cold L2. The headline value is
-the fused variant's mean us/iter; the serial (two launches back to back) and two-stream variants
-run on the same buffers for the speedup figures. `e2e` repeats the fused step through the
+Timing: CUDA events on the launching stream around each step. Between steps (outside the
+events) a 1 GiB buffer is written and a 512 MiB one read, so every step starts with a cold L2
+whose lines are clean: with the write alone, the ~126 MB of dirty lines it leaves would be
+written back during the timed step (measured: 9-19 us of extra time per step). The headline
+value is the fused variant's mean us/iter; the serial (two launches back to back) and
+two-stream variants run on the same buffers for the speedup figures. `e2e` repeats the fused step through the
 public C ABI from pinned host buffers (plan + upload + run + copies in the timed region).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
@@ -43,6 +45,26 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+L2_NOTE = ("flushed between steps: 1 GiB written, then 512 MiB read, so every step starts with a "
+           "cold L2 that holds no dirty lines of the flush itself")
+
+
+class L2Flush:
+    """Between timed steps (outside the events): write a 1 GiB buffer (evicts everything the
+    last step left in the 126 MB L2), then read a 512 MiB one, so the dirty lines of that write
+    are written back here rather than inside the next timed step. The L2 the step sees is cold
+    for all of its inputs, as under a profiler's cache flush."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(512 << 20, dtype=torch.uint8, device=device)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.max()
+
+
 def _workload_name(cfg, batch) -> str:
     from hybrid_prefill_decode_gb300 import workloads as W
     name = W.CONFIG_NAMES.get(cfg) or W.PROFILE_CASES[cfg][0]
@@ -53,7 +75,7 @@ def _config_dict(args, batch, world):
     """The workload description both arms print (identical keys and values)."""
     d = {"workload": _workload_name(args.case or args.config, batch),
          "config_index": args.case or args.config,
-         "l2": "flushed between steps (256 MiB write)",
+         "l2": L2_NOTE,
          "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
     if getattr(args, "append", False):
         d["kv_append"] = "new K/V rows written into the pools inside each step"
@@ -228,6 +250,9 @@ def main():
     ap.add_argument("--trace", default=None, choices=["a", "b"],
                     help="the 200-iteration hybrid-batching trace (mix a or b) instead of --config")
     ap.add_argument("--trace-iters", type=int, default=200)
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="decode attention over an FP8 (e4m3) cache: the decodes of --config, "
+                         "with the bf16 cache of the same decodes timed beside it")
     ap.add_argument("--append", action="store_true",
                     help="every step also writes the iteration's new K/V rows into the pools "
                          "(pod_attn_run_append); the metric then includes that step")
@@ -259,6 +284,9 @@ def main():
     if args.trace:
         run_trace(args, dev, B, R, W, rank, world, dist)
         return
+    if args.kv_fp8:
+        run_fp8(args, dev, B, R, W, rank, world, dist)
+        return
     batch = _make_batch(args, dev)
     work = R.batch_work(batch.num_q_heads, batch.num_kv_heads, batch.q_lens,
                         batch.prefill_kv_lens, batch.decode_kv_lens)
@@ -267,7 +295,7 @@ def main():
     side = torch.cuda.Stream(device=dev)
     o_p = torch.empty_like(batch.q_prefill)
     o_d = torch.empty_like(batch.q_decode)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     variants = [args.only] if args.only else ["fused", "serial", "streams"]
     plans = {}
@@ -307,7 +335,7 @@ def main():
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for a, b in evs:
-            flush.fill_(1)                       # cold L2 for every step (outside the events)
+            flush()                              # cold L2 for every step (outside the events)
             a.record(stream)
             step(v)
             b.record(stream)
@@ -382,7 +410,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
         for _ in range(args.steps):
-            flush.fill_(1)
+            flush()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             e2e_step()
@@ -460,7 +488,7 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
     ws = {v: torch.empty(max(256, wsb), dtype=torch.uint8, device=dev) for v in variants}
     stream = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     outs = [(torch.empty_like(b.q_prefill), torch.empty_like(b.q_decode)) for b in batches]
     tstar = [R.batch_work(b.num_q_heads, b.num_kv_heads, b.q_lens, b.prefill_kv_lens,
                           b.decode_kv_lens).t_star(hbm, tf_burst) * 1e6 for b in batches]
@@ -477,7 +505,7 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
         torch.cuda.synchronize()
         for i, b in enumerate(batches):
             plans[v][i].upload(ws[v], stream)
-            flush.fill_(1)
+            flush()
             evs[i][0].record(stream)
             B.run_batch(plans[v][i], b, ws[v], *outs[i], stream=stream, stream2=side)
             evs[i][1].record(stream)
@@ -500,7 +528,7 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
            "config": {"workload": f"hybrid-batching trace mix {args.trace}: Llama-3-8B attention "
                                   f"(32/8, head_dim 128, paged block 16), 2048-token budget, "
                                   f"decodes first, {len(batches)} iterations",
-                      "l2": "flushed between steps (256 MiB write)"},
+                      "l2": L2_NOTE},
            "fused": f, "serial": stats(times["serial"]), "streams": stats(times["streams"]),
            "sum_measured_over_sum_tstar": sum(times["fused"]) / sum(tstar),
            "frac_of_t_star": sum(tstar) / sum(times["fused"]),
@@ -508,6 +536,158 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
            "speedup_vs_streams": sum(times["streams"]) / sum(times["fused"]),
            "mean_t_star_us": statistics.mean(tstar),
            "pool_gb": pool.k_pool.numel() * 4 / 1e9}
+    print(json.dumps(out), flush=True)
+
+
+def cpu_baseline_fp8(fb, target_s: float = 12.0):
+    """The fp64 oracle of the FP8-cache decode on this host's cores, on the first decodes of the
+    batch (as many as fill about `target_s`), scaled to the whole batch by cached rows read."""
+    import oracle
+    from hybrid_prefill_decode_gb300 import workloads as W
+    lens = list(fb.decode_kv_lens)
+    n, elapsed = 1, 0.0
+    while True:
+        sub = W.Fp8DecodeBatch(fb.num_q_heads, fb.num_kv_heads, fb.head_dim, fb.block_size,
+                               lens[:n], fb.scale, fb.q_decode[:n], fb.k8, fb.v8, fb.k_scale,
+                               fb.v_scale, fb.block_tables[:n], fb.kv_lens[:n], fb.seed)
+        t0 = time.perf_counter()
+        oracle.decode_fp8(sub)
+        elapsed = time.perf_counter() - t0
+        if n == len(lens) or elapsed * (2 * n) / n > target_s:
+            break
+        n = min(len(lens), 2 * n)
+    us = elapsed * 1e6 * sum(lens) / sum(lens[:n])
+    return {"value": us, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"the first {n} of {len(lens)} decodes, all {fb.num_q_heads} heads "
+                       f"({sum(lens[:n]) / sum(lens):.1%} of the cached rows read, "
+                       f"{elapsed:.1f} s), scaled by cached rows")}
+
+
+def run_fp8(args, dev, B, R, W, rank, world, dist):
+    """--kv-fp8: one step = decode attention of every decode of --config over an e4m3 cache with
+    per-(kv-head, channel) K scales and per-(row, kv-head) V scales (pod_attn_run_decode_fp8).
+    The bf16-cache decode of the same decodes (pod_attn_run, decode-only plan) is timed beside it
+    on the same lengths; the roofline counts the FP8 cache's bytes."""
+    import torch
+    hbm, _, _, peak_src = _peaks()
+    Hq, Hkv, _, _, dkv = W.config_lengths(args.config)
+    fb = W.make_fp8_decode_batch(Hq, Hkv, dkv, seed=args.config, device=dev)
+    bb = W.make_batch(Hq, Hkv, [], [], dkv, seed=args.config, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    p8 = B.Plan(Hq, Hkv, [], list(dkv), len(dkv), fb.num_blocks, fb.max_blocks_per_seq, fb.scale,
+                kv_fp8=True)
+    ws8 = p8.alloc_workspace(dev)
+    p8.upload(ws8, stream)
+    o8 = torch.empty_like(fb.q_decode)
+    p16 = B.Plan.for_batch(bb)
+    ws16 = p16.alloc_workspace(dev)
+    p16.upload(ws16, stream)
+    o16 = torch.empty_like(bb.q_decode)
+    op16 = torch.empty_like(bb.q_prefill)
+
+    def step8():
+        p8.run_decode_fp8(fb.q_decode, fb.k8, fb.v8, fb.k_scale, fb.v_scale, fb.block_tables,
+                          fb.kv_lens, o8, ws8, stream=stream)
+
+    def step16():
+        B.run_batch(p16, bb, ws16, op16, o16, stream=stream)
+
+    def timed(fn, k):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        return [a.elapsed_time(b) * 1e3 for a, b in evs]
+
+    def agg(xs):
+        mean = statistics.mean(xs)
+        if dist:
+            t = torch.tensor([mean], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            mean = float(t.item())
+        return mean
+
+    for fn in (step8, step16):
+        for _ in range(args.warmup):
+            fn()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as cs:
+        t8 = timed(step8, args.steps)
+    clocks = cs.summary()
+    t16 = timed(step16, args.steps)
+    assert p8.device_status(ws8) == B.OK and p16.device_status(ws16) == B.OK
+    us8, us16 = agg(t8), agg(t16)
+
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(fb, k).cpu().pin_memory() for k in ("q_decode", "block_tables",
+                                                               "kv_lens")}
+        dq, dbt, dkv_t = (torch.empty_like(fb.q_decode), torch.empty_like(fb.block_tables),
+                          torch.empty_like(fb.kv_lens))
+        ho = torch.empty(o8.shape, dtype=o8.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+
+        def e2e_step():
+            for dst, key in ((dq, "q_decode"), (dbt, "block_tables"), (dkv_t, "kv_lens")):
+                dst.copy_(host[key], non_blocking=True)
+            plan = B.Plan(Hq, Hkv, [], list(dkv), len(dkv), fb.num_blocks,
+                          fb.max_blocks_per_seq, fb.scale, kv_fp8=True)
+            plan.upload(ws8, stream)
+            plan.run_decode_fp8(dq, fb.k8, fb.v8, fb.k_scale, fb.v_scale, dbt, dkv_t, o8, ws8,
+                                stream=stream)
+            ho.copy_(o8, non_blocking=True)
+            stream.synchronize()
+            return plan
+
+        for _ in range(args.warmup):
+            e2e_step()
+        ts = []
+        for _ in range(args.steps):
+            flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            ts.append((time.perf_counter() - t0) * 1e6)
+        e2e = {"value": agg(ts), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(ho.numel() * ho.element_size())}
+    if rank != 0:
+        return
+    nbytes = R.fp8_decode_bytes(Hq, Hkv, dkv)
+    bytes16 = R.batch_work(Hq, Hkv, [], [], dkv).bytes
+    achieved = nbytes / (us8 * 1e-6) / 1e9
+    out = {"metric": "FP8-cache decode attention µs/iter", "value": us8, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": us8 / 1e3, "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "dtype": "e4m3 cache, f16 MMA, fp32 accumulate",
+           "data": "synthetic",
+           "config": {"workload": (f"the {len(dkv)} decodes of {W.CONFIG_NAMES[args.config]}, "
+                                   f"head_dim 128, paged block 16, e4m3 K/V with per-(kv-head, "
+                                   f"channel) K and per-(row, kv-head) V fp32 scales"),
+                      "config_index": args.config,
+                      "l2": L2_NOTE,
+                      "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+           "median_us": statistics.median(t8),
+           "bf16_cache_us": us16, "speedup_vs_bf16_cache": us16 / us8,
+           "bf16_cache_tbs": bytes16 / (us16 * 1e-6) / 1e12,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                        "frac": achieved / hbm, "traffic": None,
+                        "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                        "algorithmic_bytes": nbytes},
+           "gpu_launches": args.steps, "clocks": clocks}
+    if e2e:
+        out["e2e"] = e2e
+    if not args.no_cpu and world == 1:
+        out["cpu_baseline"] = cpu_baseline_fp8(fb.to("cpu"))
     print(json.dumps(out), flush=True)
 
 

@@ -38,7 +38,8 @@ class Options(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("max_prefill_ctas", ctypes.c_int32), ("decode_splits", ctypes.c_int32),
                 ("prefill_splits", ctypes.c_int32), ("instrument", ctypes.c_int32),
-                ("variant", ctypes.c_int32), ("non_causal", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("non_causal", ctypes.c_int32),
+                ("kv_fp8", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -99,6 +100,8 @@ def load():
     lib.pod_attn_upload.argtypes = [P, P, SZ, P]
     lib.pod_attn_run.restype = I32
     lib.pod_attn_run.argtypes = [P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+    lib.pod_attn_run_decode_fp8.restype = I32
+    lib.pod_attn_run_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, P]
     lib.pod_attn_plan_bucket.restype = I32
     lib.pod_attn_plan_bucket.argtypes = [P, ctypes.POINTER(Bucket)]
     lib.pod_attn_run_append.restype = I32
@@ -163,7 +166,7 @@ class Plan:
                  max_blocks_per_seq: int, scale: float, variant: str = "fused",
                  num_sms: int = 0, ctas_per_sm: int = 0, max_prefill_ctas: int = 0,
                  decode_splits: int = 0, prefill_splits: int = 0, instrument: bool = False,
-                 non_causal: bool = False, head_dim: int = 128):
+                 non_causal: bool = False, head_dim: int = 128, kv_fp8: bool = False):
         lib = load()
         np_ = len(cu_seqlens) - 1 if len(cu_seqlens) > 0 else 0
         self.problem = Problem(num_q_heads, num_kv_heads, head_dim, 16, np_,
@@ -171,7 +174,7 @@ class Plan:
                                num_blocks, max_blocks_per_seq, scale)
         self.options = Options(num_sms, ctas_per_sm, max_prefill_ctas, decode_splits,
                                prefill_splits, 1 if instrument else 0, VARIANTS[variant],
-                               1 if non_causal else 0)
+                               1 if non_causal else 0, 1 if kv_fp8 else 0)
         self.variant = variant
         cu = _i32_array(list(cu_seqlens) if np_ > 0 else [0])
         kv = _i32_array(list(kv_lens))
@@ -255,6 +258,15 @@ class Plan:
             _stream_ptr(stream), _stream_ptr(stream2) if stream2 is not None else None)
         _check(code, "pod_attn_run_append")
 
+    def run_decode_fp8(self, q_decode, k_pool8, v_pool8, k_scale, v_scale, block_tables,
+                       kv_lens, o_decode, workspace, stream=None):
+        """pod_attn_run_decode_fp8: decode over an e4m3 cache with K / V scales."""
+        code = load().pod_attn_run_decode_fp8(
+            self.handle, _ptr(q_decode), _ptr(k_pool8), _ptr(v_pool8), _ptr(k_scale),
+            _ptr(v_scale), _ptr(block_tables), _ptr(kv_lens), _ptr(o_decode),
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+        _check(code, "pod_attn_run_decode_fp8")
+
     def device_status(self, workspace, stream=None) -> int:
         return int(load().pod_attn_last_device_status(self.handle, workspace.data_ptr(),
                                                       _stream_ptr(stream)))
@@ -319,3 +331,21 @@ def selftest_timeout(workspace, timeout_us: int, stream=None) -> int:
     _check(lib.pod_attn_selftest_timeout(workspace.data_ptr(), int(timeout_us),
                                          _stream_ptr(stream)), "selftest_timeout")
     return int(lib.pod_attn_last_device_status(None, workspace.data_ptr(), _stream_ptr(stream)))
+
+
+def decode_fp8(fb, workspace=None, stream=None, **plan_kw):
+    """Run the FP8-cache decode on an ``workloads.Fp8DecodeBatch`` whose tensors are on the GPU;
+    returns o_decode (bf16 [Nd][Hq][128])."""
+    import torch
+    plan = Plan(fb.num_q_heads, fb.num_kv_heads, [], list(fb.decode_kv_lens),
+                fb.num_decode_seqs, fb.num_blocks, fb.max_blocks_per_seq, fb.scale, kv_fp8=True,
+                **plan_kw)
+    ws = workspace if workspace is not None else plan.alloc_workspace(fb.q_decode.device)
+    plan.upload(ws, stream)
+    out = torch.empty_like(fb.q_decode)
+    plan.run_decode_fp8(fb.q_decode, fb.k8, fb.v8, fb.k_scale, fb.v_scale, fb.block_tables,
+                        fb.kv_lens, out, ws, stream=stream)
+    st = plan.device_status(ws, stream)
+    if st != OK:
+        raise PodAttnError(st, "pod_attn_run_decode_fp8 (device)")
+    return out

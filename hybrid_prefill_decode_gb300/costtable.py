@@ -138,7 +138,10 @@ def calibrate(num_q_heads: int, num_kv_heads: int, chunks: Sequence[int],
     dev = torch.device(device)
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     table = CostTable(num_q_heads, num_kv_heads, nsm)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # cold, clean L2 per timed iteration: write 1 GiB, then read 512 MiB (the write's dirty
+    # lines are written back here, not inside the timed launch)
+    wbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    rbuf = torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
     n = 0
     for c in chunks:
         for pfx in prefixes:
@@ -155,7 +158,8 @@ def calibrate(num_q_heads: int, num_kv_heads: int, chunks: Sequence[int],
                     B.run_batch(plan, b, ws)
                 times = []
                 for _ in range(iters):
-                    flush.fill_(1)
+                    wbuf.fill_(1)
+                    rbuf.max()
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
                     B.run_batch(plan, b, ws)

@@ -23,6 +23,17 @@
 // 12 blocks / 4 steps, so no single item can leave a long tail after the others finish. Items
 // are then ordered longest first. All arithmetic is integer, so the plan is reproducible bit
 // for bit.
+//
+// Decode-only plans (no prefill work; the FP8-cache decode is one) know how many items run at
+// once: S = groups x SMs 4-warp decode groups (3 per SM on a bf16 cache, where the prefill
+// slot's softmax warps become two groups beside the decode slot; 4 on an e4m3 cache, where its
+// producer and issuer warps become a third). There one chunk size c (blocks per item, before
+// each output is rebalanced into equal parts) is chosen for all outputs to minimise the makespan of
+// the items taken longest first by S groups, modelled wave by wave (each wave of S items lasts
+// as long as its longest), each item costing ceil(blocks / 4) + 2 block-times of one warp (its
+// four warps share the blocks; the 2 stand for its start and merge). A split count just past a multiple of S costs a whole extra wave
+// of items (the wave-quantisation point of §"동시 실행만으로 부족한 이유"), which the
+// W / (4 S) rule above cannot see.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -37,12 +48,56 @@ namespace {
 constexpr int64_t kDecodeBlockCost = 8;   // 16 rows x (K + V) x 128 x bf16 = 8 KiB
 constexpr int64_t kPrefillTileCost = 57;  // 4*128*128*128 FLOPs at the byte-time balance
 constexpr int kMinDecodeBlocksPerSplit = 12;
-constexpr int kMaxDecodeSplits = 64;
 constexpr int kMinPrefillTilesPerSplit = 4;
+constexpr int64_t kDecodeItemOverhead = 2;   // per-item start and merge, in warp block-times
+constexpr int kDecodeGroupsBf16 = 3;         // 4-warp decode groups per SM, bf16 cache
+constexpr int kDecodeGroupsFp8 = 4;          // ... e4m3 cache
+// chunk candidates of the decode-only rule: ceil(longest output / k)
+constexpr int kChunkDivisors[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64};
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Split of one output of `nblk` blocks for a chunk of about `c` blocks: ns parts of
+// ceil(nblk / ns) blocks (the last one shorter).
+inline void rebalanced(int64_t nblk, int64_t c, int64_t* ns, int64_t* chunk) {
+  *ns = std::max<int64_t>(1, std::min(ceil_div(nblk, c), nblk));
+  *chunk = ceil_div(nblk, *ns);
+  *ns = ceil_div(nblk, *chunk);
+}
+
+// Modelled makespan (in warp block-times) of the items that chunk size c makes of the outputs
+// `nblks` on `slots` decode groups taking them longest first: wave w holds the items ranked
+// w*slots .. (w+1)*slots - 1 and lasts as long as its first (longest) one. Item costs are
+// counted in `hist` (indexed by cost), so this is linear in the outputs and the largest cost.
+int64_t decode_makespan(const std::vector<int64_t>& nblks, int64_t c, int64_t slots,
+                        std::vector<int64_t>& hist) {
+  std::fill(hist.begin(), hist.end(), 0);
+  int64_t top = 0;
+  for (int64_t n : nblks) {
+    int64_t ns, ch;
+    rebalanced(n, c, &ns, &ch);
+    const int64_t full = ceil_div(ch, 4) + kDecodeItemOverhead;
+    const int64_t last = ceil_div(n - (ns - 1) * ch, 4) + kDecodeItemOverhead;
+    hist[full] += ns - 1;
+    hist[last] += 1;
+    top = std::max(top, full);
+  }
+  int64_t span = 0, rank = 0, next_head = 0;  // rank of the next item; rank of the next wave head
+  for (int64_t x = top; x > 0; --x) {
+    const int64_t k = hist[x];
+    if (k == 0) continue;
+    // wave heads among ranks [rank, rank + k)
+    if (next_head < rank + k) {
+      const int64_t heads = (rank + k - 1 - next_head) / slots + 1;
+      span += heads * x;
+      next_head += heads * slots;
+    }
+    rank += k;
+  }
+  return span;
+}
 
 }  // namespace
 
@@ -152,10 +207,46 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int64_t chunk = ceil_div(x.ntiles, ns);
     return Split{ceil_div(x.ntiles, chunk), chunk};
   };
+  // decode-only plans: one chunk size for all outputs, against the groups that run at once
+  int64_t chunk_do = 0;
+  if (pu.empty() && !du.empty() && opt.decode_splits <= 0) {
+    const int64_t groups =
+        (int64_t)num_sms * (opt.kv_fp8 ? kDecodeGroupsFp8 : kDecodeGroupsBf16);
+    std::vector<int64_t> nblks(du.size());
+    int64_t longest = 0;
+    for (size_t i = 0; i < du.size(); ++i) {
+      nblks[i] = du[i].nblk;
+      longest = std::max(longest, du[i].nblk);
+    }
+    std::vector<int64_t> hist((size_t)(ceil_div(longest, 4) + kDecodeItemOverhead + 1), 0);
+    int64_t best = -1, prev_c = -1;
+    for (int k : kChunkDivisors) {
+      const int64_t c = ceil_div(longest, k);
+      if (c == prev_c || (k > 1 && c < kMinDecodeBlocksPerSplit)) continue;
+      prev_c = c;
+      int64_t n_items = 0;
+      for (int64_t n : nblks) {
+        int64_t ns, ch;
+        rebalanced(n, c, &ns, &ch);
+        n_items += ns;
+      }
+      if (k > 1 && n_items > 4 * groups) break;  // past four waves the tail is already short
+      const int64_t t = decode_makespan(nblks, c, groups, hist);
+      if (best < 0 || t < best) {  // ties keep the larger chunk (fewer items, fewer merges)
+        best = t;
+        chunk_do = c;
+      }
+    }
+  }
   auto split_d = [&](const DUnit& x) {
     int64_t ns;
+    if (chunk_do > 0) {
+      int64_t chunk;
+      rebalanced(x.nblk, chunk_do, &ns, &chunk);
+      return Split{ns, chunk};
+    }
     if (opt.decode_splits > 0) {
-      ns = opt.decode_splits;
+      ns = std::min<int64_t>(opt.decode_splits, kMaxDecodeSplits);
     } else {
       ns = ceil_div(x.nblk * kDecodeBlockCost, target);
       ns = std::min<int64_t>(ns, std::max<int64_t>(1, x.nblk / kMinDecodeBlocksPerSplit));

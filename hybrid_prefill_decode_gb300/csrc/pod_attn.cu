@@ -72,6 +72,12 @@ struct Params {
   int32_t n_new;            // new tokens this launch appends (0 = no append)
   int32_t new_first;        // index of the first of them in k_new / v_new / new_rows
   int32_t wait_append;      // items wait until every CTA has done its share of the append
+  // FP8 cache (pod_attn_run_decode_fp8): e4m3 pools, K scale per (kv-head, channel), V scale
+  // per (block, kv-head, row)
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* k_scale;
+  const float* v_scale;
   int32_t n_items_p, n_items_d;
   int32_t Hq, Hkv, G, Np, Nd, num_blocks, maxb;
   int32_t pool_rows;  // num_blocks * Hkv * 16: first row past the pools (TMA fills zeros)
@@ -97,9 +103,9 @@ struct SmemCtl {
   uint64_t dslot[kWarps][kDecodeSlots];  // decode rings, by absolute warp
   uint32_t tmem_base;
   int abort;
-  int item_kind[4];                // per slot: 0 = prefill, 1 = decode, 2-3 = the prefill slot's
-  int item_idx[4];                 //   warps 4-7 / 8-11 once prefill work is drained
-  int merge_last[4];
+  int item_kind[5];                // per slot: 0 = prefill, 1 = decode, 2-3 = the prefill slot's
+  int item_idx[5];                 //   warps 4-7 / 8-11 once prefill work is drained, 4 = its
+  int merge_last[5];               //   warps 0-3 (FP8 cache decode only)
 };
 static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 
@@ -682,6 +688,31 @@ template <> struct LaneVec<2> {
 // bulk copies of whole (block, kv-head) units; q lives in registers (HD/32 dims per lane); q·k is
 // reduce-scattered across the warp with shuffles. Leaves the warp's (o, m, l) in the shared
 // scratch; returns false on abort.
+// Block-table entries of one decode warp's blocks (block i of the warp is entry i * nw of
+// `row`), read 32 at a time, one window ahead: lane j holds the entry of block 32 w + j, so the
+// copy of a block never waits on a global load of its entry. at(i) must be called by all 32
+// lanes with i = 0, 1, 2, ... in order.
+struct BtWindow {
+  const int32_t* row;
+  int nw, n;
+  int cur = 0, nxt = 0;
+  __device__ int load(int first, int lane) const {
+    const int j = first + lane;
+    return j < n ? __ldg(row + (size_t)j * nw) : 0;
+  }
+  __device__ void init(int lane) {
+    cur = load(0, lane);
+    nxt = load(32, lane);
+  }
+  __device__ int at(int i, int lane) {
+    if (i >= 32 && (i & 31) == 0) {
+      cur = nxt;
+      nxt = load(i + 32, lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, i & 31);
+  }
+};
+
 template <int GT, int HD>
 __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx& dc,
                             SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
@@ -721,9 +752,10 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
   }
 
   const uint64_t pol = policy_evict_first();
-  auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
+  BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
+  bt.init(lane);
+  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 2
     const int slot = i & 1;
-    int phys = bt_row[blk0 + wl + i * dc.nw];
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
@@ -735,15 +767,21 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
     bulk_load(dst, p.k_pool + off, kUnit, bar, pol);
     bulk_load(dst + kSmemDecodeSlot / 2, p.v_pool + off, kUnit, bar, pol);
   };
-  if (lane == 0) {
-    if (nmine > 0) issue(0);
-    if (nmine > 1) issue(1);
+  {
+    const int ph0 = bt.at(0, lane), ph1 = bt.at(1, lane);
+    if (lane == 0) {
+      if (nmine > 0) issue(0, ph0);
+      if (nmine > 1) issue(1, ph1);
+    }
   }
   bool ok = true;
   const int r = lane >> 1;  // the row whose full score this lane holds after the reduction
   for (int i = 0; i < nmine; ++i) {
     const int slot = i & 1;
-    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc, kSleepNs)) {
+    // every lane takes the same exit, so the warp's shuffles below stay converged
+    const bool got = mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc,
+                               kSleepNs);
+    if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
     }
@@ -812,7 +850,10 @@ __device__ bool decode_simt(const Params& p, const int32_t* it, const DecodeCtx&
       }
     }
     __syncwarp();
-    if (lane == 0 && i + 2 < nmine) issue(i + 2);
+    {
+      const int ph = bt.at(i + 2, lane);
+      if (lane == 0 && i + 2 < nmine) issue(i + 2, ph);
+    }
   }
 #pragma unroll
   for (int h = 0; h < GT; ++h) {
@@ -888,9 +929,10 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
   for (int mt = 0; mt < kKS; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
   float m = -INFINITY, l = 0.f;
 
-  auto issue = [&](int i) {  // lane 0 only: block i of this warp into slot i % 2
+  BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
+  bt.init(lane);
+  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 2
     const int slot = i & 1;
-    int phys = bt_row[blk0 + wl + i * dc.nw];
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
@@ -905,15 +947,21 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       tma_load_2d(dst + 4096 + hf * 2048, tmv, bar, 64 * hf, y);
     }
   };
-  if (lane == 0) {
-    if (nmine > 0) issue(0);
-    if (nmine > 1) issue(1);
+  {
+    const int ph0 = bt.at(0, lane), ph1 = bt.at(1, lane);
+    if (lane == 0) {
+      if (nmine > 0) issue(0, ph0);
+      if (nmine > 1) issue(1, ph1);
+    }
   }
   bool ok = true;
   const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
   for (int i = 0; i < nmine; ++i) {
     const int slot = i & 1;
-    if (!mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc, kSleepNs)) {
+    // every lane takes the same exit, so the warp's shuffles below stay converged
+    const bool got = mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc,
+                               kSleepNs);
+    if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
     }
@@ -993,7 +1041,10 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
       mma_16816(ot[mt], a, pb0, pb1);
     }
     __syncwarp();
-    if (lane == 0 && i + 2 < nmine) issue(i + 2);
+    {
+      const int ph = bt.at(i + 2, lane);
+      if (lane == 0 && i + 2 < nmine) issue(i + 2, ph);
+    }
   }
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
@@ -1022,19 +1073,243 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
   return ok;
 }
 
+// ---------------------------------------------------------------- FP8 cache decode
+// Decode over an e4m3 cache (head dim 128) on the warp tensor cores, in f16: every e4m3 value is
+// an f16 value, so one conversion per pair of values feeds the MMA exactly. The per-channel K
+// scale is folded into q once per item (q' = q * k_scale), the per-token V scale into the P·V
+// weights (the row sum keeps the unscaled weights).
+//
+// Each warp streams whole (block, kv-head) units: the K and V tiles (16 rows x 128 bytes each) by
+// TMA with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)) and the 16 V
+// scales by bulk copy, into a two-slot ring. The lanes read their MMA operands straight from the
+// tiles, in a channel order of their own that makes each read a contiguous 16-byte chunk and the
+// reads of a quarter-warp fall in distinct banks:
+//  * S = q' Kᵀ: in k-step ks, lane (g = lane / 4, t = lane % 4) holds channels 32t + 4ks .. +3
+//    of its key row(s) g (and g + 8) as the B fragment, and q' is permuted to match;
+//  * Oᵀ += Vᵀ Pᵀ: lane (g, t) holds channels 16g .. 16g + 15 of its four keys 2t, 2t+1, 2t+8,
+//    2t+9; output row g (g + 8) of m-tile mt is channel 16g + 2mt (+ 1).
+constexpr int kFp8Tile = kBlockSize * 128;                          // 2 KiB: one K or V tile
+constexpr int kFp8Slot = 2 * kFp8Tile;                              // K then V (1 KiB-aligned)
+constexpr int kFp8Ring = kDecodeSlots * kFp8Slot;                   // 8 KiB per warp
+constexpr int kFp8ScaleBytes = kDecodeSlots * kBlockSize * 4;       // V scales of both slots
+constexpr int kFp8GroupBytes = 33 * 1024;  // 4 rings + 4 scale areas, rounded to 1 KiB
+constexpr int kFp8Groups = 4;              // warps 0-3, 4-7, 8-11 and the decode slot 12-15
+static_assert(kDecodeWarps * (kFp8Ring + kFp8ScaleBytes) <= kFp8GroupBytes, "FP8 group size");
+static_assert(2 * kMaxGroup * kMaxDecodeSplits + kMaxGroup <= kDecodeWarps * kFp8Ring / 4 &&
+                  2 * kMaxGroup * kMaxDecodeSplits + kMaxGroup <= kSmemDecodeRing / 4,
+              "the split merge's weights must fit a decode group's ring");
+static_assert(kDecodeWarps * kMaxGroup * kScr * 4 <= kDecodeWarps * kFp8Ring,
+              "the combine scratch must fit the rings");
+static_assert(kFp8Groups * kFp8GroupBytes + kFp8Groups * kDecodeWarps * kSmemScoresPerWarp <=
+                  kSmemCtlOff,
+              "four FP8 decode groups must fit below the control block");
+
+template <int GT>
+__device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                              const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl, PipeState& ps,
+                              const WaitCtx& wc) {
+  constexpr int kKS = 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wl = warp - dc.w0;
+  const int d = it[1], g = it[2], kb = it[4], ke = it[5];
+  const int G = p.G;
+  const int32_t* bt_row = p.block_tables + (size_t)(p.Np + d) * p.maxb;
+  const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
+  const int blk0 = kb / kBlockSize;
+  const bool mine = wl >= 0 && wl < dc.nw;
+  const int nmine = mine && nblk > wl ? (nblk - wl + dc.nw - 1) / dc.nw : 0;
+  uint8_t* ring = dc.ring + (mine ? wl : 0) * kFp8Ring;
+  const float* vscales =
+      reinterpret_cast<const float*>(dc.ring + kDecodeWarps * kFp8Ring + (mine ? wl : 0) * kFp8ScaleBytes);
+  const uint32_t ring_s = smem_u32(ring);
+  const int hr = lane >> 2, qd = lane & 3;
+
+  // A fragments of q' = q * k_scale, channels 32qd + 4ks + {0,1} (a0) and {2,3} (a2)
+  uint32_t qa0[kKS], qa2[kKS];
+#pragma unroll
+  for (int ks = 0; ks < kKS; ++ks) qa0[ks] = qa2[ks] = 0u;
+  if (hr < G) {
+    const uint4* qv = reinterpret_cast<const uint4*>(
+        p.q_decode + ((size_t)d * p.Hq + (size_t)g * G + hr) * 128 + 32 * qd);
+    const float4* kv = reinterpret_cast<const float4*>(p.k_scale + (size_t)g * 128 + 32 * qd);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // 8 channels per uint4: k-steps 2j and 2j + 1
+      const uint4 w = qv[j];
+      const float4 s0 = kv[2 * j], s1 = kv[2 * j + 1];
+      qa0[2 * j] = pack_f16x2_sat(bf16lo(w.x) * s0.x, bf16hi(w.x) * s0.y);
+      qa2[2 * j] = pack_f16x2_sat(bf16lo(w.y) * s0.z, bf16hi(w.y) * s0.w);
+      qa0[2 * j + 1] = pack_f16x2_sat(bf16lo(w.z) * s1.x, bf16hi(w.z) * s1.y);
+      qa2[2 * j + 1] = pack_f16x2_sat(bf16lo(w.w) * s1.z, bf16hi(w.w) * s1.w);
+    }
+  }
+  float ot[kKS][4];  // Oᵀ: channels 16hr + 2mt (+1) x heads 2qd, 2qd+1
+#pragma unroll
+  for (int mt = 0; mt < kKS; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+  float m = -INFINITY, l = 0.f;
+
+  BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
+  bt.init(lane);
+  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 2
+    const int slot = i & 1;
+    if (phys < 0 || phys >= p.num_blocks) {
+      record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+      phys = 0;
+    }
+    const size_t unit = (size_t)phys * p.Hkv + g;
+    const uint32_t bar = smem_u32(&ctl->dslot[warp][slot]);
+    const uint32_t dst = ring_s + slot * kFp8Slot;
+    mbar_arrive_expect_tx(bar, kFp8Slot + kBlockSize * 4);
+    tma_load_2d(dst, tmk, bar, 0, (int)(unit * kBlockSize));
+    tma_load_2d(dst + kFp8Tile, tmv, bar, 0, (int)(unit * kBlockSize));
+    bulk_load(smem_u32(vscales + slot * kBlockSize), p.v_scale + unit * kBlockSize,
+              kBlockSize * 4, bar, policy_evict_first());
+  };
+  {
+    const int ph0 = bt.at(0, lane), ph1 = bt.at(1, lane);
+    if (lane == 0) {
+      if (nmine > 0) issue(0, ph0);
+      if (nmine > 1) issue(1, ph1);
+    }
+  }
+  bool ok = true;
+  const int kx[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};  // this lane's keys (S, P, V)
+  for (int i = 0; i < nmine; ++i) {
+    const int slot = i & 1;
+    // every lane takes the same exit, so the warp's shuffles below stay converged
+    const bool got = mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc,
+                               kSleepNs);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    ps.dphase ^= 1u << slot;
+    const int key0 = kb + (wl + i * dc.nw) * kBlockSize;
+    const int nv = min(kBlockSize, ke - key0);
+    const uint8_t* Kt = ring + slot * kFp8Slot;
+    const uint8_t* Vt = Kt + kFp8Tile;
+    // K rows hr and hr + 8: chunks 2qd, 2qd + 1 (swizzled by the row, whose low bits are hr)
+    uint4 kw[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        kw[j][h] = *reinterpret_cast<const uint4*>(Kt + (hr + 8 * j) * 128 + (((2 * qd + h) ^ hr) << 4));
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks) {
+      const uint32_t w0 = u4_word(kw[0][ks >> 2], ks & 3), w1 = u4_word(kw[1][ks >> 2], ks & 3);
+      const uint32_t a[4] = {qa0[ks], 0u, qa2[ks], 0u};
+      mma_16816_f16(s0, a, e4m3x2_to_f16x2(w0 & 0xFFFFu), e4m3x2_to_f16x2(w0 >> 16));
+      mma_16816_f16(s1, a, e4m3x2_to_f16x2(w1 & 0xFFFFu), e4m3x2_to_f16x2(w1 >> 16));
+    }
+    float x[4] = {s0[0], s0[1], s1[0], s1[1]};
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = kx[e] < nv ? x[e] * p.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, x[e]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const bool resc = m_new > m + 8.f;
+    float alpha = 1.f;
+    if (resc) {
+      alpha = ex2(m - m_new);
+      m = m_new;
+    }
+    if (__any_sync(0xffffffffu, resc)) {
+      l *= alpha;
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * qd);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * qd + 4);
+#pragma unroll
+      for (int mt = 0; mt < kKS; ++mt) {
+        ot[mt][0] *= a0;
+        ot[mt][1] *= a1;
+        ot[mt][2] *= a0;
+        ot[mt][3] *= a1;
+      }
+    }
+    // V rows kx[0..3]: chunk hr (read after S, so the K and V words are never live together)
+    uint4 vw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      vw[k] = *reinterpret_cast<const uint4*>(Vt + kx[k] * 128 + ((hr ^ (kx[k] & 7)) << 4));
+    float vsc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) vsc[k] = vscales[slot * kBlockSize + kx[k]];
+    __syncwarp();
+    // the slot is read: fetch the block after next while this one is computed
+    {
+      const int ph = bt.at(i + 2, lane);
+      if (lane == 0 && i + 2 < nmine) issue(i + 2, ph);
+    }
+    if (nv < kBlockSize) {  // rows past the end may hold anything (even NaN): weight-0 V is 0
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (kx[k] >= nv) vw[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float mref = m == -INFINITY ? 0.f : m;
+    float pw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float pr = ex2(x[e] - mref);
+      l += pr;
+      pw[e] = kx[e] < nv ? fminf(pr * vsc[e], kF16Max) : 0.f;  // P·V weight: P x V scale
+    }
+    const uint32_t pb0 = pack_f16x2(pw[0], pw[1]);
+    const uint32_t pb1 = pack_f16x2(pw[2], pw[3]);
+#pragma unroll
+    for (int mt = 0; mt < kKS; ++mt) {
+      // channels 16hr + 2mt, +1 of keys (kx0, kx1) and (kx2, kx3): bytes 2(mt&1), 2(mt&1)+1
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+      const uint32_t u01 = __byte_perm(u4_word(vw[0], mt >> 1), u4_word(vw[1], mt >> 1), sel);
+      const uint32_t u23 = __byte_perm(u4_word(vw[2], mt >> 1), u4_word(vw[3], mt >> 1), sel);
+      const uint32_t a[4] = {e4m3x2_to_f16x2(u01 & 0xFFFFu), e4m3x2_to_f16x2(u01 >> 16),
+                             e4m3x2_to_f16x2(u23 & 0xFFFFu), e4m3x2_to_f16x2(u23 >> 16)};
+      mma_16816_f16(ot[mt], a, pb0, pb1);
+    }
+  }
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  named_bar_sync(dc.bar_id, dc.bar_threads);
+  float* scr = reinterpret_cast<float*>(dc.ring);  // [nw][GT][kScr]
+  if (ok && mine) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int head = 2 * qd + e;
+      if (head < G) {
+        float* dst = scr + (wl * GT + head) * kScr + 16 * hr;
+#pragma unroll
+        for (int mt = 0; mt < kKS; ++mt)
+          *reinterpret_cast<float2*>(dst + 2 * mt) = make_float2(ot[mt][e], ot[mt][2 + e]);
+      }
+    }
+    if (hr < G && qd == 0) {
+      float* dst = scr + (wl * GT + hr) * kScr;
+      dst[kHeadDim] = m;
+      dst[kHeadDim + 1] = l;
+    }
+  }
+  return ok;
+}
+
 // Combine the warps' states of a decode item, then write the output or the split's partial and,
 // for the last split of a unit to arrive, merge all partials.
-template <int GT, int HD>
+template <int GT, int HD, bool FP8>
 __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                             const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl,
                             PipeState& ps, const WaitCtx& wc) {
   const int d = it[1], g = it[2], unit = it[6], split = it[7];
   const int G = p.G;
   const int ltid = threadIdx.x - dc.first_thread;
-  if constexpr (GT == 1)
+  if constexpr (FP8) {
+    decode_tc_fp8<GT>(p, tmk, tmv, it, dc, ctl, ps, wc);
+  } else if constexpr (GT == 1) {
     decode_simt<GT, HD>(p, it, dc, ctl, ps, wc);
-  else
+  } else {
     decode_tc<GT, HD>(p, tmk, tmv, it, dc, ctl, ps, wc);
+  }
   named_bar_sync(dc.bar_id, dc.bar_threads);
   const float* scr = reinterpret_cast<const float*>(dc.ring);
   if (!ctl->abort) {
@@ -1071,21 +1346,57 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
       named_bar_sync(dc.bar_id, dc.bar_threads);
       if (ctl->merge_last[dc.slot]) {
         __threadfence();
-        for (int idx = ltid; idx < G * HD; idx += dc.bar_threads) {
-          const int h = idx / HD, c = idx % HD;
+        // the splits' (m, l) once into shared memory (the scratch is free again), one weight
+        // per (head, split), then every output element as a weighted sum over the splits with
+        // the loads of all of this thread's elements in flight together
+        const size_t stride = (size_t)decode_slot_floats(G);
+        const float* part0 = p.partial_d + (size_t)slot0 * stride;
+        float* wts = reinterpret_cast<float*>(dc.ring);   // [G][nsplit]: m, then the weight
+        float* ls = wts + kMaxGroup * kMaxDecodeSplits;    // [G][nsplit]: l
+        float* inv = ls + kMaxGroup * kMaxDecodeSplits;    // [G]: 1 / merged l
+        for (int idx = ltid; idx < G * nsplit; idx += dc.bar_threads) {
+          const int h = idx / nsplit, k = idx - h * nsplit;
+          const float* sl = part0 + (size_t)k * stride + h * kRow;
+          wts[idx] = __ldcg(sl + kHeadDim);
+          ls[idx] = __ldcg(sl + kHeadDim + 1);
+        }
+        named_bar_sync(dc.bar_id, dc.bar_threads);
+        if (ltid < G) {
+          float* w = wts + ltid * nsplit;
+          const float* l = ls + ltid * nsplit;
           float mx = -INFINITY;
-          for (int k = 0; k < nsplit; ++k)
-            mx = fmaxf(mx, __ldcg(p.partial_d + (size_t)(slot0 + k) * decode_slot_floats(G) + h * kRow + kHeadDim));
-          float num = 0.f, den = 0.f;
+          for (int k = 0; k < nsplit; ++k) mx = fmaxf(mx, w[k]);
+          float den = 0.f;
           for (int k = 0; k < nsplit; ++k) {
-            const float* sl = p.partial_d + (size_t)(slot0 + k) * decode_slot_floats(G) + h * kRow;
-            const float mk = __ldcg(sl + kHeadDim);
-            if (mk == -INFINITY) continue;
-            const float f = ex2(mk - mx);
-            num += f * __ldcg(sl + c);
-            den += f * __ldcg(sl + kHeadDim + 1);
+            const float f = w[k] == -INFINITY ? 0.f : ex2(w[k] - mx);
+            w[k] = f;
+            den += f * l[k];
           }
-          p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * HD + c] = f2bf(num / den);
+          inv[ltid] = 1.f / den;
+        }
+        named_bar_sync(dc.bar_id, dc.bar_threads);
+        constexpr int kPer = (GT * HD + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
+        float num[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) num[e] = 0.f;
+        for (int k = 0; k < nsplit; ++k) {
+          const float* sl = part0 + (size_t)k * stride;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) {
+            const int idx = ltid + e * kDecodeWarps * 32;
+            if (idx < G * HD) {
+              const int h = idx / HD, c = idx % HD;
+              num[e] += wts[h * nsplit + k] * __ldcg(sl + h * kRow + c);
+            }
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          const int idx = ltid + e * kDecodeWarps * 32;
+          if (idx < G * HD) {
+            const int h = idx / HD, c = idx % HD;
+            p.o_decode[((size_t)d * p.Hq + (size_t)g * G + h) * HD + c] = f2bf(num[e] * inv[h]);
+          }
         }
         if (ltid == 0) p.arrive[unit] = 0;
       }
@@ -1131,7 +1442,7 @@ __device__ __forceinline__ void record_item(const Params& p, int kind, int idx, 
 }
 
 // A decode slot's ticket loop; `first` >= 0 is an item already taken for it.
-template <int GT, int HD>
+template <int GT, int HD, bool FP8>
 __device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
                             const DecodeCtx& dc, int first, int sm, uint32_t sm_raw, SmemCtl* ctl,
                             PipeState& ps, const WaitCtx& wc) {
@@ -1150,12 +1461,12 @@ __device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUten
     const int kind = ctl->item_kind[dc.slot], idx = ctl->item_idx[dc.slot];
     if (kind < 0 || ctl->abort) break;
     const uint64_t t0 = (p.records != nullptr && leader) ? globaltimer() : 0;
-    decode_item<GT, HD>(p, tmk, tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
+    decode_item<GT, HD, FP8>(p, tmk, tmv, p.items_d + (size_t)idx * kItemWords, dc, ctl, ps, wc);
     if (p.records != nullptr && leader) record_item(p, kind, idx, sm_raw, t0);
   }
 }
 
-template <int GT, int HD>
+template <int GT, int HD, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -1222,10 +1533,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
-      prefill_item<HD>(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+      if constexpr (!FP8)
+        prefill_item<HD>(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
       if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
     }
-    if (handoff >= 0 && warp >= kSoftmaxWarp0) {
+    if (handoff >= 0 && FP8) {
+      // FP8 cache decode: warps 4-7, 8-11 and 0-3 become three 4-warp decode slots (the
+      // producer and issuer warps have no prefill work here), each with a region of
+      // kFp8GroupBytes (the decode slot's is the fourth)
+      const int sub = warp >= kSoftmaxWarp0 ? (warp - kSoftmaxWarp0) / kDecodeWarps : 2;
+      const int w0 = (warp / kDecodeWarps) * kDecodeWarps;
+      const int grp = w0 / kDecodeWarps;
+      const DecodeCtx dc{w0, kDecodeWarps, smem + grp * kFp8GroupBytes,
+                         reinterpret_cast<float*>(smem + kFp8Groups * kFp8GroupBytes +
+                                                  grp * kDecodeWarps * kSmemScoresPerWarp),
+                         4 + sub, kDecodeWarps * 32, w0 * 32, 2 + sub};
+      decode_loop<GT, HD, FP8>(p, &tmk, &tmv, dc, sub == 0 ? handoff : -1, sm, sm_raw, ctl, ps,
+                               wc);
+    } else if (handoff >= 0 && warp >= kSoftmaxWarp0) {
       // the softmax warps become two 4-warp decode slots over the prefill region
       const int sub = (warp - kSoftmaxWarp0) / kDecodeWarps;
       const int w0 = kSoftmaxWarp0 + sub * kDecodeWarps;
@@ -1233,14 +1558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                          reinterpret_cast<float*>(smem + 2 * kSmemDecodeRing +
                                                   sub * kDecodeWarps * kSmemScoresPerWarp),
                          4 + sub, kDecodeWarps * 32, w0 * 32, 2 + sub};
-      decode_loop<GT, HD>(p, &tmk, &tmv, dc, sub == 0 ? handoff : -1, sm, sm_raw, ctl, ps, wc);
+      decode_loop<GT, HD, FP8>(p, &tmk, &tmv, dc, sub == 0 ? handoff : -1, sm, sm_raw, ctl, ps,
+                               wc);
     }
   } else {
     // ------------------------------------------------------------------ decode slot
-    const DecodeCtx dc{kDecodeWarp0, kDecodeWarps, smem + kSmemDecodeOff,
-                       reinterpret_cast<float*>(smem + kSmemScoresOff), 3, kDecodeWarps * 32,
+    const int ring_off = FP8 ? 3 * kFp8GroupBytes : kSmemDecodeOff;
+    const int scores_off =
+        FP8 ? kFp8Groups * kFp8GroupBytes + 3 * kDecodeWarps * kSmemScoresPerWarp : kSmemScoresOff;
+    const DecodeCtx dc{kDecodeWarp0, kDecodeWarps, smem + ring_off,
+                       reinterpret_cast<float*>(smem + scores_off), 3, kDecodeWarps * 32,
                        kDecodeWarp0 * 32, 1};
-    decode_loop<GT, HD>(p, &tmk, &tmv, dc, -1, sm, sm_raw, ctl, ps, wc);
+    decode_loop<GT, HD, FP8>(p, &tmk, &tmv, dc, -1, sm, sm_raw, ctl, ps, wc);
   }
   tc_fence_before();
   __syncthreads();
@@ -1303,6 +1632,8 @@ struct CudaState {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   CUtensorMap tmq{}, tmk{}, tmv{};
   const void *kq = nullptr, *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
+  CUtensorMap tmk8{}, tmv8{};                               // e4m3 pools (FP8 cache decode)
+  const void *kk8 = nullptr, *kv8 = nullptr;
 };
 
 // Q: 3-D {dim, head, token} so one box is 64 dims of hp heads x 128/hp tokens: the 128 rows of
@@ -1332,17 +1663,32 @@ static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows, int hd) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int GT, int HD>
+// e4m3 K or V pool: 2-D {byte, row}; one box is one paged block's 16 rows x 128 bytes.
+static bool encode_pool8(CUtensorMap* m, const void* pool, int64_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)kBlockSize};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int GT, int HD, bool FP8 = false>
 static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
+  const CUtensorMap& tmk = FP8 ? cs.tmk8 : cs.tmk;
+  const CUtensorMap& tmv = FP8 ? cs.tmv8 : cs.tmv;
   static std::atomic<int> attr_set{0};
   if (!attr_set.load()) {
-    cudaError_t e = cudaFuncSetAttribute(pod_attn_kernel<GT, HD>,
+    cudaError_t e = cudaFuncSetAttribute(pod_attn_kernel<GT, HD, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
     if (e != cudaSuccess) return e;
     attr_set.store(1);
   }
   if (!p.wait_append) {
-    pod_attn_kernel<GT, HD><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, cs.tmk, cs.tmv);
+    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, tmk, tmv);
     return cudaGetLastError();
   }
   // Items wait for every CTA's share of the append: a cooperative launch guarantees that all
@@ -1357,7 +1703,7 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD>, p, cs.tmq, cs.tmk, cs.tmv);
+  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, cs.tmq, tmk, tmv);
 }
 
 template <int HD>
@@ -1374,6 +1720,18 @@ static cudaError_t launch_hd(const Params& p, int grid, cudaStream_t st, const C
 static cudaError_t launch(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
   if (grid <= 0) return cudaSuccess;
   return p.head_dim == 64 ? launch_hd<64>(p, grid, st, cs) : launch_hd<128>(p, grid, st, cs);
+}
+
+// The FP8-cache decode launch (head dim 128).
+static cudaError_t launch_fp8(const Params& p, int grid, cudaStream_t st, const CudaState& cs) {
+  if (grid <= 0) return cudaSuccess;
+  switch (p.G) {
+    case 1: return launch_mode<1, 128, true>(p, grid, st, cs);
+    case 2: return launch_mode<2, 128, true>(p, grid, st, cs);
+    case 3:
+    case 4: return launch_mode<4, 128, true>(p, grid, st, cs);
+    default: return launch_mode<8, 128, true>(p, grid, st, cs);
+  }
 }
 
 // ---------------------------------------------------------------- allocation-free scratch
@@ -1593,6 +1951,7 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   if (!plan) return POD_ATTN_ERR_INVALID_ARG;
   pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
   if (st != POD_ATTN_OK) return st;
+  if (plan->opt.kv_fp8) return POD_ATTN_ERR_UNSUPPORTED;  // a plan for the e4m3 cache
   const pod_attn_problem& pr = plan->prob;
   const int n_p = (int)(plan->items_p.size() / kItemWords);
   const int n_d = (int)(plan->items_d.size() / kItemWords);
@@ -1755,6 +2114,83 @@ pod_attn_status pod_attn_run_append(pod_attn_plan_t plan, const void* q_prefill,
                   stream, stream2);
 }
 
+pod_attn_status pod_attn_run_decode_fp8(pod_attn_plan_t plan, const void* q_decode,
+                                        const void* k_pool8, const void* v_pool8,
+                                        const float* d_k_scale, const float* d_v_scale,
+                                        const int32_t* d_block_tables, const int32_t* d_kv_lens,
+                                        void* o_decode, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  if (!plan) return POD_ATTN_ERR_INVALID_ARG;
+  pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
+  if (st != POD_ATTN_OK) return st;
+  const pod_attn_problem& pr = plan->prob;
+  if (!plan->opt.kv_fp8 || pr.num_prefill_seqs != 0 || pr.head_dim != kHeadDim)
+    return POD_ATTN_ERR_UNSUPPORTED;
+  const int n_d = (int)(plan->items_d.size() / kItemWords);
+  if (n_d == 0) return POD_ATTN_OK;
+  if (!q_decode || !o_decode || !k_pool8 || !v_pool8 || !d_k_scale || !d_v_scale ||
+      !d_block_tables || !d_kv_lens)
+    return POD_ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_decode) | reinterpret_cast<uintptr_t>(o_decode) |
+       reinterpret_cast<uintptr_t>(k_pool8) | reinterpret_cast<uintptr_t>(v_pool8) |
+       reinterpret_cast<uintptr_t>(d_k_scale) | reinterpret_cast<uintptr_t>(d_v_scale)) & 15)
+    return POD_ATTN_ERR_INVALID_ARG;
+  CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const WorkspaceLayout& w = plan->ws;
+  Params p{};
+  p.q_decode = static_cast<const uint16_t*>(q_decode);
+  p.o_decode = static_cast<uint16_t*>(o_decode);
+  p.k8 = static_cast<const uint8_t*>(k_pool8);
+  p.v8 = static_cast<const uint8_t*>(v_pool8);
+  p.k_scale = d_k_scale;
+  p.v_scale = d_v_scale;
+  p.block_tables = d_block_tables;
+  p.kv_lens = d_kv_lens;
+  p.items_p = reinterpret_cast<const int32_t*>(ws + w.items_p);
+  p.items_d = reinterpret_cast<const int32_t*>(ws + w.items_d);
+  p.units = reinterpret_cast<const int32_t*>(ws + w.units);
+  p.partial_p = reinterpret_cast<float*>(ws + w.partial_p);
+  p.partial_d = reinterpret_cast<float*>(ws + w.partial_d);
+  p.arrive = reinterpret_cast<int32_t*>(ws + w.arrive);
+  p.status = reinterpret_cast<int32_t*>(ws + w.status);
+  p.records = plan->opt.instrument ? reinterpret_cast<pod_attn_item_record*>(ws + w.records) : nullptr;
+  p.n_items_p = 0;
+  p.n_items_d = n_d;
+  p.Hq = pr.num_q_heads;
+  p.Hkv = pr.num_kv_heads;
+  p.G = plan->group;
+  p.Np = 0;
+  p.Nd = pr.num_decode_seqs;
+  p.num_blocks = pr.num_blocks;
+  p.maxb = pr.max_blocks_per_seq;
+  p.pool_rows = (int32_t)((int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize);
+  p.num_sms = plan->num_sms;
+  p.max_prefill_per_sm = plan->max_prefill_per_sm;
+  p.hp_log2 = 0;
+  p.tq = kTileM;
+  p.causal = 1;
+  p.head_dim = kHeadDim;
+  p.scale_log2 = pr.scale * 1.4426950408889634f;
+  p.timeout_ns = kWaitTimeoutNs;
+  p.mode = kModeFused;
+  p.counters = reinterpret_cast<int32_t*>(ws + w.counters);  // the fused launch's block
+  if (cs->kk8 != k_pool8) {
+    if (!encode_pool8(&cs->tmk8, k_pool8, p.pool_rows)) return POD_ATTN_ERR_CUDA;
+    cs->kk8 = k_pool8;
+  }
+  if (cs->kv8 != v_pool8) {
+    if (!encode_pool8(&cs->tmv8, v_pool8, p.pool_rows)) return POD_ATTN_ERR_CUDA;
+    cs->kv8 = v_pool8;
+  }
+  const cudaError_t e = launch_fp8(p, plan->grid_fused, static_cast<cudaStream_t>(stream), *cs);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return POD_ATTN_ERR_CUDA;
+  }
+  return POD_ATTN_OK;
+}
+
 pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspace, void* stream) {
   (void)plan;
   if (!workspace) return POD_ATTN_ERR_INVALID_ARG;
@@ -1794,6 +2230,7 @@ pod_attn_status pod_attn_run_static(pod_attn_plan_t plan, const void* q_prefill,
                                     const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
                                     void* o_prefill, void* o_decode, void* stream) {
   if (!plan || plan->opt.variant != POD_ATTN_FUSED) return POD_ATTN_ERR_INVALID_ARG;
+  if (plan->opt.kv_fp8) return POD_ATTN_ERR_UNSUPPORTED;
   if (plan->ws.total > kStaticScratchBytes) return POD_ATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
   pod_attn_status st = static_scratch(&scratch);

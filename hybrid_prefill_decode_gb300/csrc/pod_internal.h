@@ -90,6 +90,9 @@ constexpr int kUnitWords = 4;
 
 // Most splits of one prefill output (the planner's cap; the merge keeps one weight per split).
 constexpr int kMaxPrefillSplits = 8;
+// Most splits of one decode output (the planner's cap; the merge keeps G weights per split in
+// shared memory).
+constexpr int kMaxDecodeSplits = 64;
 
 // Partial-result slots: fp32 o[rows][128] then m[rows] then l[rows] (m, l in log2 units).
 constexpr int kPrefillSlotFloats = kTileM * (kHeadDim + 2);

@@ -276,6 +276,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// The same with f16 inputs.
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 // Four 8x8 b16 matrices from shared memory; lane i supplies the row address of matrix i / 8.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -304,6 +313,30 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
       : "r"((uint32_t)pred), "r"(id), "r"(count)
       : "memory");
   return r != 0;
+}
+
+// Two e4m3 values (low byte first) as an f16 pair (low half first). Exact: every e4m3 value,
+// subnormals included, is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
+  return r;
+}
+// Largest finite f16.
+constexpr float kF16Max = 65504.f;
+// Two floats as an f16 pair (low half first), rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// As pack_f16x2, with magnitudes above the f16 range clamped to its largest finite value.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  return pack_f16x2(fmaxf(fminf(lo, kF16Max), -kF16Max), fmaxf(fminf(hi, kF16Max), -kF16Max));
+}
+// Word i (0-3) of a uint4; i must be a compile-time constant after unrolling.
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 // max(a, b, c) in one instruction.

@@ -67,3 +67,13 @@ def batch_work(num_q_heads: int, num_kv_heads: int, q_lens: Sequence[int],
     db = sum(float(L) * row for L in decode_kv_lens) + 2.0 * len(decode_kv_lens) * Hq * d * 2
     df = sum(4.0 * d * Hq * L for L in decode_kv_lens)
     return Work(pf, pb, db, df)
+
+
+def fp8_decode_bytes(num_q_heads: int, num_kv_heads: int, decode_kv_lens: Sequence[int],
+                     head_dim: int = 128) -> float:
+    """Algorithmic bytes of decode attention over an e4m3 cache: one byte per K and V value, a
+    4-byte V scale per cached (row, kv-head), the [Hkv][d] fp32 K scales, and the bf16 queries
+    read and outputs written."""
+    d, Hq, Hkv = head_dim, num_q_heads, num_kv_heads
+    rows = float(sum(decode_kv_lens)) * Hkv
+    return rows * (2 * d + 4) + Hkv * d * 4 + 2.0 * len(decode_kv_lens) * Hq * d * 2

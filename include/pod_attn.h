@@ -102,7 +102,8 @@ typedef struct {
                                item at a time by construction (its one prefill slot), so decode
                                is never crowded out ("POD-Attention" digest, §"가상 CTA와 SM별
                                균형") */
-  int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head); 0 = auto */
+  int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head), at most 64
+                               (more are capped); 0 = auto */
   int32_t prefill_splits;   /* force this many KV splits per prefill (tile, head block), at
                                most 8; 0 = auto */
   int32_t instrument;       /* nonzero: record (SM, kind, start, end) per work item */
@@ -111,6 +112,10 @@ typedef struct {
                                sequence, later chunk tokens included ("Week 6: Beyond PyTorch:
                                Custom Kernel과 vLLM", §"Non-Causal vs. Causal Attention");
                                0 = causal (default) */
+  int32_t kv_fp8;           /* nonzero: the plan is for pod_attn_run_decode_fp8 (an e4m3 cache;
+                               decode work only), which runs four 4-warp decode groups per SM
+                               and sizes its items for them; such a plan is rejected by the
+                               bf16 entry points, and a plan without it by the FP8 one */
 } pod_attn_options;
 
 typedef struct pod_attn_plan_s* pod_attn_plan_t;
@@ -223,6 +228,27 @@ pod_attn_status pod_attn_run_append(pod_attn_plan_t plan, const void* q_prefill,
                                     const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
                                     void* o_prefill, void* o_decode, void* workspace,
                                     size_t workspace_bytes, void* stream, void* stream2);
+
+/* Decode attention over an FP8 KV cache: e4m3 values (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, no infinities) with one fp32 scale per (kv-head, channel) for K and one per
+ * cached (row, kv-head) for V, so the cache takes half the bytes of bf16 ("LLMSO - W4 -
+ * Optimization & Frameworks", §"KV 헤드 줄이기": the decode step is bound by the bytes of the
+ * cache it reads). Cached K row j, channel c = e4m3(k_pool8[..][j][c]) * k_scale[g][c]; V row j,
+ * channel c = e4m3(v_pool8[..][j][c]) * v_scale[..][j]. The query and output stay bf16.
+ *   plan          : a plan made with options.kv_fp8 set, no prefill sequences and head_dim 128
+ *                   (else UNSUPPORTED); its variant is not used: the work runs as one launch.
+ *   q_decode, o_decode : device bf16 [Nd][Hq][128], as pod_attn_run.
+ *   k_pool8, v_pool8   : device uint8 [num_blocks][Hkv][16][128], 16-byte aligned.
+ *   d_k_scale          : device fp32 [Hkv][128], 16-byte aligned.
+ *   d_v_scale          : device fp32 [num_blocks][Hkv][16], 16-byte aligned.
+ *   d_block_tables, d_kv_lens, workspace, stream : as pod_attn_run.
+ * Errors: as pod_attn_run. */
+pod_attn_status pod_attn_run_decode_fp8(pod_attn_plan_t plan, const void* q_decode,
+                                        const void* k_pool8, const void* v_pool8,
+                                        const float* d_k_scale, const float* d_v_scale,
+                                        const int32_t* d_block_tables, const int32_t* d_kv_lens,
+                                        void* o_decode, void* workspace, size_t workspace_bytes,
+                                        void* stream);
 
 /* Synchronise `stream`, read and clear the device status word of `workspace`.
  * Returns OK, BAD_INDEX, TIMEOUT, or CUDA if the synchronisation itself failed. After

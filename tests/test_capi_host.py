@@ -96,7 +96,44 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
-def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True):
+def _wave_span(costs, slots):
+    """Items taken longest first by `slots` groups, wave by wave: the sum over waves of the
+    wave's longest item (costs sorted longest first)."""
+    return sum(costs[w] for w in range(0, len(costs), slots))
+
+
+def _rebalanced(nblk, c):
+    ns = max(1, min(_cdiv(nblk, c), nblk))
+    chunk = _cdiv(nblk, ns)
+    return _cdiv(nblk, chunk), chunk
+
+
+def restated_decode_only_chunk(nblks, num_sms, kv_fp8):
+    """Decode-only plans: the chunk ceil(longest / k), k in the divisor list, that minimises the
+    wave-by-wave makespan over (3 or 4) x SMs groups of items costing ceil(blocks / 4) + 2;
+    chunks under 12 blocks are not tried (but k = 1 always is), the search stops past four
+    waves of items, and ties keep the larger chunk."""
+    groups = num_sms * (4 if kv_fp8 else 3)
+    longest = max(nblks)
+    best, best_c, prev = None, 0, None
+    for k in (1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64):
+        c = _cdiv(longest, k)
+        if c == prev or (k > 1 and c < 12):
+            continue
+        prev = c
+        items = []
+        for n in nblks:
+            ns, ch = _rebalanced(n, c)
+            items += [_cdiv(min(n, (j + 1) * ch) - j * ch, 4) + 2 for j in range(ns)]
+        if k > 1 and len(items) > 4 * groups:
+            break
+        t = _wave_span(sorted(items, reverse=True), groups)
+        if best is None or t < best:
+            best, best_c = t, c
+    return best_c
+
+
+def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True, kv_fp8=False):
     """Items: prefill = (chunk, query tile of 128/hp tokens x hp heads, first head, split) over
     128-key steps (cost 57 each), with hp the largest power of two dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
     item slots per SM; split when an output costs more than a quarter of a slot's share."""
@@ -144,9 +181,13 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True)
         for k in range(ns):
             t0, t1 = k * chunk, min(nt, (k + 1) * chunk)
             lp.append(((t1 - t0) * 57, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
+    chunk_do = (restated_decode_only_chunk([x[3] for x in du], num_sms, kv_fp8)
+                if not pu and du and not dsplit else 0)
     for d, g, L, nblk in du:
-        if dsplit:
-            ns = dsplit
+        if chunk_do:
+            ns = _cdiv(nblk, chunk_do)
+        elif dsplit:
+            ns = min(dsplit, 64)
         else:
             ns = min(_cdiv(nblk * 8, target), max(1, nblk // 12), 64)
         ns = max(1, min(ns, nblk))
@@ -182,7 +223,7 @@ def test_planner_matches_python_restatement(lib, seed):
         cu.append(cu[-1] + q)
     num_sms = rng.choice([148, 152, 7])
     psplit = rng.choice([0, 0, 3])
-    dsplit = rng.choice([0, 0, 5])
+    dsplit = rng.choice([0, 0, 5, 100])
     maxb = _cdiv(max(pkv + dkv + [1]), 16)
     p = B.Plan(Hq, Hkv, cu if q_lens else [], pkv + dkv, len(dkv), 100, maxb, 0.1,
                num_sms=num_sms, prefill_splits=psplit, decode_splits=dsplit)
@@ -195,6 +236,52 @@ def test_planner_matches_python_restatement(lib, seed):
     assert got_u == exp_u
     inf = p.info()
     assert inf["max_prefill_ctas"] == cap and inf["grid_fused"] == grid
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_decode_only_planner_matches_restatement(lib, seed):
+    """Decode-only batches take the wave-aware chunk rule (both caches, both SM counts)."""
+    rng = random.Random(1000 + seed)
+    Hkv = rng.choice([1, 2, 4, 8])
+    Hq = Hkv * rng.choice([1, 2, 4, 8])
+    nd = rng.randint(1, 80)
+    lo = rng.choice([1, 500, 8000])
+    dkv = [rng.randint(lo, lo + rng.choice([100, 5000, 30000])) for _ in range(nd)]
+    num_sms = rng.choice([152, 148, 7])
+    kv_fp8 = bool(seed % 2)
+    maxb = _cdiv(max(dkv), 16)
+    p = B.Plan(Hq, Hkv, [], dkv, nd, 100, maxb, 0.1, num_sms=num_sms, kv_fp8=kv_fp8)
+    got_p, got_d, got_u = p.items()
+    exp_p, exp_d, exp_u, _, grid = restated_plan(Hq, Hkv, [], dkv, nd, num_sms, kv_fp8=kv_fp8)
+    assert got_p == [] and got_d == exp_d and got_u == exp_u
+    assert p.info()["grid_fused"] == grid
+
+
+def test_decode_only_rule_avoids_a_near_empty_last_wave():
+    """16 long decodes x 4 kv-heads on 152 SMs: the W / (4 S) rule would cut about 1250 equal
+    items (2.05 waves of 608 FP8 groups); the wave-aware rule keeps the modelled makespan of its
+    choice no worse than any other candidate's, including the old rule's chunk."""
+    dkv = [16384 + (16384 * k) // 16 for k in range(16)]
+    nblks = [_cdiv(L, 16) for L in dkv for _ in range(4)]
+    target = sum(n * 8 for n in nblks) // (304 * 4)
+
+    def span(split):
+        items = []
+        for n in nblks:
+            ns, ch = split(n)
+            items += [_cdiv(min(n, (j + 1) * ch) - j * ch, 4) + 2 for j in range(ns)]
+        return _wave_span(sorted(items, reverse=True), 608), len(items)
+
+    def old(n):
+        ns = max(1, min(_cdiv(n * 8, target), max(1, n // 12), 64, n))
+        ch = _cdiv(n, ns)
+        return _cdiv(n, ch), ch
+
+    c = restated_decode_only_chunk(nblks, 152, True)
+    new_span, _ = span(lambda n: _rebalanced(n, c))
+    old_span, old_items = span(old)
+    assert 608 * 2 < old_items < 608 * 2.1
+    assert new_span < old_span
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -261,3 +348,30 @@ def test_workspace_grows_with_instrumentation(lib):
     n = a.info()["num_prefill_items"] + a.info()["num_decode_items"]
     assert b.workspace_bytes - a.workspace_bytes >= n * ctypes.sizeof(B.ItemRecord)
 
+
+
+def test_run_decode_fp8_validation(lib):
+    big = 1 << 40
+    # a plan with prefill work is not an FP8 decode plan
+    p = B.Plan(4, 2, [0, 5], [9, 7], 1, 10, 4, 0.1, num_sms=148, kv_fp8=True)
+    code = lib.pod_attn_run_decode_fp8(p.handle, *([None] * 8), 256, big, None)
+    assert code == B.ERR_UNSUPPORTED
+    # head dim 64 is not built for the FP8 cache
+    p64 = B.Plan(4, 2, [], [7], 1, 10, 4, 0.1, num_sms=148, head_dim=64, kv_fp8=True)
+    code = lib.pod_attn_run_decode_fp8(p64.handle, *([None] * 8), 256, big, None)
+    assert code == B.ERR_UNSUPPORTED
+    # a plan made for the bf16 cache is not an FP8 plan, and an FP8 plan runs nowhere else
+    d16 = B.Plan(4, 2, [], [7, 40], 2, 10, 4, 0.1, num_sms=148)
+    code = lib.pod_attn_run_decode_fp8(d16.handle, *([None] * 8), 256, big, None)
+    assert code == B.ERR_UNSUPPORTED
+    d = B.Plan(4, 2, [], [7, 40], 2, 10, 4, 0.1, num_sms=148, kv_fp8=True)
+    code = lib.pod_attn_run(d.handle, *([None] * 9), 256, big, None, None)
+    assert code == B.ERR_UNSUPPORTED
+    code = lib.pod_attn_run_decode_fp8(d.handle, *([None] * 8), 256, big, None)
+    assert code == B.ERR_INVALID_ARG                     # missing pointers
+    ptrs = [4096 * (i + 1) for i in range(8)]
+    ptrs[3] += 4                                         # misaligned V scales
+    code = lib.pod_attn_run_decode_fp8(d.handle, *ptrs, 256, big, None)
+    assert code == B.ERR_INVALID_ARG
+    code = lib.pod_attn_run_decode_fp8(d.handle, *([None] * 8), 257, big, None)
+    assert code == B.ERR_WORKSPACE

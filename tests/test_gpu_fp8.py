@@ -1,0 +1,83 @@
+"""GPU parity of the decode over an FP8 (e4m3) KV cache against the fp64 oracle's reading.
+
+Each cached K value is e4m3 x a per-(kv-head, channel) scale and each V value e4m3 x a
+per-(row, kv-head) scale ("LLMSO - W4 - Optimization & Frameworks", §"KV 헤드 줄이기": a smaller
+cache is fewer bytes per decode step). The kernel decodes e4m3 exactly (every e4m3 value is a
+bf16 value), folds the K scales into the query and the V scales into the P·V weights, so the
+only extra rounding is of the scaled query and weights to bf16: the tolerance stays the library's
+|err| <= 2e-2 + 2e-2 |ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_prefill_decode_gb300 import binding as B
+from hybrid_prefill_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-2
+RTOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def assert_close(got, ref, what=""):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert g.shape == ref.shape, (what, g.shape, ref.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    if bad.any():
+        idx = np.argwhere(bad)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
+                             f"max err {err.max():.4g}; first bad {idx[:5].tolist()}")
+
+
+LENS = [1, 15, 16, 17, 300, 2047]
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (16, 2)])
+def test_fp8_decode_group_sizes(hq, hkv):
+    fb = W.make_fp8_decode_batch(hq, hkv, LENS, seed=31 + hq * 7 + hkv)
+    ref = oracle.decode_fp8(fb)
+    out = B.decode_fp8(fb.to("cuda"))
+    torch.cuda.synchronize()
+    assert_close(out, ref, f"fp8 G={hq // hkv}")
+
+
+@pytest.mark.parametrize("splits", [1, 3, 64])
+def test_fp8_decode_forced_splits(splits):
+    fb = W.make_fp8_decode_batch(16, 2, [5, 190, 1000, 2047], seed=400 + splits)
+    ref = oracle.decode_fp8(fb)
+    out = B.decode_fp8(fb.to("cuda"), decode_splits=splits)
+    torch.cuda.synchronize()
+    assert_close(out, ref, f"fp8 splits={splits}")
+
+
+def test_fp8_decode_few_sms_and_repeat_bitwise():
+    fb = W.make_fp8_decode_batch(32, 8, [3000] * 5 + [17, 1], seed=12).to("cuda")
+    a = B.decode_fp8(fb, num_sms=3)
+    b = B.decode_fp8(fb, num_sms=3)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert_close(a, oracle.decode_fp8(fb.to("cpu")), "fp8 few SMs")
+
+
+def test_fp8_pow2_scales_match_bf16_path():
+    """With power-of-two scales the dequantised cache is exact in bf16, so the FP8 path and the
+    bf16 library path compute from the same values: both within tolerance of the same oracle."""
+    fb = W.make_fp8_decode_batch(32, 8, [40, 513, 2000], seed=8, pow2_scales=True)
+    bb = W.dequantised_batch(fb)
+    ref = oracle.hybrid_attention(bb)[1]
+    np.testing.assert_allclose(oracle.decode_fp8(fb), ref, rtol=1e-12, atol=1e-12)
+    out8 = B.decode_fp8(fb.to("cuda"))
+    _, out16 = B.hybrid_attention(bb.to("cuda"))
+    torch.cuda.synchronize()
+    assert_close(out8, ref, "fp8 pow2")
+    assert_close(out16, ref, "bf16 of the dequantised cache")

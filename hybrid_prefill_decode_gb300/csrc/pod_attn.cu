@@ -98,7 +98,7 @@ struct SmemCtl {
   uint64_t k_empty[kKStages];      // S of the stage's last step completed
   uint64_t v_full[kVStages];
   uint64_t s_full[2];              // S buffer 0 / 1 computed
-  uint64_t p_ready[2];             // P buffer 0 / 1 written (256 softmax arrivals each)
+  uint64_t p_ready[2][2];          // [S buffer][group]: the group's P written (128 arrivals)
   uint64_t pv_done[2];             // P·V of P buffer 0 / 1 done (also frees V stage 0 / 1)
   uint64_t dslot[kWarps][kDecodeSlots];  // decode rings, by absolute warp
   uint32_t tmem_base;
@@ -187,14 +187,15 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 
 // ============================================================================ prefill item
 // One prefill item: a 128-row query tile of a chunk, one head, a range of keys in 128-key
-// steps. Steps are numbered n by a counter that runs on across items; step n uses K/V stage,
-// S buffer and P buffer n & 1. Two warps feed the tensor cores, whose instruction queue is only
-// a few MMAs deep: warp 1 issues S(j) as soon as the softmax of step j-2 has read its buffer,
-// warp 3 issues P·V(j) as soon as P(j) is written, so one issuer's waits do not idle the pipe.
-// The two softmax warpgroups split each score tile by columns (64 keys each) and keep one
-// reference max per row in common: when no score of the step exceeds it by more than 2^8 (the
-// lazy-rescale threshold) — which a vote over both groups establishes — nothing is exchanged;
-// otherwise both groups read the whole row of S and move the reference alike.
+// steps. Steps are numbered n by a counter that runs on across items; step n uses K/V stage and
+// S buffer n & 1. Two warps feed the tensor cores, whose instruction queue is only a few MMAs
+// deep: warp 1 issues S(j) as soon as P·V of step j-2 has released its buffer, warp 3 issues
+// each group's half of P·V(j) as soon as that group's P(j) is written, so one issuer's waits do
+// not idle the pipe. The two softmax warpgroups split each score tile by keys (64 each) and
+// never wait for each other inside the item: each keeps its own running max and sum per row
+// (rescaling its own O only when a score exceeds the max by more than 2^8, the lazy-rescale
+// threshold) and its own O accumulator; the two (m, l, O) of a row are merged once, in the
+// epilogue, as two splits of the row's keys are.
 // HD (head dim) is 128 or 64; shared memory and TMEM keep the layout of 128 (a 64-dim head
 // uses the first 64-column half of every tile and the first 64 columns of O).
 template <int HD>
@@ -289,14 +290,15 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ S issuer
-    // S(j) = Q K(j)ᵀ into S buffer n & 1, once the softmax of step j-2 has read that buffer.
+    // S(j) = Q K(j)ᵀ into S buffer n & 1, once P·V of step j-2 (which read the P written over
+    // that buffer) has completed.
     const uint32_t tmem = ctl->tmem_base;
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc, kSleepNs);
     tc_fence_after();
     for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t n = n0 + j;
-      // completion (n-2)/2 of p_ready[n & 1]; the steps before this item's first two are done
-      if (j >= 2 && !mbar_wait(smem_u32(&ctl->p_ready[n & 1]), ((n >> 1) & 1) ^ 1, wc)) {
+      // completion (n-2)/2 of pv_done[n & 1]; the steps before this item's first two are done
+      if (j >= 2 && !mbar_wait(smem_u32(&ctl->pv_done[n & 1]), ((n >> 1) & 1) ^ 1, wc)) {
         ok = false;
         break;
       }
@@ -323,15 +325,13 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------------ P·V issuer
-    // O += P(j) V(j) once the softmax of step j has written P(j). S and P·V use disjoint TMEM
-    // columns, so the two issuers need no order between them; each commit tracks only its own
-    // thread's MMAs.
+    // O_g += P_g(j) V_g(j) for each group g (its 64 keys of the step) once that group has
+    // written P_g(j); one commit per step (pv_done) covers both halves.
     const uint32_t tmem = ctl->tmem_base;
     bool ok = true;
     for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t n = n0 + j;
-      if (!mbar_wait(smem_u32(&ctl->p_ready[n & 1]), (n >> 1) & 1, wc) ||
-          !mbar_wait(smem_u32(&ctl->v_full[n & 1]), (n >> 1) & 1, wc)) {
+      if (!mbar_wait(smem_u32(&ctl->v_full[n & 1]), (n >> 1) & 1, wc)) {
         ok = false;
         break;
       }
@@ -349,19 +349,29 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         fence_proxy_async_smem();
         __syncwarp();
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sV = sVring + (n & 1) * kSmemKTile;
-        const uint32_t aP = tmem + kTmemP + (n & 1) * 64;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // P of keys 16kk.. at column 8kk of its buffer; V is N-major: 64-column halves
-          // 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
-          const uint64_t bd = sdesc_sw128(sV + kk * 2048, kSmemKTile / 2, 1024);
-          umma_ts(tmem + kTmemO, aP + kk * 8, bd, kIdescPVh, (j == 0 && kk == 0) ? 0u : 1u);
+      const uint32_t sV = sVring + (n & 1) * kSmemKTile;
+      const uint32_t aS = tmem + kTmemS + (n & 1) * 128;
+#pragma unroll 1
+      for (int grp = 0; grp < 2; ++grp) {
+        if (!mbar_wait(smem_u32(&ctl->p_ready[n & 1][grp]), (n >> 1) & 1, wc)) {
+          ok = false;
+          break;
         }
-        umma_commit(smem_u32(&ctl->pv_done[n & 1]));
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // P of the group's keys 16kk.. at column 64 grp + 8kk of the S buffer; V is
+            // N-major: 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
+            const uint64_t bd = sdesc_sw128(sV + (grp * 4 + kk) * 2048, kSmemKTile / 2, 1024);
+            umma_ts(tmem + kTmemO + grp * 128, aS + grp * 64 + kk * 8, bd, kIdescPVh,
+                    (j == 0 && kk == 0) ? 0u : 1u);
+          }
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) umma_commit(smem_u32(&ctl->pv_done[n & 1]));
       __syncwarp();
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
@@ -371,51 +381,27 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     const int row = quarter * 32 + lane;
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tO = trow + kTmemO + grp * kOG;  // this group's O columns
+    const uint32_t tOg = trow + kTmemO + grp * 128;  // this group's O accumulator
     const int qi = t * p.tq + (row >> p.hp_log2);  // this row's token (index in the chunk)
     const int h = h0 + (row & ((1 << p.hp_log2) - 1));  // and query head
     const bool valid = qi < qlen;
     const int lim = p.causal ? min(P + qi + 1, ke) : ke;  // keys [.., lim) are visible
-    // max over 64 columns of S from `taddr`, of which the first `vis` are visible
-    auto rowmax64 = [&](uint32_t taddr, int vis) -> float {
-      const bool full = __all_sync(0xffffffffu, vis >= 64);
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sr[32];
-        tmem_ld32(taddr + ch * 32, sr);
-        tmem_ld_wait();
-        if (!full) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (ch * 32 + c >= vis) sr[c] = f2u(-INFINITY);
-        }
-#pragma unroll
-        for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(sr[c]));
-      }
-      return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-    };
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // this group's running max (log2 units) and sum of the row
     bool ok = true;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     for (int j = 0; j < ntiles; ++j) {
       const uint32_t n = n0 + j;
-      const uint32_t tS = trow + kTmemS + (n & 1) * 128;
-      const uint32_t tP = trow + kTmemP + (n & 1) * 64 + grp * 32;
-      // After a failed wait the loop still runs (every wait then fails at once), so that both
-      // warpgroups pass the same named barriers whatever happened.
+      const uint32_t tS = trow + kTmemS + (n & 1) * 128 + grp * 64;  // this group's 64 scores
+      // After a failed wait the loop still runs (every wait then fails at once), so that the
+      // warps pass the same barriers whatever happened.
       ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[n & 1]), (n >> 1) & 1, wc));
       tc_fence_after();
-      const int nvis = lim - (kb + j * kTileN);  // visible columns of this step: [0, nvis)
-      const int vis = nvis - grp * 64;            // visible columns of this group: [0, vis)
+      const int vis = lim - (kb + j * kTileN) - grp * 64;  // visible columns: [0, vis)
       const bool full = __all_sync(0xffffffffu, vis >= 64);
-      // this group's 64 scores stay in registers from the max to the exponentials
+      // the 64 scores stay in registers from the max to the exponentials
       uint32_t sa[32], sb[32];
-      tmem_ld32(tS + grp * 64, sa);
-      tmem_ld32(tS + grp * 64 + 32, sb);
+      tmem_ld32(tS, sa);
+      tmem_ld32(tS + 32, sb);
       tmem_ld_wait();
       if (!full) {
 #pragma unroll
@@ -436,43 +422,34 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const float mine = fmaxf(fmax3(mx[0], mx[1], mx[2]),
                                fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       // scale > 0, so the max of the scaled scores is the scaled max
-      const bool need = mine * p.scale_log2 > m + 8.f;
+      const float m_new = fmaxf(m, mine * p.scale_log2);
+      const bool resc = m_new > m + 8.f;
       float alpha = 1.f;
-      if (bar_red_or(2, 256, need)) {
-        // some row moves its reference: both groups take the max of the whole row, so they move
-        // it alike (m, O and l stay consistent with whichever reference is current)
-        const float other = rowmax64(tS + (grp ^ 1) * 64, nvis - (grp ^ 1) * 64);
-        const float m_new = fmaxf(m, fmaxf(mine, other) * p.scale_log2);
-        const bool resc = m_new > m + 8.f;
-        if (resc) {
-          alpha = ex2(m - m_new);
-          m = m_new;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O holds P·V of the earlier steps once step j-1's product completed (all before it
-          // completed first); at most one completion of that barrier is pending.
-          ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done[(n - 1) & 1]),
-                                                       ((n - 1) >> 1) & 1, wc));
-          tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < kOG / 32; ++ch) {  // this group's columns of O
-            uint32_t o[32];
-            tmem_ld32(tO + ch * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-            tmem_st32(tO + ch * 32, o);
-          }
-          tmem_st_wait();
-        }
+      if (resc) {
+        alpha = ex2(m - m_new);
+        m = m_new;
       }
-      // P buffer n & 1 is free once P·V of step n-2 completed (a fresh barrier passes)
-      ok = __all_sync(0xffffffffu,
-                      ok && mbar_wait(smem_u32(&ctl->pv_done[n & 1]), ((n >> 1) & 1) ^ 1, wc));
-      tc_fence_after();
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O_g holds P·V of the earlier steps once step j-1's product completed (all before it
+        // completed first); at most one completion of that barrier is pending.
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done[(n - 1) & 1]),
+                                                     ((n - 1) >> 1) & 1, wc));
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < HD / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tOg + ch * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+          tmem_st32(tOg + ch * 32, o);
+        }
+        tmem_st_wait();
+      }
       const float mref = m == -INFINITY ? 0.f : m;
       const float2 nm2 = make_float2(-mref, -mref);
-      // exponentials of this group's 64 columns, their sum, and P as bf16 pairs
+      // exponentials, their sum, and P as bf16 pairs over the first 32 columns of the group's
+      // scores (all of which are in registers already)
       float2 sum[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
@@ -484,7 +461,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         sum[c & 3] = fadd2(sum[c & 3], e);
         pk[c] = pack_bf16x2(e.x, e.y);
       }
-      tmem_st16(tP, pk);
+      tmem_st16(tS, pk);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float2 xv = ffma2(make_float2(u2f(sb[2 * c]), u2f(sb[2 * c + 1])), c2, nm2);
@@ -492,42 +469,59 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         sum[c & 3] = fadd2(sum[c & 3], e);
         pk[c] = pack_bf16x2(e.x, e.y);
       }
-      tmem_st16(tP + 16, pk);
+      tmem_st16(tS + 16, pk);
       const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
-      l = l * alpha + (s01.x + s01.y);  // this group's share of the row sum
+      l = l * alpha + (s01.x + s01.y);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->p_ready[n & 1]));
+      mbar_arrive(smem_u32(&ctl->p_ready[n & 1][grp]));
     }
     if (ok && ntiles > 0) {  // the last P·V; every S completed before the softmax that fed it
       const uint32_t nl = n0 + ntiles - 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[nl & 1]), (nl >> 1) & 1, wc));
       tc_fence_after();
     }
-    // the full row sum: swap the two groups' shares through two columns of the last step's P
-    // buffer, whose P·V has completed (and every MMA of the item before it)
-    const uint32_t tX = trow + kTmemP + ((n0 + (ntiles > 0 ? ntiles : 1) - 1) & 1) * 64;
-    tmem_st1(tX + grp, f2u(l));
+    // ------------------------------------------------------------------ epilogue
+    // The two groups' (m, l) of a row meet through four columns of S buffer 0: every P·V of the
+    // item has completed, and the next item's S waits for the end-of-item barrier. Then the row
+    // is the merge of two key splits: m* = max(m_0, m_1), weights 2^(m_g - m*), and group g
+    // writes output columns [g HD/2, (g+1) HD/2) from both accumulators.
+    const uint32_t tX = trow + kTmemS;
+    tmem_st1(tX + 2 * grp, f2u(m));
+    tmem_st1(tX + 2 * grp + 1, f2u(l));
     tmem_st_wait();
     tc_fence_before();
     named_bar_sync(2, 256);
     tc_fence_after();
-    const float lt = l + u2f(tmem_ld1(tX + (grp ^ 1)));
+    uint32_t mo_u = tmem_ld1(tX + 2 * (grp ^ 1));
+    uint32_t lo_u = tmem_ld1(tX + 2 * (grp ^ 1) + 1);
     tmem_ld_wait();
-    // ------------------------------------------------------------------ epilogue
+    reg_fence(mo_u);
+    reg_fence(lo_u);
+    const float m_o = u2f(mo_u), l_o = u2f(lo_u);
+    const float mm = fmaxf(m, m_o);
+    const float w_me = m == -INFINITY ? 0.f : ex2(m - mm);
+    const float w_ot = m_o == -INFINITY ? 0.f : ex2(m_o - mm);
+    const float lt = w_me * l + w_ot * l_o;
+    const float w0 = grp == 0 ? w_me : w_ot, w1 = grp == 0 ? w_ot : w_me;  // of O_0, O_1
+    const uint32_t tO0 = trow + kTmemO + grp * kOG, tO1 = tO0 + 128;  // this group's columns
     {
       if (unit < 0) {
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float f0 = w0 * inv, f1 = w1 * inv;
         uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD + grp * kOG;
 #pragma unroll 1
         for (int ch = 0; ch < kOG / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
+          uint32_t a[32], b[32];
+          tmem_ld32(tO0 + ch * 32, a);
+          tmem_ld32(tO1 + ch * 32, b);
           tmem_ld_wait();
           if (valid && ok) {
             uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(u2f(a[2 * i]) * f0 + u2f(b[2 * i]) * f1,
+                                 u2f(a[2 * i + 1]) * f0 + u2f(b[2 * i + 1]) * f1);
             uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -539,17 +533,21 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         float* slot = p.partial_p + (size_t)(slot0 + split) * kPrefillSlotFloats;
 #pragma unroll 1
         for (int ch = 0; ch < kOG / 32 && ok; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
+          uint32_t a[32], b[32];
+          tmem_ld32(tO0 + ch * 32, a);
+          tmem_ld32(tO1 + ch * 32, b);
           tmem_ld_wait();
           // slot rows keep a stride of 128 columns whatever the head dim
           float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + grp * kOG + ch * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(u2f(o[4 * i]), u2f(o[4 * i + 1]), u2f(o[4 * i + 2]), u2f(o[4 * i + 3]));
+            d4[i] = make_float4(u2f(a[4 * i]) * w0 + u2f(b[4 * i]) * w1,
+                                u2f(a[4 * i + 1]) * w0 + u2f(b[4 * i + 1]) * w1,
+                                u2f(a[4 * i + 2]) * w0 + u2f(b[4 * i + 2]) * w1,
+                                u2f(a[4 * i + 3]) * w0 + u2f(b[4 * i + 3]) * w1);
         }
         if (grp == 0 && ok) {
-          slot[kTileM * kHeadDim + row] = m;
+          slot[kTileM * kHeadDim + row] = mm;
           slot[kTileM * kHeadDim + kTileM + row] = lt;
         }
         __threadfence();
@@ -1074,7 +1072,9 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 }
 
 // ---------------------------------------------------------------- FP8 cache decode
-// Decode over an e4m3 cache (head dim 128) on the warp tensor cores, in f16: every e4m3 value is
+// Decode over an e4m3 cache with per-channel K and per-token V scales ("LLMSO - W4 -
+// Optimization & Frameworks", §"2-4. 고급 KV 캐싱 기법"), head dim 128, on the warp tensor
+// cores in f16: every e4m3 value is
 // an f16 value, so one conversion per pair of values feeds the MMA exactly. The per-channel K
 // scale is folded into q once per item (q' = q * k_scale), the per-token V scale into the P·V
 // weights (the row sum keeps the unscaled weights).
@@ -1488,7 +1488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kVStages; ++i) mbar_init(smem_u32(&ctl->v_full[i]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctl->p_ready[i]), 256);
+      mbar_init(smem_u32(&ctl->p_ready[i][0]), 128);
+      mbar_init(smem_u32(&ctl->p_ready[i][1]), 128);
       mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     }
     for (int w = 0; w < kWarps; ++w)

@@ -20,8 +20,8 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 // §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
 //  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns — warp 0 issues
 //    the TMA loads of Q and K, warp 2 those of V, warps 1 and 3 issue the S and P·V tcgen05
-//    MMAs, and warps 4-7 and 8-11 are two softmax warpgroups that share each 128x128 score
-//    tile (64 columns each);
+//    MMAs, and warps 4-7 and 8-11 are two softmax warpgroups that split each 128x128 score
+//    tile by keys (64 columns each), each with its own O accumulator;
 //  * the decode slot (warps 12-15): decode items, on their own ticket loop.
 // Once the prefill list is drained, the prefill slot's warps 4-7 and 8-11 become two more
 // 4-warp decode slots. Every decode item thus runs on exactly 4 warps, whichever slot takes it,
@@ -64,14 +64,14 @@ static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
 static_assert(2 * (kSmemDecodeRing + kDecodeWarps * kSmemScoresPerWarp) <= kSmemPrefill,
               "the two decode slots of the prefill warps must fit the prefill region");
 
-// TMEM columns (the whole SM): O (fp32, 128 columns), two S buffers (fp32, 128 columns each)
-// and two P buffers (bf16 pairs, 64 columns each). P has its own columns so that S of step j+2
-// can be computed into the buffer of step j as soon as the softmax of step j has read it, before
-// P·V of step j.
+// TMEM columns (the whole SM): one O accumulator per softmax warpgroup (fp32, 128 columns each:
+// group g sums P·V over its own 64 keys of every step, with its own running max and sum, and the
+// two are merged once per item) and two S buffers (fp32, 128 columns each). Group g writes its
+// P (bf16 pairs) over the first 32 of its own 64 columns of the S buffer it has just read, so S
+// of step j+2 is issued into that buffer once P·V of step j has completed.
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 0;
-constexpr int kTmemS = 128;    // + 128 * (step & 1)
-constexpr int kTmemP = 384;    // + 64 * (step & 1)
+constexpr int kTmemO = 0;      // + 128 * group
+constexpr int kTmemS = 256;    // + 128 * (step & 1)
 
 // Work item: kItemWords int32 words.
 //   [0] kind         0 = prefill, 1 = decode

@@ -260,6 +260,9 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
                : "memory");
 }
+// Makes `x` depend on everything before this point (an empty asm that "rewrites" it), so that
+// uses of a register loaded by tcgen05.ld cannot be scheduled before the tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence(uint32_t& x) { asm volatile("" : "+r"(x)::"memory"); }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

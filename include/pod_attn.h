@@ -231,10 +231,14 @@ pod_attn_status pod_attn_run_append(pod_attn_plan_t plan, const void* q_prefill,
 
 /* Decode attention over an FP8 KV cache: e4m3 values (1 sign, 4 exponent bits with bias 7, 3
  * mantissa bits, no infinities) with one fp32 scale per (kv-head, channel) for K and one per
- * cached (row, kv-head) for V, so the cache takes half the bytes of bf16 ("LLMSO - W4 -
- * Optimization & Frameworks", §"KV 헤드 줄이기": the decode step is bound by the bytes of the
- * cache it reads). Cached K row j, channel c = e4m3(k_pool8[..][j][c]) * k_scale[g][c]; V row j,
+ * cached (row, kv-head) for V ([LLMSO] §"2-4. 고급 KV 캐싱 기법": per-channel scales suit K,
+ * whose outliers sit in particular channels, per-token scales suit V), so the cache takes half
+ * the bytes of bf16 and the decode step, which reads the whole cache ([BEYOND] §"KV Cache"),
+ * about half the time. Cached K row j, channel c = e4m3(k_pool8[..][j][c]) * k_scale[g][c]; V row j,
  * channel c = e4m3(v_pool8[..][j][c]) * v_scale[..][j]. The query and output stay bf16.
+ * Arithmetic: e4m3 is converted to f16 exactly; q * k_scale and the softmax weights times
+ * v_scale are rounded to f16 for the tensor cores (magnitudes above 65504 saturate there);
+ * scores, softmax and accumulation are fp32.
  *   plan          : a plan made with options.kv_fp8 set, no prefill sequences and head_dim 128
  *                   (else UNSUPPORTED); its variant is not used: the work runs as one launch.
  *   q_decode, o_decode : device bf16 [Nd][Hq][128], as pod_attn_run.

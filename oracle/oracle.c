@@ -281,8 +281,10 @@ int oracle_hybrid_attention(int Hq, int Hkv, int D, int BS, int Np, int Nd, int6
 }
 
 /*
- * FP8 KV cache (the 8-bit cache of "Week 6: Beyond PyTorch: Custom Kernel과 vLLM" and "LLMSO -
- * W4", §"KV 헤드 줄이기": the cache shrinks when each element takes fewer bytes).
+ * FP8 KV cache. Every decode step reads the whole cache ("Week 6: Beyond PyTorch: Custom
+ * Kernel과 vLLM", §"KV Cache"), so fewer bytes per element mean a shorter step; "LLMSO - W4 -
+ * Optimization & Frameworks", §"2-4. 고급 KV 캐싱 기법", scales K per channel (its outliers sit
+ * in particular channels) and V per token.
  *
  * e4m3 (the 8-bit floating-point format with 4 exponent and 3 mantissa bits and no
  * infinities): bit 7 sign; bits 6..3 exponent E (bias 7); bits 2..0 mantissa M.

@@ -1,11 +1,11 @@
 """GPU parity of the decode over an FP8 (e4m3) KV cache against the fp64 oracle's reading.
 
 Each cached K value is e4m3 x a per-(kv-head, channel) scale and each V value e4m3 x a
-per-(row, kv-head) scale ("LLMSO - W4 - Optimization & Frameworks", §"KV 헤드 줄이기": a smaller
-cache is fewer bytes per decode step). The kernel decodes e4m3 exactly (every e4m3 value is a
-bf16 value), folds the K scales into the query and the V scales into the P·V weights, so the
-only extra rounding is of the scaled query and weights to bf16: the tolerance stays the library's
-|err| <= 2e-2 + 2e-2 |ref|.
+per-(row, kv-head) scale ("LLMSO - W4 - Optimization & Frameworks", §"2-4. 고급 KV 캐싱 기법":
+K per channel, V per token). The kernel decodes e4m3 exactly (every e4m3 value is an
+f16 value), folds the K scales into the query and the V scales into the P·V weights, and rounds
+those to f16 for the tensor cores (11 significant bits, finer than bf16's 8): the tolerance
+stays the library's |err| <= 2e-2 + 2e-2 |ref|.
 """
 import numpy as np
 import pytest

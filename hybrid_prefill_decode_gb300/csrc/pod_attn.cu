@@ -100,7 +100,8 @@ struct SmemCtl {
   uint64_t s_full[2];              // S buffer 0 / 1 computed
   uint64_t p_ready[2][2];          // [S buffer][group]: the group's P written (128 arrivals)
   uint64_t pv_done[2];             // P·V of P buffer 0 / 1 done (also frees V stage 0 / 1)
-  uint64_t dslot[kWarps][kDecodeSlots];  // decode rings, by absolute warp
+  uint64_t dslot[kWarps][kDecodeSlotsFp8];  // decode rings, by absolute warp (slots in use:
+                                            // kDecodeSlots on a bf16 cache, kDecodeSlotsFp8 on e4m3)
   uint32_t tmem_base;
   int abort;
   int item_kind[5];                // per slot: 0 = prefill, 1 = decode, 2-3 = the prefill slot's
@@ -1081,7 +1082,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 //
 // Each warp streams whole (block, kv-head) units: the K and V tiles (16 rows x 128 bytes each) by
 // TMA with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)) and the 16 V
-// scales by bulk copy, into a two-slot ring. The lanes read their MMA operands straight from the
+// scales by bulk copy, into a three-slot ring. The lanes read their MMA operands straight from the
 // tiles, in a channel order of their own that makes each read a contiguous 16-byte chunk and the
 // reads of a quarter-warp fall in distinct banks:
 //  * S = q' Kᵀ: in k-step ks, lane (g = lane / 4, t = lane % 4) holds channels 32t + 4ks .. +3
@@ -1090,9 +1091,9 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 //    2t+9; output row g (g + 8) of m-tile mt is channel 16g + 2mt (+ 1).
 constexpr int kFp8Tile = kBlockSize * 128;                          // 2 KiB: one K or V tile
 constexpr int kFp8Slot = 2 * kFp8Tile;                              // K then V (1 KiB-aligned)
-constexpr int kFp8Ring = kDecodeSlots * kFp8Slot;                   // 8 KiB per warp
-constexpr int kFp8ScaleBytes = kDecodeSlots * kBlockSize * 4;       // V scales of both slots
-constexpr int kFp8GroupBytes = 33 * 1024;  // 4 rings + 4 scale areas, rounded to 1 KiB
+constexpr int kFp8Ring = kDecodeSlotsFp8 * kFp8Slot;                // 12 KiB per warp
+constexpr int kFp8ScaleBytes = kDecodeSlotsFp8 * kBlockSize * 4;    // V scales of the slots
+constexpr int kFp8GroupBytes = 49 * 1024;  // 4 rings + 4 scale areas, rounded to 1 KiB
 constexpr int kFp8Groups = 4;              // warps 0-3, 4-7, 8-11 and the decode slot 12-15
 static_assert(kDecodeWarps * (kFp8Ring + kFp8ScaleBytes) <= kFp8GroupBytes, "FP8 group size");
 static_assert(2 * kMaxGroup * kMaxDecodeSplits + kMaxGroup <= kDecodeWarps * kFp8Ring / 4 &&
@@ -1149,8 +1150,8 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
 
   BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
   bt.init(lane);
-  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 2
-    const int slot = i & 1;
+  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 3
+    const int slot = i % kDecodeSlotsFp8;
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
@@ -1164,17 +1165,14 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
     bulk_load(smem_u32(vscales + slot * kBlockSize), p.v_scale + unit * kBlockSize,
               kBlockSize * 4, bar, policy_evict_first());
   };
-  {
-    const int ph0 = bt.at(0, lane), ph1 = bt.at(1, lane);
-    if (lane == 0) {
-      if (nmine > 0) issue(0, ph0);
-      if (nmine > 1) issue(1, ph1);
-    }
+#pragma unroll
+  for (int i = 0; i < kDecodeSlotsFp8; ++i) {
+    const int ph = bt.at(i, lane);
+    if (lane == 0 && nmine > i) issue(i, ph);
   }
   bool ok = true;
   const int kx[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};  // this lane's keys (S, P, V)
-  for (int i = 0; i < nmine; ++i) {
-    const int slot = i & 1;
+  for (int i = 0, slot = 0; i < nmine; ++i, slot = slot == kDecodeSlotsFp8 - 1 ? 0 : slot + 1) {
     // every lane takes the same exit, so the warp's shuffles below stay converged
     const bool got = mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc,
                                kSleepNs);
@@ -1239,10 +1237,10 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
 #pragma unroll
     for (int k = 0; k < 4; ++k) vsc[k] = vscales[slot * kBlockSize + kx[k]];
     __syncwarp();
-    // the slot is read: fetch the block after next while this one is computed
+    // the slot is read: refill it with the block kDecodeSlotsFp8 ahead
     {
-      const int ph = bt.at(i + 2, lane);
-      if (lane == 0 && i + 2 < nmine) issue(i + 2, ph);
+      const int ph = bt.at(i + kDecodeSlotsFp8, lane);
+      if (lane == 0 && i + kDecodeSlotsFp8 < nmine) issue(i + kDecodeSlotsFp8, ph);
     }
     if (nv < kBlockSize) {  // rows past the end may hold anything (even NaN): weight-0 V is 0
 #pragma unroll
@@ -1493,7 +1491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     }
     for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < kDecodeSlots; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);
+      for (int s = 0; s < kDecodeSlotsFp8; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);
     ctl->abort = 0;
     fence_barrier_init();
     prefetch_tmap(&tmk);

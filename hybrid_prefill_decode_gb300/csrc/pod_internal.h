@@ -32,7 +32,8 @@ constexpr int kPrefillThreads = 384;    // warps 0-11
 constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (column group 0: 4-7, 1: 8-11)
 constexpr int kDecodeWarp0 = 12;        // decode slot: warps 12-15
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp
+constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp (bf16 cache)
+constexpr int kDecodeSlotsFp8 = 3;      // ... on the e4m3 cache (half the bytes per block)
 
 // Prefill tile: 128 query rows = T tokens x hp query heads of one kv-head group (hp = the largest
 // power of two dividing the group size, T = 128 / hp; row r is token r / hp, head h0 + r % hp).
@@ -57,7 +58,7 @@ constexpr int kSmemScoresPerWarp = kMaxGroup * kBlockSize * 4;     // p exchange
 constexpr int kSmemDecodeOff = kSmemPrefill;                       // decode slot's region
 constexpr int kSmemScoresOff = kSmemDecodeOff + kSmemDecodeRing;   // its score exchange
 constexpr int kSmemCtlOff = kSmemScoresOff + kDecodeWarps * kSmemScoresPerWarp;
-constexpr int kSmemBarriers = 512;                                  // mbarriers + scalars
+constexpr int kSmemBarriers = 1024;                                 // mbarriers + scalars
 constexpr int kSmemTotal = kSmemCtlOff + kSmemBarriers;
 static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
 // the prefill slot's region also serves as the rings and score areas of its two decode slots

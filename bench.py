@@ -65,6 +65,17 @@ class L2Flush:
         self.r.max()
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks (the list itself for one process).
+    Every rank times the same work on its own GPU, so the job takes as long as its slowest rank."""
+    if not dist:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _workload_name(cfg, batch) -> str:
     from hybrid_prefill_decode_gb300 import workloads as W
     name = W.CONFIG_NAMES.get(cfg) or W.PROFILE_CASES[cfg][0]
@@ -366,12 +377,7 @@ def main():
         assert plans[v][0].device_status(plans[v][1]) == B.OK, v
 
     def agg(us_list):
-        mean = statistics.mean(us_list)
-        if dist:
-            t = torch.tensor([mean], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            mean = float(t.item())
-        return mean
+        return max_over_ranks([statistics.mean(us_list)], dist, dev)[0]
 
     us = {v: agg(results[v][0]) for v in variants}
     med = {v: statistics.median(results[v][0]) for v in variants}
@@ -510,7 +516,8 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
             B.run_batch(plans[v][i], b, ws[v], *outs[i], stream=stream, stream2=side)
             evs[i][1].record(stream)
         torch.cuda.synchronize()
-        times[v] = [a.elapsed_time(e) * 1e3 for a, e in evs]
+        # per iteration, the slowest rank's time
+        times[v] = max_over_ranks([a.elapsed_time(e) * 1e3 for a, e in evs], dist, dev)
         assert plans[v][-1].device_status(ws[v]) == B.OK, v
     if rank != 0:
         return
@@ -610,12 +617,7 @@ def run_fp8(args, dev, B, R, W, rank, world, dist):
         return [a.elapsed_time(b) * 1e3 for a, b in evs]
 
     def agg(xs):
-        mean = statistics.mean(xs)
-        if dist:
-            t = torch.tensor([mean], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            mean = float(t.item())
-        return mean
+        return max_over_ranks([statistics.mean(xs)], dist, dev)[0]
 
     for fn in (step8, step16):
         for _ in range(args.warmup):

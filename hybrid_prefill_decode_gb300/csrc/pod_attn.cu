@@ -1082,9 +1082,9 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 //
 // Each warp streams whole (block, kv-head) units: the K and V tiles (16 rows x 128 bytes each) by
 // TMA with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)) and the 16 V
-// scales by bulk copy, into a three-slot ring. The lanes read their MMA operands straight from the
-// tiles, in a channel order of their own that makes each read a contiguous 16-byte chunk and the
-// reads of a quarter-warp fall in distinct banks:
+// scales by bulk copy, into a ring of 3 slots (MHA) or 2 (GQA). The lanes read their MMA
+// operands straight from the tiles, in a channel order of their own that makes each read a
+// contiguous 16-byte chunk and the reads of a quarter-warp fall in distinct banks:
 //  * S = q' Kᵀ: in k-step ks, lane (g = lane / 4, t = lane % 4) holds channels 32t + 4ks .. +3
 //    of its key row(s) g (and g + 8) as the B fragment, and q' is permuted to match;
 //  * Oᵀ += Vᵀ Pᵀ: lane (g, t) holds channels 16g .. 16g + 15 of its four keys 2t, 2t+1, 2t+8,
@@ -1110,6 +1110,9 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
                               const int32_t* it, const DecodeCtx& dc, SmemCtl* ctl, PipeState& ps,
                               const WaitCtx& wc) {
   constexpr int kKS = 8;
+  // ring slots in use: three for MHA (one head per block: the least work per byte), two for GQA,
+  // where a third measured slower (more copies in flight than the memory system serves better)
+  constexpr int kSlots = GT == 1 ? kDecodeSlotsFp8 : 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wl = warp - dc.w0;
   const int d = it[1], g = it[2], kb = it[4], ke = it[5];
@@ -1150,8 +1153,8 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
 
   BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
   bt.init(lane);
-  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 3
-    const int slot = i % kDecodeSlotsFp8;
+  auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % kSlots
+    const int slot = i % kSlots;
     if (phys < 0 || phys >= p.num_blocks) {
       record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
       phys = 0;
@@ -1166,13 +1169,13 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
               kBlockSize * 4, bar, policy_evict_first());
   };
 #pragma unroll
-  for (int i = 0; i < kDecodeSlotsFp8; ++i) {
+  for (int i = 0; i < kSlots; ++i) {
     const int ph = bt.at(i, lane);
     if (lane == 0 && nmine > i) issue(i, ph);
   }
   bool ok = true;
   const int kx[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};  // this lane's keys (S, P, V)
-  for (int i = 0, slot = 0; i < nmine; ++i, slot = slot == kDecodeSlotsFp8 - 1 ? 0 : slot + 1) {
+  for (int i = 0, slot = 0; i < nmine; ++i, slot = slot == kSlots - 1 ? 0 : slot + 1) {
     // every lane takes the same exit, so the warp's shuffles below stay converged
     const bool got = mbar_wait(smem_u32(&ctl->dslot[warp][slot]), (ps.dphase >> slot) & 1, wc,
                                kSleepNs);
@@ -1237,10 +1240,10 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
 #pragma unroll
     for (int k = 0; k < 4; ++k) vsc[k] = vscales[slot * kBlockSize + kx[k]];
     __syncwarp();
-    // the slot is read: refill it with the block kDecodeSlotsFp8 ahead
+    // the slot is read: refill it with the block kSlots ahead
     {
-      const int ph = bt.at(i + kDecodeSlotsFp8, lane);
-      if (lane == 0 && i + kDecodeSlotsFp8 < nmine) issue(i + kDecodeSlotsFp8, ph);
+      const int ph = bt.at(i + kSlots, lane);
+      if (lane == 0 && i + kSlots < nmine) issue(i + kSlots, ph);
     }
     if (nv < kBlockSize) {  // rows past the end may hold anything (even NaN): weight-0 V is 0
 #pragma unroll

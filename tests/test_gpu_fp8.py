@@ -81,3 +81,15 @@ def test_fp8_pow2_scales_match_bf16_path():
     torch.cuda.synchronize()
     assert_close(out8, ref, "fp8 pow2")
     assert_close(out16, ref, "bf16 of the dequantised cache")
+
+
+def test_fp8_bad_block_index_is_reported_not_faulted():
+    fb = W.make_fp8_decode_batch(8, 2, [40, 300], seed=19)
+    fb.block_tables[1, 3] = 1 << 28         # inside the visible range of decode 1
+    dev = fb.to("cuda")
+    with pytest.raises(B.PodAttnError) as e:
+        B.decode_fp8(dev)
+    assert e.value.code == B.ERR_BAD_INDEX
+    # the context stays usable
+    ok = W.make_fp8_decode_batch(8, 2, [1, 17, 300], seed=5)
+    assert_close(B.decode_fp8(ok.to("cuda")), oracle.decode_fp8(ok), "fp8 after bad index")

@@ -3,19 +3,20 @@
 // One persistent kernel runs two kinds of virtual CTAs ("POD-Attention" digest, Silicon &
 // Systems, §"동시 실행만으로 부족한 이유" and §"가상 CTA와 SM별 균형"):
 //
-//  * prefill item — 128 query rows of one chunk and one query head against a range of keys:
-//    S = Q·Kᵀ and O += P·V on the tcgen05 tensor cores with S and O in TMEM, Q/K/V staged by TMA
-//    through the paged block table, causal mask and online softmax (running max m and sum l,
-//    rescale by 2^(m_old - m_new); "Week 6: Beyond PyTorch: Custom Kernel과 vLLM",
-//    §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를 줄이는 방향").
-//    Warps 0 and 2 issue TMA (Q and K / V), warps 1 and 3 issue the S and P·V MMAs, and two
-//    warpgroups (4-7, 8-11) do the softmax, one query row per thread and 64 of each step's 128
-//    keys per warpgroup.
+//  * prefill item — 128 query rows (128/hp tokens x hp heads of one kv-head group) of one chunk
+//    against a range of keys: S = Q·Kᵀ and O += P·V on the tcgen05 tensor cores with S and O in
+//    TMEM, Q/K/V staged by TMA through the paged block table, causal mask and online softmax
+//    (running max m and sum l, rescale by 2^(m_old - m_new); "Week 6: Beyond PyTorch: Custom
+//    Kernel과 vLLM", §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를
+//    줄이는 방향"). Warps 0 and 2 issue TMA (Q and K / V), warps 1 and 3 issue the S and P·V
+//    MMAs, and two warpgroups (4-7, 8-11) do the softmax, one query row per thread and 64 of
+//    each step's 128 keys per warpgroup, each with its own running max and O accumulator.
 //  * decode item — one sequence, one kv-head with its G query heads, a range of 16-row paged
-//    blocks: each warp streams its blocks into a private two-slot shared-memory ring with 4 KiB
-//    bulk copies, holds q in registers (4 dims per lane), reduces q·k across the warp with
-//    shuffles, and keeps an online softmax per head ("LLMSO - W4", §"FlashDecoding — decode 단계의
-//    병렬성 확보", §"KV 헤드 줄이기").
+//    blocks: each warp streams its blocks into a private two-slot shared-memory ring (4 KiB bulk
+//    copies for MHA, TMA boxes for GQA), keeps an online softmax per head, and reduces q·k with
+//    warp shuffles (MHA) or warp-level MMAs over the G heads (GQA) ("LLMSO - W4",
+//    §"FlashDecoding — decode 단계의 병렬성 확보", §"KV 헤드 줄이기"). Over an e4m3 cache
+//    (pod_attn_run_decode_fp8) every group size runs on f16 warp MMAs.
 //
 // One hardware CTA per SM runs a prefill slot and a decode slot side by side, each pulling
 // tickets from its own list, so both kinds share every SM (§"가상 CTA와 SM별 균형"); %smid is
@@ -99,7 +100,8 @@ struct SmemCtl {
   uint64_t v_full[kVStages];
   uint64_t s_full[2];              // S buffer 0 / 1 computed
   uint64_t p_ready[2][2];          // [S buffer][group]: the group's P written (128 arrivals)
-  uint64_t pv_done[2];             // P·V of P buffer 0 / 1 done (also frees V stage 0 / 1)
+  uint64_t pv_done[2];             // P·V of step n (S buffer n & 1) done (also frees V stage
+                                   // n & 1)
   uint64_t dslot[kWarps][kDecodeSlotsFp8];  // decode rings, by absolute warp (slots in use:
                                             // kDecodeSlots on a bf16 cache, kDecodeSlotsFp8 on e4m3)
   uint32_t tmem_base;

@@ -261,6 +261,9 @@ def main():
     ap.add_argument("--trace", default=None, choices=["a", "b"],
                     help="the 200-iteration hybrid-batching trace (mix a or b) instead of --config")
     ap.add_argument("--trace-iters", type=int, default=200)
+    ap.add_argument("--mix", action="store_true",
+                    help="diagnostic: one instrumented fused launch of --config; prints the per-SM "
+                         "prefill/decode mix from the kernel's own per-item records")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="decode attention over an FP8 (e4m3) cache: the decodes of --config, "
                          "with the bf16 cache of the same decodes timed beside it")
@@ -297,6 +300,9 @@ def main():
         return
     if args.kv_fp8:
         run_fp8(args, dev, B, R, W, rank, world, dist)
+        return
+    if args.mix:
+        run_mix(args, dev, B, W, rank)
         return
     batch = _make_batch(args, dev)
     work = R.batch_work(batch.num_q_heads, batch.num_kv_heads, batch.q_lens,
@@ -543,6 +549,52 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
            "speedup_vs_streams": sum(times["streams"]) / sum(times["fused"]),
            "mean_t_star_us": statistics.mean(tstar),
            "pool_gb": pool.k_pool.numel() * 4 / 1e9}
+    print(json.dumps(out), flush=True)
+
+
+def run_mix(args, dev, B, W, rank):
+    """--mix: the per-SM mix of one fused launch, from the per-item records the kernel writes
+    when the plan is instrumented (SM id, kind, start and end on the global timer). Cold L2 as
+    in the timed runs; a diagnostic line, not a benchmark value."""
+    import torch
+    if rank != 0:
+        return
+    batch = _make_batch(args, dev)
+    plan = B.Plan.for_batch(batch, instrument=True)
+    ws = plan.alloc_workspace(dev)
+    plan.upload(ws)
+    flush = L2Flush(dev)
+    for _ in range(max(3, args.warmup)):
+        B.run_batch(plan, batch, ws)
+    flush()
+    B.run_batch(plan, batch, ws)
+    torch.cuda.synchronize()
+    assert plan.device_status(ws) == B.OK
+    recs = plan.records(ws)
+    t0 = min(r["t_start"] for r in recs)
+    t1 = max(r["t_end"] for r in recs)
+    span = (t1 - t0) / 1e3
+    kinds = {}
+    busy = {}
+    end = {0: 0.0, 1: 0.0}
+    dur = {0: [], 1: []}
+    for r in recs:
+        kinds.setdefault(r["smid"], set()).add(r["kind"])
+        busy[r["cta"]] = busy.get(r["cta"], 0.0) + (r["t_end"] - r["t_start"]) / 1e3
+        end[r["kind"]] = max(end[r["kind"]], (r["t_end"] - t0) / 1e3)
+        dur[r["kind"]].append((r["t_end"] - r["t_start"]) / 1e3)
+    n_sm = len(kinds)
+    out = {"diagnostic": "per-SM prefill/decode mix of one fused launch (kernel records)",
+           "config": _config_dict(args, batch, 1),
+           "span_us": round(span, 1), "sms": n_sm,
+           "sms_with_both_kinds": sum(1 for v in kinds.values() if v == {0, 1}),
+           "sms_prefill_only": sum(1 for v in kinds.values() if v == {0}),
+           "sms_decode_only": sum(1 for v in kinds.values() if v == {1}),
+           "items": {"prefill": len(dur[0]), "decode": len(dur[1])},
+           "mean_item_us": {k: (round(statistics.mean(v), 1) if v else None)
+                            for k, v in (("prefill", dur[0]), ("decode", dur[1]))},
+           "last_item_end_us": {"prefill": round(end[0], 1), "decode": round(end[1], 1)},
+           "items_in_flight_per_cta": round(sum(busy.values()) / (span * max(1, len(busy))), 2)}
     print(json.dumps(out), flush=True)
 
 

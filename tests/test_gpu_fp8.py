@@ -93,3 +93,14 @@ def test_fp8_bad_block_index_is_reported_not_faulted():
     # the context stays usable
     ok = W.make_fp8_decode_batch(8, 2, [1, 17, 300], seed=5)
     assert_close(B.decode_fp8(ok.to("cuda")), oracle.decode_fp8(ok), "fp8 after bad index")
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_fp8_full_size_decodes_of_each_configuration(cfg):
+    """The decodes the benchmark times (--kv-fp8 --config cfg), in its launch configuration
+    (default plan, one launch), every output against the oracle."""
+    Hq, Hkv, _, _, dkv = W.config_lengths(cfg)
+    fb = W.make_fp8_decode_batch(Hq, Hkv, dkv, seed=cfg, device="cuda")
+    out = B.decode_fp8(fb)
+    torch.cuda.synchronize()
+    assert_close(out, oracle.decode_fp8(fb.to("cpu")), f"fp8 config {cfg}")

@@ -494,6 +494,31 @@ def make_fp8_decode_batch(num_q_heads: int, num_kv_heads: int, decode_kv_lens: S
                           b.block_tables, b.kv_lens, seed=seed)
 
 
+def fp8_append_case(num_q_heads: int, num_kv_heads: int, decode_kv_lens: Sequence[int],
+                    seed: int, device="cpu"):
+    """An FP8 decode batch whose newest row (position kv_len - 1) of every decode sequence and
+    kv-head is missing from the cache (K and V bytes 0x7F = e4m3 NaN, V scale NaN), plus those
+    rows in bf16 ([Nd][Hkv][D], the seeded batch's own values) to append. The K scales are those
+    of the whole pool, new rows included, as a serving stack that fixed them earlier would have.
+    Returns (batch, k_new, v_new)."""
+    b = make_batch(num_q_heads, num_kv_heads, [], [], list(decode_kv_lens), seed=seed,
+                   device=device)
+    fb = make_fp8_decode_batch(num_q_heads, num_kv_heads, decode_kv_lens, seed=seed,
+                               device=device)
+    Nd, Hkv, D = len(decode_kv_lens), num_kv_heads, b.head_dim
+    k_new = torch.empty((Nd, Hkv, D), dtype=torch.bfloat16, device=device)
+    v_new = torch.empty_like(k_new)
+    for d, L in enumerate(decode_kv_lens):
+        pos = L - 1
+        phys = int(b.block_tables[d, pos // 16])
+        k_new[d] = b.k_pool[phys, :, pos % 16]
+        v_new[d] = b.v_pool[phys, :, pos % 16]
+        fb.k8[phys, :, pos % 16] = 0x7F
+        fb.v8[phys, :, pos % 16] = 0x7F
+        fb.v_scale[phys, :, pos % 16] = float("nan")
+    return fb, k_new, v_new
+
+
 def dequantised_batch(fb: Fp8DecodeBatch) -> HybridBatch:
     """The bf16 decode batch holding the dequantised cache e4m3(bits) * scale, rounded to bf16
     (exact when the scales are powers of two)."""

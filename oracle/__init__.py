@@ -71,6 +71,10 @@ def _load():
             lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.oracle_decode_fp8.restype = I
             lib.oracle_decode_fp8.argtypes = [I, I, I, I, I, L, I, D, P, P, P, P, P, P, P, P]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_append_fp8.restype = I
+            lib.oracle_append_fp8.argtypes = [I, I, I, I, L, I, P, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -192,6 +196,32 @@ def merge(ms, ls, os_) -> np.ndarray:
 def e4m3_to_double(bits: int) -> float:
     """The value of one e4m3 bit pattern (see oracle.c)."""
     return float(_load().oracle_e4m3_to_double(int(bits) & 0xFF))
+
+
+def e4m3_from_float(x) -> int:
+    """The e4m3 code of a float32 value (round to nearest even, saturating; see oracle.c)."""
+    return int(_load().oracle_e4m3_from_float(float(x)))
+
+
+def append_fp8(batch, k_new, v_new):
+    """The FP8 cache of ``batch`` (an ``Fp8DecodeBatch``) after appending one token per decode
+    sequence (rows of bf16 k_new / v_new [Nd][Hkv][D]) at position kv_len - 1: returns new
+    (k8, v8, v_scale) numpy arrays; the inputs are not modified."""
+    k8 = np.array(batch.k8.cpu().numpy(), dtype=np.uint8, copy=True)
+    v8 = np.array(batch.v8.cpu().numpy(), dtype=np.uint8, copy=True)
+    vs = np.array(batch.v_scale.cpu().numpy(), dtype=np.float32, copy=True)
+    ks = np.ascontiguousarray(batch.k_scale.cpu().numpy(), dtype=np.float32)
+    kn, vn = _u16(k_new), _u16(v_new)
+    bt = _i32(batch.block_tables)
+    kv = _i32(batch.kv_lens)
+    Nd = int(kv.shape[0])
+    rc = _load().oracle_append_fp8(int(batch.num_kv_heads), int(batch.head_dim),
+                                   int(batch.block_size), Nd, int(k8.shape[0]),
+                                   int(bt.shape[1]) if bt.ndim == 2 else 0, _ptr(kn), _ptr(vn),
+                                   _ptr(ks), _ptr(bt), _ptr(kv), _ptr(k8), _ptr(v8), _ptr(vs))
+    if rc != 0:
+        raise ValueError(f"oracle_append_fp8 failed with code {rc}")
+    return k8, v8, vs
 
 
 def decode_fp8(batch):

@@ -304,6 +304,73 @@ double oracle_e4m3_to_double(uint8_t bits) {
 }
 
 /*
+ * e4m3 code of a float: the nearest e4m3 value, ties to the one with an even mantissa (round to
+ * nearest even), magnitudes from 448 up saturating to +-448, the sign kept (a negative value
+ * that rounds to zero is -0, 0x80), NaN to 0x7F. Written from the format's definition: the
+ * candidates are the 127 finite magnitudes oracle_e4m3_to_double gives for codes 0x00..0x7E.
+ */
+uint8_t oracle_e4m3_from_float(float x) {
+  if (x != x) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  int best = 0;
+  double best_d = a;  /* distance to code 0 (value 0) */
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double d = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+    /* codes ascend with their values, so an equal distance is a tie between neighbours: keep
+       the even mantissa */
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/*
+ * Append of one new token per decode sequence to an FP8 cache. The token's row goes to
+ * position kv_len - 1 of its sequence, through the block table. K row, channel c:
+ * e4m3((float)k / k_scale[g][c]); V row: scale = max_c |v| / 448 (1 when that max is 0), values
+ * e4m3((float)v / scale), the scale stored in v_scale. Every division and the max are
+ * binary32 (round to nearest), the precision the quantised codes are decided in. k_new / v_new
+ * are bf16 [Nd][Hkv][D]. Returns 0, or -1 on a bad table entry (that row is not written).
+ */
+int oracle_append_fp8(int Hkv, int D, int BS, int Nd, int64_t num_blocks, int max_blocks,
+                      const uint16_t* k_new, const uint16_t* v_new, const float* k_scale,
+                      const int32_t* block_tables, const int32_t* kv_lens, uint8_t* k8,
+                      uint8_t* v8, float* v_scale) {
+  int err = 0;
+  for (int d = 0; d < Nd; ++d) {
+    const int pos = kv_lens[d] - 1;
+    const int32_t phys = block_tables[(int64_t)d * max_blocks + pos / BS];
+    if (phys < 0 || phys >= num_blocks) {
+      err = -1;
+      continue;
+    }
+    for (int g = 0; g < Hkv; ++g) {
+      const int64_t row = ((int64_t)phys * Hkv + g) * BS + pos % BS;
+      const uint16_t* kr = k_new + ((int64_t)d * Hkv + g) * D;
+      const uint16_t* vr = v_new + ((int64_t)d * Hkv + g) * D;
+      float amax = 0.f;
+      for (int c = 0; c < D; ++c) {
+        const float v = (float)widen_bf16(vr[c]);
+        if (fabsf(v) > amax) amax = fabsf(v);
+      }
+      const float vs = amax > 0.f ? amax / 448.0f : 1.0f;
+      for (int c = 0; c < D; ++c) {
+        const float kq = (float)widen_bf16(kr[c]) / k_scale[g * D + c];
+        const float vq = (float)widen_bf16(vr[c]) / vs;
+        k8[row * D + c] = oracle_e4m3_from_float(kq);
+        v8[row * D + c] = oracle_e4m3_from_float(vq);
+      }
+      v_scale[row] = vs;
+    }
+  }
+  return err;
+}
+
+/*
  * Decode attention over an FP8 cache. K row j, channel c of kv-head g is
  * e4m3(k8[row j][c]) * k_scale[g][c] (one scale per kv-head and channel); V row j is
  * e4m3(v8[row j][c]) * v_scale[row j] (one scale per cached token and kv-head). Every decode

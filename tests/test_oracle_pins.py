@@ -351,3 +351,49 @@ def test_fp8_decode_zero_query_gives_mean_of_dequantised_rows():
         rows = torch.stack([v[int(bt[d, j // 16]), 0, j % 16] for j in range(L)])
         for h in range(2):
             assert np.abs(out[d, h] - rows.mean(dim=0).numpy()).max() <= 1e-12
+
+
+# ---- the FP8 (e4m3) append: quantising the iteration's new rows into the cache
+
+def test_e4m3_quantiser_round_trips_every_code_and_rounds_to_even():
+    for code in list(range(0x00, 0x7F)) + list(range(0x80, 0xFF)):
+        v = oracle.e4m3_to_double(code)
+        assert oracle.e4m3_from_float(np.float32(v)) == code, hex(code)
+    # midpoints between neighbours go to the even mantissa, both within a binade and across one
+    for lo in (0x38, 0x39, 0x3E, 0x07, 0x00, 0x76):
+        mid = (oracle.e4m3_to_double(lo) + oracle.e4m3_to_double(lo + 1)) / 2
+        want = lo if lo % 2 == 0 else lo + 1
+        assert oracle.e4m3_from_float(np.float32(mid)) == want, hex(lo)
+        assert oracle.e4m3_from_float(np.float32(-mid)) == (want | 0x80), hex(lo)
+    # saturation at 448, sign of zero kept, NaN
+    assert oracle.e4m3_from_float(448.0) == 0x7E and oracle.e4m3_from_float(1e9) == 0x7E
+    assert oracle.e4m3_from_float(-500.0) == 0xFE
+    assert oracle.e4m3_from_float(-1e-30) == 0x80 and oracle.e4m3_from_float(0.0) == 0x00
+    assert oracle.e4m3_from_float(float("nan")) == 0x7F
+
+
+def test_e4m3_quantiser_matches_torch_in_range():
+    g = torch.Generator().manual_seed(91)
+    x = (torch.randn(20000, generator=g) * torch.exp2(torch.randint(-12, 8, (20000,),
+                                                                     generator=g).float()))
+    x = x.clamp(-440.0, 440.0)
+    want = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    got = torch.tensor([oracle.e4m3_from_float(float(v)) for v in x], dtype=torch.uint8)
+    assert torch.equal(got, want)
+
+
+def test_fp8_append_rebuilds_the_quantised_rows():
+    """The seeded cache was quantised by torch from the same bf16 rows with the same rules
+    (binary32 division, V scale = row max / 448): appending those rows again must give back the
+    very bytes and scales that were removed, and touch nothing else."""
+    lens = [1, 16, 17, 300]
+    fb, k_new, v_new = W.fp8_append_case(8, 2, lens, seed=93)
+    full = W.make_fp8_decode_batch(8, 2, lens, seed=93)
+    k8, v8, vs = oracle.append_fp8(fb, k_new, v_new)
+    assert np.array_equal(k8, full.k8.numpy()) and np.array_equal(v8, full.v8.numpy())
+    same = np.isnan(full.v_scale.numpy()) == np.isnan(vs)
+    assert same.all() and np.array_equal(vs[~np.isnan(vs)], full.v_scale.numpy()[~np.isnan(vs)])
+    # and the decode over the appended cache equals the decode over the original one
+    fb.k8, fb.v8 = torch.from_numpy(k8), torch.from_numpy(v8)
+    fb.v_scale = torch.from_numpy(vs)
+    assert np.array_equal(oracle.decode_fp8(fb), oracle.decode_fp8(full))

@@ -102,6 +102,8 @@ def load():
     lib.pod_attn_run.argtypes = [P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
     lib.pod_attn_run_decode_fp8.restype = I32
     lib.pod_attn_run_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, P]
+    lib.pod_attn_append_fp8.restype = I32
+    lib.pod_attn_append_fp8.argtypes = [P, P, P, P, P, P, P, P, P, SZ, P]
     lib.pod_attn_plan_bucket.restype = I32
     lib.pod_attn_plan_bucket.argtypes = [P, ctypes.POINTER(Bucket)]
     lib.pod_attn_run_append.restype = I32
@@ -266,6 +268,15 @@ class Plan:
             _ptr(v_scale), _ptr(block_tables), _ptr(kv_lens), _ptr(o_decode),
             workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
         _check(code, "pod_attn_run_decode_fp8")
+
+    def append_fp8(self, k_new, v_new, k_pool8, v_pool8, k_scale, v_scale, block_tables,
+                   workspace, stream=None):
+        """pod_attn_append_fp8: quantise one new token per decode into the e4m3 cache."""
+        code = load().pod_attn_append_fp8(
+            self.handle, _ptr(k_new), _ptr(v_new), _ptr(k_pool8), _ptr(v_pool8), _ptr(k_scale),
+            _ptr(v_scale), _ptr(block_tables), workspace.data_ptr(), workspace.numel(),
+            _stream_ptr(stream))
+        _check(code, "pod_attn_append_fp8")
 
     def device_status(self, workspace, stream=None) -> int:
         return int(load().pod_attn_last_device_status(self.handle, workspace.data_ptr(),

@@ -1297,6 +1297,55 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
   return ok;
 }
 
+// Append of one new token per decode sequence to an e4m3 cache. One warp per (sequence,
+// kv-head), 4 channels per lane. K: e4m3(k / k_scale[g][c]); V: scale = max |v| / 448 over the
+// row (1 if 0), e4m3(v / scale). Divisions are IEEE binary32 (round to nearest), so the codes
+// are decided in the precision the format's reference quantiser uses.
+struct AppendFp8Args {
+  const uint16_t* k_new;  // bf16 [Nd][Hkv][128]
+  const uint16_t* v_new;
+  uint8_t* k8;            // e4m3 [NB][Hkv][16][128]
+  uint8_t* v8;
+  const float* k_scale;   // [Hkv][128]
+  float* v_scale;         // [NB][Hkv][16]
+  const int32_t* block_tables;
+  const int32_t* new_rows;  // (sequence, position) per new token
+  int32_t* status;
+  int n_new, Hkv, maxb, num_blocks;
+};
+
+__global__ void __launch_bounds__(256) append_fp8_kernel(const __grid_constant__ AppendFp8Args a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = a.n_new * a.Hkv;
+  for (int u = blockIdx.x * 8 + warp; u < units; u += gridDim.x * 8) {
+    const int tok = u / a.Hkv, g = u % a.Hkv;
+    const int seq = a.new_rows[2 * tok], pos = a.new_rows[2 * tok + 1];
+    const int phys = a.block_tables[(size_t)seq * a.maxb + pos / kBlockSize];
+    if (phys < 0 || phys >= a.num_blocks) {
+      if (lane == 0) record_error(a.status, POD_ATTN_ERR_BAD_INDEX);
+      continue;
+    }
+    const size_t row = ((size_t)phys * a.Hkv + g) * kBlockSize + pos % kBlockSize;
+    const size_t src = ((size_t)tok * a.Hkv + g) * 128 + lane * 4;
+    const uint2 kw = *reinterpret_cast<const uint2*>(a.k_new + src);
+    const uint2 vw = *reinterpret_cast<const uint2*>(a.v_new + src);
+    const float4 ks = *reinterpret_cast<const float4*>(a.k_scale + (size_t)g * 128 + lane * 4);
+    const float k[4] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y)};
+    const float v[4] = {bf16lo(vw.x), bf16hi(vw.x), bf16lo(vw.y), bf16hi(vw.y)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float vs = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const uint32_t kq = (uint32_t)e4m3x2_from_f32(__fdiv_rn(k[0], ks.x), __fdiv_rn(k[1], ks.y)) |
+                        ((uint32_t)e4m3x2_from_f32(__fdiv_rn(k[2], ks.z), __fdiv_rn(k[3], ks.w)) << 16);
+    const uint32_t vq = (uint32_t)e4m3x2_from_f32(__fdiv_rn(v[0], vs), __fdiv_rn(v[1], vs)) |
+                        ((uint32_t)e4m3x2_from_f32(__fdiv_rn(v[2], vs), __fdiv_rn(v[3], vs)) << 16);
+    *reinterpret_cast<uint32_t*>(a.k8 + row * 128 + lane * 4) = kq;
+    *reinterpret_cast<uint32_t*>(a.v8 + row * 128 + lane * 4) = vq;
+    if (lane == 0) a.v_scale[row] = vs;
+  }
+}
+
 // Combine the warps' states of a decode item, then write the output or the split's partial and,
 // for the last split of a unit to arrive, merge all partials.
 template <int GT, int HD, bool FP8>
@@ -2192,6 +2241,46 @@ pod_attn_status pod_attn_run_decode_fp8(pod_attn_plan_t plan, const void* q_deco
     cudaGetLastError();
     return POD_ATTN_ERR_CUDA;
   }
+  return POD_ATTN_OK;
+}
+
+pod_attn_status pod_attn_append_fp8(pod_attn_plan_t plan, const void* k_new, const void* v_new,
+                                    void* k_pool8, void* v_pool8, const float* d_k_scale,
+                                    float* d_v_scale, const int32_t* d_block_tables,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan) return POD_ATTN_ERR_INVALID_ARG;
+  pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
+  if (st != POD_ATTN_OK) return st;
+  const pod_attn_problem& pr = plan->prob;
+  if (!plan->opt.kv_fp8 || pr.num_prefill_seqs != 0 || pr.head_dim != kHeadDim)
+    return POD_ATTN_ERR_UNSUPPORTED;
+  const int n_new = pr.num_decode_seqs;
+  if (n_new == 0) return POD_ATTN_OK;
+  if (!k_new || !v_new || !k_pool8 || !v_pool8 || !d_k_scale || !d_v_scale || !d_block_tables)
+    return POD_ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+       reinterpret_cast<uintptr_t>(k_pool8) | reinterpret_cast<uintptr_t>(v_pool8) |
+       reinterpret_cast<uintptr_t>(d_k_scale) | reinterpret_cast<uintptr_t>(d_v_scale)) & 15)
+    return POD_ATTN_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AppendFp8Args a{};
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k8 = static_cast<uint8_t*>(k_pool8);
+  a.v8 = static_cast<uint8_t*>(v_pool8);
+  a.k_scale = d_k_scale;
+  a.v_scale = d_v_scale;
+  a.block_tables = d_block_tables;
+  a.new_rows = reinterpret_cast<const int32_t*>(ws + plan->ws.new_rows);
+  a.status = reinterpret_cast<int32_t*>(ws + plan->ws.status);
+  a.n_new = n_new;
+  a.Hkv = pr.num_kv_heads;
+  a.maxb = pr.max_blocks_per_seq;
+  a.num_blocks = pr.num_blocks;
+  const int units = n_new * pr.num_kv_heads;
+  const int grid = std::max(1, std::min(plan->num_sms * 4, (units + 7) / 8));
+  append_fp8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return POD_ATTN_ERR_CUDA;
   return POD_ATTN_OK;
 }
 

@@ -314,6 +314,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
   return r;
 }
+// Two floats as an e4m3 pair (low byte first): round to nearest even, saturating at +-448.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Largest finite f16.
 constexpr float kF16Max = 65504.f;
 // Two floats as an f16 pair (low half first), rounded to nearest even.

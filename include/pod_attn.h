@@ -254,6 +254,28 @@ pod_attn_status pod_attn_run_decode_fp8(pod_attn_plan_t plan, const void* q_deco
                                         void* o_decode, void* workspace, size_t workspace_bytes,
                                         void* stream);
 
+/* The iteration's KV append for an FP8 cache: one new token per decode sequence, written at
+ * position kv_len - 1 of its sequence (the plan's lengths) through the block tables, quantised to
+ * e4m3 ([LLMSO] §"2-4. 고급 KV 캐싱 기법": K per channel, V per token).
+ *   K row, channel c : e4m3(k / k_scale[g][c]) with the given per-(kv-head, channel) scales.
+ *   V row            : scale = max over the row's channels of |v| / 448 (1 when that max is 0),
+ *                      stored in v_scale at the row; values e4m3(v / scale).
+ *   Divisions are IEEE binary32 (round to nearest); e4m3 codes round to nearest even and
+ *   saturate at +-448.
+ *   plan            : a plan made with options.kv_fp8 set (decode work only, head_dim 128), whose
+ *                     work lists were uploaded to `workspace` (pod_attn_upload); else UNSUPPORTED.
+ *   k_new, v_new    : device bf16 [Nd][Hkv][128], 16-byte aligned, decode d's row at index d.
+ *   k_pool8, v_pool8: device uint8 [num_blocks][Hkv][16][128]; only the new rows are written.
+ *   d_k_scale       : device fp32 [Hkv][128], read only.
+ *   d_v_scale       : device fp32 [num_blocks][Hkv][16]; the new rows' entries are written.
+ * One small launch on `stream`, ahead of pod_attn_run_decode_fp8 on the same stream. A
+ * block-table entry outside the pool is reported as BAD_INDEX in the workspace status word
+ * (pod_attn_last_device_status), and that row is not written. */
+pod_attn_status pod_attn_append_fp8(pod_attn_plan_t plan, const void* k_new, const void* v_new,
+                                    void* k_pool8, void* v_pool8, const float* d_k_scale,
+                                    float* d_v_scale, const int32_t* d_block_tables,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, read and clear the device status word of `workspace`.
  * Returns OK, BAD_INDEX, TIMEOUT, or CUDA if the synchronisation itself failed. After
  * BAD_INDEX or TIMEOUT the outputs of that run are unspecified and the workspace must be

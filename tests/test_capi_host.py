@@ -375,3 +375,19 @@ def test_run_decode_fp8_validation(lib):
     assert code == B.ERR_INVALID_ARG
     code = lib.pod_attn_run_decode_fp8(d.handle, *([None] * 8), 257, big, None)
     assert code == B.ERR_WORKSPACE
+
+
+def test_append_fp8_validation(lib):
+    big = 1 << 40
+    p16 = B.Plan(4, 2, [], [7, 40], 2, 10, 4, 0.1, num_sms=148)          # bf16-cache plan
+    assert lib.pod_attn_append_fp8(p16.handle, *([None] * 7), 256, big, None) == B.ERR_UNSUPPORTED
+    pp = B.Plan(4, 2, [0, 5], [9, 7], 1, 10, 4, 0.1, num_sms=148, kv_fp8=True)  # has prefill
+    assert lib.pod_attn_append_fp8(pp.handle, *([None] * 7), 256, big, None) == B.ERR_UNSUPPORTED
+    d = B.Plan(4, 2, [], [7, 40], 2, 10, 4, 0.1, num_sms=148, kv_fp8=True)
+    assert lib.pod_attn_append_fp8(d.handle, *([None] * 7), 256, big, None) == B.ERR_INVALID_ARG
+    ptrs = [4096 * (i + 1) for i in range(7)]
+    ptrs[1] += 8                                                           # misaligned v_new
+    assert lib.pod_attn_append_fp8(d.handle, *ptrs, 256, big, None) == B.ERR_INVALID_ARG
+    assert lib.pod_attn_append_fp8(d.handle, *([None] * 7), 257, big, None) == B.ERR_WORKSPACE
+    empty = B.Plan(4, 2, [], [], 0, 1, 1, 0.1, num_sms=148, kv_fp8=True)  # nothing to append
+    assert lib.pod_attn_append_fp8(empty.handle, *([None] * 7), 256, big, None) == B.OK

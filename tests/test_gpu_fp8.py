@@ -104,3 +104,56 @@ def test_fp8_full_size_decodes_of_each_configuration(cfg):
     out = B.decode_fp8(fb)
     torch.cuda.synchronize()
     assert_close(out, oracle.decode_fp8(fb.to("cpu")), f"fp8 config {cfg}")
+
+
+def _append_plan(fb, **kw):
+    return B.Plan(fb.num_q_heads, fb.num_kv_heads, [], list(fb.decode_kv_lens),
+                  fb.num_decode_seqs, fb.num_blocks, fb.max_blocks_per_seq, fb.scale,
+                  kv_fp8=True, **kw)
+
+
+@pytest.mark.parametrize("hq,hkv,lens", [(8, 2, [1, 16, 17, 300]), (32, 8, [2047, 5, 64, 4096]),
+                                         (4, 4, [1, 2, 3])])
+def test_fp8_append_bit_exact_then_decode(hq, hkv, lens):
+    fb, k_new, v_new = W.fp8_append_case(hq, hkv, lens, seed=hq + hkv + len(lens))
+    want_k8, want_v8, want_vs = oracle.append_fp8(fb, k_new, v_new)
+    dev = fb.to("cuda")
+    plan = _append_plan(dev)
+    ws = plan.alloc_workspace()
+    plan.upload(ws)
+    plan.append_fp8(k_new.to("cuda"), v_new.to("cuda"), dev.k8, dev.v8, dev.k_scale, dev.v_scale,
+                    dev.block_tables, ws)
+    assert plan.device_status(ws) == B.OK
+    assert np.array_equal(dev.k8.cpu().numpy(), want_k8)
+    assert np.array_equal(dev.v8.cpu().numpy(), want_v8)
+    got_vs = dev.v_scale.cpu().numpy()
+    assert np.array_equal(np.isnan(got_vs), np.isnan(want_vs))
+    assert np.array_equal(got_vs[~np.isnan(got_vs)], want_vs[~np.isnan(want_vs)])
+    # the decode over the appended cache, against the oracle on the oracle-appended cache
+    ref_fb = fb.to("cpu")
+    ref_fb.k8, ref_fb.v8 = torch.from_numpy(want_k8), torch.from_numpy(want_v8)
+    ref_fb.v_scale = torch.from_numpy(want_vs)
+    out = torch.empty_like(dev.q_decode)
+    plan.run_decode_fp8(dev.q_decode, dev.k8, dev.v8, dev.k_scale, dev.v_scale,
+                        dev.block_tables, dev.kv_lens, out, ws)
+    assert plan.device_status(ws) == B.OK
+    assert_close(out, oracle.decode_fp8(ref_fb), "fp8 decode after append")
+
+
+def test_fp8_append_bad_block_index_is_reported():
+    fb, k_new, v_new = W.fp8_append_case(8, 2, [40, 300], seed=7)
+    fb.block_tables[1, 299 // 16] = -3          # the block of decode 1's new row
+    dev = fb.to("cuda")
+    before = dev.k8.clone()
+    plan = _append_plan(dev)
+    ws = plan.alloc_workspace()
+    plan.upload(ws)
+    plan.append_fp8(k_new.to("cuda"), v_new.to("cuda"), dev.k8, dev.v8, dev.k_scale, dev.v_scale,
+                    dev.block_tables, ws)
+    assert plan.device_status(ws) == B.ERR_BAD_INDEX
+    # decode 0's row was written, decode 1's was not (and nothing else changed)
+    changed = (dev.k8 != before).nonzero()
+    assert changed.numel() > 0
+    pos0 = 39
+    phys0 = int(fb.block_tables[0, pos0 // 16])
+    assert torch.all(changed[:, 0] == phys0) and torch.all(changed[:, 2] == pos0 % 16)

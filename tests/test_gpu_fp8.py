@@ -157,3 +157,24 @@ def test_fp8_append_bad_block_index_is_reported():
     pos0 = 39
     phys0 = int(fb.block_tables[0, pos0 // 16])
     assert torch.all(changed[:, 0] == phys0) and torch.all(changed[:, 2] == pos0 % 16)
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_fp8_random_batches(seed):
+    """Seeded random FP8 decode batches: group sizes 1-8 (3 included), ragged lengths, forced
+    or automatic splits, small SM counts."""
+    import random
+    rng = random.Random(seed)
+    Hkv = rng.choice([1, 2, 4])
+    Hq = Hkv * rng.choice([1, 2, 3, 4, 8])
+    lens = [rng.choice([1, rng.randint(2, 40), rng.randint(40, 3000)])
+            for _ in range(rng.choice([1, 3, 12, 30]))]
+    opts = {}
+    if rng.random() < 0.3:
+        opts["decode_splits"] = rng.choice([2, 7, 64])
+    if rng.random() < 0.3:
+        opts["num_sms"] = rng.choice([1, 5, 33])
+    fb = W.make_fp8_decode_batch(Hq, Hkv, lens, seed=500 + seed)
+    out = B.decode_fp8(fb.to("cuda"), **opts)
+    torch.cuda.synchronize()
+    assert_close(out, oracle.decode_fp8(fb), f"fp8 seed {seed}")

@@ -308,17 +308,14 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
       std::memcpy(&words_d[id * kItemWords], w, sizeof(w));
     }
   }
-  // longest first, ties in enumeration order: a stable counting sort over the few distinct
-  // costs (items of one split size share a cost)
+  // longest first, ties in enumeration order: a stable counting sort over the distinct costs
+  // (items of one split size share a cost)
   auto order = [](const std::vector<int64_t>& cost, const std::vector<int32_t>& words,
                   std::vector<int32_t>& out) {
     const size_t n = cost.size();
-    std::vector<int64_t> distinct;
-    for (size_t i = 0; i < n; ++i)  // few distinct values: a scan from the last one found
-      if (distinct.empty() || (distinct.back() != cost[i] &&
-                               std::find(distinct.begin(), distinct.end(), cost[i]) == distinct.end()))
-        distinct.push_back(cost[i]);
+    std::vector<int64_t> distinct(cost);  // the distinct costs, largest first
     std::sort(distinct.begin(), distinct.end(), std::greater<int64_t>());
+    distinct.erase(std::unique(distinct.begin(), distinct.end()), distinct.end());
     std::vector<size_t> start(distinct.size() + 1, 0);
     std::vector<uint32_t> bucket(n);
     for (size_t i = 0; i < n; ++i) {  // bucket = rank of the cost, largest first

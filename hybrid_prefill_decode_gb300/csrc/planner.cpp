@@ -6,23 +6,28 @@
 // count just above a multiple of what the SMs hold at once costs a whole extra wave.
 //
 // This file turns one hybrid batch into two work lists (virtual CTAs):
-//   prefill item = (chunk s, query tile t, block of hp query heads, KV split k) — a tile is
-//                  128 rows = 128/hp tokens x hp heads of one kv-head group, so every K/V tile
-//                  it loads serves hp heads
+//   prefill item = (chunk s, tile pair t, block of hp query heads, KV split k) — a tile is
+//                  128 rows = 128/hp tokens x hp heads of one kv-head group, and an item runs
+//                  two consecutive tiles, so every K/V tile it loads serves 2 x 128 rows
 //   decode item  = (sequence d, kv-head g, KV split k)   — one item serves all G query heads
 //                  of the kv-head (GQA grouping, "LLMSO - W4", §"KV 헤드 줄이기")
 // and sizes the persistent grid: one CTA per SM, each with a prefill slot and a decode slot
 // that pull items from the two lists.
 //
 // Split planning. Every item gets a cost (decode: 8 per 16-row K/V block, i.e. its bytes in
-// KiB; prefill: 57 per 128x128 step, its tensor-core time expressed in the same byte-time
-// units at a 6.8 TB/s : 1 PFLOP/s balance). With W the total cost and S the item slots, an
-// output whose cost exceeds W / (4 S) (prefill: also W_prefill / (4 x SMs), as only the SMs'
-// prefill slots run it) is split along the keys ("LLMSO - W4", §"FlashDecoding —
-// decode 단계의 병렬성 확보") into at most 64 (decode) or 8 (prefill) parts of at least
-// 12 blocks / 4 steps, so no single item can leave a long tail after the others finish. Items
-// are then ordered longest first. All arithmetic is integer, so the plan is reproducible bit
-// for bit.
+// KiB; prefill: 114 per 128-key step of its 256 rows, its tensor-core time expressed in the
+// same byte-time units at a 6.8 TB/s : 1 PFLOP/s balance). Outputs are split along the keys
+// ("LLMSO - W4", §"FlashDecoding — decode 단계의 병렬성 확보"), so no single item can leave a
+// long tail after the others finish:
+//  * prefill: one chunk size c (steps per item) for all outputs, c = ceil(longest / k) for
+//    k = 1..8 (at least 4 steps), the one that minimises the makespan of the items taken
+//    longest first by the SMs' prefill slots, each to the slot that frees first, with a fixed
+//    per-item overhead. A split count just past a multiple of the SMs costs a whole extra
+//    round of items (§"동시 실행만으로 부족한 이유"), which this model sees.
+//  * decode: with W the total cost and S the item slots, an output whose cost exceeds
+//    W / (4 S) is split into at most 64 parts of at least 12 blocks.
+// Items are then ordered longest first. All arithmetic is integer, so the plan is reproducible
+// bit for bit.
 //
 // Decode-only plans (no prefill work; the FP8-cache decode is one) know how many items run at
 // once: S = groups x SMs 4-warp decode groups (3 per SM on a bf16 cache, where the prefill
@@ -39,6 +44,7 @@
 #include <cstring>
 #include <functional>
 #include <numeric>
+#include <queue>
 
 #include "pod_internal.h"
 
@@ -46,9 +52,10 @@ namespace pod {
 namespace {
 
 constexpr int64_t kDecodeBlockCost = 8;   // 16 rows x (K + V) x 128 x bf16 = 8 KiB
-constexpr int64_t kPrefillTileCost = 57;  // 4*128*128*128 FLOPs at the byte-time balance
+constexpr int64_t kPrefillStepCost = 114;  // 2 x 4*128*128*128 FLOPs at the byte-time balance
 constexpr int kMinDecodeBlocksPerSplit = 12;
 constexpr int kMinPrefillTilesPerSplit = 4;
+constexpr int64_t kPrefillItemOverhead = 4;  // per-item start and epilogue, in steps
 constexpr int64_t kDecodeItemOverhead = 2;   // per-item start and merge, in warp block-times
 constexpr int kDecodeGroupsBf16 = 3;         // 4-warp decode groups per SM, bf16 cache
 constexpr int kDecodeGroupsFp8 = 4;          // ... e4m3 cache
@@ -99,6 +106,31 @@ int64_t decode_makespan(const std::vector<int64_t>& nblks, int64_t c, int64_t sl
   return span;
 }
 
+// Modelled makespan (in steps) of the prefill items that chunk size c makes of the outputs
+// `nts` on `slots` prefill slots taking them longest first, each to the slot that frees first
+// (list scheduling); an item costs its steps plus kPrefillItemOverhead.
+int64_t prefill_makespan(const std::vector<int64_t>& nts, int64_t c, int64_t slots,
+                         std::vector<int64_t>& costs) {
+  costs.clear();
+  for (int64_t n : nts) {
+    int64_t ns, ch;
+    rebalanced(n, c, &ns, &ch);
+    for (int64_t k = 0; k + 1 < ns; ++k) costs.push_back(ch + kPrefillItemOverhead);
+    costs.push_back(n - (ns - 1) * ch + kPrefillItemOverhead);
+  }
+  std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
+  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> freeat;
+  for (int64_t i = 0; i < slots; ++i) freeat.push(0);
+  int64_t span = 0;
+  for (int64_t x : costs) {
+    const int64_t t = freeat.top() + x;
+    freeat.pop();
+    freeat.push(t);
+    span = std::max(span, t);
+  }
+  return span;
+}
+
 }  // namespace
 
 pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, const int32_t* kv,
@@ -140,6 +172,7 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->group = G;
   const int hp = G & -G;  // largest power of two dividing G (G <= 8)
   const int tq = kTileM / hp;
+  const int64_t pair_tokens = 2 * tq;  // tokens of one prefill item (tiles A and B)
   plan->head_pack = hp;
   plan->tile_tokens = tq;
   plan->num_sms = num_sms;
@@ -161,13 +194,13 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
     pf += 4.0 * D * Hq * (double)(causal ? q * P + q * (q + 1) / 2 : q * L);
     pb += (double)L * row_bytes + 4.0 * q * Hq * D;
-    for (int64_t t = 0; t < ceil_div(q, tq); ++t) {
-      // causal: the tile's last token sees up to its own position; otherwise every row
-      const int64_t kend = causal ? P + std::min(q, (t + 1) * tq) : L;
+    for (int64_t t = 0; t < ceil_div(q, pair_tokens); ++t) {
+      // causal: the pair's last token sees up to its own position; otherwise every row
+      const int64_t kend = causal ? P + std::min(q, (t + 1) * pair_tokens) : L;
       const int64_t nt = ceil_div(kend, kTileN);
       for (int h0 = 0; h0 < Hq; h0 += hp) {
         pu.push_back({s, (int)t, h0, kend, nt});
-        total += nt * kPrefillTileCost;
+        total += nt * kPrefillStepCost;
       }
     }
   }
@@ -185,25 +218,43 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->est_decode_bytes = db;
   plan->est_decode_flops = df;
   const int64_t target = std::max<int64_t>(1, total / (slots * 4));
-  // prefill items run only on the prefill slots (one per SM): size them against that capacity
-  // too, so a prefill-heavy batch is not cut into more splits (each with a merge) than needed
-  int64_t total_p = 0;
-  for (const auto& x : pu) total_p += x.ntiles * kPrefillTileCost;
-  const int64_t target_p = std::max<int64_t>(target, total_p / ((int64_t)num_sms * 4));
 
   // ---- split and emit ----------------------------------------------------------------------
   // Items are written in enumeration order into flat arrays (cost, 8 words), then ordered
   // longest first; ties keep enumeration order (the sort key carries the item's index).
   struct Split { int64_t ns, chunk; };
+  // prefill: one chunk size (steps per item) for all outputs, the one whose items the SMs'
+  // prefill slots finish first in the model above; ties keep the larger chunk
+  int64_t chunk_p = 0;
+  if (!pu.empty() && opt.prefill_splits <= 0) {
+    std::vector<int64_t> nts(pu.size()), costs;
+    int64_t longest = 0;
+    for (size_t i = 0; i < pu.size(); ++i) {
+      nts[i] = pu[i].ntiles;
+      longest = std::max(longest, pu[i].ntiles);
+    }
+    int64_t best = -1, prev_c = -1;
+    for (int k = 1; k <= kMaxPrefillSplits; ++k) {
+      const int64_t c = ceil_div(longest, k);
+      if (c == prev_c) continue;
+      if (k > 1 && c < kMinPrefillTilesPerSplit) break;
+      prev_c = c;
+      const int64_t t = prefill_makespan(nts, c, num_sms, costs);
+      if (best < 0 || t < best) {
+        best = t;
+        chunk_p = c;
+      }
+    }
+  }
   auto split_p = [&](const PUnit& x) {
     int64_t ns;
-    if (opt.prefill_splits > 0) {
-      ns = opt.prefill_splits;
-    } else {
-      ns = ceil_div(x.ntiles * kPrefillTileCost, target_p);
-      ns = std::min<int64_t>(ns, std::max<int64_t>(1, x.ntiles / kMinPrefillTilesPerSplit));
+    if (chunk_p > 0) {
+      int64_t chunk;
+      rebalanced(x.ntiles, chunk_p, &ns, &chunk);
+      return Split{ns, chunk};
     }
-    ns = std::max<int64_t>(1, std::min<int64_t>({ns, x.ntiles, (int64_t)kMaxPrefillSplits}));
+    ns = std::max<int64_t>(1, std::min<int64_t>({opt.prefill_splits, x.ntiles,
+                                                  (int64_t)kMaxPrefillSplits}));
     const int64_t chunk = ceil_div(x.ntiles, ns);
     return Split{ceil_div(x.ntiles, chunk), chunk};
   };
@@ -290,7 +341,7 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int u = ns > 1 ? add_unit((int)ns, 0) : -1;
     for (int64_t k = 0; k < ns; ++k, ++ip) {
       const int64_t t0 = k * chunk, t1 = std::min(x.ntiles, (k + 1) * chunk);
-      cost_p[ip] = (t1 - t0) * kPrefillTileCost;
+      cost_p[ip] = (t1 - t0) * kPrefillStepCost;
       const int32_t w[kItemWords] = {0, x.s, x.t, x.h, (int32_t)(t0 * kTileN),
                                      (int32_t)std::min(x.kend, t1 * kTileN), u, (int32_t)k};
       std::memcpy(&words_p[ip * kItemWords], w, sizeof(w));
@@ -376,7 +427,7 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   w.new_rows = off;
   off = align256(off + plan->new_rows.size() * 4);
   w.partial_p = off;
-  off = align256(off + (size_t)p_slots * kPrefillSlotFloats * 4);
+  off = align256(off + (size_t)p_slots * kPrefillSlotBytes);
   w.partial_d = off;
   off = align256(off + (size_t)d_slots * decode_slot_floats(G) * 4);
   w.records = off;

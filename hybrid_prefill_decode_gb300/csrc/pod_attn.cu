@@ -3,14 +3,15 @@
 // One persistent kernel runs two kinds of virtual CTAs ("POD-Attention" digest, Silicon &
 // Systems, §"동시 실행만으로 부족한 이유" and §"가상 CTA와 SM별 균형"):
 //
-//  * prefill item — 128 query rows (128/hp tokens x hp heads of one kv-head group) of one chunk
-//    against a range of keys: S = Q·Kᵀ and O += P·V on the tcgen05 tensor cores with S and O in
-//    TMEM, Q/K/V staged by TMA through the paged block table, causal mask and online softmax
-//    (running max m and sum l, rescale by 2^(m_old - m_new); "Week 6: Beyond PyTorch: Custom
-//    Kernel과 vLLM", §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를
-//    줄이는 방향"). Warps 0 and 2 issue TMA (Q and K / V), warps 1 and 3 issue the S and P·V
-//    MMAs, and two warpgroups (4-7, 8-11) do the softmax, one query row per thread and 64 of
-//    each step's 128 keys per warpgroup, each with its own running max and O accumulator.
+//  * prefill item — two 128-row query tiles (each 128/hp tokens x hp heads of one kv-head
+//    group) of one chunk against a range of keys: S = Q·Kᵀ and O += P·V on the tcgen05 tensor
+//    cores with S and O in TMEM, Q/K/V staged by TMA through the paged block table, causal mask
+//    and online softmax (running max m and sum l, rescale by 2^(m_old - m_new); "Week 6: Beyond
+//    PyTorch: Custom Kernel과 vLLM", §"FlashAttention의 single-pass 트릭"; "LLMSO - W4",
+//    §"FlashAttention — I/O를 줄이는 방향"). Warp 0 issues TMA (Q, then K and V through one
+//    ring), warp 1 issues the MMAs of both tiles, alternating between them, and two warpgroups
+//    (4-7, 8-11) do the softmax of tile A and tile B, one query row per thread, so one tile's
+//    softmax runs while the tensor cores work on the other tile.
 //  * decode item — one sequence, one kv-head with its G query heads, a range of 16-row paged
 //    blocks: each warp streams its blocks into a private two-slot shared-memory ring (4 KiB bulk
 //    copies for MHA, TMA boxes for GQA), keeps an online softmax per head, and reduces q·k with
@@ -94,14 +95,12 @@ struct Params {
 };
 
 struct SmemCtl {
-  uint64_t q_full;                 // the query tile of a prefill item landed
-  uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];      // S of the stage's last step completed
-  uint64_t v_full[kVStages];
-  uint64_t s_full[2];              // S buffer 0 / 1 computed
-  uint64_t p_ready[2][2];          // [S buffer][group]: the group's P written (128 arrivals)
-  uint64_t pv_done[2];             // P·V of step n (S buffer n & 1) done (also frees V stage
-                                   // n & 1)
+  uint64_t q_full;                 // both query tiles of a prefill item landed
+  uint64_t kv_full[kKVStages];     // the ring stage holds its K or V tile
+  uint64_t kv_empty[kKVStages];    // both tiles' MMAs that read the stage completed
+  uint64_t s_full[2];              // [tile] S of the tile's step computed
+  uint64_t p_ready[2];             // [tile] the tile's P written (128 arrivals)
+  uint64_t o_done[2];              // [tile] the tile's last P·V of the item completed
   uint64_t dslot[kWarps][kDecodeSlotsFp8];  // decode rings, by absolute warp (slots in use:
                                             // kDecodeSlots on a bf16 cache, kDecodeSlotsFp8 on e4m3)
   uint32_t tmem_base;
@@ -116,7 +115,7 @@ static_assert(sizeof(SmemCtl) <= kSmemBarriers, "control block too big");
 struct PipeState {
   uint32_t q_cnt = 0;   // prefill items (query-tile loads)
   bool appended = false;  // this thread has seen the launch's KV append complete
-  uint32_t t_cnt = 0;   // 128-key steps whose S, P and P·V barriers have turned over
+  uint32_t t_cnt = 0;   // 128-key steps (K/V ring entries 2n, 2n + 1; S and P barriers)
   uint32_t dphase = 0;  // decode ring: one parity bit per slot of this warp
 };
 
@@ -189,430 +188,460 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 }
 
 // ============================================================================ prefill item
-// One prefill item: a 128-row query tile of a chunk, one head, a range of keys in 128-key
-// steps. Steps are numbered n by a counter that runs on across items; step n uses K/V stage and
-// S buffer n & 1. Two warps feed the tensor cores, whose instruction queue is only a few MMAs
-// deep: warp 1 issues S(j) as soon as P·V of step j-2 has released its buffer, warp 3 issues
-// each group's half of P·V(j) as soon as that group's P(j) is written, so one issuer's waits do
-// not idle the pipe. The two softmax warpgroups split each score tile by keys (64 each) and
-// never wait for each other inside the item: each keeps its own running max and sum per row
-// (rescaling its own O only when a score exceeds the max by more than 2^8, the lazy-rescale
-// threshold) and its own O accumulator; the two (m, l, O) of a row are merged once, in the
-// epilogue, as two splits of the row's keys are.
+// One prefill item: tiles A and B (two consecutive 128-row query tiles of one chunk and head
+// block) against a range of keys in 128-key steps. Steps are numbered n by a counter that runs
+// on across items; step n reads K(n) and V(n), entries 2n and 2n + 1 of one ring of kKVStages
+// tiles. Warp 0 loads; warp 1 issues both tiles' MMAs, each tile into its own S buffer and O
+// accumulator; warps 4-7 and 8-11 run the softmax of tile A and tile B, one query row per thread
+// and all 128 keys of a step. While one tile's softmax runs, the tensor cores work through the
+// other tile's P·V and next S, and every K/V tile brought into shared memory serves 256 query
+// rows. Each row keeps its running max m and sum l (log2 units);
+// O is rescaled only when the row's max grows by more than 2^8 (the lazy-rescale threshold),
+// and the epilogue divides by l.
 // HD (head dim) is 128 or 64; shared memory and TMEM keep the layout of 128 (a 64-dim head
 // uses the first 64-column half of every tile and the first 64 columns of O).
 template <int HD>
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
                              const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
                              SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
-  static_assert(kVStages == 2, "V stages and TMEM buffers are indexed by n & 1");
   static_assert(HD == 64 || HD == 128, "head dim");
   constexpr int kHalves = HD / 64;                  // 64-dim halves (128-byte swizzle atoms)
-  constexpr int kOG = HD / 2;                       // O columns of one softmax group
-  constexpr uint32_t kIdescPVh = idesc_bf16(kTileM, HD, 0, 1);  // O += P V, V N-major
+  constexpr uint32_t kIdescPV = idesc_bf16(kTileM, HD, 0, 1);  // O += P V, V N-major
   constexpr uint32_t kQBytes = kTileM * HD * 2, kTileBytes = kTileN * HD * 2;
+  constexpr uint32_t kBlockBytes = kBlockSize * HD * 2;
+  constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = it[1], t = it[2], h0 = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
-  const int g = h0 / p.G;  // the tile's heads h0 .. h0 + hp - 1 share kv-head g
+  const int g = h0 / p.G;  // the tiles' heads h0 .. h0 + hp - 1 share kv-head g
   const int q0 = p.cu_seqlens[s];
   const int qlen = p.cu_seqlens[s + 1] - q0;
   const int L = p.kv_lens[s];
   const int P = L - qlen;  // cached prefix rows before this chunk
   const int ntiles = (ke - kb + kTileN - 1) / kTileN;
+  const bool has_b = (2 * t + 1) * p.tq < qlen;  // tile B holds a token of the chunk
   const uint32_t n0 = ps.t_cnt;  // this item's first step
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sKring = sQ + kSmemQ;
-  const uint32_t sVring = sKring + kKStages * kSmemKTile;
+  const uint32_t sQ = smem_u32(smem);  // tile A's query rows, then tile B's
+  const uint32_t sRing = sQ + 2 * kSmemQ;
 
-  if (warp == 0 || warp == 2) {
-    // ------------------------------------------------------------------ TMA producers
-    // Warp 0 loads Q and the K tiles, warp 2 the V tiles. Lane i holds the block-table entry of
-    // block i of the next 4 steps (32 blocks): one coalesced read instead of a dependent global
-    // read per block. A K stage is free once the S that read it completed (k_empty); V stage
-    // n & 1 once P·V of step n-2 completed (pv_done, which the softmax also waits on).
-    const bool is_k = warp == 0;
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    // Lane i holds the block-table entry of block i of the next 4 steps (32 blocks): one
+    // coalesced read instead of a dependent global read per block. A stage is free once both
+    // tiles' MMAs that read it completed (kv_empty, two commits).
     const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
     const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
     const int blk0 = kb / kBlockSize;
-    constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
-    if (is_k && lane == 0) {
+    {
+      // box {64 dims, hp heads, tq tokens}: tile row r = token r / hp, head h0 + r % hp; tokens
+      // past the last chunk read as zeros. Lane 2x + hf copies half hf of tile x (one warp
+      // instruction issues all the copies).
       const uint32_t qbar = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qbar, kQBytes);
-      // box {64 dims, hp heads, tq tokens}: tile row r = token r / hp, head h0 + r % hp
-#pragma unroll
-      for (int hf = 0; hf < kHalves; ++hf)
-        tma_load_3d(sQ + hf * (kSmemQ / 2), tmq, qbar, 64 * hf, h0, q0 + t * p.tq);
+      if (lane == 0) mbar_arrive_expect_tx(qbar, 2 * kQBytes);
+      __syncwarp();
+      if (lane < 2 * kHalves) {
+        const int x = lane / kHalves, hf = lane % kHalves;
+        tma_load_3d(sQ + x * kSmemQ + hf * (kSmemQ / 2), tmq, qbar, 64 * hf, h0,
+                    q0 + (2 * t + x) * p.tq);
+      }
     }
-    uint64_t* free_bar = is_k ? ctl->k_empty : ctl->pv_done;
-    const uint32_t nst = is_k ? kKStages : kVStages;
-    uint64_t* full_bar = is_k ? ctl->k_full : ctl->v_full;
-    const uint32_t ring = is_k ? sKring : sVring;
-    const CUtensorMap* tm = is_k ? tmk : tmv;
-    // entries of the next group of 4 steps are requested one group ahead
-    auto bt_fetch = [&](int j4) -> int {
+    auto bt_fetch = [&](int j4) -> int {  // entries of steps j4 .. j4 + 3
       const int bi = j4 * kBlocksPerTile + lane;
       return bi < nblk_item ? bt_row[blk0 + bi] : -1;
     };
-    int bt_next = bt_fetch(0), btv = -1;
+    // K(j) and V(j) are ring entries 2n and 2n + 1 (stage e % kKVStages). Each stream keeps its
+    // own window of block-table entries (the one of its current 4 steps and the next).
+    int cur_k = -1, nxt_k = bt_fetch(0), win_k = -1;
+    int cur_v = -1, nxt_v = nxt_k, win_v = -1;
+    auto advance = [&](int& cur, int& nxt, int& win, int j) {
+      const int w = j >> 2;
+      if (w == win) return;
+      win = w;
+      const bool in_range = w * 4 * kBlocksPerTile + lane < nblk_item;
+      cur = nxt;
+      if ((w + 1) * 4 < ntiles) nxt = bt_fetch((w + 1) * 4);
+      if (in_range && (cur < 0 || cur >= p.num_blocks)) {
+        record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
+        cur = 0;
+      }
+      if (!in_range) cur = -1;
+    };
+    // Rows past the sequence end inside its last block may hold anything (even NaN); P is zero
+    // there but 0 * NaN is not. So when the item reads that block, this warp writes its V rows
+    // itself (the valid rows, then zeros) in the layout TMA's 128-byte swizzle gives.
+    const int tail_blk = ((L & 15) && ke > (L & ~15)) ? L / kBlockSize - blk0 : -1;
     // the chunk's own rows [P, P + qlen) may be appended by this launch
     int oka = 1;
     if (lane == 0 && ke > P) oka = wait_appended(p, ps, wc);
-    for (int j = 0; __shfl_sync(0xffffffffu, oka, 0) && j < ntiles; ++j) {
-      if ((j & 3) == 0) {
-        const bool in_range = j * kBlocksPerTile + lane < nblk_item;
-        btv = bt_next;
-        if (j + 4 < ntiles) bt_next = bt_fetch(j + 4);
-        if (in_range && (btv < 0 || btv >= p.num_blocks)) {
-          record_error(p.status, POD_ATTN_ERR_BAD_INDEX);
-          btv = 0;
-        }
-        if (!in_range) btv = -1;
-      }
-      int y[kBlocksPerTile];
+    for (int ei = 0; __shfl_sync(0xffffffffu, oka, 0) && ei < 2 * ntiles; ++ei) {
+      const int kv = ei & 1, j = ei >> 1;  // entry ei of the item: K(0), V(0), K(1), V(1), ...
+      if (kv) advance(cur_v, nxt_v, win_v, j);
+      else advance(cur_k, nxt_k, win_k, j);
+      const int cur = kv ? cur_v : cur_k;
+      // lane i copies block i / kHalves, half i % kHalves of the tile (one warp instruction
+      // issues all 8 x kHalves copies)
+      const int bl = (lane / kHalves) % kBlocksPerTile, hl = lane % kHalves;
+      const int el = __shfl_sync(0xffffffffu, cur, (j & 3) * kBlocksPerTile + bl);
+      const int yl = el < 0 ? p.pool_rows : (el * p.Hkv + g) * kBlockSize;  // past the pool: zeros
+      const uint32_t e = 2 * n0 + ei, stage = e % kKVStages;
+      int w = 1;
+      // completion e/3 - 1 of the stage's barrier (a fresh barrier passes); polled without a
+      // sleep hint, as a stage often frees while the next load is already due
+      if (lane == 0) w = mbar_wait(smem_u32(&ctl->kv_empty[stage]), ((e / kKVStages) & 1) ^ 1, wc);
+      if (!__shfl_sync(0xffffffffu, w, 0)) break;
+      const uint32_t dst = sRing + stage * kSmemKTile;
+      const int tb = kv == 1 ? tail_blk - j * kBlocksPerTile : -1;
+      const bool tail = tb >= 0 && tb < kBlocksPerTile;  // V's partly filled block is here
+      if (tail) {
+        const int r = L & 15;
+        const int yt = __shfl_sync(0xffffffffu, yl, tb * kHalves);  // the block's first row
+        const uint16_t* src = p.v_pool + (size_t)yt * HD;
+        uint8_t* base = smem + (dst - sQ) + tb * 2048;
 #pragma unroll
-      for (int b = 0; b < kBlocksPerTile; ++b) {
-        const int e = __shfl_sync(0xffffffffu, btv, (j & 3) * kBlocksPerTile + b);
-        y[b] = e < 0 ? p.pool_rows : (e * p.Hkv + g) * kBlockSize;  // past the pool: zeros
-      }
-      const uint32_t n = n0 + j;
-      const uint32_t stage = n % nst;
-      int okw = 1;
-      if (lane == 0)  // completion n/nst - 1 of the stage's barrier; a fresh barrier passes
-        okw = mbar_wait(smem_u32(&free_bar[stage]), ((n / nst) & 1) ^ 1, wc, kSleepNs);
-      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-      if (lane == 0) {
-        const uint32_t full = smem_u32(&full_bar[stage]);
-        const uint32_t dst = ring + stage * kSmemKTile;
-        mbar_arrive_expect_tx(full, kTileBytes);
-#pragma unroll
-        for (int b = 0; b < kBlocksPerTile; ++b)
-#pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf)
-            tma_load_2d(dst + hf * (kSmemKTile / 2) + b * 2048, tm, full, 64 * hf, y[b]);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ S issuer
-    // S(j) = Q K(j)ᵀ into S buffer n & 1, once P·V of step j-2 (which read the P written over
-    // that buffer) has completed.
-    const uint32_t tmem = ctl->tmem_base;
-    bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc, kSleepNs);
-    tc_fence_after();
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const uint32_t n = n0 + j;
-      // completion (n-2)/2 of pv_done[n & 1]; the steps before this item's first two are done
-      if (j >= 2 && !mbar_wait(smem_u32(&ctl->pv_done[n & 1]), ((n >> 1) & 1) ^ 1, wc)) {
-        ok = false;
-        break;
-      }
-      const uint32_t ks = n % kKStages;
-      if (!mbar_wait(smem_u32(&ctl->k_full[ks]), (n / kKStages) & 1, wc)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sK = sKring + ks * kSmemKTile;
-        const uint32_t dS = tmem + kTmemS + (n & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t half = kk >> 2, koff = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + half * (kSmemQ / 2) + koff, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + half * (kSmemKTile / 2) + koff, 16, 1024);
-          umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&ctl->s_full[n & 1]));
-        umma_commit(smem_u32(&ctl->k_empty[ks]));
-      }
-      __syncwarp();
-    }
-  } else if (warp == 3) {
-    // ------------------------------------------------------------------ P·V issuer
-    // O_g += P_g(j) V_g(j) for each group g (its 64 keys of the step) once that group has
-    // written P_g(j); one commit per step (pv_done) covers both halves.
-    const uint32_t tmem = ctl->tmem_base;
-    bool ok = true;
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const uint32_t n = n0 + j;
-      if (!mbar_wait(smem_u32(&ctl->v_full[n & 1]), (n >> 1) & 1, wc)) {
-        ok = false;
-        break;
-      }
-      const int tile0 = kb + j * kTileN;
-      if (tile0 < L && L < tile0 + kTileN && (L & 15)) {
-        // Rows past the sequence end inside its last block may hold anything (even NaN); P is
-        // zero there but 0 * NaN is not, so clear those V rows before the P·V product.
-        const int r0 = L - tile0, r1 = ((L + 15) & ~15) - tile0;
-        uint8_t* vbase = smem + (sVring - sQ) + (n & 1) * kSmemKTile;
-        for (int c = lane; c < (r1 - r0) * 8 * kHalves; c += 32) {  // 16-byte chunks
-          const int r = r0 + c / (8 * kHalves), half = (c >> 3) % kHalves, q16 = c & 7;
-          *reinterpret_cast<uint4*>(vbase + half * (kSmemKTile / 2) + r * 128 + q16 * 16) =
-              make_uint4(0, 0, 0, 0);
+        for (int c = lane; c < kBlockSize * 8 * kHalves; c += 32) {  // 16-byte chunks
+          const int i = c / (8 * kHalves), hf = (c >> 3) % kHalves, q16 = c & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (i < r) v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)i * HD + hf * 64) + q16);
+          *reinterpret_cast<uint4*>(base + hf * (kSmemKTile / 2) + i * 128 + ((q16 ^ (i & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
-      const uint32_t sV = sVring + (n & 1) * kSmemKTile;
-      const uint32_t aS = tmem + kTmemS + (n & 1) * 128;
+      const uint32_t full = smem_u32(&ctl->kv_full[stage]);
+      if (lane == 0) mbar_arrive_expect_tx(full, tail ? kTileBytes - kBlockBytes : kTileBytes);
+      __syncwarp();
+      if (lane < kBlocksPerTile * kHalves && !(tail && bl == tb))
+        tma_load_2d(dst + hl * (kSmemKTile / 2) + bl * 2048, kv == 0 ? tmk : tmv, full, 64 * hl, yl);
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    // One thread issues both tiles' MMAs in the order S_A(0), S_B(0), then per step j:
+    // P·V_A(j), S_A(j+1), P·V_B(j), S_B(j+1). The tensor cores run them in that order, so tile
+    // B settles half a period behind tile A: the MMAs of one tile run while the other tile's
+    // softmax does (two issuers would interleave their MMAs and keep the tiles in lockstep,
+    // both softmaxes idling the pipe at once). S_x(j+1) overwrites P_x(j) only after the P·V
+    // that reads it, as this thread issued them in that order. A tile B with no token of the
+    // chunk gets no MMAs but every commit and wait, so each barrier keeps its count.
+    const uint32_t tmem = ctl->tmem_base;
+    static_assert(kSmemQ == kSmemKTile, "Q and K tiles share one layout (and descriptor offsets)");
+    // A descriptor's start-address field is bits 0-13 of (address >> 4); the tiles lie within
+    // the first 256 KiB of shared memory, so a descriptor of (address + offset) is the
+    // descriptor of the address plus (offset >> 4), and each batch builds its two base
+    // descriptors once.
+    auto issue_s = [&](int x, uint32_t stK) {
+      if (x == 0 || has_b) {
+        const uint64_t ad0 = sdesc_sw128(sQ + x * kSmemQ, 16, 1024);
+        const uint64_t bd0 = sdesc_sw128(sRing + stK * kSmemKTile, 16, 1024);
+        const uint32_t dS = tmem + kTmemS + x * 128;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * (kSmemQ / 2) + (kk & 3) * 32) >> 4;
+          umma_ss(dS, ad0 + off, bd0 + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+      }
+      umma_commit(smem_u32(&ctl->s_full[x]));
+    };
+    auto issue_pv = [&](int x, uint32_t stV, bool first) {
+      if (x == 0 || has_b) {
+        // V is N-major: 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
+        const uint64_t bd0 = sdesc_sw128(sRing + stV * kSmemKTile, kSmemKTile / 2, 1024);
+        const uint32_t dS = tmem + kTmemS + x * 128, dO = tmem + kTmemO + x * 128;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 16kk.. at column 8kk of S
+          umma_ts(dO, dS + kk * 8, bd0 + (kk * 2048 >> 4), kIdescPV, (first && kk == 0) ? 0u : 1u);
+      }
+    };
+    bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc);
+    // K(0)
+    ok = ok && mbar_wait(smem_u32(&ctl->kv_full[(2 * n0) % kKVStages]), ((2 * n0) / kKVStages) & 1, wc);
+    tc_fence_after();
+    if (ok && lane == 0) {
+      const uint32_t stK = (2 * n0) % kKVStages;
+      issue_s(0, stK);
+      issue_s(1, stK);
+      umma_commit(smem_u32(&ctl->kv_empty[stK]));
+    }
+    __syncwarp();
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const uint32_t n = n0 + j;
+      const uint32_t stV = (2 * n + 1) % kKVStages;  // ring entries of V(j) and K(j+1)
+      const uint32_t stK = (2 * n + 2) % kKVStages;
 #pragma unroll 1
-      for (int grp = 0; grp < 2; ++grp) {
-        if (!mbar_wait(smem_u32(&ctl->p_ready[n & 1][grp]), (n >> 1) & 1, wc)) {
+      for (int x = 0; x < 2; ++x) {
+        if (!mbar_wait(smem_u32(&ctl->p_ready[x]), n & 1, wc) ||
+            (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stV]), ((2 * n + 1) / kKVStages) & 1, wc))) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // P of the group's keys 16kk.. at column 64 grp + 8kk of the S buffer; V is
-            // N-major: 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
-            const uint64_t bd = sdesc_sw128(sV + (grp * 4 + kk) * 2048, kSmemKTile / 2, 1024);
-            umma_ts(tmem + kTmemO + grp * 128, aS + grp * 64 + kk * 8, bd, kIdescPVh,
-                    (j == 0 && kk == 0) ? 0u : 1u);
-          }
+          issue_pv(x, stV, j == 0);
+          if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stV]));
+          if (j + 1 == ntiles) umma_commit(smem_u32(&ctl->o_done[x]));
+        }
+        __syncwarp();
+        if (j + 1 == ntiles) continue;
+        if (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stK]), ((2 * n + 2) / kKVStages) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(x, stK);
+          if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stK]));
         }
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(smem_u32(&ctl->pv_done[n & 1]));
-      __syncwarp();
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
     // ------------------------------------------------------------------ softmax (1 row/thread)
-    const int grp = (warp - kSoftmaxWarp0) >> 2;  // keys 64*grp .. 64*grp + 63 of each step
+    const int x = (warp - kSoftmaxWarp0) >> 2;  // tile
+    const bool act = x == 0 || has_b;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const int rp = x * kTileM + row;  // row of the item (partial slots)
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tOg = trow + kTmemO + grp * 128;  // this group's O accumulator
-    const int qi = t * p.tq + (row >> p.hp_log2);  // this row's token (index in the chunk)
-    const int h = h0 + (row & ((1 << p.hp_log2) - 1));  // and query head
+    const uint32_t tO = trow + kTmemO + x * 128;  // this tile's O accumulator
+    const uint32_t tS = trow + kTmemS + x * 128;  // and S buffer
+    const int qi = (2 * t + x) * p.tq + (row >> p.hp_log2);  // this row's token (in the chunk)
+    const int h = h0 + (row & ((1 << p.hp_log2) - 1));      // and query head
     const bool valid = qi < qlen;
     const int lim = p.causal ? min(P + qi + 1, ke) : ke;  // keys [.., lim) are visible
-    float m = -INFINITY, l = 0.f;  // this group's running max (log2 units) and sum of the row
+    float m = -INFINITY, l = 0.f;  // running max (log2 units) and sum of the row
     bool ok = true;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    for (int j = 0; j < ntiles; ++j) {
-      const uint32_t n = n0 + j;
-      const uint32_t tS = trow + kTmemS + (n & 1) * 128 + grp * 64;  // this group's 64 scores
-      // After a failed wait the loop still runs (every wait then fails at once), so that the
-      // warps pass the same barriers whatever happened.
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[n & 1]), (n >> 1) & 1, wc));
-      tc_fence_after();
-      const int vis = lim - (kb + j * kTileN) - grp * 64;  // visible columns: [0, vis)
-      const bool full = __all_sync(0xffffffffu, vis >= 64);
-      // the 64 scores stay in registers from the max to the exponentials
-      uint32_t sa[32], sb[32];
-      tmem_ld32(tS, sa);
-      tmem_ld32(tS + 32, sb);
-      tmem_ld_wait();
-      if (!full) {
+    // scores of columns [0, 64) visible below v (others -inf), then their max
+    auto mask64 = [&](uint32_t(&a)[32], uint32_t(&b)[32], int v) {
+      if (!__all_sync(0xffffffffu, v >= 64)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (c >= vis) sa[c] = f2u(-INFINITY);
-          if (c + 32 >= vis) sb[c] = f2u(-INFINITY);
+          if (c >= v) a[c] = f2u(-INFINITY);
+          if (c + 32 >= v) b[c] = f2u(-INFINITY);
         }
       }
+    };
+    auto max64 = [](const uint32_t(&a)[32], const uint32_t(&b)[32]) {
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmax3(u2f(sa[i]), u2f(sa[i + 8]), u2f(sa[i + 16]));
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(u2f(a[i]), u2f(a[i + 8]), u2f(a[i + 16]));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], u2f(sa[i + 24]), u2f(sb[i]));
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], u2f(a[i + 24]), u2f(b[i]));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], u2f(sb[i + 8]), u2f(sb[i + 16]));
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], u2f(b[i + 8]), u2f(b[i + 16]));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], u2f(sb[i + 24]));
-      const float mine = fmaxf(fmax3(mx[0], mx[1], mx[2]),
-                               fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
-      // scale > 0, so the max of the scaled scores is the scaled max
-      const float m_new = fmaxf(m, mine * p.scale_log2);
-      const bool resc = m_new > m + 8.f;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2(m - m_new);
-        m = m_new;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // O_g holds P·V of the earlier steps once step j-1's product completed (all before it
-        // completed first); at most one completion of that barrier is pending.
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done[(n - 1) & 1]),
-                                                     ((n - 1) >> 1) & 1, wc));
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < HD / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tOg + ch * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-          tmem_st32(tOg + ch * 32, o);
-        }
-        tmem_st_wait();
-      }
-      const float mref = m == -INFINITY ? 0.f : m;
-      const float2 nm2 = make_float2(-mref, -mref);
-      // exponentials, their sum, and P as bf16 pairs over the first 32 columns of the group's
-      // scores (all of which are in registers already)
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], u2f(b[i + 24]));
+      return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+    };
+    // exponentials of 64 scores against the reference max; P as bf16 pairs at columns
+    // [pc, pc + 32) of the S buffer; returns their sum
+    auto exp64 = [&](const uint32_t(&a)[32], const uint32_t(&b)[32], float2 nm2, uint32_t pc) {
       float2 sum[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const float2 xv = ffma2(make_float2(u2f(sa[2 * c]), u2f(sa[2 * c + 1])), c2, nm2);
+        const float2 xv = ffma2(make_float2(u2f(a[2 * c]), u2f(a[2 * c + 1])), c2, nm2);
         const float2 e = make_float2(ex2(xv.x), ex2(xv.y));
         sum[c & 3] = fadd2(sum[c & 3], e);
         pk[c] = pack_bf16x2(e.x, e.y);
       }
-      tmem_st16(tS, pk);
+      tmem_st16(tS + pc, pk);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const float2 xv = ffma2(make_float2(u2f(sb[2 * c]), u2f(sb[2 * c + 1])), c2, nm2);
+        const float2 xv = ffma2(make_float2(u2f(b[2 * c]), u2f(b[2 * c + 1])), c2, nm2);
         const float2 e = make_float2(ex2(xv.x), ex2(xv.y));
         sum[c & 3] = fadd2(sum[c & 3], e);
         pk[c] = pack_bf16x2(e.x, e.y);
       }
-      tmem_st16(tS + 16, pk);
+      tmem_st16(tS + pc + 16, pk);
       const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
-      l = l * alpha + (s01.x + s01.y);
-      tmem_st_wait();
+      return s01.x + s01.y;
+    };
+    for (int j = 0; j < ntiles; ++j) {
+      const uint32_t n = n0 + j;
+      // After a failed wait the loop still runs (every wait then fails at once), so that the
+      // warps pass the same barriers whatever happened.
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[x]), n & 1, wc));
+      tc_fence_after();
+      if (act) {
+        const int vis = lim - (kb + j * kTileN);  // visible columns of the step: [0, vis)
+        uint32_t sa[32], sb[32];
+        // the row max over keys 64..127, then over keys 0..63, which stay in registers
+        tmem_ld32(tS + 64, sa);
+        tmem_ld32(tS + 96, sb);
+        tmem_ld_wait();
+        mask64(sa, sb, vis - 64);
+        const float mx_hi = max64(sa, sb);
+        tmem_ld32(tS, sa);
+        tmem_ld32(tS + 32, sb);
+        tmem_ld_wait();
+        mask64(sa, sb, vis);
+        const float mine = fmaxf(mx_hi, max64(sa, sb));
+        // scale > 0, so the max of the scaled scores is the scaled max
+        const float m_new = fmaxf(m, mine * p.scale_log2);
+        const bool resc = m_new > m + 8.f;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m - m_new);
+          m = m_new;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // O holds P·V of the earlier steps: the commit that signalled this step's S covers
+          // every MMA its issuer issued before it
+#pragma unroll 1
+          for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(tO + ch * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+            tmem_st32(tO + ch * 32, o);
+          }
+          tmem_st_wait();
+        }
+        const float mref = m == -INFINITY ? 0.f : m;
+        const float2 nm2 = make_float2(-mref, -mref);
+        // P of keys 0..63 over columns 0..31 (those scores are in registers), then keys
+        // 64..127, read again, over columns 32..63 (one copy of the code: fewer live registers)
+        float sum = 0.f;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          if (hh) {
+            tmem_ld32(tS + 64, sa);
+            tmem_ld32(tS + 96, sb);
+            tmem_ld_wait();
+            mask64(sa, sb, vis - 64);
+          }
+          sum += exp64(sa, sb, nm2, hh * 32);
+        }
+        l = l * alpha + sum;
+        tmem_st_wait();
+      }
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->p_ready[n & 1][grp]));
+      mbar_arrive(smem_u32(&ctl->p_ready[x]));
     }
-    if (ok && ntiles > 0) {  // the last P·V; every S completed before the softmax that fed it
-      const uint32_t nl = n0 + ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[nl & 1]), (nl >> 1) & 1, wc));
+    if (ok && ntiles > 0) {  // the tile's last P·V (and with it every MMA of the item)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[x]), ps.q_cnt & 1, wc));
       tc_fence_after();
     }
     // ------------------------------------------------------------------ epilogue
-    // The two groups' (m, l) of a row meet through four columns of S buffer 0: every P·V of the
-    // item has completed, and the next item's S waits for the end-of-item barrier. Then the row
-    // is the merge of two key splits: m* = max(m_0, m_1), weights 2^(m_g - m*), and group g
-    // writes output columns [g HD/2, (g+1) HD/2) from both accumulators.
-    const uint32_t tX = trow + kTmemS;
-    tmem_st1(tX + 2 * grp, f2u(m));
-    tmem_st1(tX + 2 * grp + 1, f2u(l));
-    tmem_st_wait();
-    tc_fence_before();
-    named_bar_sync(2, 256);
-    tc_fence_after();
-    uint32_t mo_u = tmem_ld1(tX + 2 * (grp ^ 1));
-    uint32_t lo_u = tmem_ld1(tX + 2 * (grp ^ 1) + 1);
-    tmem_ld_wait();
-    reg_fence(mo_u);
-    reg_fence(lo_u);
-    const float m_o = u2f(mo_u), l_o = u2f(lo_u);
-    const float mm = fmaxf(m, m_o);
-    const float w_me = m == -INFINITY ? 0.f : ex2(m - mm);
-    const float w_ot = m_o == -INFINITY ? 0.f : ex2(m_o - mm);
-    const float lt = w_me * l + w_ot * l_o;
-    const float w0 = grp == 0 ? w_me : w_ot, w1 = grp == 0 ? w_ot : w_me;  // of O_0, O_1
-    const uint32_t tO0 = trow + kTmemO + grp * kOG, tO1 = tO0 + 128;  // this group's columns
-    {
-      if (unit < 0) {
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float f0 = w0 * inv, f1 = w1 * inv;
-        uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD + grp * kOG;
+    if (unit < 0) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD;
 #pragma unroll 1
-        for (int ch = 0; ch < kOG / 32; ++ch) {
-          uint32_t a[32], b[32];
-          tmem_ld32(tO0 + ch * 32, a);
-          tmem_ld32(tO1 + ch * 32, b);
-          tmem_ld_wait();
-          if (valid && ok) {
-            uint32_t w[16];
+      for (int ch = 0; ch < HD / 32; ++ch) {
+        uint32_t a[32];
+        tmem_ld32(tO + ch * 32, a);
+        tmem_ld_wait();
+        if (valid && ok) {
+          uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[i] = pack_bf16x2(u2f(a[2 * i]) * f0 + u2f(b[2 * i]) * f1,
-                                 u2f(a[2 * i + 1]) * f0 + u2f(b[2 * i + 1]) * f1);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(u2f(a[2 * i]) * inv, u2f(a[2 * i + 1]) * inv);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
-      } else {
-        const int nsplit = p.units[unit * kUnitWords + 0];
-        const int slot0 = p.units[unit * kUnitWords + 1];
-        float* slot = p.partial_p + (size_t)(slot0 + split) * kPrefillSlotFloats;
+      }
+    } else {
+      const int nsplit = p.units[unit * kUnitWords + 0];
+      const int slot0 = p.units[unit * kUnitWords + 1];
+      uint8_t* const slots = reinterpret_cast<uint8_t*>(p.partial_p);
+      uint8_t* slot = slots + (size_t)(slot0 + split) * kPrefillSlotBytes;
+      // The partial is O / l in bf16 (the final output's precision) with the row's m and l in
+      // fp32, written with streaming stores so that it does not push K/V tiles out of L2. O is
+      // stored in 8-column chunks interleaved across the 32 rows of a warp (chunk c of row rp at
+      // uint4 ((rp / 32) * 16 + c) * 32 + rp % 32), so that each store and each load of the
+      // merge moves 512 contiguous bytes per warp.
+      const size_t row_off = (size_t)(rp >> 5) * (kHeadDim / 8) * 32 + (rp & 31);
+      uint4* o8 = reinterpret_cast<uint4*>(slot) + row_off;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-        for (int ch = 0; ch < kOG / 32 && ok; ++ch) {
-          uint32_t a[32], b[32];
-          tmem_ld32(tO0 + ch * 32, a);
-          tmem_ld32(tO1 + ch * 32, b);
-          tmem_ld_wait();
-          // slot rows keep a stride of 128 columns whatever the head dim
-          float4* d4 = reinterpret_cast<float4*>(slot + row * kHeadDim + grp * kOG + ch * 32);
+      for (int ch = 0; ch < HD / 32 && ok; ++ch) {
+        uint32_t a[32];
+        tmem_ld32(tO + ch * 32, a);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(u2f(a[4 * i]) * w0 + u2f(b[4 * i]) * w1,
-                                u2f(a[4 * i + 1]) * w0 + u2f(b[4 * i + 1]) * w1,
-                                u2f(a[4 * i + 2]) * w0 + u2f(b[4 * i + 2]) * w1,
-                                u2f(a[4 * i + 3]) * w0 + u2f(b[4 * i + 3]) * w1);
-        }
-        if (grp == 0 && ok) {
-          slot[kTileM * kHeadDim + row] = mm;
-          slot[kTileM * kHeadDim + kTileM + row] = lt;
-        }
+        for (int i = 0; i < 4; ++i)
+          __stcs(o8 + (ch * 4 + i) * 32,
+                 make_uint4(pack_bf16x2(u2f(a[8 * i]) * inv_l, u2f(a[8 * i + 1]) * inv_l),
+                            pack_bf16x2(u2f(a[8 * i + 2]) * inv_l, u2f(a[8 * i + 3]) * inv_l),
+                            pack_bf16x2(u2f(a[8 * i + 4]) * inv_l, u2f(a[8 * i + 5]) * inv_l),
+                            pack_bf16x2(u2f(a[8 * i + 6]) * inv_l, u2f(a[8 * i + 7]) * inv_l)));
+      }
+      constexpr int kMlOff = kPairRows * kHeadDim * 2;  // m[256] then l[256], fp32
+      if (ok) {
+        float* ml = reinterpret_cast<float*>(slot + kMlOff);
+        __stcs(ml + rp, m);
+        __stcs(ml + kPairRows + rp, l);
+      }
+      __threadfence();
+      named_bar_sync(2, 256);
+      if (rp == 0) ctl->merge_last[0] = ok && (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+      named_bar_sync(2, 256);
+      if (ctl->merge_last[0] && ok) {
         __threadfence();
-        named_bar_sync(2, 256);
-        if (grp == 0 && row == 0)
-          ctl->merge_last[0] = ok && (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
-        named_bar_sync(2, 256);
-        if (ctl->merge_last[0] && ok) {
-          __threadfence();
-          if (valid) {
-            // the planner makes at most kMaxPrefillSplits splits; all loads of one pass are
-            // independent, so each pass costs one memory latency rather than one per split
-            const float* ml = p.partial_p + (size_t)slot0 * kPrefillSlotFloats + kTileM * kHeadDim;
-            float f[kMaxPrefillSplits];
-            float mx = -INFINITY;
+        if (valid) {
+          // the planner makes at most kMaxPrefillSplits splits; all loads of one pass are
+          // independent, so each pass costs one memory latency rather than one per split.
+          // Split k weighs 2^(m_k - m*) l_k (its O / l is stored).
+          const uint8_t* base = slots + (size_t)slot0 * kPrefillSlotBytes;
+          float f[kMaxPrefillSplits];
+          float mx = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < kMaxPrefillSplits; ++k) {
-              f[k] = k < nsplit ? __ldcg(ml + (size_t)k * kPrefillSlotFloats + row) : -INFINITY;
-              mx = fmaxf(mx, f[k]);
-            }
-            float den = 0.f;
+          for (int k = 0; k < kMaxPrefillSplits; ++k) {
+            f[k] = k < nsplit
+                       ? __ldcg(reinterpret_cast<const float*>(base + (size_t)k * kPrefillSlotBytes + kMlOff) + rp)
+                       : -INFINITY;
+            mx = fmaxf(mx, f[k]);
+          }
+          float den = 0.f;
 #pragma unroll
-            for (int k = 0; k < kMaxPrefillSplits; ++k) {
-              const float lk = k < nsplit ? __ldcg(ml + (size_t)k * kPrefillSlotFloats + kTileM + row) : 0.f;
-              f[k] = f[k] == -INFINITY ? 0.f : ex2(f[k] - mx);  // weight of split k
-              den += f[k] * lk;
-            }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD + grp * kOG;
-            const float* ob = p.partial_p + (size_t)slot0 * kPrefillSlotFloats + row * kHeadDim + grp * kOG;
+          for (int k = 0; k < kMaxPrefillSplits; ++k) {
+            const float lk =
+                k < nsplit ? __ldcg(reinterpret_cast<const float*>(base + (size_t)k * kPrefillSlotBytes + kMlOff) +
+                                    kPairRows + rp)
+                           : 0.f;
+            f[k] = f[k] == -INFINITY ? 0.f : ex2(f[k] - mx) * lk;  // weight of split k
+            den += f[k];
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD;
 #pragma unroll 1
-            for (int ch = 0; ch < kOG / 16; ++ch) {  // 16 columns at a time
-              float acc[16];
+          for (int ch = 0; ch < HD / 16; ++ch) {  // 16 columns (two chunks) at a time
+            float acc[16];
 #pragma unroll
-              for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+            for (int c = 0; c < 16; ++c) acc[c] = 0.f;
 #pragma unroll
-              for (int k = 0; k < kMaxPrefillSplits; ++k) {
-                if (k < nsplit) {
-                  const float4* src =
-                      reinterpret_cast<const float4*>(ob + (size_t)k * kPrefillSlotFloats + ch * 16);
-                  const float fk = f[k] * inv;
+            for (int k = 0; k < kMaxPrefillSplits; ++k) {
+              if (k < nsplit) {
+                const uint4* src = reinterpret_cast<const uint4*>(base + (size_t)k * kPrefillSlotBytes) +
+                                   row_off + (size_t)ch * 2 * 32;
+                const float fk = f[k] * inv;
 #pragma unroll
-                  for (int c = 0; c < 4; ++c) {
-                    const float4 v = __ldcg(src + c);
-                    acc[4 * c] += fk * v.x;
-                    acc[4 * c + 1] += fk * v.y;
-                    acc[4 * c + 2] += fk * v.z;
-                    acc[4 * c + 3] += fk * v.w;
+                for (int c = 0; c < 2; ++c) {
+                  const uint4 v = __ldcs(src + c * 32);
+#pragma unroll
+                  for (int w = 0; w < 4; ++w) {
+                    const uint32_t u = u4_word(v, w);
+                    acc[8 * c + 2 * w] += fk * bf16lo(u);
+                    acc[8 * c + 2 * w + 1] += fk * bf16hi(u);
                   }
                 }
               }
-              uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 16);
-#pragma unroll
-              for (int i = 0; i < 2; ++i)
-                d4[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
-                                   pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
-                                   pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
-                                   pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
             }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 16);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              d4[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
+                                 pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
+                                 pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
+                                 pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
           }
-          if (grp == 0 && row == 0) p.arrive[unit] = 0;  // ready for the next run
         }
+        if (rp == 0) p.arrive[unit] = 0;  // ready for the next run
       }
     }
     tc_fence_before();
@@ -932,6 +961,7 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
 
   BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
   bt.init(lane);
+  const uint64_t pol = policy_evict_first();  // decode K/V is read once: keep L2 for the rest
   auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % 2
     const int slot = i & 1;
     if (phys < 0 || phys >= p.num_blocks) {
@@ -944,8 +974,8 @@ __device__ bool decode_tc(const Params& p, const CUtensorMap* tmk, const CUtenso
     mbar_arrive_expect_tx(bar, 2 * kBlockSize * HD * 2);
 #pragma unroll
     for (int hf = 0; hf < kHalves; ++hf) {  // K at +0, V at +4 KiB; 64-dim halves 2 KiB apart
-      tma_load_2d(dst + hf * 2048, tmk, bar, 64 * hf, y);
-      tma_load_2d(dst + 4096 + hf * 2048, tmv, bar, 64 * hf, y);
+      tma_load_2d_hint(dst + hf * 2048, tmk, bar, 64 * hf, y, pol);
+      tma_load_2d_hint(dst + 4096 + hf * 2048, tmv, bar, 64 * hf, y, pol);
     }
   };
   {
@@ -1155,6 +1185,7 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
 
   BtWindow bt{bt_row + blk0 + wl, dc.nw, nmine};
   bt.init(lane);
+  const uint64_t pol = policy_evict_first();  // the cache is read once: keep L2 for the rest
   auto issue = [&](int i, int phys) {  // lane 0 only: block i of this warp into slot i % kSlots
     const int slot = i % kSlots;
     if (phys < 0 || phys >= p.num_blocks) {
@@ -1165,10 +1196,10 @@ __device__ bool decode_tc_fp8(const Params& p, const CUtensorMap* tmk, const CUt
     const uint32_t bar = smem_u32(&ctl->dslot[warp][slot]);
     const uint32_t dst = ring_s + slot * kFp8Slot;
     mbar_arrive_expect_tx(bar, kFp8Slot + kBlockSize * 4);
-    tma_load_2d(dst, tmk, bar, 0, (int)(unit * kBlockSize));
-    tma_load_2d(dst + kFp8Tile, tmv, bar, 0, (int)(unit * kBlockSize));
+    tma_load_2d_hint(dst, tmk, bar, 0, (int)(unit * kBlockSize), pol);
+    tma_load_2d_hint(dst + kFp8Tile, tmv, bar, 0, (int)(unit * kBlockSize), pol);
     bulk_load(smem_u32(vscales + slot * kBlockSize), p.v_scale + unit * kBlockSize,
-              kBlockSize * 4, bar, policy_evict_first());
+              kBlockSize * 4, bar, pol);
   };
 #pragma unroll
   for (int i = 0; i < kSlots; ++i) {
@@ -1533,16 +1564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(smem_u32(&ctl->q_full), 1);
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(smem_u32(&ctl->k_full[i]), 1);
-      mbar_init(smem_u32(&ctl->k_empty[i]), 1);
+    for (int i = 0; i < kKVStages; ++i) {
+      mbar_init(smem_u32(&ctl->kv_full[i]), 1);
+      mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
     }
-    for (int i = 0; i < kVStages; ++i) mbar_init(smem_u32(&ctl->v_full[i]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctl->p_ready[i][0]), 128);
-      mbar_init(smem_u32(&ctl->p_ready[i][1]), 128);
-      mbar_init(smem_u32(&ctl->pv_done[i]), 1);
+      mbar_init(smem_u32(&ctl->p_ready[i]), 128);
+      mbar_init(smem_u32(&ctl->o_done[i]), 1);
     }
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kDecodeSlotsFp8; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);

@@ -18,10 +18,11 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 
 // One persistent CTA per SM holds two concurrent virtual-CTA slots ("POD-Attention" digest,
 // §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
-//  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns — warp 0 issues
-//    the TMA loads of Q and K, warp 2 those of V, warps 1 and 3 issue the S and P·V tcgen05
-//    MMAs, and warps 4-7 and 8-11 are two softmax warpgroups that split each 128x128 score
-//    tile by keys (64 columns each), each with its own O accumulator;
+//  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns that runs two
+//    128-row query tiles (A and B) against each K/V tile — warp 0 issues the TMA loads of the
+//    query tiles and of one ring of K and V tiles, warp 1 issues the S and P·V tcgen05 MMAs of
+//    both tiles (alternating between them), and warps 4-7 and 8-11 are the softmax warpgroups
+//    of tile A and tile B (one query row per thread, all 128 keys of a step);
 //  * the decode slot (warps 12-15): decode items, on their own ticket loop.
 // Once the prefill list is drained, the prefill slot's warps 4-7 and 8-11 become two more
 // 4-warp decode slots. Every decode item thus runs on exactly 4 warps, whichever slot takes it,
@@ -29,7 +30,7 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPrefillThreads = 384;    // warps 0-11
-constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (column group 0: 4-7, 1: 8-11)
+constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (tile A: 4-7, tile B: 8-11)
 constexpr int kDecodeWarp0 = 12;        // decode slot: warps 12-15
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp (bf16 cache)
@@ -39,19 +40,21 @@ constexpr int kDecodeSlotsFp8 = 3;      // ... on the e4m3 cache (half the bytes
 // power of two dividing the group size, T = 128 / hp; row r is token r / hp, head h0 + r % hp).
 // All hp heads read the same K and V, so one K/V tile serves hp heads ("LLMSO - W4", §"KV 헤드
 // 줄이기": the heads of a group share their K/V).
-// Prefill step: one 128-row query tile x 128 keys. S and P are double-buffered in TMEM, so the
-// tensor cores compute S of the next steps while the softmax of this one runs; K stages
-// (step % kKStages) and V stages (step & 1) keep the loads ahead of both.
+// Prefill item: two consecutive tiles of one chunk and head block (tile A: tokens 2tT .. 2tT+T-1,
+// tile B: the next T), so every K/V tile staged in shared memory serves 256 query rows.
+// Prefill step: both tiles x 128 keys. Each tile has one S buffer in TMEM; while one tile's
+// softmax runs, the tensor cores compute the other tile's P·V and next S. K and V tiles share
+// one ring of kKVStages tiles, loaded in the order K(0), V(0), K(1), V(1), ...
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
+constexpr int kPairRows = 2 * kTileM;   // query rows of one prefill item
+constexpr int kKVStages = 3;
 
 // Shared-memory map (bytes from the dynamic shared-memory base, which the hardware places at
 // a 1024-byte boundary; the kernel checks this and reports an error otherwise).
 constexpr int kSmemQ = kTileM * kHeadDim * 2;                      // 32 KiB query tile
 constexpr int kSmemKTile = kTileN * kHeadDim * 2;                  // 32 KiB (K or V tile)
-constexpr int kSmemPrefill = kSmemQ + (kKStages + kVStages) * kSmemKTile;  // 160 KiB
+constexpr int kSmemPrefill = 2 * kSmemQ + kKVStages * kSmemKTile;  // 160 KiB
 constexpr int kSmemDecodeSlot = 2 * kBlockSize * kHeadDim * 2;     // 8 KiB (K block + V block)
 constexpr int kSmemDecodeRing = kDecodeWarps * kDecodeSlots * kSmemDecodeSlot;  // 64 KiB
 constexpr int kSmemScoresPerWarp = kMaxGroup * kBlockSize * 4;     // p exchange of one warp
@@ -65,19 +68,18 @@ static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
 static_assert(2 * (kSmemDecodeRing + kDecodeWarps * kSmemScoresPerWarp) <= kSmemPrefill,
               "the two decode slots of the prefill warps must fit the prefill region");
 
-// TMEM columns (the whole SM): one O accumulator per softmax warpgroup (fp32, 128 columns each:
-// group g sums P·V over its own 64 keys of every step, with its own running max and sum, and the
-// two are merged once per item) and two S buffers (fp32, 128 columns each). Group g writes its
-// P (bf16 pairs) over the first 32 of its own 64 columns of the S buffer it has just read, so S
-// of step j+2 is issued into that buffer once P·V of step j has completed.
+// TMEM columns (the whole SM): one O accumulator per tile (fp32, 128 columns each) and one S
+// buffer per tile (fp32, 128 columns each). A tile's softmax writes its P (bf16 pairs, 128 keys)
+// over the first 64 columns of the tile's S buffer; the tile's issuer issues S of the next step
+// into that buffer after the P·V that reads P (MMAs of one thread run in issue order).
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 0;      // + 128 * group
-constexpr int kTmemS = 256;    // + 128 * (step & 1)
+constexpr int kTmemO = 0;      // + 128 * tile
+constexpr int kTmemS = 256;    // + 128 * tile
 
 // Work item: kItemWords int32 words.
 //   [0] kind         0 = prefill, 1 = decode
 //   [1] seq          prefill: chunk index s in [0, Np); decode: d in [0, Nd)
-//   [2] tile / kvh   prefill: index t of the query tile (chunk tokens T t .. T t + T - 1, with
+//   [2] tile / kvh   prefill: index t of the tile pair (chunk tokens 2Tt .. 2Tt + 2T - 1, with
 //                    T = 128 / hp tokens per tile); decode: kv-head g
 //   [3] head         prefill: first query head h0 of the tile's hp heads; decode: 0
 //   [4] key_begin    first key row of this split (prefill: multiple of 128; decode: of 16)
@@ -95,8 +97,10 @@ constexpr int kMaxPrefillSplits = 8;
 // shared memory).
 constexpr int kMaxDecodeSplits = 64;
 
-// Partial-result slots: fp32 o[rows][128] then m[rows] then l[rows] (m, l in log2 units).
-constexpr int kPrefillSlotFloats = kTileM * (kHeadDim + 2);
+// Partial-result slots. A prefill slot holds the 256 rows of a tile pair (tile A's rows first):
+// O / l as bf16 [rows][128] (in 8-column chunks interleaved across each 32 rows), then fp32
+// m[rows] and l[rows] (m in log2 units). A decode slot: fp32 o[rows][128] then m[rows], l[rows].
+constexpr int kPrefillSlotBytes = kPairRows * kHeadDim * 2 + 2 * kPairRows * 4;
 #ifdef __CUDACC__
 __host__ __device__
 #endif

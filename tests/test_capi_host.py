@@ -108,6 +108,39 @@ def _rebalanced(nblk, c):
     return _cdiv(nblk, chunk), chunk
 
 
+def _list_span(costs, slots):
+    """Items taken longest first, each by the slot that frees first: the last finish time."""
+    free = [0] * slots
+    for x in sorted(costs, reverse=True):
+        i = min(range(slots), key=free.__getitem__)
+        free[i] += x
+    return max(free)
+
+
+def restated_prefill_chunk(nts, num_sms):
+    """Prefill: the chunk ceil(longest / k), k = 1..8, that minimises the makespan of the items
+    (steps + 4 each) taken longest first by one slot per SM, each going to the slot that frees
+    first; chunks under 4 steps are not tried (but k = 1 always is); ties keep the larger
+    chunk."""
+    longest = max(nts)
+    best, best_c, prev = None, 0, None
+    for k in range(1, 9):
+        c = _cdiv(longest, k)
+        if c == prev:
+            continue
+        if k > 1 and c < 4:
+            break
+        prev = c
+        items = []
+        for n in nts:
+            ns, ch = _rebalanced(n, c)
+            items += [min(n, (j + 1) * ch) - j * ch + 4 for j in range(ns)]
+        t = _list_span(items, num_sms)
+        if best is None or t < best:
+            best, best_c = t, c
+    return best_c
+
+
 def restated_decode_only_chunk(nblks, num_sms, kv_fp8):
     """Decode-only plans: the chunk ceil(longest / k), k in the divisor list, that minimises the
     wave-by-wave makespan over (3 or 4) x SMs groups of items costing ceil(blocks / 4) + 2;
@@ -134,32 +167,33 @@ def restated_decode_only_chunk(nblks, num_sms, kv_fp8):
 
 
 def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True, kv_fp8=False):
-    """Items: prefill = (chunk, query tile of 128/hp tokens x hp heads, first head, split) over
-    128-key steps (cost 57 each), with hp the largest power of two dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8 each); two
-    item slots per SM; split when an output costs more than a quarter of a slot's share."""
+    """Items: prefill = (chunk, pair of query tiles of 128/hp tokens x hp heads, first head,
+    split) over 128-key steps of both tiles (cost 114 each), with hp the largest power of two
+    dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8
+    each); two item slots per SM; split when an output costs more than a quarter of a slot's
+    share."""
     np_ = len(cu) - 1 if cu else 0
     slots = num_sms * 2
     G = Hq // Hkv
     hp = max(x for x in (1, 2, 4, 8) if G % x == 0)
-    tq = 128 // hp
+    pair = 2 * (128 // hp)                                        # tokens of one prefill item
     pu, du, total = [], [], 0
     for s in range(np_):
         q, L = cu[s + 1] - cu[s], kv[s]
         P = L - q
-        for t in range(_cdiv(q, tq)):
-            kend = P + min(q, (t + 1) * tq) if causal else L      # non-causal: every row
+        for t in range(_cdiv(q, pair)):
+            kend = P + min(q, (t + 1) * pair) if causal else L    # non-causal: every row
             nt = _cdiv(kend, 128)
             for h in range(0, Hq, hp):
                 pu.append((s, t, h, kend, nt))
-                total += nt * 57
+                total += nt * 114
     for d in range(nd):
         L = kv[np_ + d]
         for g in range(Hkv):
             du.append((d, g, L, _cdiv(L, 16)))
             total += _cdiv(L, 16) * 8
     target = max(1, total // (slots * 4))
-    total_p = sum(nt * 57 for *_, nt in pu)
-    target_p = max(target, total_p // (num_sms * 4))
+    chunk_p = restated_prefill_chunk([x[4] for x in pu], num_sms) if pu and not psplit else 0
     units, lp, ld = [], [], []
     slots_used = [0, 0]
 
@@ -170,17 +204,16 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
         return u
 
     for s, t, h, kend, nt in pu:
-        if psplit:
-            ns = psplit
+        if chunk_p:
+            ns, chunk = _rebalanced(nt, chunk_p)
         else:
-            ns = min(_cdiv(nt * 57, target_p), max(1, nt // 4))
-        ns = max(1, min(ns, nt, 8))
-        chunk = _cdiv(nt, ns)
-        ns = _cdiv(nt, chunk)
+            ns = max(1, min(psplit, nt, 8))
+            chunk = _cdiv(nt, ns)
+            ns = _cdiv(nt, chunk)
         u = add_unit(ns, 0) if ns > 1 else -1
         for k in range(ns):
             t0, t1 = k * chunk, min(nt, (k + 1) * chunk)
-            lp.append(((t1 - t0) * 57, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
+            lp.append(((t1 - t0) * 114, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
     chunk_do = (restated_decode_only_chunk([x[3] for x in du], num_sms, kv_fp8)
                 if not pu and du and not dsplit else 0)
     for d, g, L, nblk in du:
@@ -314,7 +347,7 @@ def test_planner_covers_every_key_once(lib, i):
     p = B.Plan(Hq, Hkv, cu, pkv + dkv, len(dkv), 10, _cdiv(max(pkv + dkv), 16), 0.1,
                num_sms=152)
     hp = max(x for x in (1, 2, 4, 8) if (Hq // Hkv) % x == 0)   # heads per prefill tile
-    tq = 128 // hp                                                # tokens per prefill tile
+    pair = 2 * (128 // hp)                                        # tokens per prefill item
     items_p, items_d, units = p.items()
     cover = {}
     for it in items_p + items_d:
@@ -334,10 +367,10 @@ def test_planner_covers_every_key_once(lib, i):
         else:
             t = key[2]
             q = q_lens[seq]
-            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * tq)
+            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * pair)
             assert key[3] % hp == 0
-    # every (query tile, block of hp heads) and (decode seq, kv-head) appears
-    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, tq) for q in q_lens) * (Hq // hp)
+    # every (tile pair, block of hp heads) and (decode seq, kv-head) appears
+    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, pair) for q in q_lens) * (Hq // hp)
     assert len([k for k in cover if k[0] == 1]) == len(dkv) * Hkv
 
 

@@ -100,6 +100,7 @@ struct SmemCtl {
   uint64_t kv_empty[kKVStages];    // both tiles' MMAs that read the stage completed
   uint64_t s_full[2];              // [tile] S of the tile's step computed
   uint64_t p_ready[2];             // [tile] the tile's P written (128 arrivals)
+  uint64_t pv_done[2];             // [tile] the tile's P·V of the step completed
   uint64_t o_done[2];              // [tile] the tile's last P·V of the item completed
   uint64_t dslot[kWarps][kDecodeSlotsFp8];  // decode rings, by absolute warp (slots in use:
                                             // kDecodeSlots on a bf16 cache, kDecodeSlotsFp8 on e4m3)
@@ -191,8 +192,8 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 // One prefill item: tiles A and B (two consecutive 128-row query tiles of one chunk and head
 // block) against a range of keys in 128-key steps. Steps are numbered n by a counter that runs
 // on across items; step n reads K(n) and V(n), entries 2n and 2n + 1 of one ring of kKVStages
-// tiles. Warp 0 loads; warp 1 issues both tiles' MMAs, each tile into its own S buffer and O
-// accumulator; warps 4-7 and 8-11 run the softmax of tile A and tile B, one query row per thread
+// tiles. Warp 0 loads; warp 1 issues both tiles' S MMAs and warp 3 their P·V MMAs, each tile
+// into its own S buffer and O accumulator; warps 4-7 and 8-11 run the softmax of tile A and tile B, one query row per thread
 // and all 128 keys of a step. While one tile's softmax runs, the tensor cores work through the
 // other tile's P·V and next S, and every K/V tile brought into shared memory serves 256 query
 // rows. Each row keeps its running max m and sum l (log2 units);
@@ -202,14 +203,18 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 // uses the first 64-column half of every tile and the first 64 columns of O).
 template <int HD>
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
-                             const CUtensorMap* tmv, const int32_t* it, uint8_t* smem,
-                             SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
+                             const CUtensorMap* tmv, const CUtensorMap* tmvb, const int32_t* it,
+                             uint8_t* smem, SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
   static_assert(HD == 64 || HD == 128, "head dim");
   constexpr int kHalves = HD / 64;                  // 64-dim halves (128-byte swizzle atoms)
   constexpr uint32_t kIdescPV = idesc_bf16(kTileM, HD, 0, 1);  // O += P V, V N-major
   constexpr uint32_t kQBytes = kTileM * HD * 2, kTileBytes = kTileN * HD * 2;
   constexpr uint32_t kBlockBytes = kBlockSize * HD * 2;
   constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
+  // V tiles are laid out block by block ([block][64-dim half][16 rows][128 bytes]), so that one
+  // box of the pool's per-block map brings a block's two halves; each P·V MMA reads one block.
+  // K tiles keep [half][128 keys][128 bytes]: an S MMA reads 16 dims of all 128 keys.
+  constexpr uint32_t kVBlockBytes = kBlockBytes;      // 4 KiB (head dim 128) or 2 KiB (64)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = it[1], t = it[2], h0 = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
   const int g = h0 / p.G;  // the tiles' heads h0 .. h0 + hp - 1 share kv-head g
@@ -277,9 +282,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       if (kv) advance(cur_v, nxt_v, win_v, j);
       else advance(cur_k, nxt_k, win_k, j);
       const int cur = kv ? cur_v : cur_k;
-      // lane i copies block i / kHalves, half i % kHalves of the tile (one warp instruction
-      // issues all 8 x kHalves copies)
-      const int bl = (lane / kHalves) % kBlocksPerTile, hl = lane % kHalves;
+      // K: lane i copies block i / kHalves, half i % kHalves of the tile; V: lane i copies block i
+      // (both halves in one box). One warp instruction issues all the copies.
+      const int bl = kv ? (lane % kBlocksPerTile) : (lane / kHalves) % kBlocksPerTile;
+      const int hl = lane % kHalves;
       const int el = __shfl_sync(0xffffffffu, cur, (j & 3) * kBlocksPerTile + bl);
       const int yl = el < 0 ? p.pool_rows : (el * p.Hkv + g) * kBlockSize;  // past the pool: zeros
       const uint32_t e = 2 * n0 + ei, stage = e % kKVStages;
@@ -293,15 +299,15 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const bool tail = tb >= 0 && tb < kBlocksPerTile;  // V's partly filled block is here
       if (tail) {
         const int r = L & 15;
-        const int yt = __shfl_sync(0xffffffffu, yl, tb * kHalves);  // the block's first row
+        const int yt = __shfl_sync(0xffffffffu, yl, tb);  // the block's first row
         const uint16_t* src = p.v_pool + (size_t)yt * HD;
-        uint8_t* base = smem + (dst - sQ) + tb * 2048;
+        uint8_t* base = smem + (dst - sQ) + tb * kVBlockBytes;
 #pragma unroll
         for (int c = lane; c < kBlockSize * 8 * kHalves; c += 32) {  // 16-byte chunks
           const int i = c / (8 * kHalves), hf = (c >> 3) % kHalves, q16 = c & 7;
           uint4 v = make_uint4(0, 0, 0, 0);
           if (i < r) v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)i * HD + hf * 64) + q16);
-          *reinterpret_cast<uint4*>(base + hf * (kSmemKTile / 2) + i * 128 + ((q16 ^ (i & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(base + hf * 2048 + i * 128 + ((q16 ^ (i & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -309,25 +315,30 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const uint32_t full = smem_u32(&ctl->kv_full[stage]);
       if (lane == 0) mbar_arrive_expect_tx(full, tail ? kTileBytes - kBlockBytes : kTileBytes);
       __syncwarp();
-      if (lane < kBlocksPerTile * kHalves && !(tail && bl == tb))
-        tma_load_2d(dst + hl * (kSmemKTile / 2) + bl * 2048, kv == 0 ? tmk : tmv, full, 64 * hl, yl);
+      if (kv == 0) {
+        if (lane < kBlocksPerTile * kHalves)
+          tma_load_2d(dst + hl * (kSmemKTile / 2) + bl * 2048, tmk, full, 64 * hl, yl);
+      } else if (lane < kBlocksPerTile && !(tail && bl == tb)) {
+        if constexpr (HD == 128) tma_load_3d(dst + bl * kVBlockBytes, tmvb, full, 0, yl, 0);
+        else tma_load_2d(dst + bl * kVBlockBytes, tmv, full, 0, yl);
+      }
       __syncwarp();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // One thread issues both tiles' MMAs in the order S_A(0), S_B(0), then per step j:
-    // P·V_A(j), S_A(j+1), P·V_B(j), S_B(j+1). The tensor cores run them in that order, so tile
-    // B settles half a period behind tile A: the MMAs of one tile run while the other tile's
-    // softmax does (two issuers would interleave their MMAs and keep the tiles in lockstep,
-    // both softmaxes idling the pipe at once). S_x(j+1) overwrites P_x(j) only after the P·V
-    // that reads it, as this thread issued them in that order. A tile B with no token of the
-    // chunk gets no MMAs but every commit and wait, so each barrier keeps its count.
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the S MMAs and warp 3 the P·V MMAs of both tiles, each in the order of
+    // the steps and, within a step, tile A first (a single thread issuing all of them runs out
+    // of issue rate before the tensor cores do). S_x(j+1) overwrites P_x(j), so it is issued
+    // once P·V_x(j) has completed (pv_done): tile B's P·V then runs while that wait and tile
+    // A's next softmax do, and the two tiles settle half a period apart. A tile B with no
+    // token of the chunk gets no MMAs but every commit and wait, so each barrier keeps its
+    // count.
     const uint32_t tmem = ctl->tmem_base;
     static_assert(kSmemQ == kSmemKTile, "Q and K tiles share one layout (and descriptor offsets)");
     // A descriptor's start-address field is bits 0-13 of (address >> 4); the tiles lie within
     // the first 256 KiB of shared memory, so a descriptor of (address + offset) is the
-    // descriptor of the address plus (offset >> 4), and each batch builds its two base
-    // descriptors once.
+    // descriptor of the address plus (offset >> 4), and each batch builds its base descriptors
+    // once.
     auto issue_s = [&](int x, uint32_t stK) {
       if (x == 0 || has_b) {
         const uint64_t ad0 = sdesc_sw128(sQ + x * kSmemQ, 16, 1024);
@@ -343,54 +354,73 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     };
     auto issue_pv = [&](int x, uint32_t stV, bool first) {
       if (x == 0 || has_b) {
-        // V is N-major: 64-column halves 16 KiB apart (LBO), 8-key groups 1 KiB apart (SBO)
-        const uint64_t bd0 = sdesc_sw128(sRing + stV * kSmemKTile, kSmemKTile / 2, 1024);
+        // V (block kk for keys 16kk..) is N-major: 64-column halves 2 KiB apart (LBO), 8-key
+        // groups 1 KiB apart (SBO); P of keys 16kk.. is at column 8kk of the S buffer
+        const uint64_t bd0 = sdesc_sw128(sRing + stV * kSmemKTile, 2048, 1024);
         const uint32_t dS = tmem + kTmemS + x * 128, dO = tmem + kTmemO + x * 128;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // P of keys 16kk.. at column 8kk of S
-          umma_ts(dO, dS + kk * 8, bd0 + (kk * 2048 >> 4), kIdescPV, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          umma_ts(dO, dS + kk * 8, bd0 + ((kk * kVBlockBytes) >> 4), kIdescPV,
+                  (first && kk == 0) ? 0u : 1u);
       }
+      umma_commit(smem_u32(&ctl->pv_done[x]));
     };
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc);
-    // K(0)
-    ok = ok && mbar_wait(smem_u32(&ctl->kv_full[(2 * n0) % kKVStages]), ((2 * n0) / kKVStages) & 1, wc);
-    tc_fence_after();
-    if (ok && lane == 0) {
-      const uint32_t stK = (2 * n0) % kKVStages;
-      issue_s(0, stK);
-      issue_s(1, stK);
-      umma_commit(smem_u32(&ctl->kv_empty[stK]));
-    }
-    __syncwarp();
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const uint32_t n = n0 + j;
-      const uint32_t stV = (2 * n + 1) % kKVStages;  // ring entries of V(j) and K(j+1)
-      const uint32_t stK = (2 * n + 2) % kKVStages;
+    if (warp == 1) {
+      // S of step 0 (its K is ring entry 2 n0), then S of step j + 1 once P·V of step j is done
+      ok = ok && mbar_wait(smem_u32(&ctl->kv_full[(2 * n0) % kKVStages]), ((2 * n0) / kKVStages) & 1, wc);
+      tc_fence_after();
+      if (ok && lane == 0) {
+        const uint32_t stK = (2 * n0) % kKVStages;
+        issue_s(0, stK);
+        issue_s(1, stK);
+        umma_commit(smem_u32(&ctl->kv_empty[stK]));
+      }
+      __syncwarp();
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const uint32_t n = n0 + j;
+        const uint32_t stK = (2 * n + 2) % kKVStages;  // ring entry of K(j+1)
 #pragma unroll 1
-      for (int x = 0; x < 2; ++x) {
-        if (!mbar_wait(smem_u32(&ctl->p_ready[x]), n & 1, wc) ||
-            (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stV]), ((2 * n + 1) / kKVStages) & 1, wc))) {
-          ok = false;
-          break;
+        for (int x = 0; x < 2; ++x) {
+          // every completion of pv_done is waited for, the last step's too, so the parity of
+          // the next item's first wait is unambiguous
+          if (!mbar_wait(smem_u32(&ctl->pv_done[x]), n & 1, wc)) {
+            ok = false;
+            break;
+          }
+          if (j + 1 == ntiles) continue;
+          if (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stK]), ((2 * n + 2) / kKVStages) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_s(x, stK);
+            if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stK]));
+          }
+          __syncwarp();
         }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv(x, stV, j == 0);
-          if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stV]));
-          if (j + 1 == ntiles) umma_commit(smem_u32(&ctl->o_done[x]));
+      }
+    } else {
+      // P·V of step j once its P is written and V(j) (ring entry 2n + 1) has landed
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const uint32_t n = n0 + j;
+        const uint32_t stV = (2 * n + 1) % kKVStages;
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+          if (!mbar_wait(smem_u32(&ctl->p_ready[x]), n & 1, wc) ||
+              (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stV]), ((2 * n + 1) / kKVStages) & 1, wc))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(x, stV, j == 0);
+            if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stV]));
+            if (j + 1 == ntiles) umma_commit(smem_u32(&ctl->o_done[x]));
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if (j + 1 == ntiles) continue;
-        if (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stK]), ((2 * n + 2) / kKVStages) & 1, wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_s(x, stK);
-          if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stK]));
-        }
-        __syncwarp();
       }
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
@@ -488,8 +518,8 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           m = m_new;
         }
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O holds P·V of the earlier steps: the commit that signalled this step's S covers
-          // every MMA its issuer issued before it
+          // O holds P·V of the earlier steps: this step's S was issued only after the tile's
+          // last P·V had completed
 #pragma unroll 1
           for (int ch = 0; ch < HD / 32; ++ch) {
             uint32_t o[32];
@@ -1552,7 +1582,8 @@ __device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUten
 template <int GT, int HD, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
-                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmvb) {
   extern __shared__ __align__(1024) uint8_t smem[];
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemCtlOff);
   if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte-aligned tiles
@@ -1571,6 +1602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
       mbar_init(smem_u32(&ctl->p_ready[i]), 128);
+      mbar_init(smem_u32(&ctl->pv_done[i]), 1);
       mbar_init(smem_u32(&ctl->o_done[i]), 1);
     }
     for (int w = 0; w < kWarps; ++w)
@@ -1579,7 +1611,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
-    if (use_tmem) prefetch_tmap(&tmq);
+    if (use_tmem) {
+      prefetch_tmap(&tmq);
+      prefetch_tmap(&tmvb);
+    }
   }
   if (use_tmem && warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -1616,7 +1651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
       if constexpr (!FP8)
-        prefill_item<HD>(p, &tmq, &tmk, &tmv, p.items_p + (size_t)idx * kItemWords, smem, ctl, ps, wc);
+        prefill_item<HD>(p, &tmq, &tmk, &tmv, &tmvb, p.items_p + (size_t)idx * kItemWords, smem, ctl,
+                         ps, wc);
       if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
     }
     if (handoff >= 0 && FP8) {
@@ -1712,7 +1748,7 @@ static EncodeTiledFn get_encode_fn() {
 
 struct CudaState {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  CUtensorMap tmq{}, tmk{}, tmv{};
+  CUtensorMap tmq{}, tmk{}, tmv{}, tmvb{};
   const void *kq = nullptr, *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
   CUtensorMap tmk8{}, tmv8{};                               // e4m3 pools (FP8 cache decode)
   const void *kk8 = nullptr, *kv8 = nullptr;
@@ -1745,6 +1781,21 @@ static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows, int hd) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// V pool (head dim 128) seen per paged block: 3-D {64 dims, row, 64-dim half} with the half
+// (128 bytes apart) as the outermost coordinate, so one box {64, 16, 2} is a block's 16 rows of
+// both halves, landing half by half ([half][row][64 dims]).
+static bool encode_pool_blocks(CUtensorMap* m, const void* pool, int64_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kBlockSize, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // e4m3 K or V pool: 2-D {byte, row}; one box is one paged block's 16 rows x 128 bytes.
 static bool encode_pool8(CUtensorMap* m, const void* pool, int64_t rows) {
   EncodeTiledFn enc = get_encode_fn();
@@ -1770,7 +1821,7 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
     attr_set.store(1);
   }
   if (!p.wait_append) {
-    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, tmk, tmv);
+    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, tmk, tmv, cs.tmvb);
     return cudaGetLastError();
   }
   // Items wait for every CTA's share of the append: a cooperative launch guarantees that all
@@ -1785,7 +1836,7 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, cs.tmq, tmk, tmv);
+  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, cs.tmq, tmk, tmv, cs.tmvb);
 }
 
 template <int HD>
@@ -2061,6 +2112,10 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   }
   if (cs->kv != v_pool) {
     if (!encode_pool(&cs->tmv, v_pool, pool_rows, pr.head_dim)) return POD_ATTN_ERR_CUDA;
+    // the prefill tiles' per-block view (head dim 128; a 64-dim head uses the 2-D map)
+    if (pr.head_dim == kHeadDim ? !encode_pool_blocks(&cs->tmvb, v_pool, pool_rows)
+                                : !encode_pool(&cs->tmvb, v_pool, pool_rows, pr.head_dim))
+      return POD_ATTN_ERR_CUDA;
     cs->kv = v_pool;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);

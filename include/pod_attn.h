@@ -104,8 +104,8 @@ typedef struct {
                                균형") */
   int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head), at most 64
                                (more are capped); 0 = auto */
-  int32_t prefill_splits;   /* force this many KV splits per prefill (tile, head block), at
-                               most 8; 0 = auto */
+  int32_t prefill_splits;   /* force this many KV splits per prefill (tile pair, head block),
+                               at most 8; 0 = auto */
   int32_t instrument;       /* nonzero: record (SM, kind, start, end) per work item */
   pod_attn_variant variant; /* launch variant, see above */
   int32_t non_causal;       /* nonzero: prefill chunk tokens attend to every row of their
@@ -122,8 +122,8 @@ typedef struct pod_attn_plan_s* pod_attn_plan_t;
 
 /* Summary of a plan (what the planner decided). */
 typedef struct {
-  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, 128-row tile = 128/hp tokens x hp
-                                 q-heads of one kv-head group, kv-split) */
+  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, pair of 128-row tiles, each
+                                 128/hp tokens x hp q-heads of one kv-head group, kv-split) */
   int32_t num_decode_items;   /* virtual decode CTAs: (seq, kv-head, kv-split) */
   int32_t num_units;          /* outputs assembled from more than one split */
   int32_t num_sms;            /* SM count the grid was sized for */

@@ -193,12 +193,12 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 // block) against a range of keys in 128-key steps. Steps are numbered n by a counter that runs
 // on across items; step n reads K(n) and V(n), entries 2n and 2n + 1 of one ring of kKVStages
 // tiles. Warp 0 loads; warp 1 issues both tiles' S MMAs and warp 3 their P·V MMAs, each tile
-// into its own S buffer and O accumulator; warps 4-7 and 8-11 run the softmax of tile A and tile B, one query row per thread
-// and all 128 keys of a step. While one tile's softmax runs, the tensor cores work through the
-// other tile's P·V and next S, and every K/V tile brought into shared memory serves 256 query
-// rows. Each row keeps its running max m and sum l (log2 units);
-// O is rescaled only when the row's max grows by more than 2^8 (the lazy-rescale threshold),
-// and the epilogue divides by l.
+// into its own S buffer and O accumulator; warps 4-7 and 8-11 run the softmax of tile A and
+// tile B, one query row per thread and all 128 keys of a step. While one tile's softmax runs,
+// the tensor cores work through the other tile's P·V and next S, and every K/V tile brought
+// into shared memory serves 256 query rows. Each row keeps its running max m and sum l (log2
+// units); O is rescaled only when the row's max grows by more than 2^8 (the lazy-rescale
+// threshold), and the epilogue divides by l.
 // HD (head dim) is 128 or 64; shared memory and TMEM keep the layout of 128 (a 64-dim head
 // uses the first 64-column half of every tile and the first 64 columns of O).
 template <int HD>
@@ -232,7 +232,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     // ------------------------------------------------------------------ TMA producer
     // Lane i holds the block-table entry of block i of the next 4 steps (32 blocks): one
     // coalesced read instead of a dependent global read per block. A stage is free once both
-    // tiles' MMAs that read it completed (kv_empty, two commits).
+    // tiles' MMAs that read it completed (kv_empty: one commit after the last of them).
     const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
     const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
     const int blk0 = kb / kBlockSize;

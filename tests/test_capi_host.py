@@ -424,3 +424,22 @@ def test_append_fp8_validation(lib):
     assert lib.pod_attn_append_fp8(d.handle, *([None] * 7), 257, big, None) == B.ERR_WORKSPACE
     empty = B.Plan(4, 2, [], [], 0, 1, 1, 0.1, num_sms=148, kv_fp8=True)  # nothing to append
     assert lib.pod_attn_append_fp8(empty.handle, *([None] * 7), 256, big, None) == B.OK
+
+
+@pytest.mark.parametrize("i,items,max_steps", [(2, 128, 16), (3, 128, 63), (4, 1024, 60)])
+def test_prefill_chunk_choice_on_configs(lib, i, items, max_steps):
+    """The prefill chunk rule's choice on the full-size configurations at 152 SMs: configs 2
+    and 3 keep their 128 tile-pair outputs whole; config 4 cuts its 256 outputs of ~232 steps
+    into 4 splits (1024 items of at most 60 steps), the count that measured fastest of 1-8
+    forced splits on the GB300."""
+    Hq, Hkv, q_lens, pkv, dkv = W.config_lengths(i)
+    cu = [0]
+    for q in q_lens:
+        cu.append(cu[-1] + q)
+    nb = sum(_cdiv(x, 16) for x in pkv + dkv) + 8
+    p = B.Plan(Hq, Hkv, cu, pkv + dkv, len(dkv), nb, _cdiv(max(pkv + dkv), 16), 0.1,
+               num_sms=152)
+    items_p, _, _ = p.items()
+    steps = [_cdiv(it[5] - it[4], 128) for it in items_p]
+    assert len(items_p) == items
+    assert max(steps) == max_steps

@@ -9,7 +9,7 @@
 //    and online softmax (running max m and sum l, rescale by 2^(m_old - m_new); "Week 6: Beyond
 //    PyTorch: Custom Kernel과 vLLM", §"FlashAttention의 single-pass 트릭"; "LLMSO - W4",
 //    §"FlashAttention — I/O를 줄이는 방향"). Warp 0 issues TMA (Q, then K and V through one
-//    ring), warp 1 issues the MMAs of both tiles, alternating between them, and two warpgroups
+//    ring), warp 1 issues the S MMAs and warp 3 the P·V MMAs of both tiles, and two warpgroups
 //    (4-7, 8-11) do the softmax of tile A and tile B, one query row per thread, so one tile's
 //    softmax runs while the tensor cores work on the other tile.
 //  * decode item — one sequence, one kv-head with its G query heads, a range of 16-row paged
@@ -99,7 +99,7 @@ struct SmemCtl {
   uint64_t kv_full[kKVStages];     // the ring stage holds its K or V tile
   uint64_t kv_empty[kKVStages];    // both tiles' MMAs that read the stage completed
   uint64_t s_full[2];              // [tile] S of the tile's step computed
-  uint64_t p_ready[2];             // [tile] the tile's P written (128 arrivals)
+  uint64_t p_ready[2];             // [tile] the tile's P written (one arrival per warp)
   uint64_t pv_done[2];             // [tile] the tile's P·V of the step completed
   uint64_t o_done[2];              // [tile] the tile's last P·V of the item completed
   uint64_t dslot[kWarps][kDecodeSlotsFp8];  // decode rings, by absolute warp (slots in use:
@@ -203,7 +203,8 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 // uses the first 64-column half of every tile and the first 64 columns of O).
 template <int HD>
 __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
-                             const CUtensorMap* tmv, const CUtensorMap* tmvb, const int32_t* it,
+                             const CUtensorMap* tmv, const CUtensorMap* tmkb,
+                             const CUtensorMap* tmvb, const int32_t* it,
                              uint8_t* smem, SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
   static_assert(HD == 64 || HD == 128, "head dim");
   constexpr int kHalves = HD / 64;                  // 64-dim halves (128-byte swizzle atoms)
@@ -211,10 +212,16 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   constexpr uint32_t kQBytes = kTileM * HD * 2, kTileBytes = kTileN * HD * 2;
   constexpr uint32_t kBlockBytes = kBlockSize * HD * 2;
   constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
-  // V tiles are laid out block by block ([block][64-dim half][16 rows][128 bytes]), so that one
-  // box of the pool's per-block map brings a block's two halves; each P·V MMA reads one block.
-  // K tiles keep [half][128 keys][128 bytes]: an S MMA reads 16 dims of all 128 keys.
+  // Both tiles are laid out block by block, so that one box of a per-block map brings all of a
+  // paged block (the TMA unit takes ~60 cycles per box, whatever its size):
+  //  * V: [block][64-dim half][16 rows][128 bytes]; each P·V MMA reads one block;
+  //  * K (head dim 128): [block][8-row group][64-dim half][8 rows][128 bytes], so that the 8-row
+  //    groups of one half lie 2 KiB apart throughout the tile and an S MMA reads 16 dims of all
+  //    128 keys with one descriptor (stride 2 KiB, the second half 1 KiB further on); with head
+  //    dim 64 a block is [16 rows][128 bytes] and the groups lie 1 KiB apart.
   constexpr uint32_t kVBlockBytes = kBlockBytes;      // 4 KiB (head dim 128) or 2 KiB (64)
+  constexpr uint32_t kKGroupStride = HD == 128 ? 2048 : 1024;  // 8-row groups of one K half
+  constexpr uint32_t kKHalfOff = 1024;                // second 64-dim half of a K group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = it[1], t = it[2], h0 = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
   const int g = h0 / p.G;  // the tiles' heads h0 .. h0 + hp - 1 share kv-head g
@@ -282,10 +289,9 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       if (kv) advance(cur_v, nxt_v, win_v, j);
       else advance(cur_k, nxt_k, win_k, j);
       const int cur = kv ? cur_v : cur_k;
-      // K: lane i copies block i / kHalves, half i % kHalves of the tile; V: lane i copies block i
-      // (both halves in one box). One warp instruction issues all the copies.
-      const int bl = kv ? (lane % kBlocksPerTile) : (lane / kHalves) % kBlocksPerTile;
-      const int hl = lane % kHalves;
+      // lane i copies block i of the tile (all of its dims in one box); one warp instruction
+      // issues all the copies
+      const int bl = lane % kBlocksPerTile;
       const int el = __shfl_sync(0xffffffffu, cur, (j & 3) * kBlocksPerTile + bl);
       const int yl = el < 0 ? p.pool_rows : (el * p.Hkv + g) * kBlockSize;  // past the pool: zeros
       const uint32_t e = 2 * n0 + ei, stage = e % kKVStages;
@@ -316,8 +322,11 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       if (lane == 0) mbar_arrive_expect_tx(full, tail ? kTileBytes - kBlockBytes : kTileBytes);
       __syncwarp();
       if (kv == 0) {
-        if (lane < kBlocksPerTile * kHalves)
-          tma_load_2d(dst + hl * (kSmemKTile / 2) + bl * 2048, tmk, full, 64 * hl, yl);
+        if (lane < kBlocksPerTile) {
+          // head dim 128: box {64 dims, 8 rows, 2 halves, 2 row groups}; 64: {64 dims, 16 rows}
+          if constexpr (HD == 128) tma_load_4d(dst + bl * kBlockBytes, tmkb, full, 0, 0, 0, yl / 8);
+          else tma_load_2d(dst + bl * kBlockBytes, tmk, full, 0, yl);
+        }
       } else if (lane < kBlocksPerTile && !(tail && bl == tb)) {
         if constexpr (HD == 128) tma_load_3d(dst + bl * kVBlockBytes, tmvb, full, 0, yl, 0);
         else tma_load_2d(dst + bl * kVBlockBytes, tmv, full, 0, yl);
@@ -334,20 +343,21 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     // token of the chunk gets no MMAs but every commit and wait, so each barrier keeps its
     // count.
     const uint32_t tmem = ctl->tmem_base;
-    static_assert(kSmemQ == kSmemKTile, "Q and K tiles share one layout (and descriptor offsets)");
     // A descriptor's start-address field is bits 0-13 of (address >> 4); the tiles lie within
     // the first 256 KiB of shared memory, so a descriptor of (address + offset) is the
     // descriptor of the address plus (offset >> 4), and each batch builds its base descriptors
-    // once.
+    // once. Q tiles are [half][128 rows][128 bytes] (8-row groups 1 KiB apart); K tiles are
+    // laid out by paged block (above).
     auto issue_s = [&](int x, uint32_t stK) {
       if (x == 0 || has_b) {
         const uint64_t ad0 = sdesc_sw128(sQ + x * kSmemQ, 16, 1024);
-        const uint64_t bd0 = sdesc_sw128(sRing + stK * kSmemKTile, 16, 1024);
+        const uint64_t bd0 = sdesc_sw128(sRing + stK * kSmemKTile, 16, kKGroupStride);
         const uint32_t dS = tmem + kTmemS + x * 128;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * (kSmemQ / 2) + (kk & 3) * 32) >> 4;
-          umma_ss(dS, ad0 + off, bd0 + off, kIdescS, kk > 0 ? 1u : 0u);
+          const uint32_t aoff = ((kk >> 2) * (kSmemQ / 2) + (kk & 3) * 32) >> 4;
+          const uint32_t boff = ((kk >> 2) * kKHalfOff + (kk & 3) * 32) >> 4;
+          umma_ss(dS, ad0 + aoff, bd0 + boff, kIdescS, kk > 0 ? 1u : 0u);
         }
       }
       umma_commit(smem_u32(&ctl->s_full[x]));
@@ -549,8 +559,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         l = l * alpha + sum;
         tmem_st_wait();
       }
+      // every lane's P stores have completed (tcgen05.wait::st above); one arrival per warp
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->p_ready[x]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_ready[x]));
     }
     if (ok && ntiles > 0) {  // the tile's last P·V (and with it every MMA of the item)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[x]), ps.q_cnt & 1, wc));
@@ -1583,6 +1595,7 @@ template <int GT, int HD, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmkb,
                     const __grid_constant__ CUtensorMap tmvb) {
   extern __shared__ __align__(1024) uint8_t smem[];
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemCtlOff);
@@ -1601,7 +1614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctl->p_ready[i]), 128);
+      mbar_init(smem_u32(&ctl->p_ready[i]), 4);
       mbar_init(smem_u32(&ctl->pv_done[i]), 1);
       mbar_init(smem_u32(&ctl->o_done[i]), 1);
     }
@@ -1613,6 +1626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmv);
     if (use_tmem) {
       prefetch_tmap(&tmq);
+      prefetch_tmap(&tmkb);
       prefetch_tmap(&tmvb);
     }
   }
@@ -1651,7 +1665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
       if constexpr (!FP8)
-        prefill_item<HD>(p, &tmq, &tmk, &tmv, &tmvb, p.items_p + (size_t)idx * kItemWords, smem, ctl,
+        prefill_item<HD>(p, &tmq, &tmk, &tmv, &tmkb, &tmvb, p.items_p + (size_t)idx * kItemWords, smem, ctl,
                          ps, wc);
       if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
     }
@@ -1748,7 +1762,7 @@ static EncodeTiledFn get_encode_fn() {
 
 struct CudaState {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  CUtensorMap tmq{}, tmk{}, tmv{}, tmvb{};
+  CUtensorMap tmq{}, tmk{}, tmv{}, tmkb{}, tmvb{};
   const void *kq = nullptr, *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
   CUtensorMap tmk8{}, tmv8{};                               // e4m3 pools (FP8 cache decode)
   const void *kk8 = nullptr, *kv8 = nullptr;
@@ -1796,6 +1810,21 @@ static bool encode_pool_blocks(CUtensorMap* m, const void* pool, int64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K pool (head dim 128) seen per paged block for the prefill tiles: 4-D {64 dims, row within an
+// 8-row group, 64-dim half, 8-row group} (strides 256, 128 and 2048 bytes), so one box
+// {64, 8, 2, 2} is a block's 16 rows of both halves, landing as [group][half][8 rows][64 dims].
+static bool encode_pool_kblocks(CUtensorMap* m, const void* pool, int64_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+  cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, 128, (cuuint64_t)kHeadDim * 2 * 8};
+  cuuint32_t box[4] = {64, 8, 2, 2};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // e4m3 K or V pool: 2-D {byte, row}; one box is one paged block's 16 rows x 128 bytes.
 static bool encode_pool8(CUtensorMap* m, const void* pool, int64_t rows) {
   EncodeTiledFn enc = get_encode_fn();
@@ -1821,7 +1850,8 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
     attr_set.store(1);
   }
   if (!p.wait_append) {
-    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, tmk, tmv, cs.tmvb);
+    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, tmk, tmv, cs.tmkb,
+                                                                     cs.tmvb);
     return cudaGetLastError();
   }
   // Items wait for every CTA's share of the append: a cooperative launch guarantees that all
@@ -1836,7 +1866,8 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, cs.tmq, tmk, tmv, cs.tmvb);
+  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, cs.tmq, tmk, tmv, cs.tmkb,
+                            cs.tmvb);
 }
 
 template <int HD>
@@ -2108,6 +2139,10 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   // the pools' maps serve the prefill tiles and the grouped-query decode path
   if (cs->kk != k_pool) {
     if (!encode_pool(&cs->tmk, k_pool, pool_rows, pr.head_dim)) return POD_ATTN_ERR_CUDA;
+    // the prefill tiles' per-block view (head dim 128; a 64-dim head uses the 2-D map)
+    if (pr.head_dim == kHeadDim ? !encode_pool_kblocks(&cs->tmkb, k_pool, pool_rows)
+                                : !encode_pool(&cs->tmkb, k_pool, pool_rows, pr.head_dim))
+      return POD_ATTN_ERR_CUDA;
     cs->kk = k_pool;
   }
   if (cs->kv != v_pool) {

@@ -20,9 +20,9 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 // §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
 //  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns that runs two
 //    128-row query tiles (A and B) against each K/V tile — warp 0 issues the TMA loads of the
-//    query tiles and of one ring of K and V tiles, warp 1 issues the S and P·V tcgen05 MMAs of
-//    both tiles (alternating between them), and warps 4-7 and 8-11 are the softmax warpgroups
-//    of tile A and tile B (one query row per thread, all 128 keys of a step);
+//    query tiles and of one ring of K and V tiles, warp 1 issues the S tcgen05 MMAs and warp 3
+//    the P·V tcgen05 MMAs of both tiles, and warps 4-7 and 8-11 are the softmax warpgroups of
+//    tile A and tile B (one query row per thread, all 128 keys of a step);
 //  * the decode slot (warps 12-15): decode items, on their own ticket loop.
 // Once the prefill list is drained, the prefill slot's warps 4-7 and 8-11 become two more
 // 4-warp decode slots. Every decode item thus runs on exactly 4 warps, whichever slot takes it,

@@ -2,19 +2,22 @@
 
 One step = one pass of the whole hot path over one hybrid batch: the fused persistent kernel
 computes the chunked-prefill attention and every decode attention of the batch (one attention
-layer of one serving iteration). Default workload: the Llama-2-7B attention shape (32 query /
-32 KV heads, head_dim 128, one 512-token chunk after a 3584-token prefix, 32 decodes with
-contexts uniform in [2048, 4096], paged block 16), synthetic N(0,1) bf16 inputs.
+layer of one serving iteration). The default run times the Yi-6B attention shape (32 query / 4 KV
+heads, head_dim 128, one 2048-token chunk after a 28672-token prefix, 16 decodes with contexts
+uniform in [16384, 32768], paged block 16) as the headline, the prefill-bound configuration;
+the same JSON line carries, as keyed extras, the Llama-2-7B and Llama-3-8B configurations
+(HBM-bound) and the two 200-iteration hybrid-batching trace mixes. Synthetic N(0,1) bf16 inputs.
 
 Timing: CUDA events on the launching stream around each step. Between steps (outside the
 events) a 1 GiB buffer is written and a 512 MiB one read, so every step starts with a cold L2
 whose lines are clean: with the write alone, the ~126 MB of dirty lines it leaves would be
 written back during the timed step (measured: 9-19 us of extra time per step). The headline
 value is the fused variant's mean us/iter; the serial (two launches back to back) and
-two-stream variants run on the same buffers for the speedup figures. `e2e` repeats the fused step through the
-public C ABI from pinned host buffers (plan + upload + run + copies in the timed region).
+two-stream variants run on the same buffers for the speedup figures. `e2e` repeats the fused
+step through the public C ABI from pinned host buffers (plan + upload + run + copies in the
+timed region) and splits it into its parts.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 """
 from __future__ import annotations
 
@@ -246,17 +249,26 @@ def run_reference(args, rank, world):
     print(json.dumps(out), flush=True)
 
 
+HEADLINE_CONFIG = 4           # Yi-6B shape, 2048-token chunk at 28K: the prefill-bound batch
+EXTRA_CONFIGS = (2, 3)        # the HBM-bound batches
+EXTRA_TRACES = ("a", "b")     # the long-context hybrid-batching mixes
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=None,
+                    help="one configuration only (default: configuration 4 as the headline, with "
+                         "configurations 2, 3 and the trace mixes a, b as extras in the same line)")
     ap.add_argument("--case", default=None, help="a small profiling case instead of --config")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="the headline configuration alone (no configurations 2, 3 or traces)")
     ap.add_argument("--only", default=None, help="profile mode: run only this variant, no extras")
     ap.add_argument("--trace", default=None, choices=["a", "b"],
                     help="the 200-iteration hybrid-batching trace (mix a or b) instead of --config")
@@ -271,6 +283,10 @@ def main():
                     help="every step also writes the iteration's new K/V rows into the pools "
                          "(pod_attn_run_append); the metric then includes that step")
     args = ap.parse_args()
+    with_extras = (args.config is None and not args.case and not args.no_extras and
+                   not args.only and not args.append)
+    if args.config is None:
+        args.config = HEADLINE_CONFIG
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -296,7 +312,9 @@ def main():
 
     dev = torch.device(f"cuda:{local}")
     if args.trace:
-        run_trace(args, dev, B, R, W, rank, world, dist)
+        out = run_trace(args, args.trace, dev, B, R, W, world, dist)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
         return
     if args.kv_fp8:
         run_fp8(args, dev, B, R, W, rank, world, dist)
@@ -304,7 +322,57 @@ def main():
     if args.mix:
         run_mix(args, dev, B, W, rank)
         return
-    batch = _make_batch(args, dev)
+
+    out = measure_config(args, args.config, args.case, dev, B, R, W, world, dist, local,
+                         full=True)
+    if out is None:                      # profile mode printed its own line
+        return
+    if with_extras:
+        extras = {}
+        for c in EXTRA_CONFIGS:
+            extras[f"config{c}"] = _summary(
+                measure_config(args, c, None, dev, B, R, W, world, dist, local, full=False))
+        for mix in EXTRA_TRACES:
+            extras[f"trace_{mix}"] = _trace_summary(
+                run_trace(args, mix, dev, B, R, W, world, dist))
+        out["extras"] = extras
+        out["gpu_launches"] += sum(e.get("gpu_launches", 0) for e in extras.values())
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _summary(d):
+    """The keyed extra of one configuration: its us/iter, fraction of the hybrid roofline and
+    speedups over the serial and two-stream variants."""
+    keys = ("value", "median_us", "serial_us", "streams_us", "speedup_vs_serial",
+            "speedup_vs_streams", "tbs", "prefill_tflops", "gpu_launches")
+    r = {k: d[k] for k in keys if k in d}
+    r["workload"] = d["config"]["workload"]
+    r["frac_of_t_star"] = d["hybrid_roofline"]["frac_of_t_star"]
+    r["t_star_us"] = d["hybrid_roofline"]["t_star_us"]
+    r["bound"] = d["roofline"]["bound"]
+    r["clocks"] = d.get("clocks")
+    return r
+
+
+def _trace_summary(d):
+    keys = ("value", "fused", "serial", "streams", "frac_of_t_star", "speedup_vs_serial",
+            "speedup_vs_streams", "mean_t_star_us", "steps", "gpu_launches")
+    r = {k: d[k] for k in keys if k in d}
+    r["workload"] = d["config"]["workload"]
+    return r
+
+
+def measure_config(args, cfg, case, dev, B, R, W, world, dist, local, full):
+    """One hybrid batch (configuration `cfg`, or the profiling case `case`): the fused, serial and
+    two-stream variants timed on identical device buffers, cold L2 before every step. With
+    `full`, also the step end to end through the C ABI (plan, upload, host copies, launch) with
+    a breakdown of its parts, and the CPU oracle baseline. Returns the JSON dict (every rank),
+    or None in profile mode."""
+    import torch
+    batch = W.profile_case(case, device=dev) if case else W.config(cfg, device=dev)
     work = R.batch_work(batch.num_q_heads, batch.num_kv_heads, batch.q_lens,
                         batch.prefill_kv_lens, batch.decode_kv_lens)
     hbm, tf_burst, tf_sust, peak_src = _peaks()
@@ -342,25 +410,23 @@ def main():
         torch.cuda.synchronize()
         st = plans[args.only][0].device_status(plans[args.only][1])
         print(json.dumps({"profile_run": args.only, "status": st}))
-        return
+        return None
 
-    def timed(v, k, sampler=None):
+    def timed(v, k):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(k)]
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        wall0 = time.perf_counter()
         for a, b in evs:
             flush()                              # cold L2 for every step (outside the events)
             a.record(stream)
             step(v)
             b.record(stream)
         torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
         if dist:
             dist.barrier()
-        return [a.elapsed_time(b) * 1e3 for a, b in evs], wall
+        return [a.elapsed_time(b) * 1e3 for a, b in evs]
 
     for v in variants:
         for _ in range(args.warmup):
@@ -378,62 +444,18 @@ def main():
             clocks = cs.summary()
         else:
             results[v] = timed(v, args.steps)
-    # outputs of the timed runs agree bit for bit across variants (same items, same arithmetic)
     for v in variants:
         assert plans[v][0].device_status(plans[v][1]) == B.OK, v
 
     def agg(us_list):
         return max_over_ranks([statistics.mean(us_list)], dist, dev)[0]
 
-    us = {v: agg(results[v][0]) for v in variants}
-    med = {v: statistics.median(results[v][0]) for v in variants}
+    us = {v: agg(results[v]) for v in variants}
+    med = {v: statistics.median(results[v]) for v in variants}
 
-    # ---- e2e through the public C ABI from pinned host buffers --------------------------------
     e2e = None
-    if not args.no_e2e:
-        host = {k: getattr(batch, k).cpu().pin_memory() for k in
-                ("q_prefill", "q_decode", "block_tables", "cu_seqlens_q", "kv_lens")}
-        dq_p, dq_d = torch.empty_like(batch.q_prefill), torch.empty_like(batch.q_decode)
-        dbt, dcu, dkv = (torch.empty_like(batch.block_tables), torch.empty_like(batch.cu_seqlens_q),
-                         torch.empty_like(batch.kv_lens))
-        ho_p = torch.empty(o_p.shape, dtype=o_p.dtype, pin_memory=True)
-        ho_d = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
-        ws = plans["fused"][1]
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = ho_p.numel() * ho_p.element_size() + ho_d.numel() * ho_d.element_size()
-
-        def e2e_step():
-            for dst, key in ((dq_p, "q_prefill"), (dq_d, "q_decode"), (dbt, "block_tables"),
-                             (dcu, "cu_seqlens_q"), (dkv, "kv_lens")):
-                dst.copy_(host[key], non_blocking=True)
-            plan = B.Plan.for_batch(batch, variant="fused")   # host planning of this batch
-            plan.upload(ws, stream)
-            plan.run(dq_p, dq_d, batch.k_pool, batch.v_pool, dbt, dcu, dkv, o_p, o_d, ws,
-                     stream=stream)
-            ho_p.copy_(o_p, non_blocking=True)
-            ho_d.copy_(o_d, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-            return plan
-
-        for _ in range(args.warmup):
-            e2e_step()
-        ts = []
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for _ in range(args.steps):
-            flush()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            e2e_step()
-            ts.append((time.perf_counter() - t0) * 1e6)
-        e2e = {"value": agg(ts), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
-
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return
+    if full and not args.no_e2e:
+        e2e = _e2e(args, batch, plans["fused"][1], o_p, o_d, B, flush, stream, dist, dev, agg)
 
     t_fused = us["fused"] * 1e-6
     tstar = work.t_star(hbm, tf_burst)
@@ -448,15 +470,16 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
                 "frac": achieved / tf_burst, "traffic": None,
                 "peak_source": f"{peak_src} bf16 burst"}
-    traffic = _traffic_from_profiles(args.config)
+    traffic = None if case else _traffic_from_profiles(cfg)
     if traffic is not None:
         roof["traffic"] = traffic
+    cfg_args = argparse.Namespace(case=case, config=cfg, append=args.append)
     out = {
         "metric": METRIC, "value": us["fused"], "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us["fused"] / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": _config_dict(args, batch, world),
+        "config": _config_dict(cfg_args, batch, world),
         "median_us": med["fused"],
         "hybrid_roofline": {"t_star_us": tstar * 1e6, "frac_of_t_star": tstar / t_fused,
                             "bytes": work.bytes, "prefill_flops": work.prefill_flops,
@@ -476,22 +499,96 @@ def main():
         out["speedup_vs_streams"] = us["streams"] / us["fused"]
     if e2e:
         out["e2e"] = e2e
-    if not args.no_cpu and world == 1:
+    if full and not args.no_cpu and world == 1:
         cpu_batch = batch.to("cpu")
         out["cpu_baseline"] = {k: v for k, v in cpu_baseline(cpu_batch).items() if k != "seconds"}
-    print(json.dumps(out), flush=True)
+    return out
+
+
+def _e2e(args, batch, ws, o_p, o_d, B, flush, stream, dist, dev, agg):
+    """The fused step end to end through the C ABI, as a serving loop runs it: enqueue the copies
+    of this step's q, block tables and lengths from pinned host buffers, plan the batch on the
+    host while they run, upload the plan's work lists, launch, copy the outputs back, wait. Host
+    time around the whole step; CUDA events split its device-side parts (the span between the
+    input copies and the upload is the device waiting for the host's planning), host timers the
+    planning and the other host calls."""
+    import torch
+    host = {k: getattr(batch, k).cpu().pin_memory() for k in
+            ("q_prefill", "q_decode", "block_tables", "cu_seqlens_q", "kv_lens")}
+    dq_p, dq_d = torch.empty_like(batch.q_prefill), torch.empty_like(batch.q_decode)
+    dbt, dcu, dkv = (torch.empty_like(batch.block_tables), torch.empty_like(batch.cu_seqlens_q),
+                     torch.empty_like(batch.kv_lens))
+    ho_p = torch.empty(o_p.shape, dtype=o_p.dtype, pin_memory=True)
+    ho_d = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = ho_p.numel() * ho_p.element_size() + ho_d.numel() * ho_d.element_size()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    def e2e_step(parts):
+        t0 = time.perf_counter()
+        ev[0].record(stream)
+        for dst, key in ((dq_p, "q_prefill"), (dq_d, "q_decode"), (dbt, "block_tables"),
+                         (dcu, "cu_seqlens_q"), (dkv, "kv_lens")):
+            dst.copy_(host[key], non_blocking=True)
+        ev[1].record(stream)
+        t1 = time.perf_counter()
+        plan = B.Plan.for_batch(batch, variant="fused")   # host planning, beside the copies
+        t2 = time.perf_counter()
+        ev[2].record(stream)
+        plan.upload(ws, stream)
+        ev[3].record(stream)
+        plan.run(dq_p, dq_d, batch.k_pool, batch.v_pool, dbt, dcu, dkv, o_p, o_d, ws,
+                 stream=stream)
+        ev[4].record(stream)
+        ho_p.copy_(o_p, non_blocking=True)
+        ho_d.copy_(o_d, non_blocking=True)
+        ev[5].record(stream)
+        t3 = time.perf_counter()
+        stream.synchronize()
+        t4 = time.perf_counter()
+        if parts is not None:
+            parts["plan_host"].append((t2 - t1) * 1e6)
+            parts["enqueue_host"].append(((t1 - t0) + (t3 - t2)) * 1e6)
+            parts["wait_host"].append((t4 - t3) * 1e6)
+            parts["h2d_device"].append(ev[0].elapsed_time(ev[1]) * 1e3)
+            parts["idle_for_plan_device"].append(ev[1].elapsed_time(ev[2]) * 1e3)
+            parts["upload_device"].append(ev[2].elapsed_time(ev[3]) * 1e3)
+            parts["kernel_device"].append(ev[3].elapsed_time(ev[4]) * 1e3)
+            parts["d2h_device"].append(ev[4].elapsed_time(ev[5]) * 1e3)
+        return (t4 - t0) * 1e6
+
+    for _ in range(args.warmup):
+        e2e_step(None)
+    ts = []
+    parts = {k: [] for k in ("plan_host", "enqueue_host", "wait_host", "h2d_device",
+                             "idle_for_plan_device", "upload_device", "kernel_device",
+                             "d2h_device")}
     if dist:
-        dist.destroy_process_group()
+        dist.barrier()
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        flush()
+        torch.cuda.synchronize()
+        ts.append(e2e_step(parts))
+    return {"value": agg(ts), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+            "breakdown_us": {k: round(statistics.mean(v), 2) for k, v in parts.items()},
+            "breakdown_note": ("plan_host: pod_attn_plan through the binding (runs while the "
+                               "input copies do); enqueue_host: the step's other host calls; "
+                               "wait_host: the final stream synchronisation; *_device: "
+                               "CUDA-event spans on the stream in order: input copies, idle "
+                               "until the plan is ready, upload, kernel, output copies")}
 
 
-def run_trace(args, dev, B, R, W, rank, world, dist):
+def run_trace(args, mix, dev, B, R, W, world, dist):
     """Configuration 5: every iteration of a seeded hybrid-batching trace is one step. The plan
     and upload of each iteration happen before its timed events (they are host work of the
     serving loop); the events time pod_attn_run. Reports mean/p50/p99 us/iter per variant and
     the sum of measured times over the sum of per-iteration hybrid rooflines."""
     import torch
     hbm, tf_burst, _, _ = _peaks()
-    tr = W.trace(args.trace, iters=args.trace_iters)
+    tr = W.trace(mix, iters=args.trace_iters, decode_targets=W.trace_decode_targets(
+        torch.cuda.get_device_properties(dev).multi_processor_count))
     pool = W.TracePool(tr, device=dev)
     batches = [pool.batch(i) for i in range(len(tr.steps))]
     variants = ["fused", "serial", "streams"]
@@ -525,8 +622,6 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
         # per iteration, the slowest rank's time
         times[v] = max_over_ranks([a.elapsed_time(e) * 1e3 for a, e in evs], dist, dev)
         assert plans[v][-1].device_status(ws[v]) == B.OK, v
-    if rank != 0:
-        return
 
     def stats(xs):
         xs = sorted(xs)
@@ -534,22 +629,23 @@ def run_trace(args, dev, B, R, W, rank, world, dist):
                 "p99": xs[min(len(xs) - 1, int(round(0.99 * (len(xs) - 1))))]}
 
     f = stats(times["fused"])
-    out = {"metric": METRIC, "value": f["mean"], "unit": UNIT, "n_gpus": world,
-           "steps": len(batches), "warmup": args.warmup, "ms_per_step": f["mean"] / 1e3,
-           "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-           "data": "synthetic",
-           "config": {"workload": f"hybrid-batching trace mix {args.trace}: Llama-3-8B attention "
-                                  f"(32/8, head_dim 128, paged block 16), 2048-token budget, "
-                                  f"decodes first, {len(batches)} iterations",
-                      "l2": L2_NOTE},
-           "fused": f, "serial": stats(times["serial"]), "streams": stats(times["streams"]),
-           "sum_measured_over_sum_tstar": sum(times["fused"]) / sum(tstar),
-           "frac_of_t_star": sum(tstar) / sum(times["fused"]),
-           "speedup_vs_serial": sum(times["serial"]) / sum(times["fused"]),
-           "speedup_vs_streams": sum(times["streams"]) / sum(times["fused"]),
-           "mean_t_star_us": statistics.mean(tstar),
-           "pool_gb": pool.k_pool.numel() * 4 / 1e9}
-    print(json.dumps(out), flush=True)
+    return {"metric": METRIC, "value": f["mean"], "unit": UNIT, "n_gpus": world,
+            "steps": len(batches), "warmup": args.warmup, "ms_per_step": f["mean"] / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"hybrid-batching trace mix {mix}: Llama-3-8B attention "
+                                   f"(32/8, head_dim 128, paged block 16), 2048-token budget, "
+                                   f"decodes first, {len(batches)} iterations",
+                       "decode_targets": list(tr.decode_targets),
+                       "l2": L2_NOTE},
+            "fused": f, "serial": stats(times["serial"]), "streams": stats(times["streams"]),
+            "sum_measured_over_sum_tstar": sum(times["fused"]) / sum(tstar),
+            "frac_of_t_star": sum(tstar) / sum(times["fused"]),
+            "speedup_vs_serial": sum(times["serial"]) / sum(times["fused"]),
+            "speedup_vs_streams": sum(times["streams"]) / sum(times["fused"]),
+            "mean_t_star_us": statistics.mean(tstar),
+            "gpu_launches": len(batches),
+            "pool_gb": pool.k_pool.numel() * 4 / 1e9}
 
 
 def run_mix(args, dev, B, W, rank):

@@ -108,25 +108,37 @@ int64_t decode_makespan(const std::vector<int64_t>& nblks, int64_t c, int64_t sl
 
 // Modelled makespan (in steps) of the prefill items that chunk size c makes of the outputs
 // `nts` on `slots` prefill slots taking them longest first, each to the slot that frees first
-// (list scheduling); an item costs its steps plus kPrefillItemOverhead.
+// (list scheduling); an item costs its steps plus kPrefillItemOverhead. The makespan depends
+// only on the multiset of slot loads, so the items are counted by cost (`hist`) and the loads
+// kept as a histogram (`load`): the least loaded slot's load never decreases, so a cursor
+// finds it, and the whole model is linear in the items and the largest load.
 int64_t prefill_makespan(const std::vector<int64_t>& nts, int64_t c, int64_t slots,
-                         std::vector<int64_t>& costs) {
-  costs.clear();
+                         std::vector<int64_t>& hist, std::vector<int64_t>& load) {
+  int64_t top = 0, total = 0;
+  for (int64_t n : nts) top = std::max(top, std::min(c, n) + kPrefillItemOverhead);
+  hist.assign((size_t)top + 1, 0);
   for (int64_t n : nts) {
     int64_t ns, ch;
     rebalanced(n, c, &ns, &ch);
-    for (int64_t k = 0; k + 1 < ns; ++k) costs.push_back(ch + kPrefillItemOverhead);
-    costs.push_back(n - (ns - 1) * ch + kPrefillItemOverhead);
+    const int64_t last = n - (ns - 1) * ch + kPrefillItemOverhead;
+    hist[(size_t)(ch + kPrefillItemOverhead)] += ns - 1;
+    hist[(size_t)last] += 1;
+    total += (ns - 1) * (ch + kPrefillItemOverhead) + last;
   }
-  std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
-  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> freeat;
-  for (int64_t i = 0; i < slots; ++i) freeat.push(0);
-  int64_t span = 0;
-  for (int64_t x : costs) {
-    const int64_t t = freeat.top() + x;
-    freeat.pop();
-    freeat.push(t);
-    span = std::max(span, t);
+  // an item starts at the least load, which is at most total / slots
+  load.assign((size_t)(total / slots + top + 1), 0);
+  load[0] = slots;
+  int64_t cur = 0, span = 0;
+  for (int64_t x = top; x > 0; --x) {
+    // the k items of cost x go to the k least loaded slots, as many at a time as share a load
+    for (int64_t k = hist[(size_t)x]; k > 0;) {
+      while (load[(size_t)cur] == 0) ++cur;
+      const int64_t m = std::min(k, load[(size_t)cur]);
+      load[(size_t)cur] -= m;
+      load[(size_t)(cur + x)] += m;
+      span = std::max(span, cur + x);
+      k -= m;
+    }
   }
   return span;
 }
@@ -142,6 +154,9 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
       !(prob.scale > 0.f))
     return POD_ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return POD_ATTN_ERR_INVALID_ARG;
+  if (opt.ctas_per_sm < 0 || opt.max_prefill_ctas < 0) return POD_ATTN_ERR_INVALID_ARG;
+  // one persistent CTA per SM holds both slots (232 KiB of shared memory, all 512 TMEM columns)
+  if (opt.ctas_per_sm > 1) return POD_ATTN_ERR_UNSUPPORTED;
   // head dims 128 and 64 (the layouts are sized for 128; 64 uses their first half)
   if ((prob.head_dim != kHeadDim && prob.head_dim != 64) || prob.block_size != kBlockSize)
     return POD_ATTN_ERR_UNSUPPORTED;
@@ -177,6 +192,11 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->tile_tokens = tq;
   plan->num_sms = num_sms;
   plan->ctas_per_sm = 1;  // one CTA per SM holds both slots (and all 512 TMEM columns)
+  // the cap on CTAs that take prefill items ("POD-Attention" digest, §"가상 CTA와 SM별 균형": the
+  // CTAs one prefill may take are limited so decode work is not crowded out); 0 = every CTA
+  const int prefill_ctas =
+      opt.max_prefill_ctas > 0 ? std::min(opt.max_prefill_ctas, num_sms) : num_sms;
+  plan->max_prefill_ctas = prefill_ctas;
   plan->cu.assign(cu ? cu : nullptr, cu ? cu + Np + 1 : nullptr);
   plan->kv.assign(kv ? kv : nullptr, kv ? kv + Np + Nd : nullptr);
   const int64_t slots = (int64_t)num_sms * 2;  // a prefill slot and a decode slot per SM
@@ -227,7 +247,7 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   // prefill slots finish first in the model above; ties keep the larger chunk
   int64_t chunk_p = 0;
   if (!pu.empty() && opt.prefill_splits <= 0) {
-    std::vector<int64_t> nts(pu.size()), costs;
+    std::vector<int64_t> nts(pu.size()), hist, load;
     int64_t longest = 0;
     for (size_t i = 0; i < pu.size(); ++i) {
       nts[i] = pu[i].ntiles;
@@ -239,7 +259,7 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
       if (c == prev_c) continue;
       if (k > 1 && c < kMinPrefillTilesPerSplit) break;
       prev_c = c;
-      const int64_t t = prefill_makespan(nts, c, num_sms, costs);
+      const int64_t t = prefill_makespan(nts, c, prefill_ctas, hist, load);
       if (best < 0 || t < best) {
         best = t;
         chunk_p = c;
@@ -359,29 +379,23 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
       std::memcpy(&words_d[id * kItemWords], w, sizeof(w));
     }
   }
-  // longest first, ties in enumeration order: a stable counting sort over the distinct costs
-  // (items of one split size share a cost)
-  auto order = [](const std::vector<int64_t>& cost, const std::vector<int32_t>& words,
+  // longest first, ties in enumeration order: a stable counting sort over the cost, counted in
+  // its unit (a prefill step or a decode block, so the counts span the longest item)
+  auto order = [](const std::vector<int64_t>& cost, int64_t unit, const std::vector<int32_t>& words,
                   std::vector<int32_t>& out) {
     const size_t n = cost.size();
-    std::vector<int64_t> distinct(cost);  // the distinct costs, largest first
-    std::sort(distinct.begin(), distinct.end(), std::greater<int64_t>());
-    distinct.erase(std::unique(distinct.begin(), distinct.end()), distinct.end());
-    std::vector<size_t> start(distinct.size() + 1, 0);
-    std::vector<uint32_t> bucket(n);
-    for (size_t i = 0; i < n; ++i) {  // bucket = rank of the cost, largest first
-      bucket[i] = (uint32_t)(std::lower_bound(distinct.begin(), distinct.end(), cost[i],
-                                              std::greater<int64_t>()) - distinct.begin());
-      ++start[bucket[i] + 1];
-    }
+    int64_t top = 0;
+    for (int64_t c : cost) top = std::max(top, c / unit);
+    std::vector<size_t> start((size_t)top + 2, 0);  // by (top - cost units): longest first
+    for (int64_t c : cost) ++start[(size_t)(top - c / unit) + 1];
     for (size_t b = 1; b < start.size(); ++b) start[b] += start[b - 1];
     out.resize(n * kItemWords);
     for (size_t i = 0; i < n; ++i)
-      std::memcpy(&out[(start[bucket[i]]++) * kItemWords], &words[i * kItemWords],
-                  kItemWords * sizeof(int32_t));
+      std::memcpy(&out[(start[(size_t)(top - cost[i] / unit)]++) * kItemWords],
+                  &words[i * kItemWords], kItemWords * sizeof(int32_t));
   };
-  order(cost_p, words_p, plan->items_p);
-  order(cost_d, words_d, plan->items_d);
+  order(cost_p, kPrefillStepCost, words_p, plan->items_p);
+  order(cost_d, kDecodeBlockCost, words_d, plan->items_d);
   plan->num_p_slots = p_slots;
   // where each token of this iteration sits in its sequence (the KV append writes its K/V
   // row there): chunk token i of prefill sequence s at kv_len - q_len + i, a decode token at
@@ -402,9 +416,8 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   }
   plan->num_d_slots = d_slots;
 
-  plan->max_prefill_per_sm = 1;  // one prefill pipeline per SM
   plan->grid_fused = (int)std::min<int64_t>(num_sms, (int64_t)(n_p + n_d));
-  plan->grid_prefill = (int)std::min<int64_t>(num_sms, (int64_t)n_p);
+  plan->grid_prefill = (int)std::min<int64_t>(prefill_ctas, (int64_t)n_p);
   plan->grid_decode = (int)std::min<int64_t>(num_sms, (int64_t)n_d);
 
   // ---- workspace layout --------------------------------------------------------------------
@@ -433,6 +446,17 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   w.records = off;
   if (opt.instrument) off = align256(off + (size_t)(n_p + n_d) * sizeof(pod_attn_item_record));
   w.total = off;
+
+  // the upload image: zeros up to the work lists, then each list at its workspace offset
+  std::vector<uint8_t>& img = plan->upload_image;
+  img.assign(w.partial_p, 0);
+  auto put = [&](size_t at, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::memcpy(img.data() + at, v.data(), v.size() * sizeof(int32_t));
+  };
+  put(w.items_p, plan->items_p);
+  put(w.items_d, plan->items_d);
+  put(w.units, plan->units);
+  put(w.new_rows, plan->new_rows);
   return POD_ATTN_OK;
 }
 

@@ -84,7 +84,7 @@ struct Params {
   int32_t Hq, Hkv, G, Np, Nd, num_blocks, maxb;
   int32_t pool_rows;  // num_blocks * Hkv * 16: first row past the pools (TMA fills zeros)
   int32_t num_sms;
-  int32_t max_prefill_per_sm;
+  int32_t max_prefill_ctas;  // CTAs 0 .. max_prefill_ctas - 1 take prefill items
   int32_t hp_log2;    // prefill tile: 2^hp_log2 heads x tq tokens
   int32_t causal;     // 0: chunk tokens see every row of their sequence
   int32_t head_dim;   // 128 or 64 (selects the kernel instantiation)
@@ -1531,14 +1531,16 @@ __device__ void decode_item(const Params& p, const CUtensorMap* tmk, const CUten
 }
 
 // ============================================================================ scheduler
-// Next item for a slot. The prefill slot (0) takes prefill tickets, and a decode ticket once the
-// prefill list is drained (or in a decode-only launch); the decode slot (1) and the prefill
-// warps' two decode slots (2, 3) take decode tickets only. Per-SM counters record how many
-// decode items each SM's prefill warps took over.
+// Next item for a slot. The prefill slot (0) of CTAs 0 .. max_prefill_ctas - 1 takes prefill
+// tickets, and a decode ticket once the prefill list is drained (or in a decode-only launch, or
+// on a CTA past the cap); the decode slot (1) and the prefill warps' two decode slots (2, 3) take
+// decode tickets only. Per-SM counters record how many decode items each SM's prefill warps took
+// over.
 __device__ __forceinline__ void pick_item(const Params& p, int slot, int sm, SmemCtl* ctl) {
   int32_t* cnt = p.counters;
   int kind = -1, idx = 0;
-  const bool may_prefill = slot == 0 && p.mode != kModeDecodeOnly;
+  const bool may_prefill =
+      slot == 0 && p.mode != kModeDecodeOnly && (int)blockIdx.x < p.max_prefill_ctas;
   const bool may_decode = p.mode != kModePrefillOnly;
   if (may_prefill) {
     const int t = atomicAdd(&cnt[0], 1);
@@ -2038,7 +2040,7 @@ pod_attn_status pod_attn_get_plan_info(pod_attn_plan_t plan, pod_attn_plan_info*
   r.num_units = (int32_t)(plan->units.size() / kUnitWords);
   r.num_sms = plan->num_sms;
   r.ctas_per_sm = plan->ctas_per_sm;
-  r.max_prefill_ctas = plan->max_prefill_per_sm;
+  r.max_prefill_ctas = plan->max_prefill_ctas;
   r.grid_fused = plan->grid_fused;
   r.grid_prefill = plan->grid_prefill;
   r.grid_decode = plan->grid_decode;
@@ -2080,22 +2082,12 @@ pod_attn_status pod_attn_upload(pod_attn_plan_t plan, void* workspace, size_t wo
   if (!plan) return POD_ATTN_ERR_INVALID_ARG;
   pod_attn_status st = check_ws(plan, workspace, workspace_bytes);
   if (st != POD_ATTN_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const WorkspaceLayout& w = plan->ws;
-  bool ok = cudaMemsetAsync(ws, 0, w.zero_bytes, s) == cudaSuccess;
-  if (ok && !plan->items_p.empty())
-    ok = cudaMemcpyAsync(ws + w.items_p, plan->items_p.data(), plan->items_p.size() * 4,
-                         cudaMemcpyHostToDevice, s) == cudaSuccess;
-  if (ok && !plan->items_d.empty())
-    ok = cudaMemcpyAsync(ws + w.items_d, plan->items_d.data(), plan->items_d.size() * 4,
-                         cudaMemcpyHostToDevice, s) == cudaSuccess;
-  if (ok && !plan->units.empty())
-    ok = cudaMemcpyAsync(ws + w.units, plan->units.data(), plan->units.size() * 4,
-                         cudaMemcpyHostToDevice, s) == cudaSuccess;
-  if (ok && !plan->new_rows.empty())
-    ok = cudaMemcpyAsync(ws + w.new_rows, plan->new_rows.data(), plan->new_rows.size() * 4,
-                         cudaMemcpyHostToDevice, s) == cudaSuccess;
+  // one copy: the zeroed status, counters and arrival counters, then the work lists, laid out
+  // on the host as they sit in the workspace
+  const bool ok = plan->upload_image.empty() ||
+                  cudaMemcpyAsync(workspace, plan->upload_image.data(), plan->upload_image.size(),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) ==
+                      cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     return POD_ATTN_ERR_CUDA;
@@ -2184,7 +2176,7 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
   p.maxb = pr.max_blocks_per_seq;
   p.pool_rows = (int32_t)pool_rows;
   p.num_sms = plan->num_sms;
-  p.max_prefill_per_sm = plan->max_prefill_per_sm;
+  p.max_prefill_ctas = plan->max_prefill_ctas;
   p.hp_log2 = __builtin_ctz((unsigned)plan->head_pack);
   p.causal = plan->opt.non_causal == 0;
   p.head_dim = pr.head_dim;
@@ -2338,7 +2330,7 @@ pod_attn_status pod_attn_run_decode_fp8(pod_attn_plan_t plan, const void* q_deco
   p.maxb = pr.max_blocks_per_seq;
   p.pool_rows = (int32_t)((int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize);
   p.num_sms = plan->num_sms;
-  p.max_prefill_per_sm = plan->max_prefill_per_sm;
+  p.max_prefill_ctas = 0;
   p.hp_log2 = 0;
   p.tq = kTileM;
   p.causal = 1;
@@ -2405,7 +2397,10 @@ pod_attn_status pod_attn_append_fp8(pod_attn_plan_t plan, const void* k_new, con
 
 pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspace, void* stream) {
   (void)plan;
-  if (!workspace) return POD_ATTN_ERR_INVALID_ARG;
+  if (!workspace) {  // the status word of pod_attn_run_static's scratch array on this device
+    const pod_attn_status st = static_scratch(&workspace);
+    if (st != POD_ATTN_OK) return st;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t code = 0;
   if (cudaStreamSynchronize(s) != cudaSuccess ||
@@ -2441,9 +2436,21 @@ pod_attn_status pod_attn_run_static(pod_attn_plan_t plan, const void* q_prefill,
                                     const void* v_pool, const int32_t* d_block_tables,
                                     const int32_t* d_cu_seqlens_q, const int32_t* d_kv_lens,
                                     void* o_prefill, void* o_decode, void* stream) {
-  if (!plan || plan->opt.variant != POD_ATTN_FUSED) return POD_ATTN_ERR_INVALID_ARG;
+  // instrumentation records would land in the shared array, where no caller can read them
+  if (!plan || plan->opt.variant != POD_ATTN_FUSED || plan->opt.instrument)
+    return POD_ATTN_ERR_INVALID_ARG;
   if (plan->opt.kv_fp8) return POD_ATTN_ERR_UNSUPPORTED;
   if (plan->ws.total > kStaticScratchBytes) return POD_ATTN_ERR_WORKSPACE;
+  {
+    // the array's address is the current device's: the stream must belong to that device
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess ||
+        cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+      cudaGetLastError();
+      return POD_ATTN_ERR_CUDA;
+    }
+    if (sdev != cur) return POD_ATTN_ERR_INVALID_ARG;
+  }
   void* scratch = nullptr;
   pod_attn_status st = static_scratch(&scratch);
   if (st != POD_ATTN_OK) return st;

@@ -141,7 +141,8 @@ struct pod_attn_plan_s {
   int group = 1;
   int head_pack = 1;                      // hp: query heads per prefill tile
   int tile_tokens = pod::kTileM;          // T = 128 / hp: tokens per prefill tile
-  int num_sms = 0, ctas_per_sm = 2, max_prefill_per_sm = 1;
+  int num_sms = 0, ctas_per_sm = 1;
+  int max_prefill_ctas = 0;               // CTAs whose prefill slot takes prefill items (CTAs 0..)
   int grid_fused = 0, grid_prefill = 0, grid_decode = 0;
   std::vector<int32_t> cu, kv;            // host copies of the lengths
   std::vector<int32_t> items_p, items_d;  // kItemWords each
@@ -150,6 +151,10 @@ struct pod_attn_plan_s {
                                           // order, then one per decode sequence
   int num_p_slots = 0, num_d_slots = 0;
   pod::WorkspaceLayout ws;
+  // Bytes [0, ws.partial_p) of the workspace as pod_attn_upload writes them: the zeroed status,
+  // counters and arrival counters, then the work lists at their offsets (one host-to-device
+  // copy per upload).
+  std::vector<uint8_t> upload_image;
   double est_prefill_flops = 0, est_prefill_bytes = 0, est_decode_bytes = 0,
          est_decode_flops = 0;
   // CUDA-side state owned by pod_attn.cu (events for the STREAMS variant, cached tensor maps).

@@ -294,6 +294,14 @@ class Trace:
     mix: str
     steps: List[TraceStep]
     max_rows: List[int]          # per request id: the most cached rows it ever reaches
+    decode_targets: tuple = ()   # running decodes held in each quarter of the trace
+
+
+def trace_decode_targets(num_sms: int, num_kv_heads: int = 8, waves: int = 4) -> tuple:
+    """Running-decode counts whose (sequence, kv-head) units land just above 1, 2, 3, 4 times the
+    SM count: k * num_sms // num_kv_heads + 1 sequences. For 148 SMs this gives 19, 38, 56, 75
+    (152, 304, 448, 600 units); for 152 SMs 20, 39, 58, 77 (160, 312, 464, 616 units)."""
+    return tuple(k * num_sms // num_kv_heads + 1 for k in range(1, waves + 1))
 
 
 def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
@@ -304,8 +312,9 @@ def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
     (b) prompts lognormal with mean 16384 (sigma 0.5 in log space), clipped to
         [4096, 32768], outputs geometric with mean 64.
     The number of running decodes is held at a target that changes every quarter of the trace
-    (19, 38, 56, 75 sequences -> 152, 304, 448, 600 decode (seq, kv-head) units for 8 KV heads:
-    just above multiples of the SM count). A finished decode is replaced by a request whose
+    (by default 19, 38, 56, 75 sequences -> 152, 304, 448, 600 decode (seq, kv-head) units for
+    8 KV heads, just above multiples of 148; `trace_decode_targets` sizes them for another SM
+    count). A finished decode is replaced by a request whose
     prompt is already cached (a warm request); prompt chunks come from a FIFO of new requests.
     Every request has an id; `max_rows[id]` sizes its blocks in a persistent pool.
     """
@@ -362,7 +371,7 @@ def trace(mix: str, seed: int = 5, iters: int = 200, budget: int = 2048,
             left -= c
         fifo = [r for r in fifo if r[2] < r[1]]
         steps.append(TraceStep(ql, pkv, dec_lens, pids, dec_ids))
-    return Trace(mix, steps, max_rows)
+    return Trace(mix, steps, max_rows, tuple(decode_targets))
 
 
 class TracePool:

@@ -96,12 +96,17 @@ typedef struct {
 /* Planner and launch options. Zero-initialise for defaults. */
 typedef struct {
   int32_t num_sms;          /* SMs the planner sizes the grid for; 0 = query the current device */
-  int32_t ctas_per_sm;      /* accepted and ignored: one persistent CTA per SM, which holds a
-                               prefill slot and a decode slot side by side */
-  int32_t max_prefill_ctas; /* accepted and ignored: the prefill work of an SM is capped at one
-                               item at a time by construction (its one prefill slot), so decode
-                               is never crowded out ("POD-Attention" digest, §"가상 CTA와 SM별
-                               균형") */
+  int32_t ctas_per_sm;      /* 0 or 1: one persistent CTA per SM, which holds a prefill slot and
+                               a decode slot side by side and all of the SM's shared memory and
+                               TMEM; larger values return POD_ATTN_ERR_UNSUPPORTED, negative
+                               ones POD_ATTN_ERR_INVALID_ARG */
+  int32_t max_prefill_ctas; /* cap on the CTAs that take prefill items: only CTAs 0 .. cap - 1
+                               run prefill work (the others' prefill slots run decode items from
+                               the start), so a long prefill cannot crowd decode work out of
+                               every SM ([POD] §"가상 CTA와 SM별 균형"); the
+                               planner sizes prefill splits for that many slots. 0 = every CTA;
+                               values above the SM count mean every CTA; negative values return
+                               POD_ATTN_ERR_INVALID_ARG */
   int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head), at most 64
                                (more are capped); 0 = auto */
   int32_t prefill_splits;   /* force this many KV splits per prefill (tile pair, head block),
@@ -127,8 +132,8 @@ typedef struct {
   int32_t num_decode_items;   /* virtual decode CTAs: (seq, kv-head, kv-split) */
   int32_t num_units;          /* outputs assembled from more than one split */
   int32_t num_sms;            /* SM count the grid was sized for */
-  int32_t ctas_per_sm;
-  int32_t max_prefill_ctas;
+  int32_t ctas_per_sm;        /* 1 */
+  int32_t max_prefill_ctas;   /* CTAs that take prefill items (the cap, at most num_sms) */
   int32_t grid_fused;         /* CTAs of the fused launch */
   int32_t grid_prefill;       /* CTAs of the prefill-only launch (serial / streams) */
   int32_t grid_decode;        /* CTAs of the decode-only launch (serial / streams) */
@@ -176,9 +181,11 @@ pod_attn_status pod_attn_plan(const pod_attn_problem* problem, const int32_t* h_
 size_t pod_attn_workspace_bytes(pod_attn_plan_t plan);
 
 /* Copy the plan's work lists into the workspace and zero its counters and status word, on
- * `stream` (asynchronous; the plan must stay alive until the copy has run). Must be called
- * once after pod_attn_plan and before the first pod_attn_run with this workspace; a workspace
- * serves one plan at a time. Calling it again resets the device status.
+ * `stream`, as one host-to-device copy of a host image the plan keeps (the work lists at their
+ * workspace offsets after the zeroed control words). Asynchronous with respect to the device;
+ * the host image is staged before the call returns, so the plan may be destroyed afterwards.
+ * Must be called once after pod_attn_plan and before the first pod_attn_run with this
+ * workspace; a workspace serves one plan at a time. Calling it again resets the device status.
  *   workspace       : device pointer, 256-byte aligned, >= pod_attn_workspace_bytes(plan).
  * Errors: INVALID_ARG (null plan/workspace), WORKSPACE (too small / misaligned), CUDA. */
 pod_attn_status pod_attn_upload(pod_attn_plan_t plan, void* workspace, size_t workspace_bytes,
@@ -277,9 +284,11 @@ pod_attn_status pod_attn_append_fp8(pod_attn_plan_t plan, const void* k_new, con
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronise `stream`, read and clear the device status word of `workspace`.
+ * workspace NULL reads the status word of pod_attn_run_static's scratch array on the current
+ * device instead (the runs made through that entry point).
  * Returns OK, BAD_INDEX, TIMEOUT, or CUDA if the synchronisation itself failed. After
  * BAD_INDEX or TIMEOUT the outputs of that run are unspecified and the workspace must be
- * re-uploaded before the next run. */
+ * re-uploaded before the next run (pod_attn_run_static uploads on every call). */
 pod_attn_status pod_attn_last_device_status(pod_attn_plan_t plan, void* workspace, void* stream);
 
 /* Fill *info with the plan summary. Errors: INVALID_ARG. */
@@ -340,17 +349,19 @@ pod_attn_status pod_attn_read_records(pod_attn_plan_t plan, const void* workspac
  * array and clears its status word, scheduling counters and merge counters (on `stream`), then
  * launches the fused kernel exactly as pod_attn_run does. It calls no cudaMalloc, cudaFree or
  * other allocating routine.
- *   plan            : a plan made with variant POD_ATTN_FUSED; its pod_attn_workspace_bytes must
- *                     not exceed POD_ATTN_STATIC_SCRATCH_BYTES.
+ *   plan            : a plan made with variant POD_ATTN_FUSED and without instrumentation; its
+ *                     pod_attn_workspace_bytes must not exceed POD_ATTN_STATIC_SCRATCH_BYTES.
+ *   stream          : a stream of the current device (the array used is the current device's).
  *   other arguments : as for pod_attn_run (inputs read only, outputs overwritten).
  * The first call on a device looks up the array's device address on that device (with the
  * device current); make that first call before any stream capture on the device.
  * All calls share the one array, which keeps the last call's contents: calls whose work
  * overlaps on the GPU (different streams, or another host thread) race and give wrong results;
- * serialise them. Device-detected errors (bad block index, timeout) are recorded in the shared
- * array and are not reported by this entry point.
- * Errors: INVALID_ARG (null plan, variant other than FUSED, null/misaligned tensors),
- * WORKSPACE (plan needs more than POD_ATTN_STATIC_SCRATCH_BYTES), CUDA. */
+ * serialise them. Device-detected errors (bad block index, timeout) are recorded in the
+ * array's status word: read them with pod_attn_last_device_status(plan, NULL, stream).
+ * Errors: INVALID_ARG (null plan, variant other than FUSED, an instrumented plan, a stream of
+ * another device, null/misaligned tensors), UNSUPPORTED (a plan for the e4m3 cache), WORKSPACE
+ * (plan needs more than POD_ATTN_STATIC_SCRATCH_BYTES), CUDA. */
 #define POD_ATTN_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 pod_attn_status pod_attn_run_static(pod_attn_plan_t plan, const void* q_prefill,
                                     const void* q_decode, const void* k_pool,

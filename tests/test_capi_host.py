@@ -166,7 +166,8 @@ def restated_decode_only_chunk(nblks, num_sms, kv_fp8):
     return best_c
 
 
-def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True, kv_fp8=False):
+def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True, kv_fp8=False,
+                  prefill_cap=0):
     """Items: prefill = (chunk, pair of query tiles of 128/hp tokens x hp heads, first head,
     split) over 128-key steps of both tiles (cost 114 each), with hp the largest power of two
     dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8
@@ -193,7 +194,8 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
             du.append((d, g, L, _cdiv(L, 16)))
             total += _cdiv(L, 16) * 8
     target = max(1, total // (slots * 4))
-    chunk_p = restated_prefill_chunk([x[4] for x in pu], num_sms) if pu and not psplit else 0
+    prefill_ctas = min(prefill_cap, num_sms) if prefill_cap > 0 else num_sms
+    chunk_p = restated_prefill_chunk([x[4] for x in pu], prefill_ctas) if pu and not psplit else 0
     units, lp, ld = [], [], []
     slots_used = [0, 0]
 
@@ -232,7 +234,7 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
             ld.append(((b1 - b0) * 8, [1, d, g, 0, b0 * 16, min(L, b1 * 16), u, k]))
     lp.sort(key=lambda x: -x[0])   # stable: longest first, ties in enumeration order
     ld.sort(key=lambda x: -x[0])
-    return ([w for _, w in lp], [w for _, w in ld], units, 1,
+    return ([w for _, w in lp], [w for _, w in ld], units, prefill_ctas,
             min(num_sms, len(lp) + len(ld)))
 
 
@@ -257,13 +259,15 @@ def test_planner_matches_python_restatement(lib, seed):
     num_sms = rng.choice([148, 152, 7])
     psplit = rng.choice([0, 0, 3])
     dsplit = rng.choice([0, 0, 5, 100])
+    pcap = rng.choice([0, 0, 1, 5, 500])
     maxb = _cdiv(max(pkv + dkv + [1]), 16)
     p = B.Plan(Hq, Hkv, cu if q_lens else [], pkv + dkv, len(dkv), 100, maxb, 0.1,
-               num_sms=num_sms, prefill_splits=psplit, decode_splits=dsplit)
+               num_sms=num_sms, prefill_splits=psplit, decode_splits=dsplit,
+               max_prefill_ctas=pcap)
     got_p, got_d, got_u = p.items()
     exp_p, exp_d, exp_u, cap, grid = restated_plan(Hq, Hkv, cu if q_lens else [], pkv + dkv,
                                                    len(dkv), num_sms, psplit=psplit,
-                                                   dsplit=dsplit)
+                                                   dsplit=dsplit, prefill_cap=pcap)
     assert got_p == exp_p
     assert got_d == exp_d
     assert got_u == exp_u
@@ -443,3 +447,39 @@ def test_prefill_chunk_choice_on_configs(lib, i, items, max_steps):
     steps = [_cdiv(it[5] - it[4], 128) for it in items_p]
     assert len(items_p) == items
     assert max(steps) == max_steps
+
+
+def test_ctas_per_sm_option(lib):
+    """One persistent CTA per SM is the only layout: 0 and 1 plan, larger values are
+    unsupported, negative values invalid."""
+    for v in (0, 1):
+        p = B.Plan(8, 2, [0, 40], [40, 90], 1, 20, 8, 0.1, num_sms=4, ctas_per_sm=v)
+        assert p.info()["ctas_per_sm"] == 1
+    with pytest.raises(B.PodAttnError) as e:
+        B.Plan(8, 2, [0, 40], [40, 90], 1, 20, 8, 0.1, num_sms=4, ctas_per_sm=2)
+    assert e.value.code == B.ERR_UNSUPPORTED
+    with pytest.raises(B.PodAttnError) as e:
+        B.Plan(8, 2, [0, 40], [40, 90], 1, 20, 8, 0.1, num_sms=4, ctas_per_sm=-1)
+    assert e.value.code == B.ERR_INVALID_ARG
+
+
+def test_max_prefill_ctas_option(lib):
+    """The prefill cap is reported, bounds the prefill-only grid and sizes the prefill splits
+    for that many slots (a smaller cap makes the makespan model cut outputs differently); 0 or a
+    value above the SM count means every CTA; negative values are invalid."""
+    cu, kv = [0, 2048], [30720] + [20000] * 4
+    base = B.Plan(32, 4, cu, kv, 4, 12000, 1920, 0.1, num_sms=152, variant="serial")
+    assert base.info()["max_prefill_ctas"] == 152
+    for cap in (1, 3, 40):
+        p = B.Plan(32, 4, cu, kv, 4, 12000, 1920, 0.1, num_sms=152, variant="serial",
+                   max_prefill_ctas=cap)
+        inf = p.info()
+        assert inf["max_prefill_ctas"] == cap
+        assert inf["grid_prefill"] == min(cap, inf["num_prefill_items"])
+        exp_p, _, _, exp_cap, _ = restated_plan(32, 4, cu, kv, 4, 152, prefill_cap=cap)
+        assert p.items()[0] == exp_p and exp_cap == cap
+    assert B.Plan(32, 4, cu, kv, 4, 12000, 1920, 0.1, num_sms=152,
+                  max_prefill_ctas=500).info()["max_prefill_ctas"] == 152
+    with pytest.raises(B.PodAttnError) as e:
+        B.Plan(32, 4, cu, kv, 4, 12000, 1920, 0.1, num_sms=152, max_prefill_ctas=-2)
+    assert e.value.code == B.ERR_INVALID_ARG

@@ -182,3 +182,24 @@ def test_instrumentation_records_every_item_and_mixes_kinds():
         kinds_per_sm.setdefault(r["smid"], set()).add(r["kind"])
     both = sum(1 for k in kinds_per_sm.values() if k == {0, 1})
     assert both >= len(kinds_per_sm) // 2, (both, len(kinds_per_sm))
+
+
+@pytest.mark.parametrize("cap", [1, 5])
+def test_prefill_cta_cap_keeps_prefill_on_the_first_ctas(cap):
+    """max_prefill_ctas: every prefill item runs on a CTA below the cap (the kernel's own
+    records), the other CTAs run decode work only, and the outputs match the oracle."""
+    cpu = W.make_batch(32, 8, [700, 300], [2700, 300], [3000] * 24, seed=11)
+    ref_p, ref_d = oracle.hybrid_attention(cpu)
+    dev = cpu.to("cuda")
+    plan = B.Plan.for_batch(dev, instrument=True, max_prefill_ctas=cap)
+    assert plan.info()["max_prefill_ctas"] == cap
+    ws = plan.alloc_workspace()
+    plan.upload(ws)
+    o_p, o_d = B.run_batch(plan, dev, ws)
+    torch.cuda.synchronize()
+    assert plan.device_status(ws) == B.OK
+    recs = plan.records(ws)
+    assert {r["cta"] for r in recs if r["kind"] == 0} <= set(range(cap))
+    assert any(r["kind"] == 1 and r["cta"] >= cap for r in recs)
+    assert_close(o_p, ref_p, f"cap {cap} prefill")
+    assert_close(o_d, ref_d, f"cap {cap} decode")

@@ -1,6 +1,7 @@
 """GPU parity on the 200-iteration hybrid-batching trace (Llama-3-8B shape, persistent paged
-pool): selected iterations of both mixes run through the fused kernel exactly as the benchmark
-runs them; sampled outputs are checked against the fp64 oracle row by row.
+pool): selected iterations of both mixes (every quarter's first and last, two inside) run
+through the fused kernel exactly as the benchmark runs them; sampled outputs are checked against
+the fp64 oracle row by row.
 
 The oracle gets a compact CPU copy holding only the blocks of the sampled sequences (with the
 block tables renumbered), so a check needs a few hundred MB instead of the whole pool.
@@ -77,11 +78,15 @@ def _compact(batch, seqs):
 
 @pytest.fixture(scope="module", params=["a", "b"])
 def pool(request):
-    tr = W.trace(request.param)
+    # decode counts sized from this device's SM count, as the benchmark sizes them
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tr = W.trace(request.param, decode_targets=W.trace_decode_targets(sms))
     return W.TracePool(tr, device="cuda")
 
 
-@pytest.mark.parametrize("it", [0, 77, 199])
+# the first and last iterations of each quarter (each holds a different decode count) and two
+# inside them
+@pytest.mark.parametrize("it", [0, 25, 49, 50, 77, 99, 100, 149, 150, 199])
 def test_trace_iteration_sampled(pool, it):
     b = pool.batch(it)
     o_p, o_d = B.hybrid_attention(b, variant="fused")

@@ -6,7 +6,7 @@ nothing of the method. A batch is one layer of one serving iteration: some promp
 ("Week 6: Beyond PyTorch: Custom Kernel과 vLLM", §"한 스텝에 여러 종류의 request 섞기" and
 §"PagedAttention").
 
-Recipe (also stated in the design notes):
+Recipe:
   * integer choices (lengths, prefix offsets) come from ``random.Random(seed)``;
   * physical blocks are a ``torch.randperm`` of the pool (seed-derived CPU generator), so a
     sequence's logical blocks are scattered;

@@ -321,7 +321,11 @@ typedef struct {
 pod_attn_status pod_attn_plan_bucket(pod_attn_plan_t plan, pod_attn_bucket* out);
 
 /* Copy the host work lists: prefill items first, then decode items, then the unit table, each
- * item info.item_words int32 words (see DESIGN of the item encoding in the planner source).
+ * item info.item_words (8) int32 words: kind (0 prefill, 1 decode); prefill chunk index or
+ * decode sequence index; prefill tile-pair index or decode kv-head; prefill first query head
+ * (decode 0); first key row of the split; one past its last key row; the unit index of a split
+ * output (-1 when the item writes its output directly); the split's index within the unit. A
+ * unit is 4 words: split count, first partial slot, kind, 0.
  *   out   : host buffer of `capacity` int32 words, or NULL to query the size only.
  *   count : receives the number of words (written, or needed when out is NULL).
  * Used to check the planner bit for bit. Errors: INVALID_ARG (null plan/count, capacity too

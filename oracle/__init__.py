@@ -75,6 +75,8 @@ def _load():
             lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
             lib.oracle_append_fp8.restype = I
             lib.oracle_append_fp8.argtypes = [I, I, I, I, L, I, P, P, P, P, P, P, P, P]
+            lib.oracle_append_bf16.restype = I
+            lib.oracle_append_bf16.argtypes = [I, I, I, I, I, L, I, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -201,6 +203,28 @@ def e4m3_to_double(bits: int) -> float:
 def e4m3_from_float(x) -> int:
     """The e4m3 code of a float32 value (round to nearest even, saturating; see oracle.c)."""
     return int(_load().oracle_e4m3_from_float(float(x)))
+
+
+def append_bf16(batch, k_new, v_new, k_pool=None, v_pool=None):
+    """The bf16 pools after appending the iteration's new tokens (rows of k_new / v_new
+    [T_p + Nd][Hkv][D]: the prefill chunks' tokens in order, then one per decode sequence) to
+    ``batch`` (a ``HybridBatch``; its lengths and block tables say where each row goes). Starts
+    from ``k_pool`` / ``v_pool`` when given, else from the batch's pools; returns new
+    (k_pool, v_pool) numpy uint16 arrays; the inputs are not modified."""
+    kp = np.array(_u16(batch.k_pool if k_pool is None else k_pool), copy=True)
+    vp = np.array(_u16(batch.v_pool if v_pool is None else v_pool), copy=True)
+    kn, vn = _u16(k_new), _u16(v_new)
+    bt = _i32(batch.block_tables)
+    cu = _i32(batch.cu_seqlens_q)
+    kv = _i32(batch.kv_lens)
+    rc = _load().oracle_append_bf16(int(batch.num_kv_heads), int(batch.head_dim),
+                                    int(batch.block_size), int(batch.num_prefill_seqs),
+                                    int(batch.num_decode_seqs), int(kp.shape[0]),
+                                    int(bt.shape[1]) if bt.ndim == 2 else 0, _ptr(cu), _ptr(kv),
+                                    _ptr(bt), _ptr(kn), _ptr(vn), _ptr(kp), _ptr(vp))
+    if rc != 0:
+        raise ValueError(f"oracle_append_bf16 failed with code {rc}")
+    return kp, vp
 
 
 def append_fp8(batch, k_new, v_new):

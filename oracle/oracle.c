@@ -20,7 +20,7 @@
  *                                         merge exactly
  *     §"KV 헤드 줄이기 — MHA → GQA → MQA → MLA"   several query heads share one KV head
  *
- * Readings where the pages are silent (also listed in the design notes):
+ * Readings where the pages are silent:
  *   - causal alignment of a chunk with a prefix: local token i of a chunk of q_len tokens in a
  *     sequence of kv_len cached rows sits at absolute position p = kv_len - q_len + i and sees
  *     rows 0..p;
@@ -326,6 +326,44 @@ uint8_t oracle_e4m3_from_float(float x) {
     }
   }
   return sign | (uint8_t)best;
+}
+
+/*
+ * Append of an iteration's new tokens to a bf16 cache ("Week 6: Beyond PyTorch: Custom Kernel과
+ * vLLM", §"PagedAttention": the cache only grows by appended rows; §"한 스텝에 여러 종류의
+ * request 섞기": an extend chunk follows its sequence's cached rows, a decode token is its
+ * sequence's last row). New token t carries one K and one V row per kv-head (k_new / v_new are
+ * bf16 [T_p + Nd][Hkv][D]; the prefill chunks' tokens first in order, then one token per decode
+ * sequence). Chunk token i of prefill sequence s goes to position kv_len[s] - q_len(s) + i,
+ * decode d's token to position kv_len[Np + d] - 1; position j of a sequence is row j % BS of
+ * its physical block block_tables[seq][j / BS]. The rows are copied bit for bit into the pools
+ * [num_blocks][Hkv][BS][D]. Returns 0, or -1 on a bad table entry (that row is not written).
+ */
+int oracle_append_bf16(int Hkv, int D, int BS, int Np, int Nd, int64_t num_blocks, int max_blocks,
+                       const int32_t* cu_seqlens, const int32_t* kv_lens,
+                       const int32_t* block_tables, const uint16_t* k_new, const uint16_t* v_new,
+                       uint16_t* k_pool, uint16_t* v_pool) {
+  int err = 0;
+  int64_t t = 0;  /* index of the new token in k_new / v_new */
+  for (int seq = 0; seq < Np + Nd; ++seq) {
+    const int64_t q_len = seq < Np ? (int64_t)cu_seqlens[seq + 1] - cu_seqlens[seq] : 1;
+    const int64_t first = (int64_t)kv_lens[seq] - q_len;
+    for (int64_t i = 0; i < q_len; ++i, ++t) {
+      const int64_t pos = first + i;
+      const int32_t phys = block_tables[(int64_t)seq * max_blocks + pos / BS];
+      if (phys < 0 || phys >= num_blocks) {
+        err = -1;
+        continue;
+      }
+      for (int g = 0; g < Hkv; ++g) {
+        const int64_t dst = (((int64_t)phys * Hkv + g) * BS + pos % BS) * D;
+        const int64_t src = (t * Hkv + g) * D;
+        memcpy(k_pool + dst, k_new + src, (size_t)D * sizeof(uint16_t));
+        memcpy(v_pool + dst, v_new + src, (size_t)D * sizeof(uint16_t));
+      }
+    }
+  }
+  return err;
 }
 
 /*

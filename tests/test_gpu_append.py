@@ -1,8 +1,9 @@
 """GPU checks of pod_attn_run_append (the KV append in front of the attention), through the
 C ABI: the pools come in with the iteration's new rows missing (NaN), the call writes them and
-attends. The pools afterwards must equal the complete pools bit for bit, and the outputs must
-equal, bit for bit, those of pod_attn_run on the complete pools — itself checked against the
-fp64 oracle in test_gpu_parity.py (configuration 1 is checked against the oracle here too)."""
+attends. The pools afterwards must equal, bit for bit, the oracle's append of those rows
+(oracle.append_bf16), and the outputs must equal, bit for bit, those of pod_attn_run on the
+complete pools — itself checked against the fp64 oracle in test_gpu_parity.py (configuration 1
+is checked against the oracle here too)."""
 import numpy as np
 import pytest
 import torch
@@ -33,12 +34,14 @@ def _run_both(batch, variant, **kw):
     ref_p, ref_d = B.run_batch(plan, batch, ws)                 # rows already in the pools
     assert plan.device_status(ws) == B.OK
     k_new, v_new, kp, vp = W.split_off_new_rows(batch)
+    # the expected pools: the oracle's append of the new rows to the pools without them
+    exp_k, exp_v = oracle.append_bf16(batch, k_new, v_new, kp, vp)
     o_p, o_d = torch.empty_like(batch.q_prefill), torch.empty_like(batch.q_decode)
     side = torch.cuda.Stream() if variant == "streams" else None
     plan.run_append(batch.q_prefill, batch.q_decode, k_new, v_new, kp, vp, batch.block_tables,
                     batch.cu_seqlens_q, batch.kv_lens, o_p, o_d, ws, stream2=side)
     assert plan.device_status(ws) == B.OK
-    assert torch.equal(_bits(kp), _bits(batch.k_pool)) and torch.equal(_bits(vp), _bits(batch.v_pool))
+    assert np.array_equal(oracle._u16(kp), exp_k) and np.array_equal(oracle._u16(vp), exp_v)
     assert torch.equal(_bits(o_p), _bits(ref_p)) and torch.equal(_bits(o_d), _bits(ref_d))
     return o_p, o_d
 

@@ -397,3 +397,50 @@ def test_fp8_append_rebuilds_the_quantised_rows():
     fb.k8, fb.v8 = torch.from_numpy(k8), torch.from_numpy(v8)
     fb.v_scale = torch.from_numpy(vs)
     assert np.array_equal(oracle.decode_fp8(fb), oracle.decode_fp8(full))
+
+
+def test_bf16_append_places_rows_at_their_hand_computed_slots():
+    """A 5-token chunk at kv_len 20 (positions 15..19) through table [3, 1], then a decode at
+    kv_len 33 (position 32) through table [0, 2, 4]: the rows land at (block 3, row 15),
+    (block 1, rows 0..3) and (block 4, row 0), for each kv-head, and nothing else changes."""
+    Hkv, D = 2, 4
+    nb = 5
+    zero = torch.zeros((nb, Hkv, 16, D), dtype=torch.bfloat16)
+    b = W.HybridBatch(
+        num_q_heads=2, num_kv_heads=Hkv, head_dim=D, block_size=16, q_lens=[5],
+        prefill_kv_lens=[20], decode_kv_lens=[33], scale=0.5,
+        q_prefill=torch.zeros((5, 2, D), dtype=torch.bfloat16),
+        q_decode=torch.zeros((1, 2, D), dtype=torch.bfloat16), k_pool=zero, v_pool=zero,
+        block_tables=torch.tensor([[3, 1, -1], [0, 2, 4]], dtype=torch.int32),
+        cu_seqlens_q=torch.tensor([0, 5], dtype=torch.int32),
+        kv_lens=torch.tensor([20, 33], dtype=torch.int32))
+    # new token t, kv-head g, channel c holds t*10 + g + c/8 (exact in bf16); V is its negative
+    vals = torch.tensor([[[t * 10 + g + c / 8 for c in range(D)] for g in range(Hkv)]
+                         for t in range(6)], dtype=torch.float32).to(torch.bfloat16)
+    kp, vp = oracle.append_bf16(b, vals, -vals)
+    kf = torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).float()
+    vf = torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16).float()
+    slots = [(3, 15), (1, 0), (1, 1), (1, 2), (1, 3), (4, 0)]   # token t -> (block, row)
+    expect = torch.zeros((nb, Hkv, 16, D))
+    for t, (blk, row) in enumerate(slots):
+        expect[blk, :, row, :] = vals[t].float()
+    assert torch.equal(kf, expect) and torch.equal(vf, -expect)
+
+
+def test_bf16_append_rebuilds_the_removed_rows():
+    """Remove an iteration's new rows from a seeded batch (NaN in their place) and append them
+    again: the pools are the original ones bit for bit, so the attention over them is too."""
+    full = W.make_batch(8, 2, [37, 16], [100, 16], [1, 17, 48], seed=13)
+    k_new, v_new, kp0, vp0 = W.split_off_new_rows(full)
+    kp, vp = oracle.append_bf16(full, k_new, v_new, kp0, vp0)
+    assert np.array_equal(kp, oracle._u16(full.k_pool)) and np.array_equal(vp, oracle._u16(full.v_pool))
+
+
+def test_bf16_append_skips_a_bad_table_entry():
+    b = W.make_batch(4, 1, [], [], [20], seed=2)
+    bad = b.block_tables.clone()
+    bad[0, 1] = b.num_blocks + 3
+    b.block_tables = bad
+    rows = torch.ones((1, 1, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        oracle.append_bf16(b, rows, rows)

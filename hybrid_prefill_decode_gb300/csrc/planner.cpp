@@ -379,23 +379,37 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
       std::memcpy(&words_d[id * kItemWords], w, sizeof(w));
     }
   }
-  // longest first, ties in enumeration order: a stable counting sort over the cost, counted in
-  // its unit (a prefill step or a decode block, so the counts span the longest item)
-  auto order = [](const std::vector<int64_t>& cost, int64_t unit, const std::vector<int32_t>& words,
-                  std::vector<int32_t>& out) {
-    const size_t n = cost.size();
+  // Items are taken longest first. Decode items: by cost, ties in enumeration order (a stable
+  // counting sort over the cost in blocks). Prefill items: by cost rounded to a coarse relative
+  // bucket (3 significant bits, ~12 % steps), then by split index, then in enumeration order, so
+  // that the items running at once share their key ranges (split k of every output reads the
+  // same part of its sequence) and keep the K/V rows they read resident in L2, while the order
+  // stays longest first to within a bucket.
+  auto order = [](const std::vector<int64_t>& key, const std::vector<int32_t>& words,
+                  std::vector<int32_t>& out) {  // stable, largest key first
+    const size_t n = key.size();
     int64_t top = 0;
-    for (int64_t c : cost) top = std::max(top, c / unit);
-    std::vector<size_t> start((size_t)top + 2, 0);  // by (top - cost units): longest first
-    for (int64_t c : cost) ++start[(size_t)(top - c / unit) + 1];
+    for (int64_t k : key) top = std::max(top, k);
+    std::vector<size_t> start((size_t)top + 2, 0);
+    for (int64_t k : key) ++start[(size_t)(top - k) + 1];
     for (size_t b = 1; b < start.size(); ++b) start[b] += start[b - 1];
     out.resize(n * kItemWords);
     for (size_t i = 0; i < n; ++i)
-      std::memcpy(&out[(start[(size_t)(top - cost[i] / unit)]++) * kItemWords],
-                  &words[i * kItemWords], kItemWords * sizeof(int32_t));
+      std::memcpy(&out[(start[(size_t)(top - key[i])]++) * kItemWords], &words[i * kItemWords],
+                  kItemWords * sizeof(int32_t));
   };
-  order(cost_p, kPrefillStepCost, words_p, plan->items_p);
-  order(cost_d, kDecodeBlockCost, words_d, plan->items_d);
+  auto bucket = [](int64_t steps) -> int64_t {  // monotone, 3 significant bits above 15
+    if (steps < 16) return steps;
+    int bl = 0;
+    while ((steps >> bl) != 0) ++bl;
+    return 16 + (int64_t)(bl - 5) * 8 + ((steps >> (bl - 4)) & 7);
+  };
+  for (size_t i = 0; i < n_p; ++i)
+    cost_p[i] = bucket(cost_p[i] / kPrefillStepCost) * kMaxPrefillSplits +
+                (kMaxPrefillSplits - 1 - words_p[i * kItemWords + 7]);
+  for (size_t i = 0; i < n_d; ++i) cost_d[i] /= kDecodeBlockCost;
+  order(cost_p, words_p, plan->items_p);
+  order(cost_d, words_d, plan->items_d);
   plan->num_p_slots = p_slots;
   // where each token of this iteration sits in its sequence (the KV append writes its K/V
   // row there): chunk token i of prefill sequence s at kv_len - q_len + i, a decode token at

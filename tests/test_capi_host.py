@@ -108,6 +108,15 @@ def _rebalanced(nblk, c):
     return _cdiv(nblk, chunk), chunk
 
 
+def _bucket(steps):
+    """Cost buckets of the prefill order: exact below 16 steps, above that the bit length and
+    the next three bits (so two costs share a bucket when they differ by under ~12 %)."""
+    if steps < 16:
+        return steps
+    bl = steps.bit_length()
+    return 16 + (bl - 5) * 8 + ((steps >> (bl - 4)) & 7)
+
+
 def _list_span(costs, slots):
     """Items taken longest first, each by the slot that frees first: the last finish time."""
     free = [0] * slots
@@ -232,7 +241,9 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
         for k in range(ns):
             b0, b1 = k * chunk, min(nblk, (k + 1) * chunk)
             ld.append(((b1 - b0) * 8, [1, d, g, 0, b0 * 16, min(L, b1 * 16), u, k]))
-    lp.sort(key=lambda x: -x[0])   # stable: longest first, ties in enumeration order
+    # prefill: cost in a coarse relative bucket (3 significant bits), then split index; decode:
+    # cost; both stable (ties in enumeration order)
+    lp.sort(key=lambda x: (-_bucket(x[0] // 114), x[1][7]))
     ld.sort(key=lambda x: -x[0])
     return ([w for _, w in lp], [w for _, w in ld], units, prefill_ctas,
             min(num_sms, len(lp) + len(ld)))

@@ -6,16 +6,15 @@
 // count just above a multiple of what the SMs hold at once costs a whole extra wave.
 //
 // This file turns one hybrid batch into two work lists (virtual CTAs):
-//   prefill item = (chunk s, tile pair t, block of hp query heads, KV split k) — a tile is
-//                  128 rows = 128/hp tokens x hp heads of one kv-head group, and an item runs
-//                  two consecutive tiles, so every K/V tile it loads serves 2 x 128 rows
+//   prefill item = (chunk s, tile t, block of hp query heads, KV split k) — a tile is 128
+//                  rows = 128/hp tokens x hp heads of one kv-head group
 //   decode item  = (sequence d, kv-head g, KV split k)   — one item serves all G query heads
 //                  of the kv-head (GQA grouping, "LLMSO - W4", §"KV 헤드 줄이기")
 // and sizes the persistent grid: one CTA per SM, each with a prefill slot and a decode slot
 // that pull items from the two lists.
 //
 // Split planning. Every item gets a cost (decode: 8 per 16-row K/V block, i.e. its bytes in
-// KiB; prefill: 114 per 128-key step of its 256 rows, its tensor-core time expressed in the
+// KiB; prefill: 57 per 128-key step of its 128 rows, its tensor-core time expressed in the
 // same byte-time units at a 6.8 TB/s : 1 PFLOP/s balance). Outputs are split along the keys
 // ("LLMSO - W4", §"FlashDecoding — decode 단계의 병렬성 확보"), so no single item can leave a
 // long tail after the others finish:
@@ -52,10 +51,10 @@ namespace pod {
 namespace {
 
 constexpr int64_t kDecodeBlockCost = 8;   // 16 rows x (K + V) x 128 x bf16 = 8 KiB
-constexpr int64_t kPrefillStepCost = 114;  // 2 x 4*128*128*128 FLOPs at the byte-time balance
+constexpr int64_t kPrefillStepCost = 57;  // 4*128*128*128 FLOPs at the byte-time balance
 constexpr int kMinDecodeBlocksPerSplit = 12;
 constexpr int kMinPrefillTilesPerSplit = 4;
-constexpr int64_t kPrefillItemOverhead = 4;  // per-item start and epilogue, in steps
+constexpr int64_t kPrefillItemOverhead = 8;  // per-item start and epilogue, in steps
 constexpr int64_t kDecodeItemOverhead = 2;   // per-item start and merge, in warp block-times
 constexpr int kDecodeGroupsBf16 = 3;         // 4-warp decode groups per SM, bf16 cache
 constexpr int kDecodeGroupsFp8 = 4;          // ... e4m3 cache
@@ -187,7 +186,6 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
   plan->group = G;
   const int hp = G & -G;  // largest power of two dividing G (G <= 8)
   const int tq = kTileM / hp;
-  const int64_t pair_tokens = 2 * tq;  // tokens of one prefill item (tiles A and B)
   plan->head_pack = hp;
   plan->tile_tokens = tq;
   plan->num_sms = num_sms;
@@ -214,9 +212,9 @@ pod_attn_status build_plan(const pod_attn_problem& prob, const int32_t* cu, cons
     const int64_t q = (int64_t)cu[s + 1] - cu[s], L = kv[s], P = L - q;
     pf += 4.0 * D * Hq * (double)(causal ? q * P + q * (q + 1) / 2 : q * L);
     pb += (double)L * row_bytes + 4.0 * q * Hq * D;
-    for (int64_t t = 0; t < ceil_div(q, pair_tokens); ++t) {
-      // causal: the pair's last token sees up to its own position; otherwise every row
-      const int64_t kend = causal ? P + std::min(q, (t + 1) * pair_tokens) : L;
+    for (int64_t t = 0; t < ceil_div(q, (int64_t)tq); ++t) {
+      // causal: the tile's last token sees up to its own position; otherwise every row
+      const int64_t kend = causal ? P + std::min(q, (t + 1) * tq) : L;
       const int64_t nt = ceil_div(kend, kTileN);
       for (int h0 = 0; h0 < Hq; h0 += hp) {
         pu.push_back({s, (int)t, h0, kend, nt});

@@ -95,13 +95,13 @@ struct Params {
 };
 
 struct SmemCtl {
-  uint64_t q_full;                 // both query tiles of a prefill item landed
+  uint64_t q_full;                 // the item's queries are in TMEM (one arrival per warp)
   uint64_t kv_full[kKVStages];     // the ring stage holds its K or V tile
-  uint64_t kv_empty[kKVStages];    // both tiles' MMAs that read the stage completed
-  uint64_t s_full[2];              // [tile] S of the tile's step computed
-  uint64_t p_ready[2];             // [tile] the tile's P written (one arrival per warp)
-  uint64_t pv_done[2];             // [tile] the tile's P·V of the step completed
-  uint64_t o_done[2];              // [tile] the tile's last P·V of the item completed
+  uint64_t kv_empty[kKVStages];    // the MMAs that read the stage completed
+  uint64_t s_full[2];              // [buffer] S of the buffer's step computed
+  uint64_t p_ready[2];             // [buffer] P of the step written (one arrival per warp)
+  uint64_t pv_done;                // one completion per step: its P·V completed
+  uint64_t o_done;                 // the item's last P·V completed
   uint64_t dslot[kWarps][kDecodeSlotsFp8];  // decode rings, by absolute warp (slots in use:
                                             // kDecodeSlots on a bf16 cache, kDecodeSlotsFp8 on e4m3)
   uint32_t tmem_base;
@@ -189,31 +189,38 @@ __device__ bool wait_appended(const Params& p, PipeState& ps, const WaitCtx& wc)
 }
 
 // ============================================================================ prefill item
-// One prefill item: tiles A and B (two consecutive 128-row query tiles of one chunk and head
-// block) against a range of keys in 128-key steps. Steps are numbered n by a counter that runs
-// on across items; step n reads K(n) and V(n), entries 2n and 2n + 1 of one ring of kKVStages
-// tiles. Warp 0 loads; warp 1 issues both tiles' S MMAs and warp 3 their P·V MMAs, each tile
-// into its own S buffer and O accumulator; warps 4-7 and 8-11 run the softmax of tile A and
-// tile B, one query row per thread and all 128 keys of a step. While one tile's softmax runs,
-// the tensor cores work through the other tile's P·V and next S, and every K/V tile brought
-// into shared memory serves 256 query rows. Each row keeps its running max m and sum l (log2
-// units); O is rescaled only when the row's max grows by more than 2^8 (the lazy-rescale
-// threshold), and the epilogue divides by l.
-// HD (head dim) is 128 or 64; shared memory and TMEM keep the layout of 128 (a 64-dim head
-// uses the first 64-column half of every tile and the first 64 columns of O).
+// One prefill item: one 128-row query tile of one chunk and head block against a range of keys
+// in 128-key steps (the single-pass online softmax of "Week 6: Beyond PyTorch: Custom Kernel과
+// vLLM", §"FlashAttention의 single-pass 트릭"; "LLMSO - W4", §"FlashAttention — I/O를 줄이는
+// 방향"). Steps are numbered n by a counter that runs on across items. TMEM holds the tile's O
+// accumulator, two S buffers (step n uses buffer n & 1) and the tile's queries, which are the A
+// operand of every S MMA: S(j + 1) is computed while the softmax of step j runs, and the tensor
+// cores read only K and V from shared memory.
+//  * Warps 0 (K) and 2 (V) load K and V through one ring of kKVStages tiles in the order the
+//    MMAs consume them: K(0), K(1), then V(j) and K(j + 2) for each step j.
+//  * Warp 1 issues the P·V MMAs, P·V(j) once P(j) is written; warp 3 issues the S MMAs: S(0),
+//    S(1), then S(j + 2) into the S buffer whose P P·V(j) reads, once P·V(j) has completed.
+//  * Warps 4-11 load the tile's queries into TMEM and run the softmax, two threads per query
+//    row: warps w and w + 4 reach the same TMEM lanes (rows) and take keys 0-63 and 64-127 of
+//    each step. The two halves of a row exchange their maxima through TMEM, so that P of the
+//    whole row is taken against one max; each half keeps its own share of the row sum l.
+// Each row keeps its running max m (log2 units); O is rescaled only when the row's max grows by
+// more than 2^8 (the lazy-rescale threshold), once the previous P·V has completed; the epilogue
+// divides by l. HD (head dim) is 128 or 64; a 64-dim head uses the first half of every K/V tile
+// and of O.
 template <int HD>
-__device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUtensorMap* tmk,
-                             const CUtensorMap* tmv, const CUtensorMap* tmkb,
-                             const CUtensorMap* tmvb, const int32_t* it,
-                             uint8_t* smem, SmemCtl* ctl, PipeState& ps, const WaitCtx& wc) {
+__device__ void prefill_item(const Params& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                             const CUtensorMap* tmkb, const CUtensorMap* tmvb,
+                             const int32_t* it, uint8_t* smem, SmemCtl* ctl, PipeState& ps,
+                             const WaitCtx& wc) {
   static_assert(HD == 64 || HD == 128, "head dim");
   constexpr int kHalves = HD / 64;                  // 64-dim halves (128-byte swizzle atoms)
   constexpr uint32_t kIdescPV = idesc_bf16(kTileM, HD, 0, 1);  // O += P V, V N-major
-  constexpr uint32_t kQBytes = kTileM * HD * 2, kTileBytes = kTileN * HD * 2;
+  constexpr uint32_t kTileBytes = kTileN * HD * 2;
   constexpr uint32_t kBlockBytes = kBlockSize * HD * 2;
   constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
-  // Both tiles are laid out block by block, so that one box of a per-block map brings all of a
-  // paged block (the TMA unit takes ~60 cycles per box, whatever its size):
+  // K and V tiles are laid out block by block, so that one box of a per-block map brings all of
+  // a paged block (the TMA unit takes ~60 cycles per box, whatever its size):
   //  * V: [block][64-dim half][16 rows][128 bytes]; each P·V MMA reads one block;
   //  * K (head dim 128): [block][8-row group][64-dim half][8 rows][128 bytes], so that the 8-row
   //    groups of one half lie 2 KiB apart throughout the tile and an S MMA reads 16 dims of all
@@ -224,44 +231,38 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
   constexpr uint32_t kKHalfOff = 1024;                // second 64-dim half of a K group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = it[1], t = it[2], h0 = it[3], kb = it[4], ke = it[5], unit = it[6], split = it[7];
-  const int g = h0 / p.G;  // the tiles' heads h0 .. h0 + hp - 1 share kv-head g
+  const int g = h0 / p.G;  // the tile's heads h0 .. h0 + hp - 1 share kv-head g
   const int q0 = p.cu_seqlens[s];
   const int qlen = p.cu_seqlens[s + 1] - q0;
   const int L = p.kv_lens[s];
   const int P = L - qlen;  // cached prefix rows before this chunk
-  const int ntiles = (ke - kb + kTileN - 1) / kTileN;
-  const bool has_b = (2 * t + 1) * p.tq < qlen;  // tile B holds a token of the chunk
+  const int ntiles = (ke - kb + kTileN - 1) / kTileN;  // >= 1 (every item has keys)
   const uint32_t n0 = ps.t_cnt;  // this item's first step
-  const uint32_t sQ = smem_u32(smem);  // tile A's query rows, then tile B's
-  const uint32_t sRing = sQ + 2 * kSmemQ;
+  const uint32_t sRing = smem_u32(smem);
+  // The item's 2 ntiles ring entries in consumption order: K(0), K(1), then V(j), K(j + 2) for
+  // j < ntiles - 2, then the last two V. Entry ei is ring entry 2 n0 + ei overall (stage
+  // (2 n0 + ei) % kKVStages).
+  auto ek = [&](int i) { return i < 2 ? i : 2 * i - 1; };              // entry of K(i)
+  auto ev = [&](int j) { return j < ntiles - 2 ? 2 + 2 * j : ntiles + j; };  // entry of V(j)
+  auto stage_of = [&](int ei) { return (2 * n0 + (uint32_t)ei) % kKVStages; };
+  auto phase_of = [&](int ei) { return ((2 * n0 + (uint32_t)ei) / kKVStages) & 1u; };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    // Lane i holds the block-table entry of block i of the next 4 steps (32 blocks): one
-    // coalesced read instead of a dependent global read per block. A stage is free once both
-    // tiles' MMAs that read it completed (kv_empty: one commit after the last of them).
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 0 loads the K entries and warp 2 the V entries (a warp issues about one box per 100
+    // cycles, and a step needs 16). Lane i holds the block-table entry of block i of the next 4
+    // steps (32 blocks): one coalesced read instead of a dependent global read per block. A stage
+    // is free once the MMAs that read it completed (kv_empty: one commit after them).
+    const int my_kv = warp == 2;
     const int32_t* bt_row = p.block_tables + (size_t)s * p.maxb;
     const int nblk_item = (ke - kb + kBlockSize - 1) / kBlockSize;
     const int blk0 = kb / kBlockSize;
-    {
-      // box {64 dims, hp heads, tq tokens}: tile row r = token r / hp, head h0 + r % hp; tokens
-      // past the last chunk read as zeros. Lane 2x + hf copies half hf of tile x (one warp
-      // instruction issues all the copies).
-      const uint32_t qbar = smem_u32(&ctl->q_full);
-      if (lane == 0) mbar_arrive_expect_tx(qbar, 2 * kQBytes);
-      __syncwarp();
-      if (lane < 2 * kHalves) {
-        const int x = lane / kHalves, hf = lane % kHalves;
-        tma_load_3d(sQ + x * kSmemQ + hf * (kSmemQ / 2), tmq, qbar, 64 * hf, h0,
-                    q0 + (2 * t + x) * p.tq);
-      }
-    }
     auto bt_fetch = [&](int j4) -> int {  // entries of steps j4 .. j4 + 3
       const int bi = j4 * kBlocksPerTile + lane;
       return bi < nblk_item ? bt_row[blk0 + bi] : -1;
     };
-    // K(j) and V(j) are ring entries 2n and 2n + 1 (stage e % kKVStages). Each stream keeps its
-    // own window of block-table entries (the one of its current 4 steps and the next).
+    // Each stream (K, V) keeps its own window of block-table entries (the one of its current 4
+    // steps and the next); each stream reads its steps in order.
     int cur_k = -1, nxt_k = bt_fetch(0), win_k = -1;
     int cur_v = -1, nxt_v = nxt_k, win_v = -1;
     auto advance = [&](int& cur, int& nxt, int& win, int j) {
@@ -285,7 +286,20 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     int oka = 1;
     if (lane == 0 && ke > P) oka = wait_appended(p, ps, wc);
     for (int ei = 0; __shfl_sync(0xffffffffu, oka, 0) && ei < 2 * ntiles; ++ei) {
-      const int kv = ei & 1, j = ei >> 1;  // entry ei of the item: K(0), V(0), K(1), V(1), ...
+      // which tile entry ei brings (the inverse of ek / ev above)
+      int kv, j;
+      if (ntiles == 1) {
+        kv = ei, j = 0;
+      } else if (ei < 2) {
+        kv = 0, j = ei;
+      } else if (ei - 2 < 2 * (ntiles - 2)) {
+        const int r = ei - 2;
+        kv = (r & 1) ? 0 : 1;
+        j = (r & 1) ? (r >> 1) + 2 : r >> 1;
+      } else {
+        kv = 1, j = ei - ntiles;
+      }
+      if (kv != my_kv) continue;
       if (kv) advance(cur_v, nxt_v, win_v, j);
       else advance(cur_k, nxt_k, win_k, j);
       const int cur = kv ? cur_v : cur_k;
@@ -294,11 +308,11 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const int bl = lane % kBlocksPerTile;
       const int el = __shfl_sync(0xffffffffu, cur, (j & 3) * kBlocksPerTile + bl);
       const int yl = el < 0 ? p.pool_rows : (el * p.Hkv + g) * kBlockSize;  // past the pool: zeros
-      const uint32_t e = 2 * n0 + ei, stage = e % kKVStages;
+      const uint32_t stage = stage_of(ei);
       int w = 1;
-      // completion e/3 - 1 of the stage's barrier (a fresh barrier passes); polled without a
+      // the stage's previous use has completed (a fresh barrier passes); polled without a
       // sleep hint, as a stage often frees while the next load is already due
-      if (lane == 0) w = mbar_wait(smem_u32(&ctl->kv_empty[stage]), ((e / kKVStages) & 1) ^ 1, wc);
+      if (lane == 0) w = mbar_wait(smem_u32(&ctl->kv_empty[stage]), phase_of(ei) ^ 1u, wc);
       if (!__shfl_sync(0xffffffffu, w, 0)) break;
       const uint32_t dst = sRing + stage * kSmemKTile;
       const int tb = kv == 1 ? tail_blk - j * kBlocksPerTile : -1;
@@ -307,7 +321,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
         const int r = L & 15;
         const int yt = __shfl_sync(0xffffffffu, yl, tb);  // the block's first row
         const uint16_t* src = p.v_pool + (size_t)yt * HD;
-        uint8_t* base = smem + (dst - sQ) + tb * kVBlockBytes;
+        uint8_t* base = smem + (dst - sRing) + tb * kVBlockBytes;
 #pragma unroll
         for (int c = lane; c < kBlockSize * 8 * kHalves; c += 32) {  // 16-byte chunks
           const int i = c / (8 * kHalves), hf = (c >> 3) % kHalves, q16 = c & 7;
@@ -335,123 +349,113 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
     }
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------------ MMA issuers
-    // Warp 1 issues the S MMAs and warp 3 the P·V MMAs of both tiles, each in the order of
-    // the steps and, within a step, tile A first (a single thread issuing all of them runs out
-    // of issue rate before the tensor cores do). S_x(j+1) overwrites P_x(j), so it is issued
-    // once P·V_x(j) has completed (pv_done): tile B's P·V then runs while that wait and tile
-    // A's next softmax do, and the two tiles settle half a period apart. A tile B with no
-    // token of the chunk gets no MMAs but every commit and wait, so each barrier keeps its
-    // count.
-    const uint32_t tmem = ctl->tmem_base;
+    // Warp 1 issues the P·V MMAs and warp 3 the S MMAs: the tensor cores queue only a couple of
+    // MMAs, so one thread that waits on a barrier between its batches leaves them idle, while
+    // two threads keep them fed. S(j + 2) overwrites P(j), so it is issued once P·V(j) has
+    // completed; with two S buffers that wait is a step ahead of the softmax that needs it.
     // A descriptor's start-address field is bits 0-13 of (address >> 4); the tiles lie within
     // the first 256 KiB of shared memory, so a descriptor of (address + offset) is the
-    // descriptor of the address plus (offset >> 4), and each batch builds its base descriptors
-    // once. Q tiles are [half][128 rows][128 bytes] (8-row groups 1 KiB apart); K tiles are
-    // laid out by paged block (above).
-    auto issue_s = [&](int x, uint32_t stK) {
-      if (x == 0 || has_b) {
-        const uint64_t ad0 = sdesc_sw128(sQ + x * kSmemQ, 16, 1024);
-        const uint64_t bd0 = sdesc_sw128(sRing + stK * kSmemKTile, 16, kKGroupStride);
-        const uint32_t dS = tmem + kTmemS + x * 128;
+    // descriptor of the address plus (offset >> 4).
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t tQ = tmem + kTmemQ;  // the tile's queries: column c holds dims 2c, 2c + 1
+    // S(i) = Q K(i)ᵀ into the S buffer of step n0 + i; then the stage of K(i) is released
+    auto issue_s = [&](int i) {
+      const int e = ek(i);
+      const uint32_t st = stage_of(e), b = (n0 + (uint32_t)i) & 1u;
+      const uint64_t bd0 = sdesc_sw128(sRing + st * kSmemKTile, 16, kKGroupStride);
+      const uint32_t dS = tmem + kTmemS + b * 128;
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t aoff = ((kk >> 2) * (kSmemQ / 2) + (kk & 3) * 32) >> 4;
-          const uint32_t boff = ((kk >> 2) * kKHalfOff + (kk & 3) * 32) >> 4;
-          umma_ss(dS, ad0 + aoff, bd0 + boff, kIdescS, kk > 0 ? 1u : 0u);
-        }
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t boff = ((kk >> 2) * kKHalfOff + (kk & 3) * 32) >> 4;
+        umma_ts(dS, tQ + kk * 8, bd0 + boff, kIdescS, kk > 0 ? 1u : 0u);
       }
-      umma_commit(smem_u32(&ctl->s_full[x]));
+      umma_commit(smem_u32(&ctl->s_full[b]));
+      umma_commit(smem_u32(&ctl->kv_empty[st]));
     };
-    auto issue_pv = [&](int x, uint32_t stV, bool first) {
-      if (x == 0 || has_b) {
-        // V (block kk for keys 16kk..) is N-major: 64-column halves 2 KiB apart (LBO), 8-key
-        // groups 1 KiB apart (SBO); P of keys 16kk.. is at column 8kk of the S buffer
-        const uint64_t bd0 = sdesc_sw128(sRing + stV * kSmemKTile, 2048, 1024);
-        const uint32_t dS = tmem + kTmemS + x * 128, dO = tmem + kTmemO + x * 128;
+    // O (+)= P(j) V(j); then the stage of V(j) is released
+    auto issue_pv = [&](int j) {
+      const int e = ev(j);
+      const uint32_t st = stage_of(e), b = (n0 + (uint32_t)j) & 1u;
+      // V (block kk for keys 16kk..) is N-major: 64-column halves 2 KiB apart (LBO), 8-key
+      // groups 1 KiB apart (SBO); P of keys 16kk.. is at column 8kk of the S buffer
+      const uint64_t bd0 = sdesc_sw128(sRing + st * kSmemKTile, 2048, 1024);
+      const uint32_t dS = tmem + kTmemS + b * 128, dO = tmem + kTmemO;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          umma_ts(dO, dS + kk * 8, bd0 + ((kk * kVBlockBytes) >> 4), kIdescPV,
-                  (first && kk == 0) ? 0u : 1u);
-      }
-      umma_commit(smem_u32(&ctl->pv_done[x]));
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        umma_ts(dO, dS + kk * 8, bd0 + ((kk * kVBlockBytes) >> 4), kIdescPV,
+                (j == 0 && kk == 0) ? 0u : 1u);
+      umma_commit(smem_u32(&ctl->pv_done));
+      umma_commit(smem_u32(&ctl->kv_empty[st]));
+      if (j + 1 == ntiles) umma_commit(smem_u32(&ctl->o_done));
     };
     bool ok = mbar_wait(smem_u32(&ctl->q_full), ps.q_cnt & 1, wc);
-    if (warp == 1) {
-      // S of step 0 (its K is ring entry 2 n0), then S of step j + 1 once P·V of step j is done
-      ok = ok && mbar_wait(smem_u32(&ctl->kv_full[(2 * n0) % kKVStages]), ((2 * n0) / kKVStages) & 1, wc);
-      tc_fence_after();
-      if (ok && lane == 0) {
-        const uint32_t stK = (2 * n0) % kKVStages;
-        issue_s(0, stK);
-        issue_s(1, stK);
-        umma_commit(smem_u32(&ctl->kv_empty[stK]));
+    if (warp == 3) {
+      // S(0), S(1), then S(j + 2) once P·V(j) has completed (completion n of pv_done: every one
+      // is waited for, so the parity is unambiguous) and K(j + 2) has landed
+      for (int i = 0; ok && i < 2 && i < ntiles; ++i) {
+        ok = mbar_wait(smem_u32(&ctl->kv_full[stage_of(ek(i))]), phase_of(ek(i)), wc);
+        tc_fence_after();
+        if (ok && lane == 0) issue_s(i);
+        __syncwarp();
       }
-      __syncwarp();
       for (int j = 0; ok && j < ntiles; ++j) {
         const uint32_t n = n0 + j;
-        const uint32_t stK = (2 * n + 2) % kKVStages;  // ring entry of K(j+1)
-#pragma unroll 1
-        for (int x = 0; x < 2; ++x) {
-          // every completion of pv_done is waited for, the last step's too, so the parity of
-          // the next item's first wait is unambiguous
-          if (!mbar_wait(smem_u32(&ctl->pv_done[x]), n & 1, wc)) {
-            ok = false;
-            break;
-          }
-          if (j + 1 == ntiles) continue;
-          if (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stK]), ((2 * n + 2) / kKVStages) & 1, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            issue_s(x, stK);
-            if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stK]));
-          }
-          __syncwarp();
-        }
+        ok = mbar_wait(smem_u32(&ctl->pv_done), n & 1, wc);
+        if (!ok || j + 2 >= ntiles) continue;
+        ok = mbar_wait(smem_u32(&ctl->kv_full[stage_of(ek(j + 2))]), phase_of(ek(j + 2)), wc);
+        tc_fence_after();
+        if (ok && lane == 0) issue_s(j + 2);
+        __syncwarp();
       }
     } else {
-      // P·V of step j once its P is written and V(j) (ring entry 2n + 1) has landed
+      // P·V(j) once P(j) is written and V(j) has landed
       for (int j = 0; ok && j < ntiles; ++j) {
         const uint32_t n = n0 + j;
-        const uint32_t stV = (2 * n + 1) % kKVStages;
-#pragma unroll 1
-        for (int x = 0; x < 2; ++x) {
-          if (!mbar_wait(smem_u32(&ctl->p_ready[x]), n & 1, wc) ||
-              (x == 0 && !mbar_wait(smem_u32(&ctl->kv_full[stV]), ((2 * n + 1) / kKVStages) & 1, wc))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            issue_pv(x, stV, j == 0);
-            if (x == 1) umma_commit(smem_u32(&ctl->kv_empty[stV]));
-            if (j + 1 == ntiles) umma_commit(smem_u32(&ctl->o_done[x]));
-          }
-          __syncwarp();
-        }
+        ok = mbar_wait(smem_u32(&ctl->p_ready[n & 1]), (n >> 1) & 1, wc) &&
+             mbar_wait(smem_u32(&ctl->kv_full[stage_of(ev(j))]), phase_of(ev(j)), wc);
+        tc_fence_after();
+        if (ok && lane == 0) issue_pv(j);
+        __syncwarp();
       }
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
-    // ------------------------------------------------------------------ softmax (1 row/thread)
-    const int x = (warp - kSoftmaxWarp0) >> 2;  // tile
-    const bool act = x == 0 || has_b;
+    // ------------------------------------------------------------------ queries and softmax
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int rp = x * kTileM + row;  // row of the item (partial slots)
-    const uint32_t tmem = ctl->tmem_base;
-    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tO = trow + kTmemO + x * 128;  // this tile's O accumulator
-    const uint32_t tS = trow + kTmemS + x * 128;  // and S buffer
-    const int qi = (2 * t + x) * p.tq + (row >> p.hp_log2);  // this row's token (in the chunk)
+    const int hf = (warp - kSoftmaxWarp0) >> 2;  // this thread's half of the keys and of O
+    const int row = quarter * 32 + lane;         // the tile row (TMEM lane)
+    const uint32_t trow = ctl->tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tO = trow + kTmemO + hf * (HD / 2);  // this half's O columns
+    const uint32_t tX = trow + kTmemX;                  // the halves' exchange columns
+    const int qi = t * p.tq + (row >> p.hp_log2);  // this row's token (in the chunk)
     const int h = h0 + (row & ((1 << p.hp_log2) - 1));      // and query head
     const bool valid = qi < qlen;
     const int lim = p.causal ? min(P + qi + 1, ke) : ke;  // keys [.., lim) are visible
-    float m = -INFINITY, l = 0.f;  // running max (log2 units) and sum of the row
+    {
+      // the row's queries (this half's dims; zeros past the chunk) into TMEM, bf16 pairs in the
+      // order the S MMAs read them; one arrival per warp once its stores have completed
+      constexpr int kWords = HD / 4;  // 32-bit words of half a row
+      uint32_t qw[32];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q_prefill + ((size_t)(q0 + (valid ? qi : 0)) * p.Hq + h) * HD + hf * (HD / 2));
+#pragma unroll
+      for (int i = 0; i < kWords / 4; ++i) {
+        const uint4 v = valid ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        qw[4 * i] = v.x;
+        qw[4 * i + 1] = v.y;
+        qw[4 * i + 2] = v.z;
+        qw[4 * i + 3] = v.w;
+      }
+      if constexpr (HD == 128) tmem_st32(trow + kTmemQ + hf * kWords, qw);
+      else tmem_st16(trow + kTmemQ + hf * kWords, qw);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->q_full));
+    }
+    float m = -INFINITY, l = 0.f;  // the row's running max (log2 units), this half's sum
     bool ok = true;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    // scores of columns [0, 64) visible below v (others -inf), then their max
+    // scores of the half's 64 columns visible below v (others -inf)
     auto mask64 = [&](uint32_t(&a)[32], uint32_t(&b)[32], int v) {
       if (!__all_sync(0xffffffffu, v >= 64)) {
 #pragma unroll
@@ -473,9 +477,10 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], u2f(b[i + 24]));
       return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
     };
-    // exponentials of 64 scores against the reference max; P as bf16 pairs at columns
-    // [pc, pc + 32) of the S buffer; returns their sum
-    auto exp64 = [&](const uint32_t(&a)[32], const uint32_t(&b)[32], float2 nm2, uint32_t pc) {
+    // exponentials of the half's 64 scores against the reference max; P as bf16 pairs at
+    // columns [pc, pc + 32) of the S buffer at tS; returns their sum
+    auto exp64 = [&](const uint32_t(&a)[32], const uint32_t(&b)[32], float2 nm2, uint32_t tS,
+                     uint32_t pc) {
       float2 sum[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
@@ -499,81 +504,81 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       const float2 s01 = fadd2(fadd2(sum[0], sum[1]), fadd2(sum[2], sum[3]));
       return s01.x + s01.y;
     };
+    // The other half's value of this row through TMEM column `col` (this half writes
+    // col + hf, reads col + 1 - hf); both halves of every row pass the same barrier.
+    auto exchange = [&](uint32_t col, float mine) {
+      tmem_st1(tX + col + hf, f2u(mine));
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_sync(2, 256);
+      tc_fence_after();
+      const uint32_t o = tmem_ld1(tX + col + (hf ^ 1));
+      tmem_ld_wait();
+      return u2f(o);
+    };
     for (int j = 0; j < ntiles; ++j) {
-      const uint32_t n = n0 + j;
+      const uint32_t n = n0 + j, b = n & 1;
       // After a failed wait the loop still runs (every wait then fails at once), so that the
       // warps pass the same barriers whatever happened.
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[x]), n & 1, wc));
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->s_full[b]), (n >> 1) & 1, wc));
       tc_fence_after();
-      if (act) {
-        const int vis = lim - (kb + j * kTileN);  // visible columns of the step: [0, vis)
-        uint32_t sa[32], sb[32];
-        // the row max over keys 64..127, then over keys 0..63, which stay in registers
-        tmem_ld32(tS + 64, sa);
-        tmem_ld32(tS + 96, sb);
-        tmem_ld_wait();
-        mask64(sa, sb, vis - 64);
-        const float mx_hi = max64(sa, sb);
-        tmem_ld32(tS, sa);
-        tmem_ld32(tS + 32, sb);
-        tmem_ld_wait();
-        mask64(sa, sb, vis);
-        const float mine = fmaxf(mx_hi, max64(sa, sb));
-        // scale > 0, so the max of the scaled scores is the scaled max
-        const float m_new = fmaxf(m, mine * p.scale_log2);
-        const bool resc = m_new > m + 8.f;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ex2(m - m_new);
-          m = m_new;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O holds P·V of the earlier steps: this step's S was issued only after the tile's
-          // last P·V had completed
+      const uint32_t tS = trow + kTmemS + b * 128;
+      const int vis = lim - (kb + j * kTileN) - hf * 64;  // visible columns of the half: [0, vis)
+      uint32_t sa[32], sb[32];
+      tmem_ld32(tS + hf * 64, sa);
+      tmem_ld32(tS + hf * 64 + 32, sb);
+      tmem_ld_wait();
+      mask64(sa, sb, vis);
+      const float mine = max64(sa, sb);
+      // the row's max over both halves (exchange columns alternate with the step's parity, so
+      // a half never overwrites a value its partner has yet to read)
+      const float mx = fmaxf(mine, exchange(2 * b, mine));
+      // scale > 0, so the max of the scaled scores is the scaled max
+      const float m_new = fmaxf(m, mx * p.scale_log2);
+      const bool resc = m_new > m + 8.f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2(m - m_new);
+        m = m_new;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O holds P·V of the earlier steps once P·V(n - 1) has completed (completion n - 1 of
+        // pv_done; S(n), which this step waited for, was issued after P·V(n - 2), so the
+        // barrier is at completion n - 1 or n: its parity is unambiguous)
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done), (n - 1) & 1, wc));
+        tc_fence_after();
 #pragma unroll 1
-          for (int ch = 0; ch < HD / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(tO + ch * 32, o);
-            tmem_ld_wait();
+        for (int ch = 0; ch < HD / 64; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tO + ch * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-            tmem_st32(tO + ch * 32, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+          tmem_st32(tO + ch * 32, o);
         }
-        const float mref = m == -INFINITY ? 0.f : m;
-        const float2 nm2 = make_float2(-mref, -mref);
-        // P of keys 0..63 over columns 0..31 (those scores are in registers), then keys
-        // 64..127, read again, over columns 32..63 (one copy of the code: fewer live registers)
-        float sum = 0.f;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          if (hh) {
-            tmem_ld32(tS + 64, sa);
-            tmem_ld32(tS + 96, sb);
-            tmem_ld_wait();
-            mask64(sa, sb, vis - 64);
-          }
-          sum += exp64(sa, sb, nm2, hh * 32);
-        }
-        l = l * alpha + sum;
         tmem_st_wait();
       }
-      // every lane's P stores have completed (tcgen05.wait::st above); one arrival per warp
+      const float mref = m == -INFINITY ? 0.f : m;
+      l = l * alpha + exp64(sa, sb, make_float2(-mref, -mref), tS, hf * 32);
+      tmem_st_wait();
+      // every lane's P stores have completed; one arrival per warp
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_ready[x]));
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_ready[b]));
     }
-    if (ok && ntiles > 0) {  // the tile's last P·V (and with it every MMA of the item)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[x]), ps.q_cnt & 1, wc));
+    if (ok) {  // the last P·V (and with it every MMA of the item)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done), ps.q_cnt & 1, wc));
       tc_fence_after();
     }
+    // the row sum over both halves
+    const float lrow = l + exchange(4, l);
     // ------------------------------------------------------------------ epilogue
+    // Each thread writes its half of the row's O columns.
     if (unit < 0) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD + hf * (HD / 2);
 #pragma unroll 1
-      for (int ch = 0; ch < HD / 32; ++ch) {
+      for (int ch = 0; ch < HD / 64; ++ch) {
         uint32_t a[32];
         tmem_ld32(tO + ch * 32, a);
         tmem_ld_wait();
@@ -594,34 +599,36 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
       uint8_t* slot = slots + (size_t)(slot0 + split) * kPrefillSlotBytes;
       // The partial is O / l in bf16 (the final output's precision) with the row's m and l in
       // fp32, written with streaming stores so that it does not push K/V tiles out of L2. O is
-      // stored in 8-column chunks interleaved across the 32 rows of a warp (chunk c of row rp at
-      // uint4 ((rp / 32) * 16 + c) * 32 + rp % 32), so that each store and each load of the
-      // merge moves 512 contiguous bytes per warp.
-      const size_t row_off = (size_t)(rp >> 5) * (kHeadDim / 8) * 32 + (rp & 31);
+      // stored in 8-column chunks interleaved across the 32 rows of a warp (chunk c of row r at
+      // uint4 ((r / 32) * 16 + c) * 32 + r % 32), so that each store and each load of the merge
+      // moves 512 contiguous bytes per warp. This half holds chunks [c0, c0 + HD / 16).
+      const size_t row_off = (size_t)(row >> 5) * (kHeadDim / 8) * 32 + (row & 31);
+      const int c0 = hf * (HD / 16);
       uint4* o8 = reinterpret_cast<uint4*>(slot) + row_off;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll 1
-      for (int ch = 0; ch < HD / 32 && ok; ++ch) {
+      for (int ch = 0; ch < HD / 64 && ok; ++ch) {
         uint32_t a[32];
         tmem_ld32(tO + ch * 32, a);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          __stcs(o8 + (ch * 4 + i) * 32,
+          __stcs(o8 + (c0 + ch * 4 + i) * 32,
                  make_uint4(pack_bf16x2(u2f(a[8 * i]) * inv_l, u2f(a[8 * i + 1]) * inv_l),
                             pack_bf16x2(u2f(a[8 * i + 2]) * inv_l, u2f(a[8 * i + 3]) * inv_l),
                             pack_bf16x2(u2f(a[8 * i + 4]) * inv_l, u2f(a[8 * i + 5]) * inv_l),
                             pack_bf16x2(u2f(a[8 * i + 6]) * inv_l, u2f(a[8 * i + 7]) * inv_l)));
       }
-      constexpr int kMlOff = kPairRows * kHeadDim * 2;  // m[256] then l[256], fp32
-      if (ok) {
+      constexpr int kMlOff = kTileM * kHeadDim * 2;  // m[128] then l[128], fp32
+      if (ok && hf == 0) {
         float* ml = reinterpret_cast<float*>(slot + kMlOff);
-        __stcs(ml + rp, m);
-        __stcs(ml + kPairRows + rp, l);
+        __stcs(ml + row, m);
+        __stcs(ml + kTileM + row, lrow);
       }
       __threadfence();
       named_bar_sync(2, 256);
-      if (rp == 0) ctl->merge_last[0] = ok && (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
+      if (row == 0 && hf == 0)
+        ctl->merge_last[0] = ok && (atomicAdd(&p.arrive[unit], 1) == nsplit - 1);
       named_bar_sync(2, 256);
       if (ctl->merge_last[0] && ok) {
         __threadfence();
@@ -635,7 +642,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
 #pragma unroll
           for (int k = 0; k < kMaxPrefillSplits; ++k) {
             f[k] = k < nsplit
-                       ? __ldcg(reinterpret_cast<const float*>(base + (size_t)k * kPrefillSlotBytes + kMlOff) + rp)
+                       ? __ldcg(reinterpret_cast<const float*>(base + (size_t)k * kPrefillSlotBytes + kMlOff) + row)
                        : -INFINITY;
             mx = fmaxf(mx, f[k]);
           }
@@ -644,7 +651,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           for (int k = 0; k < kMaxPrefillSplits; ++k) {
             const float lk =
                 k < nsplit ? __ldcg(reinterpret_cast<const float*>(base + (size_t)k * kPrefillSlotBytes + kMlOff) +
-                                    kPairRows + rp)
+                                    kTileM + row)
                            : 0.f;
             f[k] = f[k] == -INFINITY ? 0.f : ex2(f[k] - mx) * lk;  // weight of split k
             den += f[k];
@@ -652,7 +659,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
           const float inv = den > 0.f ? 1.f / den : 0.f;
           uint16_t* dst = p.o_prefill + ((size_t)(q0 + qi) * p.Hq + h) * HD;
 #pragma unroll 1
-          for (int ch = 0; ch < HD / 16; ++ch) {  // 16 columns (two chunks) at a time
+          for (int ch = hf * (HD / 32); ch < (hf + 1) * (HD / 32); ++ch) {  // 16 columns at a time
             float acc[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) acc[c] = 0.f;
@@ -683,7 +690,7 @@ __device__ void prefill_item(const Params& p, const CUtensorMap* tmq, const CUte
                                  pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
           }
         }
-        if (rp == 0) p.arrive[unit] = 0;  // ready for the next run
+        if (row == 0 && hf == 0) p.arrive[unit] = 0;  // ready for the next run
       }
     }
     tc_fence_before();
@@ -1595,7 +1602,7 @@ __device__ void decode_loop(const Params& p, const CUtensorMap* tmk, const CUten
 
 template <int GT, int HD, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-    pod_attn_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq,
+    pod_attn_kernel(const __grid_constant__ Params p,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const __grid_constant__ CUtensorMap tmkb,
                     const __grid_constant__ CUtensorMap tmvb) {
@@ -1609,17 +1616,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool use_tmem = p.mode != kModeDecodeOnly && p.n_items_p > 0;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&ctl->q_full), 1);
+    mbar_init(smem_u32(&ctl->q_full), 8);
     for (int i = 0; i < kKVStages; ++i) {
       mbar_init(smem_u32(&ctl->kv_full[i]), 1);
       mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctl->p_ready[i]), 4);
-      mbar_init(smem_u32(&ctl->pv_done[i]), 1);
-      mbar_init(smem_u32(&ctl->o_done[i]), 1);
+      mbar_init(smem_u32(&ctl->p_ready[i]), 8);
     }
+    mbar_init(smem_u32(&ctl->pv_done), 1);
+    mbar_init(smem_u32(&ctl->o_done), 1);
     for (int w = 0; w < kWarps; ++w)
       for (int s = 0; s < kDecodeSlotsFp8; ++s) mbar_init(smem_u32(&ctl->dslot[w][s]), 1);
     ctl->abort = 0;
@@ -1627,7 +1634,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
     if (use_tmem) {
-      prefetch_tmap(&tmq);
       prefetch_tmap(&tmkb);
       prefetch_tmap(&tmvb);
     }
@@ -1667,7 +1673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint64_t t0 = (p.records != nullptr && tid == 0) ? globaltimer() : 0;
       if constexpr (!FP8)
-        prefill_item<HD>(p, &tmq, &tmk, &tmv, &tmkb, &tmvb, p.items_p + (size_t)idx * kItemWords, smem, ctl,
+        prefill_item<HD>(p, &tmk, &tmv, &tmkb, &tmvb, p.items_p + (size_t)idx * kItemWords, smem, ctl,
                          ps, wc);
       if (p.records != nullptr && tid == 0) record_item(p, kind, idx, sm_raw, t0);
     }
@@ -1764,25 +1770,12 @@ static EncodeTiledFn get_encode_fn() {
 
 struct CudaState {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  CUtensorMap tmq{}, tmk{}, tmv{}, tmkb{}, tmvb{};
-  const void *kq = nullptr, *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
+  CUtensorMap tmk{}, tmv{}, tmkb{}, tmvb{};
+  const void *kk = nullptr, *kv = nullptr;  // pointers the maps were built for
   CUtensorMap tmk8{}, tmv8{};                               // e4m3 pools (FP8 cache decode)
   const void *kk8 = nullptr, *kv8 = nullptr;
 };
 
-// Q: 3-D {dim, head, token} so one box is 64 dims of hp heads x 128/hp tokens: the 128 rows of
-// a prefill tile, token-major.
-static bool encode_q(CUtensorMap* m, const void* q, int Hq, int Tp, int hp, int hd) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)Hq, (cuuint64_t)Tp};
-  cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)Hq * hd * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)hp, (cuuint32_t)(kTileM / hp)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 // K or V pool: 2-D {dim, row} over num_blocks*Hkv*16 rows; one box is one paged block's 16 rows
 // x 64 dims.
 static bool encode_pool(CUtensorMap* m, const void* pool, int64_t rows, int hd) {
@@ -1852,7 +1845,7 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
     attr_set.store(1);
   }
   if (!p.wait_append) {
-    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, cs.tmq, tmk, tmv, cs.tmkb,
+    pod_attn_kernel<GT, HD, FP8><<<grid, kThreads, kSmemTotal, st>>>(p, tmk, tmv, cs.tmkb,
                                                                      cs.tmvb);
     return cudaGetLastError();
   }
@@ -1868,7 +1861,7 @@ static cudaError_t launch_mode(const Params& p, int grid, cudaStream_t st, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, cs.tmq, tmk, tmv, cs.tmkb,
+  return cudaLaunchKernelEx(&cfg, pod_attn_kernel<GT, HD, FP8>, p, tmk, tmv, cs.tmkb,
                             cs.tmvb);
 }
 
@@ -2122,12 +2115,6 @@ static pod_attn_status run_impl(pod_attn_plan_t plan, const void* q_prefill, con
     return POD_ATTN_ERR_INVALID_ARG;
   CudaState* cs = static_cast<CudaState*>(plan->cuda_state);
   const int64_t pool_rows = (int64_t)pr.num_blocks * pr.num_kv_heads * kBlockSize;
-  if (n_p > 0 && cs->kq != q_prefill) {
-    if (!encode_q(&cs->tmq, q_prefill, pr.num_q_heads, pr.num_prefill_tokens, plan->head_pack,
-                  pr.head_dim))
-      return POD_ATTN_ERR_CUDA;
-    cs->kq = q_prefill;
-  }
   // the pools' maps serve the prefill tiles and the grouped-query decode path
   if (cs->kk != k_pool) {
     if (!encode_pool(&cs->tmk, k_pool, pool_rows, pr.head_dim)) return POD_ATTN_ERR_CUDA;

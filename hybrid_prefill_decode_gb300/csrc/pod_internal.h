@@ -18,11 +18,11 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 
 // One persistent CTA per SM holds two concurrent virtual-CTA slots ("POD-Attention" digest,
 // §"가상 CTA와 SM별 균형": prefill and decode work placed side by side on every SM):
-//  * the prefill slot (warps 0-11): one pipeline over the SM's 512 TMEM columns that runs two
-//    128-row query tiles (A and B) against each K/V tile — warp 0 issues the TMA loads of the
-//    query tiles and of one ring of K and V tiles, warp 1 issues the S tcgen05 MMAs and warp 3
-//    the P·V tcgen05 MMAs of both tiles, and warps 4-7 and 8-11 are the softmax warpgroups of
-//    tile A and tile B (one query row per thread, all 128 keys of a step);
+//  * the prefill slot (warps 0-11): one pipeline over the SM's TMEM that runs a 128-row query
+//    tile against a range of K/V tiles — warps 0 and 2 issue the TMA loads (K and V) of one
+//    ring of K and V tiles, warps 1 and 3 issue the P·V and the S tcgen05 MMAs, and warps 4-11 load the tile's
+//    queries into TMEM and run the softmax, two threads per query row (warps w and w + 4
+//    share the row's TMEM lane, each takes 64 of a step's 128 keys);
 //  * the decode slot (warps 12-15): decode items, on their own ticket loop.
 // Once the prefill list is drained, the prefill slot's warps 4-7 and 8-11 become two more
 // 4-warp decode slots. Every decode item thus runs on exactly 4 warps, whichever slot takes it,
@@ -30,7 +30,7 @@ constexpr int kMaxGroup = 8;            // query heads per KV head handled by th
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPrefillThreads = 384;    // warps 0-11
-constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (tile A: 4-7, tile B: 8-11)
+constexpr int kSoftmaxWarp0 = 4;        // first softmax warp (keys 0-63: 4-7, 64-127: 8-11)
 constexpr int kDecodeWarp0 = 12;        // decode slot: warps 12-15
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeSlots = 2;         // K+V blocks in flight per decode warp (bf16 cache)
@@ -40,21 +40,20 @@ constexpr int kDecodeSlotsFp8 = 3;      // ... on the e4m3 cache (half the bytes
 // power of two dividing the group size, T = 128 / hp; row r is token r / hp, head h0 + r % hp).
 // All hp heads read the same K and V, so one K/V tile serves hp heads ("LLMSO - W4", §"KV 헤드
 // 줄이기": the heads of a group share their K/V).
-// Prefill item: two consecutive tiles of one chunk and head block (tile A: tokens 2tT .. 2tT+T-1,
-// tile B: the next T), so every K/V tile staged in shared memory serves 256 query rows.
-// Prefill step: both tiles x 128 keys. Each tile has one S buffer in TMEM; while one tile's
-// softmax runs, the tensor cores compute the other tile's P·V and next S. K and V tiles share
-// one ring of kKVStages tiles, loaded in the order K(0), V(0), K(1), V(1), ...
+// Prefill item: one tile (tokens tT .. tT+T-1 of one chunk, one head block) against a range of
+// keys. Prefill step: the tile x 128 keys. The tile has two S buffers in TMEM (step n uses
+// buffer n & 1), so S of the next step is computed while the softmax of this one runs, and its
+// queries sit in TMEM as the A operand of the S MMAs, so the tensor cores read only K and V from
+// shared memory. K and V tiles share one ring of kKVStages tiles, loaded in the order the MMAs
+// consume them: K(0), K(1), then V(j), K(j + 2) for each step j.
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
-constexpr int kPairRows = 2 * kTileM;   // query rows of one prefill item
-constexpr int kKVStages = 3;
+constexpr int kKVStages = 5;
 
 // Shared-memory map (bytes from the dynamic shared-memory base, which the hardware places at
 // a 1024-byte boundary; the kernel checks this and reports an error otherwise).
-constexpr int kSmemQ = kTileM * kHeadDim * 2;                      // 32 KiB query tile
 constexpr int kSmemKTile = kTileN * kHeadDim * 2;                  // 32 KiB (K or V tile)
-constexpr int kSmemPrefill = 2 * kSmemQ + kKVStages * kSmemKTile;  // 160 KiB
+constexpr int kSmemPrefill = kKVStages * kSmemKTile;               // 160 KiB
 constexpr int kSmemDecodeSlot = 2 * kBlockSize * kHeadDim * 2;     // 8 KiB (K block + V block)
 constexpr int kSmemDecodeRing = kDecodeWarps * kDecodeSlots * kSmemDecodeSlot;  // 64 KiB
 constexpr int kSmemScoresPerWarp = kMaxGroup * kBlockSize * 4;     // p exchange of one warp
@@ -68,18 +67,22 @@ static_assert(kSmemTotal <= 227 * 1024, "one CTA per SM must fit");
 static_assert(2 * (kSmemDecodeRing + kDecodeWarps * kSmemScoresPerWarp) <= kSmemPrefill,
               "the two decode slots of the prefill warps must fit the prefill region");
 
-// TMEM columns (the whole SM): one O accumulator per tile (fp32, 128 columns each) and one S
-// buffer per tile (fp32, 128 columns each). A tile's softmax writes its P (bf16 pairs, 128 keys)
-// over the first 64 columns of the tile's S buffer; the tile's issuer issues S of the next step
-// into that buffer after the P·V that reads P (MMAs of one thread run in issue order).
+// TMEM columns (the whole SM; lane r is tile row r): the O accumulator (fp32, 128 columns), two
+// S buffers (fp32, 128 columns each), the tile's queries (bf16 pairs, 64 columns: column c holds
+// dims 2c and 2c + 1) and a few columns through which the two softmax threads of a row exchange
+// their max and sum. A step's softmax writes its P (bf16 pairs, 128 keys) over the first 64
+// columns of its S buffer; S of step n + 2 is issued into that buffer once the P·V(n) that reads
+// P has completed.
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 0;      // + 128 * tile
-constexpr int kTmemS = 256;    // + 128 * tile
+constexpr int kTmemO = 0;
+constexpr int kTmemS = 128;    // + 128 * (step & 1)
+constexpr int kTmemQ = 384;
+constexpr int kTmemX = 448;    // [0, 4): maxima by step parity and half; [4, 6): sums by half
 
 // Work item: kItemWords int32 words.
 //   [0] kind         0 = prefill, 1 = decode
 //   [1] seq          prefill: chunk index s in [0, Np); decode: d in [0, Nd)
-//   [2] tile / kvh   prefill: index t of the tile pair (chunk tokens 2Tt .. 2Tt + 2T - 1, with
+//   [2] tile / kvh   prefill: index t of the tile (chunk tokens Tt .. Tt + T - 1, with
 //                    T = 128 / hp tokens per tile); decode: kv-head g
 //   [3] head         prefill: first query head h0 of the tile's hp heads; decode: 0
 //   [4] key_begin    first key row of this split (prefill: multiple of 128; decode: of 16)
@@ -97,10 +100,10 @@ constexpr int kMaxPrefillSplits = 8;
 // shared memory).
 constexpr int kMaxDecodeSplits = 64;
 
-// Partial-result slots. A prefill slot holds the 256 rows of a tile pair (tile A's rows first):
-// O / l as bf16 [rows][128] (in 8-column chunks interleaved across each 32 rows), then fp32
-// m[rows] and l[rows] (m in log2 units). A decode slot: fp32 o[rows][128] then m[rows], l[rows].
-constexpr int kPrefillSlotBytes = kPairRows * kHeadDim * 2 + 2 * kPairRows * 4;
+// Partial-result slots. A prefill slot holds the 128 rows of a tile: O / l as bf16 [rows][128]
+// (in 8-column chunks interleaved across each 32 rows), then fp32 m[rows] and l[rows] (m in
+// log2 units). A decode slot: fp32 o[rows][128] then m[rows], l[rows].
+constexpr int kPrefillSlotBytes = kTileM * kHeadDim * 2 + 2 * kTileM * 4;
 #ifdef __CUDACC__
 __host__ __device__
 #endif

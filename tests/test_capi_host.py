@@ -128,7 +128,7 @@ def _list_span(costs, slots):
 
 def restated_prefill_chunk(nts, num_sms):
     """Prefill: the chunk ceil(longest / k), k = 1..8, that minimises the makespan of the items
-    (steps + 4 each) taken longest first by one slot per SM, each going to the slot that frees
+    (steps + 8 each) taken longest first by one slot per SM, each going to the slot that frees
     first; chunks under 4 steps are not tried (but k = 1 always is); ties keep the larger
     chunk."""
     longest = max(nts)
@@ -143,7 +143,7 @@ def restated_prefill_chunk(nts, num_sms):
         items = []
         for n in nts:
             ns, ch = _rebalanced(n, c)
-            items += [min(n, (j + 1) * ch) - j * ch + 4 for j in range(ns)]
+            items += [min(n, (j + 1) * ch) - j * ch + 8 for j in range(ns)]
         t = _list_span(items, num_sms)
         if best is None or t < best:
             best, best_c = t, c
@@ -177,8 +177,8 @@ def restated_decode_only_chunk(nblks, num_sms, kv_fp8):
 
 def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True, kv_fp8=False,
                   prefill_cap=0):
-    """Items: prefill = (chunk, pair of query tiles of 128/hp tokens x hp heads, first head,
-    split) over 128-key steps of both tiles (cost 114 each), with hp the largest power of two
+    """Items: prefill = (chunk, query tile of 128/hp tokens x hp heads, first head, split) over
+    128-key steps of the tile (cost 57 each), with hp the largest power of two
     dividing the group size; decode = (sequence, kv-head, split) over 16-row blocks (cost 8
     each); two item slots per SM; split when an output costs more than a quarter of a slot's
     share."""
@@ -186,17 +186,17 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
     slots = num_sms * 2
     G = Hq // Hkv
     hp = max(x for x in (1, 2, 4, 8) if G % x == 0)
-    pair = 2 * (128 // hp)                                        # tokens of one prefill item
+    tile = 128 // hp                                              # tokens of one prefill item
     pu, du, total = [], [], 0
     for s in range(np_):
         q, L = cu[s + 1] - cu[s], kv[s]
         P = L - q
-        for t in range(_cdiv(q, pair)):
-            kend = P + min(q, (t + 1) * pair) if causal else L    # non-causal: every row
+        for t in range(_cdiv(q, tile)):
+            kend = P + min(q, (t + 1) * tile) if causal else L    # non-causal: every row
             nt = _cdiv(kend, 128)
             for h in range(0, Hq, hp):
                 pu.append((s, t, h, kend, nt))
-                total += nt * 114
+                total += nt * 57
     for d in range(nd):
         L = kv[np_ + d]
         for g in range(Hkv):
@@ -224,7 +224,7 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
         u = add_unit(ns, 0) if ns > 1 else -1
         for k in range(ns):
             t0, t1 = k * chunk, min(nt, (k + 1) * chunk)
-            lp.append(((t1 - t0) * 114, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
+            lp.append(((t1 - t0) * 57, [0, s, t, h, t0 * 128, min(kend, t1 * 128), u, k]))
     chunk_do = (restated_decode_only_chunk([x[3] for x in du], num_sms, kv_fp8)
                 if not pu and du and not dsplit else 0)
     for d, g, L, nblk in du:
@@ -243,7 +243,7 @@ def restated_plan(Hq, Hkv, cu, kv, nd, num_sms, psplit=0, dsplit=0, causal=True,
             ld.append(((b1 - b0) * 8, [1, d, g, 0, b0 * 16, min(L, b1 * 16), u, k]))
     # prefill: cost in a coarse relative bucket (3 significant bits), then split index; decode:
     # cost; both stable (ties in enumeration order)
-    lp.sort(key=lambda x: (-_bucket(x[0] // 114), x[1][7]))
+    lp.sort(key=lambda x: (-_bucket(x[0] // 57), x[1][7]))
     ld.sort(key=lambda x: -x[0])
     return ([w for _, w in lp], [w for _, w in ld], units, prefill_ctas,
             min(num_sms, len(lp) + len(ld)))
@@ -362,7 +362,7 @@ def test_planner_covers_every_key_once(lib, i):
     p = B.Plan(Hq, Hkv, cu, pkv + dkv, len(dkv), 10, _cdiv(max(pkv + dkv), 16), 0.1,
                num_sms=152)
     hp = max(x for x in (1, 2, 4, 8) if (Hq // Hkv) % x == 0)   # heads per prefill tile
-    pair = 2 * (128 // hp)                                        # tokens per prefill item
+    tile = 128 // hp                                              # tokens per prefill item
     items_p, items_d, units = p.items()
     cover = {}
     for it in items_p + items_d:
@@ -382,10 +382,10 @@ def test_planner_covers_every_key_once(lib, i):
         else:
             t = key[2]
             q = q_lens[seq]
-            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * pair)
+            assert parts[-1][2] == pkv[seq] - q + min(q, (t + 1) * tile)
             assert key[3] % hp == 0
-    # every (tile pair, block of hp heads) and (decode seq, kv-head) appears
-    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, pair) for q in q_lens) * (Hq // hp)
+    # every (tile, block of hp heads) and (decode seq, kv-head) appears
+    assert len([k for k in cover if k[0] == 0]) == sum(_cdiv(q, tile) for q in q_lens) * (Hq // hp)
     assert len([k for k in cover if k[0] == 1]) == len(dkv) * Hkv
 
 
@@ -441,12 +441,11 @@ def test_append_fp8_validation(lib):
     assert lib.pod_attn_append_fp8(empty.handle, *([None] * 7), 256, big, None) == B.OK
 
 
-@pytest.mark.parametrize("i,items,max_steps", [(2, 128, 16), (3, 128, 63), (4, 1024, 60)])
+@pytest.mark.parametrize("i,items,max_steps", [(2, 128, 32), (3, 256, 63), (4, 1024, 120)])
 def test_prefill_chunk_choice_on_configs(lib, i, items, max_steps):
     """The prefill chunk rule's choice on the full-size configurations at 152 SMs: configs 2
-    and 3 keep their 128 tile-pair outputs whole; config 4 cuts its 256 outputs of ~232 steps
-    into 4 splits (1024 items of at most 60 steps), the count that measured fastest of 1-8
-    forced splits on the GB300."""
+    and 3 keep their 128 and 256 tile outputs whole; config 4 cuts its 512 outputs of ~232
+    steps into 2 splits (1024 items of at most 120 steps)."""
     Hq, Hkv, q_lens, pkv, dkv = W.config_lengths(i)
     cu = [0]
     for q in q_lens:

@@ -109,8 +109,8 @@ typedef struct {
                                POD_ATTN_ERR_INVALID_ARG */
   int32_t decode_splits;    /* force this many KV splits per decode (seq, kv-head), at most 64
                                (more are capped); 0 = auto */
-  int32_t prefill_splits;   /* force this many KV splits per prefill (tile pair, head block),
-                               at most 8; 0 = auto */
+  int32_t prefill_splits;   /* force this many KV splits per prefill output (128-row tile of
+                               one chunk and head block), at most 8; 0 = auto */
   int32_t instrument;       /* nonzero: record (SM, kind, start, end) per work item */
   pod_attn_variant variant; /* launch variant, see above */
   int32_t non_causal;       /* nonzero: prefill chunk tokens attend to every row of their
@@ -127,8 +127,8 @@ typedef struct pod_attn_plan_s* pod_attn_plan_t;
 
 /* Summary of a plan (what the planner decided). */
 typedef struct {
-  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, pair of 128-row tiles, each
-                                 128/hp tokens x hp q-heads of one kv-head group, kv-split) */
+  int32_t num_prefill_items;  /* virtual prefill CTAs: (chunk, 128-row tile of 128/hp tokens
+                                 x hp q-heads of one kv-head group, kv-split) */
   int32_t num_decode_items;   /* virtual decode CTAs: (seq, kv-head, kv-split) */
   int32_t num_units;          /* outputs assembled from more than one split */
   int32_t num_sms;            /* SM count the grid was sized for */
@@ -322,7 +322,8 @@ pod_attn_status pod_attn_plan_bucket(pod_attn_plan_t plan, pod_attn_bucket* out)
 
 /* Copy the host work lists: prefill items first, then decode items, then the unit table, each
  * item info.item_words (8) int32 words: kind (0 prefill, 1 decode); prefill chunk index or
- * decode sequence index; prefill tile-pair index or decode kv-head; prefill first query head
+ * decode sequence index; prefill tile index (chunk tokens 128/hp * t ..) or decode kv-head;
+ * prefill first query head
  * (decode 0); first key row of the split; one past its last key row; the unit index of a split
  * output (-1 when the item writes its output directly); the split's index within the unit. A
  * unit is 4 words: split count, first partial slot, kind, 0.

@@ -205,19 +205,20 @@ def test_prefill_cta_cap_keeps_prefill_on_the_first_ctas(cap):
     assert_close(o_d, ref_d, f"cap {cap} decode")
 
 
-def _ramp_batch(seed, q=(300, 40), pkv=(1300, 200), dkv=(900, 17)):
+def _ramp_batch(seed, q=(300, 40), pkv=(1300, 200), dkv=(900, 17), head_dim=128, causal=True):
     """A GQA batch whose scores grow along every sequence by ~10 (log2 units) per 128 keys: K row
     p is 0.6 p / 128 along the all-ones direction plus small noise, and every query is near that
     direction. Each 128-key step then moves the row max past the lazy-rescale threshold (2^8),
     so the prefill tile rescales O at every step (waiting for the previous P·V) and splits
     merge partials whose maxima differ by far more than the threshold."""
-    b = W.make_batch(8, 2, list(q), list(pkv), list(dkv), seed=seed)
+    b = W.make_batch(8, 2, list(q), list(pkv), list(dkv), seed=seed, head_dim=head_dim,
+                     causal=causal)
     D, Hkv = b.head_dim, b.num_kv_heads
     g = torch.Generator().manual_seed(seed)
     bt = b.block_tables.long()
     for s, L in enumerate(b.host_kv_lens):
         pos = torch.arange(L)
-        rows = (0.6 / 128.0) * pos.float()[:, None, None].expand(L, Hkv, D) \
+        rows = (0.6 / D) * pos.float()[:, None, None].expand(L, Hkv, D) \
             + 0.05 * torch.randn(L, Hkv, D, generator=g)
         blk = bt[s, pos // 16]
         b.k_pool[blk, :, pos % 16, :] = rows.to(torch.bfloat16)
@@ -230,3 +231,8 @@ def _ramp_batch(seed, q=(300, 40), pkv=(1300, 200), dkv=(900, 17)):
                                         ("serial", {}), ("fused", {"num_sms": 3})])
 def test_growing_scores_rescale_every_step(variant, kw):
     run_and_check(_ramp_batch(41), variant, **kw)
+
+
+@pytest.mark.parametrize("head_dim,causal", [(64, True), (128, False)])
+def test_growing_scores_rescale_head_dim_64_and_non_causal(head_dim, causal):
+    run_and_check(_ramp_batch(43, head_dim=head_dim, causal=causal), "fused")

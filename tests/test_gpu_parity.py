@@ -236,3 +236,16 @@ def test_growing_scores_rescale_every_step(variant, kw):
 @pytest.mark.parametrize("head_dim,causal", [(64, True), (128, False)])
 def test_growing_scores_rescale_head_dim_64_and_non_causal(head_dim, causal):
     run_and_check(_ramp_batch(43, head_dim=head_dim, causal=causal), "fused")
+
+
+@pytest.mark.parametrize("variant,kw", [("fused", {"num_sms": 1}), ("fused", {"num_sms": 2, "prefill_splits": 5}),
+                                        ("serial", {"num_sms": 1, "prefill_splits": 3}),
+                                        ("fused", {})])
+def test_items_of_one_two_three_steps_through_few_ctas(variant, kw):
+    """Prefill items of 1, 2 and 3 key steps (the ends of the ring's consumption order: K(0),
+    K(1), then V(j), K(j + 2), then the last V's) and longer ones, split or not, many of them
+    through one or two CTAs, so every ring stage and barrier carries its phases across items of
+    different lengths."""
+    b = W.make_batch(8, 2, [100, 60, 10, 1, 200, 129], [100, 200, 300, 257, 700, 1000],
+                     [5, 130, 390], seed=47)
+    run_and_check(b, variant, **kw)
